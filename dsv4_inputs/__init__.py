@@ -1,0 +1,344 @@
+"""Seeded synthetic inputs for the DeepSeek-V4 hybrid compressed-attention decode step.
+
+This module is shared by the CPU oracle's tests, the GPU parity tests, ``smoke()``
+and ``bench.py``.  It draws random numbers and lays them out in the paged-cache
+byte formats; it holds none of the method's arithmetic (no fold, no indexer
+score, no top-k, no attention, no UE8M0 scale selection).
+
+Workload shapes follow the five decode configurations of the hot path:
+
+  tiny_c4_f32    1 seq, context 1024, c4, 16 heads, indexer 4 x 64, top-k 64, fp32
+  csa_c4_bf16    32 seqs, context 65536, c4, 64 heads, indexer 64 x 128 bf16, top-k 512
+  hca_c128_bf16  64 seqs, context U[65536, 131072], c128 dense, 64 heads, no indexer
+  csa_c4_fp8     128 seqs, context U[8192, 32768], 2 query tokens per seq,
+                 fp8_ds_mla caches, int8 + fp32-scale indexer keys, top-k 512
+  csa_c4_1m      4 seqs, context 1048576, 128 heads, top-k 2048
+
+plus small variants (``small_*``) of the same dtypes and head counts that the
+oracle finishes in seconds while still spanning several tiles and ragged tails.
+
+Value recipe: q, kv_new, indexer queries, cache rows ~ N(0,1)*0.1; kv_score
+~ N(0,1); indexer weights ~ N(0,1)*0.1; RMSNorm weight 1 + N(0,1)*0.1; APE
+~ N(0,1)*0.1; sink ~ N(0,1); RoPE table theta = 10000.  Large bf16 buffers are
+drawn by inverse-CDF lookup: a uniform 16-bit integer indexes a table of the
+65536 normal quantiles rounded to bf16, which is N(0,1)*0.1 at bf16 resolution
+and costs one table gather per element.  Block tables are seeded random
+permutations of the physical pages (shuffled paging).
+"""
+from __future__ import annotations
+
+import dataclasses
+from dataclasses import dataclass, field
+
+import numpy as np
+
+D = 576          # latent width: 512 no-pe + 64 rope
+DV = 512         # value width: the first 512 latent dims
+D_ROPE = 64
+WINDOW = 128
+PAGE = 64
+FP8_DS_MLA_BYTES = 656   # 512 e4m3 | 64 bf16 rope (128 B) | 8 UE8M0 scale bytes | 8 pad
+FP8_SCALE_OFF = 640
+FP8_ROPE_OFF = 512
+
+# dtype tags, equal in value to the C enum dsv4_dtype
+F32, BF16, FP8_DS_MLA, I8_ROWSCALE = 0, 1, 2, 3
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_DS_MLA: "fp8_ds_mla", I8_ROWSCALE: "i8_rowscale"}
+
+
+@dataclass(frozen=True)
+class Config:
+    name: str
+    B: int
+    q_per_seq: int
+    ctx: tuple            # (lo, hi) inclusive range of total context length per seq, or explicit tuple of lengths
+    H: int
+    ratio: int            # 4 (CSA) or 128 (HCA); 0 = SWA only
+    I_h: int              # indexer heads (0 = no indexer / dense)
+    d_I: int
+    topk: int             # 0 = dense over every compressed entry
+    act_dtype: int        # q, kv_new, indexer q dtype (F32 or BF16)
+    cache_dtype: int      # SWA + main cache dtype (F32, BF16, FP8_DS_MLA)
+    idx_dtype: int        # indexer key cache dtype (F32, BF16, I8_ROWSCALE)
+    out_dtype: int        # attention output dtype
+    seed: int = 0xD5E4
+    explicit_lens: tuple = ()
+
+    @property
+    def T(self) -> int:
+        return self.B * self.q_per_seq
+
+    @property
+    def coff(self) -> int:
+        return 2 if self.ratio == 4 else 1
+
+
+CONFIGS = {
+    "tiny_c4_f32": Config("tiny_c4_f32", B=1, q_per_seq=1, ctx=(1024, 1024), H=16, ratio=4, I_h=4, d_I=64,
+                          topk=64, act_dtype=F32, cache_dtype=F32, idx_dtype=F32, out_dtype=F32, seed=0xD5E4 + 0),
+    "csa_c4_bf16": Config("csa_c4_bf16", B=32, q_per_seq=1, ctx=(65536, 65536), H=64, ratio=4, I_h=64, d_I=128,
+                          topk=512, act_dtype=BF16, cache_dtype=BF16, idx_dtype=BF16, out_dtype=BF16, seed=0xD5E4 + 1),
+    "hca_c128_bf16": Config("hca_c128_bf16", B=64, q_per_seq=1, ctx=(65536, 131072), H=64, ratio=128, I_h=0, d_I=0,
+                            topk=0, act_dtype=BF16, cache_dtype=BF16, idx_dtype=BF16, out_dtype=BF16, seed=0xD5E4 + 2),
+    "csa_c4_fp8": Config("csa_c4_fp8", B=128, q_per_seq=2, ctx=(8192, 32768), H=64, ratio=4, I_h=64, d_I=128,
+                         topk=512, act_dtype=BF16, cache_dtype=FP8_DS_MLA, idx_dtype=I8_ROWSCALE, out_dtype=BF16,
+                         seed=0xD5E4 + 3),
+    "csa_c4_1m": Config("csa_c4_1m", B=4, q_per_seq=1, ctx=(1048576, 1048576), H=128, ratio=4, I_h=64, d_I=128,
+                        topk=2048, act_dtype=BF16, cache_dtype=BF16, idx_dtype=BF16, out_dtype=BF16, seed=0xD5E4 + 4),
+}
+
+# Small variants: same dtypes and head counts, ragged lengths spanning several key tiles,
+# short-context cases (n_c <= top-k), contexts shorter than the window and an emitting fold.
+SMALL_CONFIGS = {
+    "small_c4_f32": dataclasses.replace(CONFIGS["tiny_c4_f32"], name="small_c4_f32", B=3,
+                                        explicit_lens=(1024, 333, 50)),
+    "small_c4_bf16": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_c4_bf16", B=4,
+                                         explicit_lens=(4100, 2048, 777, 9000)),
+    "small_c128_bf16": dataclasses.replace(CONFIGS["hca_c128_bf16"], name="small_c128_bf16", B=4,
+                                           explicit_lens=(20000, 8192, 1000, 131)),
+    "small_c4_fp8": dataclasses.replace(CONFIGS["csa_c4_fp8"], name="small_c4_fp8", B=3,
+                                        explicit_lens=(4100, 2048, 1023)),
+    "small_c4_h128": dataclasses.replace(CONFIGS["csa_c4_1m"], name="small_c4_h128", B=2,
+                                         explicit_lens=(20000, 9001)),
+    "small_swa_only": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_swa_only", B=2, ratio=0, I_h=0,
+                                          d_I=0, topk=0, explicit_lens=(300, 7)),
+    "edge_first_token": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="edge_first_token", B=2,
+                                            explicit_lens=(1, 4)),
+}
+
+ALL_CONFIGS = {**CONFIGS, **SMALL_CONFIGS}
+
+
+def n_pages(rows: int) -> int:
+    return (rows + PAGE - 1) // PAGE
+
+
+def row_elems(dtype: int, width: int) -> tuple:
+    """numpy dtype and trailing shape of one stored cache row of `width` logical elements."""
+    if dtype == F32:
+        return np.float32, (width,)
+    if dtype == BF16:
+        return np.uint16, (width,)
+    if dtype == FP8_DS_MLA:
+        assert width == D
+        return np.uint8, (FP8_DS_MLA_BYTES,)
+    if dtype == I8_ROWSCALE:
+        return np.uint8, (width + 4,)
+    raise ValueError(dtype)
+
+
+class _Draw:
+    """Seeded draws; every tensor gets its own stream keyed by (seed, name)."""
+
+    _bf16_table = None
+    _e4m3_table = None
+    _i8_table = None
+
+    def __init__(self, seed: int):
+        self.seed = seed
+
+    def rng(self, name: str) -> np.random.Generator:
+        key = [self.seed] + [ord(c) for c in name]
+        return np.random.default_rng(key)
+
+    @classmethod
+    def quantiles(cls) -> np.ndarray:
+        from scipy.special import ndtri
+        return ndtri((np.arange(65536, dtype=np.float64) + 0.5) / 65536.0)
+
+    @classmethod
+    def bf16_table(cls) -> np.ndarray:
+        if cls._bf16_table is None:
+            import torch
+            t = torch.from_numpy((cls.quantiles() * 0.1).astype(np.float32)).to(torch.bfloat16)
+            cls._bf16_table = t.view(torch.int16).numpy().view(np.uint16).copy()
+        return cls._bf16_table
+
+    @classmethod
+    def e4m3_table(cls) -> np.ndarray:
+        # N(0,1)*0.1 expressed in units of 2^-7 (the nominal block scale), as e4m3fn codes
+        if cls._e4m3_table is None:
+            import torch
+            v = np.clip(cls.quantiles() * 0.1 * 128.0, -448.0, 448.0).astype(np.float32)
+            cls._e4m3_table = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+        return cls._e4m3_table
+
+    @classmethod
+    def i8_table(cls) -> np.ndarray:
+        if cls._i8_table is None:
+            cls._i8_table = np.clip(np.rint(cls.quantiles() * 40.0), -127, 127).astype(np.int8)
+        return cls._i8_table
+
+    def normal_f32(self, name, shape, scale=1.0, loc=0.0):
+        return (self.rng(name).standard_normal(shape, dtype=np.float32) * np.float32(scale)
+                + np.float32(loc)).astype(np.float32)
+
+    def bf16(self, name, shape):
+        """bf16 bit patterns of N(0,1)*0.1 by inverse-CDF lookup."""
+        u = self.rng(name).integers(0, 65536, size=shape, dtype=np.uint16)
+        return self.bf16_table()[u]
+
+    def act(self, name, shape, dtype):
+        """Activation-like values N(0,1)*0.1 stored as fp32 or bf16 bits."""
+        if dtype == F32:
+            return self.normal_f32(name, shape, 0.1)
+        if dtype == BF16:
+            return self.bf16(name, shape)
+        raise ValueError(dtype)
+
+    def cache_rows(self, name, n_rows, width, dtype):
+        """`n_rows` stored rows of `width` logical elements in cache format `dtype`."""
+        if dtype in (F32, BF16):
+            return self.act(name, (n_rows, width), dtype)
+        rng = self.rng(name)
+        if dtype == FP8_DS_MLA:
+            rec = np.zeros((n_rows, FP8_DS_MLA_BYTES), np.uint8)
+            u = rng.integers(0, 65536, size=(n_rows, 512), dtype=np.uint16)
+            rec[:, :512] = self.e4m3_table()[u]
+            rope = self.bf16(name + ".rope", (n_rows, D_ROPE))
+            rec[:, FP8_ROPE_OFF:FP8_ROPE_OFF + 128] = rope.view(np.uint8).reshape(n_rows, 128)
+            # scale bytes around 2^-7 so decoded values are ~N(0,1)*0.1
+            rec[:, FP8_SCALE_OFF:FP8_SCALE_OFF + 8] = rng.integers(119, 122, size=(n_rows, 8), dtype=np.uint8)
+            return rec
+        if dtype == I8_ROWSCALE:
+            rec = np.zeros((n_rows, width + 4), np.uint8)
+            u = rng.integers(0, 65536, size=(n_rows, width), dtype=np.uint16)
+            rec[:, :width] = self.i8_table()[u].view(np.uint8)
+            scale = (0.1 / 40.0 * rng.uniform(0.75, 1.25, size=n_rows)).astype(np.float32)
+            rec[:, width:width + 4] = scale.view(np.uint8).reshape(n_rows, 4)
+            return rec
+        raise ValueError(dtype)
+
+
+@dataclass
+class StepInputs:
+    """Everything one decode step reads, in host memory, in the exact stored formats."""
+    cfg: Config
+    ctx_len: np.ndarray          # [B] int64, total length after this step's tokens
+    positions: np.ndarray        # [T] int32
+    kv_new: np.ndarray           # [T, D] f32 or bf16 bits
+    slot_mapping: np.ndarray     # [T] int64 SWA slot (page * PAGE + offset)
+    swa_cache: np.ndarray        # [swa_pages, PAGE, row]
+    swa_bt: np.ndarray           # [B, swa_max_pages] int32 (-1 = not resident)
+    q: np.ndarray                # [T, H, D]
+    sink: np.ndarray             # [H] f32
+    softmax_scale: float
+    kv_score: np.ndarray = None  # [T, 2*coff*D] f32
+    state: np.ndarray = None     # [B, coff*ratio, 2*coff*D] f32
+    ape: np.ndarray = None       # [ratio, coff*D] f32
+    norm_w: np.ndarray = None    # [D] f32
+    eps: float = 1e-6
+    cos_sin: np.ndarray = None   # [max_pos, 64] f32: 32 cos | 32 sin
+    main_cache: np.ndarray = None
+    main_bt: np.ndarray = None   # [B, main_max_pages] int32
+    idx_cache: np.ndarray = None
+    idx_bt: np.ndarray = None
+    q_idx: np.ndarray = None     # [T, I_h, d_I]
+    w_idx: np.ndarray = None     # [T, I_h] f32
+    given_topk: np.ndarray = None  # [T, topk] int32: a fixed valid selection for standalone attention cases
+    extra: dict = field(default_factory=dict)
+
+
+def context_lengths(cfg: Config) -> np.ndarray:
+    if cfg.explicit_lens:
+        assert len(cfg.explicit_lens) == cfg.B
+        return np.asarray(cfg.explicit_lens, np.int64)
+    lo, hi = cfg.ctx
+    if lo == hi:
+        return np.full(cfg.B, lo, np.int64)
+    return _Draw(cfg.seed).rng("ctx_len").integers(lo, hi + 1, size=cfg.B).astype(np.int64)
+
+
+def rope_table(max_pos: int, theta: float = 10000.0) -> np.ndarray:
+    """Rotary table [max_pos, 64]: cos of the 32 pair angles, then their sin (model constant)."""
+    inv = theta ** (-np.arange(0, D_ROPE, 2, dtype=np.float64) / D_ROPE)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def _paged_table(draw: _Draw, name: str, rows_per_seq: np.ndarray, first_row: np.ndarray, max_rows: int):
+    """Block table covering rows [first_row[b], rows_per_seq[b]) of each seq with shuffled physical pages.
+
+    Logical pages outside that range are -1.  Returns (table [B, max_pages], n_physical_pages)."""
+    B = len(rows_per_seq)
+    max_pages = max(1, n_pages(max_rows))
+    lp_lo = first_row // PAGE
+    lp_hi = np.array([n_pages(int(r)) for r in rows_per_seq], np.int64)
+    counts = np.maximum(lp_hi - lp_lo, 0)
+    total = int(counts.sum())
+    perm = draw.rng(name + ".perm").permutation(max(total, 1)).astype(np.int32)
+    bt = np.full((B, max_pages), -1, np.int32)
+    k = 0
+    for b in range(B):
+        c = int(counts[b])
+        bt[b, lp_lo[b]:lp_lo[b] + c] = perm[k:k + c]
+        k += c
+    return bt, max(total, 1)
+
+
+def make_step(cfg: Config, with_given_topk: bool = True) -> StepInputs:
+    draw = _Draw(cfg.seed)
+    B, qps, T, H = cfg.B, cfg.q_per_seq, cfg.T, cfg.H
+    L = context_lengths(cfg)
+    assert np.all(L >= qps)
+    positions = (L[:, None] - qps + np.arange(qps)[None, :]).reshape(T).astype(np.int32)
+    max_ctx = int(L.max())
+
+    # ---- SWA cache: only pages that hold the last WINDOW + q_per_seq positions are resident
+    swa_first = np.maximum(L - qps - WINDOW + 1, 0)
+    swa_bt, swa_pages = _paged_table(draw, "swa_bt", L, swa_first, max_ctx)
+    erow_t, erow_shape = row_elems(cfg.cache_dtype, D)
+    swa_cache = draw.cache_rows("swa_cache", swa_pages * PAGE, D, cfg.cache_dtype).reshape(
+        (swa_pages, PAGE) + erow_shape)
+    tok_b = np.repeat(np.arange(B), qps)
+    slot = swa_bt[tok_b, positions // PAGE].astype(np.int64) * PAGE + positions % PAGE
+
+    kv_new = draw.act("kv_new", (T, D), cfg.act_dtype)
+    q = draw.act("q", (T, H, D), cfg.act_dtype)
+    sink = draw.normal_f32("sink", (H,), 1.0)
+    st = StepInputs(cfg=cfg, ctx_len=L, positions=positions, kv_new=kv_new, slot_mapping=slot,
+                    swa_cache=swa_cache, swa_bt=swa_bt, q=q, sink=sink, softmax_scale=float(D) ** -0.5)
+    if cfg.ratio == 0:
+        return st
+
+    r, coff = cfg.ratio, cfg.coff
+    # ---- compressor inputs and fp32 state ring (coff*r slots per seq)
+    st.kv_score = draw.normal_f32("kv_score", (T, 2 * coff * D), 1.0)
+    st.state = draw.normal_f32("state", (B, coff * r, 2 * coff * D), 1.0)
+    st.ape = draw.normal_f32("ape", (r, coff * D), 0.1)
+    st.norm_w = draw.normal_f32("norm_w", (D,), 0.1, 1.0)
+    st.cos_sin = rope_table(max_ctx + 1)
+
+    # ---- main (compressed) cache: rows j < floor(L/r) exist after the step
+    nc_after = L // r
+    main_bt, main_pages = _paged_table(draw, "main_bt", nc_after, np.zeros(B, np.int64), int(nc_after.max()))
+    st.main_bt = main_bt
+    st.main_cache = draw.cache_rows("main_cache", main_pages * PAGE, D, cfg.cache_dtype).reshape(
+        (main_pages, PAGE) + erow_shape)
+
+    if cfg.I_h > 0:
+        idx_bt, idx_pages = _paged_table(draw, "idx_bt", nc_after, np.zeros(B, np.int64), int(nc_after.max()))
+        ir_t, ir_shape = row_elems(cfg.idx_dtype, cfg.d_I)
+        st.idx_bt = idx_bt
+        st.idx_cache = draw.cache_rows("idx_cache", idx_pages * PAGE, cfg.d_I, cfg.idx_dtype).reshape(
+            (idx_pages, PAGE) + ir_shape)
+        st.q_idx = draw.act("q_idx", (T, cfg.I_h, cfg.d_I), cfg.act_dtype)
+        st.w_idx = draw.normal_f32("w_idx", (T, cfg.I_h), 0.1)
+
+    if cfg.topk > 0 and with_given_topk:
+        # an arbitrary valid selection (distinct visible indices, ascending, -1 padded) for attention-only cases
+        g = np.full((T, cfg.topk), -1, np.int32)
+        rng = draw.rng("given_topk")
+        for t in range(T):
+            nc = int((int(positions[t]) + 1) // r)
+            m = min(nc, cfg.topk)
+            if m:
+                sel = rng.choice(nc, size=m, replace=False) if nc > m else np.arange(nc)
+                g[t, :m] = np.sort(sel)
+        st.given_topk = g
+    return st
+
+
+def max_compressed(cfg: Config) -> int:
+    L = context_lengths(cfg)
+    return int(L.max() // cfg.ratio) if cfg.ratio else 0
