@@ -1,0 +1,406 @@
+"""Decode-step benchmark of the DeepSeek-V4 hybrid compressed-attention hot path on GB300.
+
+One step = SWA insert + compressor update + Lightning-Indexer scoring/top-k + sparse MLA
+attention (+ split merge) over one batch of synthetic decode tokens, inputs resident in HBM.
+Default workload: CSA c4 bf16, batch 32, context 65536 (16384 compressed entries per sequence),
+64 query heads, indexer 64 x 128, top-k 512.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Multi-GPU: each rank runs its own batch (sequences are independent; no collective on the data
+path), so per-GPU work is fixed and `value` is the total tokens of all ranks / the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA/HCA decode tokens/s per GB300 and achieved HBM TB/s vs roofline"
+DEFAULT_CONFIG = "csa_c4_bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic bytes (what the method must move, counted from the index sets actually used)
+# ------------------------------------------------------------------------------------------------
+
+def row_bytes(dtype, width):
+    return {0: 4 * width, 1: 2 * width, 2: 656, 3: width + 4}[dtype]
+
+
+def algorithmic_bytes(st, topk_idx=None):
+    """Per-call algorithmic HBM bytes of one step: each row the method reads or writes, once."""
+    import dsv4_inputs as I
+    cfg = st.cfg
+    T, H = cfg.T, cfg.H
+    act = 4 if cfg.act_dtype == I.F32 else 2
+    rb = row_bytes(cfg.cache_dtype, 576)
+    pos = st.positions.astype(np.int64)
+    qps = cfg.q_per_seq
+    b = {}
+    b["insert"] = T * 576 * act + T * 8 + T * rb
+    if cfg.ratio:
+        coff = cfg.coff
+        sw = 2 * coff * 576 * 4
+        emit = [(int(p) + 1) % cfg.ratio == 0 for p in pos]
+        fold_rows = cfg.ratio * coff
+        b["compress"] = T * sw * 2 + sum(emit) * (fold_rows * sw // 1 + rb)
+    if cfg.ratio and cfg.topk:
+        ib = row_bytes(cfg.idx_dtype, cfg.d_I)
+        nc_seq = (pos.reshape(cfg.B, qps)[:, -1] + 1) // cfg.ratio
+        keys = int(nc_seq.sum()) * ib
+        b["indexer"] = keys + T * cfg.I_h * cfg.d_I * act + T * cfg.I_h * 4 + T * cfg.topk * 8
+    # attention: q + out + SWA rows + compressed rows (union of the sequence's selections)
+    rows = 0
+    for s in range(cfg.B):
+        p_last = int(pos[s * qps + qps - 1])
+        p_first = int(pos[s * qps])
+        rows += min(p_last + 1, 128) + (p_last - p_first)  # window rows of all the seq's queries
+        if cfg.ratio:
+            if cfg.topk:
+                sel = set()
+                for t in range(s * qps, s * qps + qps):
+                    row = topk_idx[t]
+                    sel |= set(row[row >= 0].tolist())
+                rows += len(sel)
+            else:
+                rows += (p_last + 1) // cfg.ratio
+    out_b = 4 if cfg.out_dtype == I.F32 else 2
+    b["attention"] = rows * rb + T * H * 576 * act + T * H * 512 * out_b + T * H * 4
+    return b
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, pw = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": float(max(pw))}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle leg
+# ------------------------------------------------------------------------------------------------
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        return int(n)
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+def oracle_throughput(st, seconds):
+    """Times the oracle step on as many whole sequences as fit in ~`seconds` of CPU work."""
+    from oracle import dsv4_oracle as O
+    cfg = st.cfg
+    done, t0 = 0, time.perf_counter()
+    b = 0
+    while True:
+        O.decode_step(st, seqs=[b])
+        done += 1
+        b = (b + 1) % cfg.B
+        el = time.perf_counter() - t0
+        if el >= seconds or done >= 4 * cfg.B:
+            break
+    tokens = done * cfg.q_per_seq
+    return tokens / el, f"{done} of {cfg.B} sequences ({tokens} tokens), {el:.1f} s of the full step per sequence"
+
+
+# ------------------------------------------------------------------------------------------------
+
+def flush_buffer(torch):
+    return torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "deepseek_v4_hybrid_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(config, kernel_file, units):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[config]
+        if e.get("source_hash") != kernel_source_hash([kernel_file, "dsv4_common.cuh"]):
+            return None
+        return float(e["dram_bytes_per_unit"]) * units
+    except Exception:
+        return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import dsv4_inputs as I
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from deepseek_v4_hybrid_gb300.step import DeviceStep
+    cfg = I.ALL_CONFIGS[args.config]
+    cfg = dataclasses.replace(cfg, seed=cfg.seed + 1000 * rank)
+    st = I.make_step(cfg)
+    ds = DeviceStep(st)
+    stream = torch.cuda.current_stream()
+    flush = flush_buffer(torch)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        ds.run()
+    torch.cuda.synchronize()
+    topk_host = ds.topk_idx.cpu().numpy() if ds.has_indexer else None
+    alg = algorithmic_bytes(st, topk_host)
+
+    calls = ["insert", "compress", "indexer", "attention"]
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush.fill_(float(k))
+        e = ev[k]
+        e[0].record(stream)
+        ds.insert()
+        e[1].record(stream)
+        ds.compress()
+        e[2].record(stream)
+        ds.indexer()
+        e[3].record(stream)
+        ds.attention()
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    per_call = {c: 0.0 for c in calls}
+    total_ms = 0.0
+    for e in ev:
+        total_ms += e[0].elapsed_time(e[4])
+        for i, c in enumerate(calls):
+            per_call[c] += e[i].elapsed_time(e[i + 1])
+    ms_per_step = total_ms / K
+    if world > 1:
+        tt = torch.tensor([ms_per_step], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_per_step = float(tt.item())
+    tokens = cfg.T * world
+    value = tokens / (ms_per_step * 1e-3)
+    per_call_us = {c: 1e3 * v / K for c, v in per_call.items()}
+
+    # ---- end to end through host buffers: pinned H2D of the step's inputs, step, D2H of results
+    host_in = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in ds.step_input_tensors().items()}
+    for k, v in ds.step_input_tensors().items():
+        host_in[k].copy_(v)
+    host_out = torch.empty_like(ds.out, device="cpu").pin_memory()
+    host_topk = torch.empty_like(ds.topk_idx, device="cpu").pin_memory() if ds.has_indexer else None
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + (host_topk.numel() * 4 if host_topk is not None else 0)
+    Ke = max(20, min(K, 400))
+    e2e_ms = 0.0
+    for k in range(Ke):
+        flush.fill_(float(k))
+        a, bnd = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for name, dev in ds.step_input_tensors().items():
+            dev.copy_(host_in[name], non_blocking=True)
+        ds.run()
+        host_out.copy_(ds.out, non_blocking=True)
+        if host_topk is not None:
+            host_topk.copy_(ds.topk_idx, non_blocking=True)
+        bnd.record(stream)
+        bnd.synchronize()
+        e2e_ms += a.elapsed_time(bnd)
+    e2e_ms /= Ke
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    # ---- roofline of the dominant call
+    dom = max((c for c in calls if c in alg), key=lambda c: per_call_us[c])
+    peak, peak_kind = peaks()
+    achieved = alg[dom] / (per_call_us[dom] * 1e-6) / 1e9
+    dom_file = {"indexer": "indexer_topk.cu", "attention": "attention.cu", "compress": "insert_compress.cu",
+                "insert": "insert_compress.cu"}[dom]
+    units = cfg.T
+    traffic = traffic_from_profiles(args.config, dom_file, units)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {0: "f32", 1: "bf16"}[cfg.act_dtype] + "/" + I.DTYPE_NAMES[cfg.cache_dtype],
+        "data": "synthetic (seeded N(0,1)*0.1 rows, shuffled paged block tables)",
+        "config": {"workload": cfg.name, "batch_per_gpu": cfg.B, "q_per_seq": cfg.q_per_seq,
+                   "context": list(map(int, (st.ctx_len.min(), st.ctx_len.max()))), "heads": cfg.H,
+                   "ratio": cfg.ratio, "indexer": [cfg.I_h, cfg.d_I], "topk": cfg.topk, "page": 64,
+                   "l2": "flushed between steps (512 MB write)", "parallelism": f"replicas x{world} (per-sequence)"},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+        "gpu_launches": int(K * launches_per_step(ds)),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes": int(alg[dom]), "us_per_launch": per_call_us[dom]},
+        "calls_us": per_call_us,
+        "step_algorithmic_gbs": sum(alg.values()) / (ms_per_step * 1e-3) / 1e9,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample = oracle_throughput(st, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def launches_per_step(ds):
+    n = 1 + 2  # insert, attention partial + merge
+    if ds.has_compress:
+        n += 1
+    if ds.has_indexer:
+        n += 2
+    return n
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm, timed on this host's cores on a bounded sample."""
+    import dsv4_inputs as I
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = I.ALL_CONFIGS[args.config]
+    st = I.make_step(cfg)
+    from oracle import dsv4_oracle as O
+    # one reference step = the oracle's whole decode step for one sequence; the run stops after K
+    # steps or ~150 s of CPU time, whichever comes first, and reports the steps it ran
+    for _ in range(min(args.warmup, 1)):
+        O.decode_step(st, seqs=[0])
+    tokens, el, b = 0, 0.0, 0
+    K = 0
+    while K < max(1, args.steps) and el < 150.0:
+        t0 = time.perf_counter()
+        O.decode_step(st, seqs=[b % cfg.B])
+        el += time.perf_counter() - t0
+        tokens += cfg.q_per_seq
+        b += 1
+        K += 1
+    v = tokens / el
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64 (oracle)", "data": "synthetic", "impl": "reference",
+            "config": {"workload": cfg.name, "batch_per_gpu": cfg.B},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{b} sequence steps over {el:.1f} s"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,121 @@
+"""Device-resident decode step: owns the device tensors of one workload and issues the four
+library calls (insert -> compress -> indexer/top-k -> attention) on one stream.
+
+Memory comes from torch; every computation is a libdsv4 kernel.  The per-call parameter structs
+are built once, so a step is four C calls with no host synchronisation (graph-capturable).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (BF16, F32, dsv4_compress_update, dsv4_indexer_topk, dsv4_indexer_topk_workspace_bytes,
+               dsv4_kv_insert, dsv4_sparse_mla_decode, dsv4_sparse_mla_decode_workspace_bytes, indexer_topk_params,
+               sparse_mla_params, _abi)
+
+PAGE = 64
+WINDOW = 128
+
+
+def to_device(a, device):
+    """numpy array -> device tensor with the same bytes (uint16 bf16 bits become torch.bfloat16)."""
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def _ws(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+class DeviceStep:
+    # per-step inputs (copied host -> device every step in the end-to-end measurement)
+    STEP_INPUTS = ("q", "kv_new", "slot_mapping", "positions", "kv_score", "q_idx", "w_idx")
+
+    def __init__(self, st, device="cuda", topk_override=None):
+        cfg = st.cfg
+        self.cfg, self.device = cfg, device
+        dev = lambda a: to_device(a, device)  # noqa: E731
+        self.positions = dev(st.positions.astype(np.int32))
+        self.kv_new = dev(st.kv_new)
+        self.slot_mapping = dev(st.slot_mapping.astype(np.int64))
+        self.swa_cache = dev(st.swa_cache)
+        self.swa_bt = dev(st.swa_bt)
+        self.q = dev(st.q)
+        self.sink = dev(st.sink)
+        self.max_context = int(st.ctx_len.max())
+        T, H = cfg.T, cfg.H
+        odt = torch.float32 if cfg.out_dtype == F32 else torch.bfloat16
+        self.out = torch.empty((T, H, 512), dtype=odt, device=device)
+        self.lse = torch.empty((T, H), dtype=torch.float32, device=device)
+        self.has_compress = cfg.ratio > 0
+        self.has_indexer = cfg.ratio > 0 and cfg.topk > 0
+        self.kv_score = self.state = self.ape = self.norm_w = self.cos_sin = None
+        self.main_cache = self.main_bt = None
+        self.q_idx = self.w_idx = None
+        if self.has_compress:
+            self.kv_score = dev(st.kv_score)
+            self.state = dev(st.state)
+            self.ape = dev(st.ape)
+            self.norm_w = dev(st.norm_w)
+            self.cos_sin = dev(st.cos_sin)
+            self.main_cache = dev(st.main_cache)
+            self.main_bt = dev(st.main_bt)
+        self.topk_idx = None
+        if self.has_indexer:
+            self.idx_cache = dev(st.idx_cache)
+            self.idx_bt = dev(st.idx_bt)
+            self.q_idx = dev(st.q_idx)
+            self.w_idx = dev(st.w_idx)
+            self.topk_idx = torch.empty((T, cfg.topk), dtype=torch.int32, device=device)
+            self.topk_score = torch.empty((T, cfg.topk), dtype=torch.float32, device=device)
+            self.ix_params = indexer_topk_params(self.q_idx, cfg.act_dtype, self.w_idx, self.idx_cache,
+                                                 cfg.idx_dtype, self.idx_bt, self.positions, cfg.q_per_seq,
+                                                 cfg.ratio, cfg.topk, PAGE, self.max_context, self.topk_idx,
+                                                 self.topk_score)
+            self.ix_ws = _ws(dsv4_indexer_topk_workspace_bytes(self.ix_params), device)
+            self.ix_params.workspace = self.ix_ws.data_ptr()
+            self.ix_params.workspace_bytes = self.ix_ws.numel()
+        attn_topk = self.topk_idx
+        if topk_override is not None:
+            self.given_topk = dev(topk_override.astype(np.int32))
+            attn_topk = self.given_topk
+        self.at_params = sparse_mla_params(self.q, cfg.act_dtype, self.positions, cfg.q_per_seq, self.swa_cache,
+                                           self.swa_bt, self.main_cache, self.main_bt, cfg.cache_dtype, PAGE,
+                                           cfg.ratio, WINDOW, attn_topk if cfg.topk > 0 else None, self.sink,
+                                           st.softmax_scale, self.out, cfg.out_dtype, self.lse, self.max_context)
+        self.at_ws = _ws(dsv4_sparse_mla_decode_workspace_bytes(self.at_params), device)
+        self.at_params.workspace = self.at_ws.data_ptr()
+        self.at_params.workspace_bytes = self.at_ws.numel()
+        self.eps = st.eps
+
+    def insert(self, stream=None):
+        dsv4_kv_insert(self.kv_new, self.cfg.act_dtype, self.slot_mapping, self.swa_cache, self.cfg.cache_dtype,
+                       PAGE, stream=stream)
+
+    def compress(self, stream=None):
+        if self.has_compress:
+            cfg = self.cfg
+            dsv4_compress_update(self.kv_score, self.positions, cfg.q_per_seq, cfg.ratio, cfg.coff, self.state,
+                                 self.ape, self.norm_w, self.eps, self.cos_sin, self.main_cache, cfg.cache_dtype,
+                                 self.main_bt, PAGE, stream=stream)
+
+    def indexer(self, stream=None):
+        if self.has_indexer:
+            dsv4_indexer_topk(self.ix_params, stream=stream)
+
+    def attention(self, stream=None):
+        dsv4_sparse_mla_decode(self.at_params, stream=stream)
+
+    def run(self, stream=None):
+        """One decode step: insert -> compress -> indexer + top-k -> attention."""
+        self.insert(stream)
+        self.compress(stream)
+        self.indexer(stream)
+        self.attention(stream)
+
+    def step_input_tensors(self):
+        return {k: getattr(self, k) for k in self.STEP_INPUTS if getattr(self, k, None) is not None}

@@ -1,0 +1,111 @@
+"""Comparison of a device decode step's results with the oracle's (test infrastructure only).
+
+Tolerances: integer work (slots, state rows, top-k sets) must match exactly, except top-k
+entries whose oracle score lies within 1e-5 of the k-th best (near-ties may rank either way).
+Attention outputs: max |gpu - oracle| <= 2e-2 * max |oracle| per token for bf16/fp8 caches and
+<= 1e-4 * max |oracle| for fp32.  Compressed entries written by the fold: within one unit in the
+last place of their storage format (plus 1e-5 of the row max for the fp32 arithmetic).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import dsv4_oracle as O
+
+TIE_EPS = 1e-5
+
+
+def attention_tolerance(cache_dtype: int) -> float:
+    return 1e-4 if cache_dtype == O.F32 else 2e-2
+
+
+def _e4m3_ulp(v):
+    v = np.abs(v)
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** -6)))
+    return np.exp2(e - 3)
+
+
+def entry_error_ok(stored_gpu, value, dtype):
+    """Is a stored compressed entry within one storage ulp of the oracle's (unencoded) value?"""
+    dec = O.decode_rows(stored_gpu, dtype)
+    value = np.asarray(value, np.float64)
+    amax = np.max(np.abs(value))
+    if dtype == O.F32:
+        return np.max(np.abs(dec - value)) <= 1e-5 * amax, dec
+    if dtype == O.BF16:
+        bound = np.abs(value) * 2.0 ** -7 + 1e-5 * amax
+        return bool(np.all(np.abs(dec - value) <= bound)), dec
+    # fp8_ds_mla: per 64-dim block, one e4m3 ulp at the block's scale; rope dims as bf16
+    ok = True
+    for blk in range(8):
+        seg = slice(64 * blk, 64 * blk + 64)
+        eb = O.ue8m0_exponent(np.max(np.abs(value[seg])))
+        bound = _e4m3_ulp(value[seg] / 2.0 ** eb) * 2.0 ** eb + 1e-5 * amax
+        ok &= bool(np.all(np.abs(dec[seg] - value[seg]) <= bound))
+    ok &= bool(np.all(np.abs(dec[512:] - value[512:]) <= np.abs(value[512:]) * 2.0 ** -7 + 1e-5 * amax))
+    return ok, dec
+
+
+def topk_sets_match(gpu_idx, oracle_scores, k):
+    """GPU list vs the oracle's scores: same set except near-ties at the k-th score; returns
+    (ok, exact) where exact says the two sets are identical."""
+    s = np.asarray(oracle_scores, np.float32)
+    n = s.shape[0]
+    g = np.asarray(gpu_idx)
+    m = min(n, k)
+    valid = g[g >= 0]
+    if len(valid) != m or np.any(g[m:] != -1) or len(set(valid.tolist())) != m or np.any(valid >= n):
+        return False, False
+    want = set(O.topk_select(s, k)[:m].tolist())
+    got = set(valid.tolist())
+    if got == want:
+        return True, True
+    if m == 0:
+        return True, True
+    kth = np.sort(s)[::-1][m - 1]
+    diff = got ^ want
+    return bool(all(abs(float(s[j]) - float(kth)) <= TIE_EPS for j in diff)), False
+
+
+def check_step(st, res, gpu, where=""):
+    """Asserts parity of every device result in `gpu` (numpy arrays) with the oracle's `res`.
+    Returns a small report dict."""
+    cfg = st.cfg
+    rep = {"tokens": len(res["tokens"]), "max_rel_err": 0.0, "tie_tokens": 0}
+    # a1: inserted SWA rows, bit-exact
+    for (page, off), row in res["swa_written"].items():
+        assert np.array_equal(gpu["swa_cache"][page, off], row), f"{where} SWA row {(page, off)}"
+    if cfg.ratio:
+        # a2: fp32 state ring, bit-exact; emitted entries within one storage ulp
+        for b, stb in res["state"].items():
+            assert np.array_equal(gpu["state"][b], stb), f"{where} state of seq {b}"
+        for (b, j), e in res["entries"].items():
+            page = st.main_bt[b][j // O.PAGE]
+            ok, _ = entry_error_ok(gpu["main_cache"][page, j % O.PAGE], e, cfg.cache_dtype)
+            assert ok, f"{where} compressed entry {(b, j)}"
+    same_sel = {}
+    if cfg.ratio and cfg.topk:
+        for t in res["tokens"]:
+            ok, exact = topk_sets_match(gpu["topk_idx"][t], res["scores"][t], cfg.topk)
+            assert ok, f"{where} top-k of token {t}"
+            same_sel[t] = exact
+            rep["tie_tokens"] += int(not exact)
+            if "topk_score" in gpu and exact:
+                sel = gpu["topk_idx"][t]
+                sv = gpu["topk_score"][t][sel >= 0]
+                ref = res["scores"][t][sel[sel >= 0]]
+                scale = max(1e-30, float(np.max(np.abs(res["scores"][t]))) if len(res["scores"][t]) else 1.0)
+                assert np.all(np.abs(sv - ref) <= 1e-5 * scale + 1e-7), f"{where} top-k scores of token {t}"
+    tol = attention_tolerance(cfg.cache_dtype)
+    for t in res["tokens"]:
+        if same_sel.get(t, True) is False:
+            continue  # a near-tie changed the selected rows: attention is checked on given selections
+        ref, out = res["out"][t], gpu["out"][t].astype(np.float64)
+        amax = float(np.max(np.abs(ref)))
+        err = float(np.max(np.abs(out - ref)))
+        rep["max_rel_err"] = max(rep["max_rel_err"], err / amax)
+        assert err <= tol * amax, f"{where} attention of token {t}: err {err:.3e} vs {tol} * {amax:.3e}"
+        if "lse" in gpu:
+            lerr = float(np.max(np.abs(gpu["lse"][t] - res["lse"][t])))
+            assert lerr <= (1e-5 if cfg.cache_dtype == O.F32 else 2e-3), f"{where} lse of token {t}: {lerr:.3e}"
+    return rep
