@@ -13,9 +13,11 @@ HEADER = os.path.join(ROOT, "include", "dsv4.h")
 
 @pytest.fixture(scope="module")
 def abi():
-    from deepseek_v4_hybrid_gb300 import _abi, build
-    if not os.path.exists(_abi.LIB_PATH):
-        build.build()
+    import __graft_entry__
+    lib_path = os.path.join(ROOT, "deepseek_v4_hybrid_gb300", "_lib", "libdsv4.so")
+    if not os.path.exists(lib_path):
+        __graft_entry__._build_module().build()
+    from deepseek_v4_hybrid_gb300 import _abi
     _abi.load()
     return _abi
 
