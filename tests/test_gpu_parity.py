@@ -95,6 +95,9 @@ def test_bad_block_table_is_flagged_not_faulting(lib):
     import deepseek_v4_hybrid_gb300 as M
     st = I.make_step(I.SMALL_CONFIGS["small_c4_bf16"])
     ds = DeviceStep(st)
+    ds.run()
+    torch.cuda.synchronize()
+    assert M.dsv4_read_device_flags() == 0
     bad = ds.main_bt.clone()
     bad[0, 0] = ds.main_cache.shape[0] + 5
     ds.at_params.main_block_table = bad.data_ptr()
