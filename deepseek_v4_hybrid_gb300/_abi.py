@@ -52,7 +52,10 @@ class SparseMlaDecodeParams(C.Structure):
 
 EXPORTS = ["dsv4_kv_insert", "dsv4_compress_update", "dsv4_indexer_topk_workspace_bytes", "dsv4_indexer_topk",
            "dsv4_sparse_mla_decode_workspace_bytes", "dsv4_sparse_mla_decode", "dsv4_abi_version",
-           "dsv4_status_string", "dsv4_last_cuda_error", "dsv4_read_device_flags"]
+           "dsv4_status_string", "dsv4_last_cuda_error", "dsv4_read_device_flags", "dsv4_indexer_topk_noalloc"]
+
+# bytes of the scratch array built into the library for dsv4_indexer_topk_noalloc
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 _lib = None
 
@@ -67,7 +70,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                            "python -m deepseek_v4_hybrid_gb300.build")
     lib = C.CDLL(path)
     for name, st in (("dsv4_kv_insert", KvInsertParams), ("dsv4_compress_update", CompressUpdateParams),
-                     ("dsv4_indexer_topk", IndexerTopkParams), ("dsv4_sparse_mla_decode", SparseMlaDecodeParams)):
+                     ("dsv4_indexer_topk", IndexerTopkParams), ("dsv4_sparse_mla_decode", SparseMlaDecodeParams),
+                     ("dsv4_indexer_topk_noalloc", IndexerTopkParams)):
         fn = getattr(lib, name)
         fn.argtypes = [C.POINTER(st), vp]
         fn.restype = C.c_int

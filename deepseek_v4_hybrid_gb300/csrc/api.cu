@@ -30,6 +30,8 @@ bool act_dtype(int d) { return d == DSV4_F32 || d == DSV4_BF16; }
 
 }  // namespace
 
+void dsv4::record_cuda_error(int e) { g_last_cuda_error = e; }
+
 extern "C" {
 
 int dsv4_abi_version(void) { return DSV4_ABI_VERSION; }

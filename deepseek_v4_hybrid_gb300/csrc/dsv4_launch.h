@@ -22,6 +22,9 @@ cudaError_t read_flags_insert_compress(uint32_t* f);
 cudaError_t read_flags_indexer(uint32_t* f);
 cudaError_t read_flags_attention(uint32_t* f);
 
+// Makes `e` the value dsv4_last_cuda_error() reports on this thread.
+void record_cuda_error(int e);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace dsv4

@@ -163,6 +163,24 @@ size_t dsv4_indexer_topk_workspace_bytes(const dsv4_indexer_topk_params* p);
 int dsv4_indexer_topk(const dsv4_indexer_topk_params* p, dsv4_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * dsv4_indexer_topk_noalloc: dsv4_indexer_topk for callers that cannot allocate device memory
+ * (no cudaMalloc and no caching allocator: e.g. code embedded in a host runtime that owns all
+ * device memory, or a plugin that may only touch the buffers it is handed).  The source pages
+ * have no counterpart to this call; it exists for deployment only.
+ * Same arguments, computation and outputs as dsv4_indexer_topk, except that `workspace` and
+ * `workspace_bytes` are ignored: the scratch is a device array of DSV4_NOALLOC_SCRATCH_BYTES
+ * built into the library, which every GPU that loads the library holds until the process exits.
+ * The call allocates nothing.  Problems whose dsv4_indexer_topk_workspace_bytes() exceeds
+ * DSV4_NOALLOC_SCRATCH_BYTES are rejected with DSV4_ERR_INVALID before any launch.
+ * The first call on a device (made with that device current) looks up the array's device address
+ * once; make that first call outside any CUDA stream capture.  Every call on a device shares the
+ * one array and leaves its contents behind, so calls whose kernels overlap on the GPU (different
+ * streams, or graph replays that run concurrently) race on it: order them on one stream.
+ * ------------------------------------------------------------------------------------------- */
+#define DSV4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int dsv4_indexer_topk_noalloc(const dsv4_indexer_topk_params* p, dsv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * dsv4_sparse_mla_decode: shared-KV sparse MLA attention (MAP "Phase 3: forward_mqa()" items
  * 1-6 and "Layer-Type Summary"; API DeepseekV4Attention: sink init -inf = no effect).
  * For query token t at position p and head h, over the rows R = the window rows of the SWA
