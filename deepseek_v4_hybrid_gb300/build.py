@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libdsv4.so")
-SOURCES = ["api.cu", "insert_compress.cu", "indexer_topk.cu", "attention.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "insert_compress.cu", "indexer_topk.cu", "attention.cu", "noalloc.cu", "tmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"]

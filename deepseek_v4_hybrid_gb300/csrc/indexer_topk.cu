@@ -12,6 +12,8 @@
 // order-preserving uint32 keys and compacts the selection in increasing j.
 #include "dsv4_common.cuh"
 #include "dsv4_launch.h"
+#include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace dsv4 {
 
@@ -117,6 +119,307 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
     }
     if (j < nc) scores[(int64_t)t * nc_stride + j] = s;
   }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Tensor-core score kernel (bf16 keys and queries): D[128 keys x N] = K_tile[128 x d] * Q[N x d]^T
+// with N = q_per_seq * n_heads (every query head of the sequence), then per key
+// s_k = sum_h w[k][h] * ReLU(D[key][k*n_heads + h]).
+//
+// Persistent CTAs (one per SM), each owning a contiguous range of (sequence, 128-key tile) items.
+// Warp 4 streams key tiles with TMA (two 64-row pages x two 64-dim K-blocks, 128-byte swizzle)
+// into a ring of stages and the sequence's Q block into its own buffer; one thread of warp 5 issues
+// the tcgen05 MMAs (M = 128, K = 16 steps) into one of two TMEM accumulators; warps 0-3 read
+// their 32 TMEM lanes each (one key per thread), apply ReLU and the head weights and store the
+// scores.  Every wait is bounded; a timeout raises FLAG_TIMEOUT and all roles drain out.
+// ------------------------------------------------------------------------------------------------
+namespace ixtc {
+constexpr int TILE = 128;
+constexpr int KB_BYTES = TILE * 128;         // one 64-dim K-block of a key tile (128 rows x 128 B)
+constexpr int STAGE_BYTES = 2 * KB_BYTES;    // d <= 128
+constexpr int THREADS = 192;
+constexpr uint32_t FLAG_TIMEOUT = 4u;
+
+struct Args {
+  const int32_t* positions;
+  const int32_t* block_table;
+  const float* weights;
+  float* scores;
+  int64_t num_pages;
+  int T, B, qps, Ih, d, ratio, max_pages, nc_stride, tiles_max, max_context;
+  int N, kblk, stages, tmem_cols;
+};
+
+struct Smem {
+  uint64_t full[8], empty[8], dfull[2], dempty[2], qfull, qempty, done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ int seq_entries(const Args& a, int b) {
+  const int pos = a.positions[b * a.qps + a.qps - 1];
+  if (pos < 0 || pos >= a.max_context) return pos < 0 ? 0 : a.max_context / a.ratio;
+  return (pos + 1) / a.ratio;
+}
+
+__device__ __forceinline__ int tok_entries(const Args& a, int t) {
+  const int pos = a.positions[t];
+  if (pos < 0 || pos >= a.max_context) return pos < 0 ? 0 : a.max_context / a.ratio;
+  return (pos + 1) / a.ratio;
+}
+
+__device__ __forceinline__ int page_of(const Args& a, int b, int lp) {
+  if (lp >= a.max_pages) return -1;
+  const int pg = a.block_table[(int64_t)b * a.max_pages + lp];
+  if (pg < 0 || pg >= a.num_pages) {
+    atomicOr(&g_flags_ix, FLAG_PAGE);
+    return -1;
+  }
+  return pg;
+}
+
+// next valid item at or after `it` in [it, hi), or hi
+__device__ __forceinline__ int next_item(const Args& a, int it, int hi, int& b, int& tile) {
+  for (; it < hi; ++it) {
+    b = it / a.tiles_max;
+    tile = it % a.tiles_max;
+    if (tile * TILE < seq_entries(a, b)) return it;
+  }
+  return hi;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    indexer_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, Args a) {
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_mem = base;                                      // stages x STAGE_BYTES
+  uint8_t* q_mem = base + a.stages * STAGE_BYTES;                 // kblk x N x 128 B
+  float* w_s = reinterpret_cast<float*>(q_mem + a.kblk * a.N * 128);  // N floats
+  Smem* sm = reinterpret_cast<Smem*>(w_s + 256);
+  volatile int* abort = &sm->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = a.B * a.tiles_max;
+  const int lo = (int)((int64_t)blockIdx.x * total / gridDim.x);
+  const int hi = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      tc::mbar_init(&sm->full[s], 1);
+      tc::mbar_init(&sm->empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sm->dfull[i], 1);
+      tc::mbar_init(&sm->dempty[i], 4);
+    }
+    tc::mbar_init(&sm->qfull, 1);
+    tc::mbar_init(&sm->qempty, 1);
+    tc::mbar_init(&sm->done, 1);
+    sm->abort = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 5) {
+    tc::tmem_alloc(&sm->tmem_base, a.tmem_cols);
+    tc::tmem_relinquish();
+    tc::tc_fence_before();
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      tc::tma_prefetch_desc(&kmap);
+      tc::tma_prefetch_desc(&qmap);
+      int stage = 0, cur_b = -1;
+      uint32_t phase = 0, qphase = 0;
+      int b, tile;
+      for (int it = next_item(a, lo, hi, b, tile); it < hi; it = next_item(a, it + 1, hi, b, tile)) {
+        if (b != cur_b) {
+          if (cur_b >= 0) {
+            if (!tc::mbar_wait_bounded(&sm->qempty, qphase, abort)) break;
+            qphase ^= 1;
+          }
+          tc::mbar_arrive_expect_tx(&sm->qfull, a.kblk * a.N * 128);
+          for (int kb = 0; kb < a.kblk; ++kb)
+            tc::tma_load_2d(q_mem + kb * a.N * 128, &qmap, kb * 64, b * a.qps * a.Ih, &sm->qfull);
+          cur_b = b;
+        }
+        if (!tc::mbar_wait_bounded(&sm->empty[stage], phase ^ 1, abort)) break;
+        const int nc = seq_entries(a, b);
+        const int j0 = tile * TILE;
+        const int pg0 = page_of(a, b, j0 / 64);
+        const int pg1 = (j0 + 64 < nc) ? page_of(a, b, j0 / 64 + 1) : -1;
+        const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) * a.kblk * (KB_BYTES / 2);
+        uint8_t* st = stage_mem + stage * STAGE_BYTES;
+        tc::mbar_arrive_expect_tx(&sm->full[stage], bytes);
+        for (int kb = 0; kb < a.kblk; ++kb) {
+          if (pg0 >= 0) tc::tma_load_2d(st + kb * KB_BYTES, &kmap, kb * 64, pg0 * 64, &sm->full[stage]);
+          if (pg1 >= 0) tc::tma_load_2d(st + kb * KB_BYTES + KB_BYTES / 2, &kmap, kb * 64, pg1 * 64, &sm->full[stage]);
+        }
+        if (++stage == a.stages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // drain: every issued load must land before the CTA may exit
+      for (int s = 0; s < a.stages; ++s) {
+        // the most recent use of stage s completed phase `ph`; waiting on it returns at once when consumed
+        int uses_parity = (s < stage) ? (int)phase : (int)(phase ^ 1);
+        tc::mbar_wait_bounded(&sm->full[s], uses_parity, abort, 100000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      const uint32_t idesc = tc::idesc_bf16_f32(TILE, a.N);
+      const uint32_t q_addr = tc::smem_addr(q_mem);
+      int stage = 0, acc = 0, cur_b = -1;
+      uint32_t phase = 0, aphase = 0, qphase = 0;
+      int b, tile;
+      for (int it = next_item(a, lo, hi, b, tile); it < hi;) {
+        if (b != cur_b) {
+          if (!tc::mbar_wait_bounded(&sm->qfull, qphase, abort)) break;
+          qphase ^= 1;
+          cur_b = b;
+        }
+        if (!tc::mbar_wait_bounded(&sm->full[stage], phase, abort)) break;
+        if (!tc::mbar_wait_bounded(&sm->dempty[acc], aphase ^ 1, abort)) break;
+        tc::tc_fence_after();
+        const uint32_t a_addr = tc::smem_addr(stage_mem + stage * STAGE_BYTES);
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * a.N);
+        for (int kb = 0; kb < a.kblk; ++kb) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint64_t ad = tc::sdesc_k_sw128(a_addr + kb * KB_BYTES + s * 32);
+            const uint64_t bd = tc::sdesc_k_sw128(q_addr + kb * a.N * 128 + s * 32);
+            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0);
+          }
+        }
+        tc::mma_commit(&sm->empty[stage]);
+        tc::mma_commit(&sm->dfull[acc]);
+        int nb, ntile;
+        const int nx = next_item(a, it + 1, hi, nb, ntile);
+        if (nx >= hi || nb != b) tc::mma_commit(&sm->qempty);
+        if (++stage == a.stages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1;
+        }
+        it = nx;
+        b = nb;
+        tile = ntile;
+      }
+      tc::mma_commit(&sm->done);
+      tc::mbar_wait_bounded(&sm->done, 0, abort, 100000000ull);
+    }
+  } else {
+    // ---------------- epilogue: warps 0-3, thread = key row (TMEM lane)
+    const int row = warp * 32 + lane;
+    int acc = 0, cur_b = -1;
+    uint32_t aphase = 0;
+    int b, tile;
+    for (int it = next_item(a, lo, hi, b, tile); it < hi; it = next_item(a, it + 1, hi, b, tile)) {
+      if (b != cur_b) {
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        for (int x = row; x < a.N; x += 128) w_s[x] = a.weights[(int64_t)b * a.qps * a.Ih + x];
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        cur_b = b;
+      }
+      if (!tc::mbar_wait_bounded(&sm->dfull[acc], aphase, abort)) break;
+      tc::tc_fence_after();
+      float sk[DSV4_MAX_Q_PER_SEQ] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * a.N);
+      for (int c0 = 0; c0 < a.N; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(lane_addr + c0, v);
+        float part = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) part = fmaf(w_s[c0 + i], fmaxf(v[i], 0.f), part);
+        const int k = c0 / a.Ih;
+#pragma unroll
+        for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q)
+          if (q == k) sk[q] += part;
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm->dempty[acc]);
+      const int j = tile * TILE + row;
+#pragma unroll
+      for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q) {
+        if (q < a.qps) {
+          const int t = b * a.qps + q;
+          if (j < tok_entries(a, t)) a.scores[(int64_t)t * a.nc_stride + j] = sk[q];
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && sm->abort) atomicOr(&g_flags_ix, FLAG_TIMEOUT);
+  if (warp == 5) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, a.tmem_cols);
+  }
+}
+
+}  // namespace ixtc
+
+static bool use_tc_indexer(const dsv4_indexer_topk_params& p) {
+  const int N = p.q_per_seq * p.n_heads;
+  return p.k_dtype == DSV4_BF16 && p.q_dtype == DSV4_BF16 && (p.head_dim == 64 || p.head_dim == 128) &&
+         p.n_heads % 32 == 0 && N >= 32 && N <= 256 && p.page_size == 64;
+}
+
+static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, float* scores, int nc_stride,
+                                           cudaStream_t st) {
+  using namespace ixtc;
+  const int max_nc = p.max_context / p.ratio;
+  Args a;
+  a.positions = p.positions;
+  a.block_table = p.block_table;
+  a.weights = p.weights;
+  a.scores = scores;
+  a.num_pages = p.num_pages;
+  a.T = p.T;
+  a.B = p.B;
+  a.qps = p.q_per_seq;
+  a.Ih = p.n_heads;
+  a.d = p.head_dim;
+  a.ratio = p.ratio;
+  a.max_pages = p.max_pages_per_seq;
+  a.nc_stride = nc_stride;
+  a.tiles_max = (max_nc + TILE - 1) / TILE;
+  a.max_context = p.max_context;
+  a.N = p.q_per_seq * p.n_heads;
+  a.kblk = p.head_dim / 64;
+  a.stages = a.N > 128 ? 4 : 5;
+  a.tmem_cols = a.N <= 16 ? 32 : (2 * a.N <= 64 ? 64 : (2 * a.N <= 128 ? 128 : (2 * a.N <= 256 ? 256 : 512)));
+  CUtensorMap kmap, qmap;
+  cudaError_t e = make_tmap_2d_bf16(&kmap, p.k_cache, (uint64_t)p.head_dim, (uint64_t)p.num_pages * 64, 64, 64);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_2d_bf16(&qmap, p.q, (uint64_t)p.head_dim, (uint64_t)p.T * p.n_heads, 64, (uint32_t)a.N);
+  if (e != cudaSuccess) return e;
+  const size_t smem = 1024 + (size_t)a.stages * STAGE_BYTES + (size_t)a.kblk * a.N * 128 + 256 * 4 + sizeof(Smem);
+  static int attr_done = 0;
+  if (!attr_done) {
+    e = cudaFuncSetAttribute(indexer_score_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_done = 1;
+  }
+  const int total = a.B * a.tiles_max;
+  int grid = num_sms();
+  if (grid > total) grid = total;
+  if (grid <= 0) return cudaSuccess;
+  indexer_score_tc<<<grid, THREADS, smem, st>>>(kmap, qmap, a);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -235,7 +538,10 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
   IxLayout L = ix_layout(p);
   float* scores = reinterpret_cast<float*>(reinterpret_cast<char*>(p.workspace) + L.scores_off);
   const int max_nc = p.max_context / p.ratio;
-  if (max_nc > 0) {
+  if (max_nc > 0 && use_tc_indexer(p)) {
+    cudaError_t e = launch_indexer_score_tc(p, scores, (int)L.nc_stride, st);
+    if (e != cudaSuccess) return e;
+  } else if (max_nc > 0) {
     const int tiles = (max_nc + IX_TILE - 1) / IX_TILE;
     const size_t smem = sizeof(float) * ((size_t)p.q_per_seq * p.n_heads * p.head_dim +
                                          (size_t)p.q_per_seq * p.n_heads + (size_t)(p.head_dim + 1) * (IX_TILE + 1));

@@ -1,0 +1,19 @@
+// Host helpers for TMA tensor maps (driver entry point fetched through the runtime, so the library
+// needs no link-time dependency on libcuda) and the device's SM count.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsv4 {
+
+// 2-D bf16 tensor [rows, cols] (cols innermost, rows `cols * 2` bytes apart), box
+// [box_rows, box_cols] with 128-byte swizzle (box_cols * 2 must be 128).
+cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                              uint32_t box_rows);
+
+// Multiprocessor count of the current device.
+int num_sms();
+
+}  // namespace dsv4
