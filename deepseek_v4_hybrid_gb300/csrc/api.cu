@@ -113,6 +113,7 @@ int dsv4_indexer_topk(const dsv4_indexer_topk_params* p, dsv4_stream_t stream) {
   CHECK(p->n_heads >= 1 && p->n_heads <= 128 && p->head_dim >= 16 && p->head_dim <= 256 && p->head_dim % 16 == 0,
         DSV4_ERR_UNSUPPORTED);
   CHECK((int64_t)p->q_per_seq * p->n_heads <= 256, DSV4_ERR_UNSUPPORTED);
+  CHECK(p->max_context / p->ratio <= (1 << 20), DSV4_ERR_UNSUPPORTED);
   if (p->T == 0) return DSV4_OK;
   CHECK(p->q && p->weights && p->k_cache && p->block_table && p->positions && p->topk_idx, DSV4_ERR_INVALID);
   CHECK(aligned(p->q, 16) && aligned(p->k_cache, 16) && aligned(p->weights, 4), DSV4_ERR_INVALID);

@@ -6,10 +6,15 @@
 // DeepseekV4Indexer.forward (when the candidates fit in top-k, every candidate is selected).
 // Score: s[t][j] = sum_h w[t][h] * ReLU(q[t][h] . k_j) in fp32.
 //
-// Work split: the score kernel gives a CTA one tile of 128 keys of one sequence and scores them
-// for all of that sequence's query tokens, so each key row leaves HBM once per step.  Scores go
-// to the workspace; the top-k kernel then runs an exact 4-pass 8-bit radix select per token on
-// order-preserving uint32 keys and compacts the selection in increasing j.
+// Kernels of one call:
+//  1. score: a CTA works on 128-key tiles of one sequence for all of that sequence's query tokens,
+//     so each key row leaves HBM once per step.  bf16 keys run on the tensor cores (tcgen05 MMA,
+//     TMA-fed); fp32 and int8 keys on the CUDA cores.  Besides the score row of each token, the
+//     epilogue builds a 4096-bin histogram of the scores' top 12 order-preserving key bits.
+//  2. collect: from the histogram, the bin B* holding the k-th best score; every entry above B*
+//     is selected outright, every entry inside B* becomes a candidate.
+//  3. final: exact choice among the candidates (larger score first, then smaller j), then the
+//     selection sorted by j.
 #include "dsv4_common.cuh"
 #include "dsv4_launch.h"
 #include "tc_ptx.cuh"
@@ -20,20 +25,37 @@ namespace dsv4 {
 static __device__ unsigned int g_flags_ix = 0;
 
 constexpr int IX_TILE = 128;
+constexpr int HIST_BITS = 12;
+constexpr int HIST_BINS = 1 << HIST_BITS;
+constexpr int HIST_SHIFT = 32 - HIST_BITS;
+constexpr uint32_t FLAG_TIMEOUT = 4u;
+
+// Order-preserving map of an fp32 score to uint32 (larger score -> larger key).
+__device__ __forceinline__ uint32_t order_key(float s) {
+  uint32_t u = __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 // n_c of token t, clamped to what the workspace and grid were sized for (max_context); a position
 // outside [0, max_context) is flagged.
-__device__ __forceinline__ int visible_entries(const dsv4_indexer_topk_params& p, int t) {
-  const int pos = p.positions[t];
-  if (pos < 0 || pos >= p.max_context) {
+__device__ __forceinline__ int visible_entries(const int32_t* positions, int t, int max_context, int ratio) {
+  const int pos = positions[t];
+  if (pos < 0 || pos >= max_context) {
     atomicOr(&g_flags_ix, FLAG_PAGE);
-    return pos < 0 ? 0 : p.max_context / p.ratio;
+    return pos < 0 ? 0 : max_context / ratio;
   }
-  return (pos + 1) / p.ratio;
+  return (pos + 1) / ratio;
+}
+__device__ __forceinline__ int visible_entries(const dsv4_indexer_topk_params& p, int t) {
+  return visible_entries(p.positions, t, p.max_context, p.ratio);
 }
 
+// ------------------------------------------------------------------------------------------------
+// Workspace
+// ------------------------------------------------------------------------------------------------
 struct IxLayout {
-  size_t scores_off, nc_stride;
+  size_t nc_stride;
+  size_t scores_off, hist_off, cnt_off, certain_off, maybe_off, total;
 };
 
 static IxLayout ix_layout(const dsv4_indexer_topk_params& p) {
@@ -41,19 +63,38 @@ static IxLayout ix_layout(const dsv4_indexer_topk_params& p) {
   const int64_t max_nc = (int64_t)p.max_context / p.ratio;
   L.nc_stride = align_up((size_t)(max_nc > 0 ? max_nc : 1), 64);
   L.scores_off = 0;
+  L.hist_off = align_up(L.scores_off + (size_t)p.T * L.nc_stride * sizeof(float), 256);
+  L.cnt_off = L.hist_off + (size_t)p.T * HIST_BINS * sizeof(uint32_t);  // zeroed together with hist
+  L.certain_off = align_up(L.cnt_off + (size_t)p.T * 2 * sizeof(uint32_t), 256);
+  L.maybe_off = align_up(L.certain_off + (size_t)p.T * p.topk * sizeof(int32_t), 256);
+  L.total = align_up(L.maybe_off + (size_t)p.T * L.nc_stride * sizeof(uint64_t), 256);
   return L;
 }
 
-size_t indexer_topk_workspace(const dsv4_indexer_topk_params& p) {
-  IxLayout L = ix_layout(p);
-  return align_up((size_t)p.T * L.nc_stride * sizeof(float), 256);
+size_t indexer_topk_workspace(const dsv4_indexer_topk_params& p) { return ix_layout(p).total; }
+
+struct TopkBufs {
+  float* scores;
+  uint32_t* hist;      // [T][HIST_BINS]
+  uint32_t* cnt;       // [T][2]: selected-outright count, candidate count
+  int32_t* certain;    // [T][topk]
+  uint64_t* maybe;     // [T][nc_stride] candidates: (low 20 key bits << 32) | ~j
+  int nc_stride;
+};
+
+// Adds one to bin `bin` of `hist` for each lane with `on`, one atomic per distinct bin of the warp.
+// Every lane of the warp must call it.
+__device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool on) {
+  const unsigned active = __ballot_sync(0xffffffffu, on);
+  if (!on) return;
+  const unsigned peers = __match_any_sync(active, bin);
+  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
 }
 
 // ------------------------------------------------------------------------------------------------
-// SIMT score kernel (all key dtypes): thread jj of the CTA owns key tile*128 + jj.
+// SIMT score kernel (any key dtype): thread jj of the CTA owns key tile*128 + jj.
 // ------------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_params p, float* scores,
-                                                              int nc_stride) {
+__global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_params p, TopkBufs bufs) {
   extern __shared__ float smem[];
   const int b = blockIdx.y, tile = blockIdx.x, jj = threadIdx.x;
   const int Ih = p.n_heads, d = p.head_dim, qps = p.q_per_seq;
@@ -65,7 +106,7 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
   float* q_s = smem;                         // [qps][Ih][d]
   float* w_s = q_s + qps * Ih * d;           // [qps][Ih]
   const int ld = IX_TILE + 1;
-  float* kt_s = w_s + qps * Ih;              // [d][IX_TILE + 1] transposed keys
+  float* kt_s = w_s + qps * Ih;              // [d + 1][IX_TILE + 1] transposed keys, then row scales
 
   for (int x = jj; x < qps * Ih * d; x += IX_TILE) {
     const int64_t g = (int64_t)t0 * Ih * d + x;
@@ -99,7 +140,7 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
       }
       kt_s[e * ld + kk] = v;
     }
-    if (lane == 0) kt_s[d * ld + kk] = scale;  // scale row after the d key rows
+    if (lane == 0) kt_s[d * ld + kk] = scale;
   }
   __syncthreads();
 
@@ -114,10 +155,12 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
       float acc = 0.f;
       const float* qh = qk + h * d;
       for (int e = 0; e < d; ++e) acc = fmaf(qh[e], kt_s[e * ld + jj], acc);
-      acc *= kscale;
+      acc *= kscale;  // int8 keys: code . q, then the row scale
       s = fmaf(w_s[k * Ih + h], fmaxf(acc, 0.f), s);
     }
-    if (j < nc) scores[(int64_t)t * nc_stride + j] = s;
+    const bool on = j < nc;
+    if (on) bufs.scores[(int64_t)t * bufs.nc_stride + j] = s;
+    hist_add_warp(bufs.hist + (int64_t)t * HIST_BINS, order_key(s) >> HIST_SHIFT, on);
   }
 }
 
@@ -127,45 +170,38 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
 // s_k = sum_h w[k][h] * ReLU(D[key][k*n_heads + h]).
 //
 // Persistent CTAs (one per SM), each owning a contiguous range of (sequence, 128-key tile) items.
-// Warp 4 streams key tiles with TMA (two 64-row pages x two 64-dim K-blocks, 128-byte swizzle)
-// into a ring of stages and the sequence's Q block into its own buffer; one thread of warp 5 issues
-// the tcgen05 MMAs (M = 128, K = 16 steps) into one of two TMEM accumulators; warps 0-3 read
-// their 32 TMEM lanes each (one key per thread), apply ReLU and the head weights and store the
-// scores.  Every wait is bounded; a timeout raises FLAG_TIMEOUT and all roles drain out.
+// Warp 4 streams key tiles with TMA (two 64-row pages x d/64 K-blocks of 128 B, 128-byte swizzle)
+// into a ring of stages, and each sequence's Q block into one of two Q slots; its 32 lanes look up
+// the block-table pages of 32 items at a time.  One thread of warp 5 issues the tcgen05 MMAs
+// (M = 128, K = 16 steps) into one of two TMEM accumulators; warps 0-3 read their 32 TMEM lanes
+// each (one key per thread), apply ReLU and the head weights, store the scores and count them
+// into a shared-memory histogram that is added to the global one when the sequence changes.
+// Every wait is bounded; a timeout raises FLAG_TIMEOUT and all roles drain out.
 // ------------------------------------------------------------------------------------------------
 namespace ixtc {
 constexpr int TILE = 128;
 constexpr int KB_BYTES = TILE * 128;         // one 64-dim K-block of a key tile (128 rows x 128 B)
-constexpr int STAGE_BYTES = 2 * KB_BYTES;    // d <= 128
 constexpr int THREADS = 192;
-constexpr uint32_t FLAG_TIMEOUT = 4u;
+constexpr int MAX_STAGES = 8;
 
 struct Args {
   const int32_t* positions;
   const int32_t* block_table;
   const float* weights;
-  float* scores;
+  TopkBufs bufs;
   int64_t num_pages;
-  int T, B, qps, Ih, d, ratio, max_pages, nc_stride, tiles_max, max_context;
-  int N, kblk, stages, tmem_cols;
+  int T, B, qps, Ih, d, ratio, max_pages, tiles_max, max_context;
+  int N, kblk, stages, tmem_cols, nacc;
 };
 
 struct Smem {
-  uint64_t full[8], empty[8], dfull[2], dempty[2], qfull, qempty, done;
+  uint64_t full[MAX_STAGES], empty[MAX_STAGES], dfull[4], dempty[4], qfull[2], qempty[2], done;
   uint32_t tmem_base;
   int abort;
 };
 
 __device__ __forceinline__ int seq_entries(const Args& a, int b) {
-  const int pos = a.positions[b * a.qps + a.qps - 1];
-  if (pos < 0 || pos >= a.max_context) return pos < 0 ? 0 : a.max_context / a.ratio;
-  return (pos + 1) / a.ratio;
-}
-
-__device__ __forceinline__ int tok_entries(const Args& a, int t) {
-  const int pos = a.positions[t];
-  if (pos < 0 || pos >= a.max_context) return pos < 0 ? 0 : a.max_context / a.ratio;
-  return (pos + 1) / a.ratio;
+  return visible_entries(a.positions, b * a.qps + a.qps - 1, a.max_context, a.ratio);
 }
 
 __device__ __forceinline__ int page_of(const Args& a, int b, int lp) {
@@ -178,24 +214,64 @@ __device__ __forceinline__ int page_of(const Args& a, int b, int lp) {
   return pg;
 }
 
-// next valid item at or after `it` in [it, hi), or hi
-__device__ __forceinline__ int next_item(const Args& a, int it, int hi, int& b, int& tile) {
-  for (; it < hi; ++it) {
-    b = it / a.tiles_max;
-    tile = it % a.tiles_max;
-    if (tile * TILE < seq_entries(a, b)) return it;
+// Walks the valid (sequence, tile) items of the flat range [lo, hi) in order without divisions.
+struct ItemIter {
+  int it, hi, b, tile, nc;
+  __device__ __forceinline__ void init(const Args& a, int lo, int hi_) {
+    it = lo;
+    hi = hi_;
+    b = lo / a.tiles_max;
+    tile = lo % a.tiles_max;
+    nc = it < hi ? seq_entries(a, b) : 0;
+    skip(a);
   }
-  return hi;
+  // moves past tiles beyond the end of the current sequence
+  __device__ __forceinline__ void skip(const Args& a) {
+    while (it < hi && tile * TILE >= nc) {
+      it += a.tiles_max - tile;
+      ++b;
+      tile = 0;
+      if (it < hi) nc = seq_entries(a, b);
+    }
+  }
+  __device__ __forceinline__ void next(const Args& a) {
+    ++it;
+    if (++tile == a.tiles_max) {
+      ++b;
+      tile = 0;
+      if (it < hi) nc = seq_entries(a, b);
+    }
+    skip(a);
+  }
+  __device__ __forceinline__ bool valid() const { return it < hi; }
+};
+
+// Adds the shared histogram of sequence b (if any) to the global one and clears it.
+__device__ __forceinline__ void flush_hist(const Args& a, uint32_t* hist_s, int b, int row) {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  if (b >= 0) {
+    for (int x = row; x < a.qps * HIST_BINS; x += 128) {
+      const uint32_t v = hist_s[x];
+      if (v) {
+        atomicAdd(&a.bufs.hist[(int64_t)(b * a.qps + x / HIST_BINS) * HIST_BINS + (x % HIST_BINS)], v);
+        hist_s[x] = 0;
+      }
+    }
+  }
+  asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
     indexer_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, Args a) {
   extern __shared__ __align__(1024) uint8_t dsm[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
-  uint8_t* stage_mem = base;                                      // stages x STAGE_BYTES
-  uint8_t* q_mem = base + a.stages * STAGE_BYTES;                 // kblk x N x 128 B
-  float* w_s = reinterpret_cast<float*>(q_mem + a.kblk * a.N * 128);  // N floats
-  Smem* sm = reinterpret_cast<Smem*>(w_s + 256);
+  const int q_bytes = a.kblk * a.N * 128;
+  const int stage_bytes = a.kblk * KB_BYTES;
+  uint8_t* stage_mem = base;                                               // stages x stage_bytes
+  uint8_t* q_mem = base + a.stages * stage_bytes;                          // 2 slots x q_bytes
+  float* w_s = reinterpret_cast<float*>(q_mem + 2 * q_bytes);              // 256 floats
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(w_s + 256);               // qps x HIST_BINS
+  Smem* sm = reinterpret_cast<Smem*>(hist_s + a.qps * HIST_BINS);
   volatile int* abort = &sm->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -208,16 +284,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_init(&sm->full[s], 1);
       tc::mbar_init(&sm->empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       tc::mbar_init(&sm->dfull[i], 1);
       tc::mbar_init(&sm->dempty[i], 4);
     }
-    tc::mbar_init(&sm->qfull, 1);
-    tc::mbar_init(&sm->qempty, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sm->qfull[i], 1);
+      tc::mbar_init(&sm->qempty[i], 1);
+    }
     tc::mbar_init(&sm->done, 1);
     sm->abort = 0;
     tc::fence_barrier_init();
   }
+  for (int x = threadIdx.x; x < a.qps * HIST_BINS; x += THREADS) hist_s[x] = 0;
   if (warp == 5) {
     tc::tmem_alloc(&sm->tmem_base, a.tmem_cols);
     tc::tmem_relinquish();
@@ -228,66 +307,100 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = sm->tmem_base;
 
   if (warp == 4) {
+    // ---------------- TMA producer (lane 0 issues; all lanes look up pages 32 items at a time)
     if (lane == 0) {
-      // ---------------- TMA producer
       tc::tma_prefetch_desc(&kmap);
       tc::tma_prefetch_desc(&qmap);
-      int stage = 0, cur_b = -1;
-      uint32_t phase = 0, qphase = 0;
-      int b, tile;
-      for (int it = next_item(a, lo, hi, b, tile); it < hi; it = next_item(a, it + 1, hi, b, tile)) {
-        if (b != cur_b) {
-          if (cur_b >= 0) {
-            if (!tc::mbar_wait_bounded(&sm->qempty, qphase, abort)) break;
-            qphase ^= 1;
-          }
-          tc::mbar_arrive_expect_tx(&sm->qfull, a.kblk * a.N * 128);
-          for (int kb = 0; kb < a.kblk; ++kb)
-            tc::tma_load_2d(q_mem + kb * a.N * 128, &qmap, kb * 64, b * a.qps * a.Ih, &sm->qfull);
-          cur_b = b;
-        }
-        if (!tc::mbar_wait_bounded(&sm->empty[stage], phase ^ 1, abort)) break;
+    }
+    int stage = 0, cur_b = -1, qn = 0;
+    uint32_t phase = 0;
+    bool stop = false;
+    for (int base_it = lo; base_it < hi && !stop; base_it += 32) {
+      const int it = base_it + lane;
+      int vb = -1, pg0 = -1, pg1 = -1;
+      if (it < hi) {
+        const int b = it / a.tiles_max, tile = it % a.tiles_max;
         const int nc = seq_entries(a, b);
         const int j0 = tile * TILE;
-        const int pg0 = page_of(a, b, j0 / 64);
-        const int pg1 = (j0 + 64 < nc) ? page_of(a, b, j0 / 64 + 1) : -1;
-        const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) * a.kblk * (KB_BYTES / 2);
-        uint8_t* st = stage_mem + stage * STAGE_BYTES;
-        tc::mbar_arrive_expect_tx(&sm->full[stage], bytes);
-        for (int kb = 0; kb < a.kblk; ++kb) {
-          if (pg0 >= 0) tc::tma_load_2d(st + kb * KB_BYTES, &kmap, kb * 64, pg0 * 64, &sm->full[stage]);
-          if (pg1 >= 0) tc::tma_load_2d(st + kb * KB_BYTES + KB_BYTES / 2, &kmap, kb * 64, pg1 * 64, &sm->full[stage]);
-        }
-        if (++stage == a.stages) {
-          stage = 0;
-          phase ^= 1;
+        if (j0 < nc) {
+          vb = b;
+          pg0 = page_of(a, b, j0 / 64);
+          pg1 = (j0 + 64 < nc) ? page_of(a, b, j0 / 64 + 1) : -1;
         }
       }
-      // drain: every issued load must land before the CTA may exit
+      for (int i = 0; i < 32; ++i) {
+        const int b = __shfl_sync(0xffffffffu, vb, i);
+        const int p0 = __shfl_sync(0xffffffffu, pg0, i);
+        const int p1 = __shfl_sync(0xffffffffu, pg1, i);
+        if (b < 0) continue;
+        int ok = 1;
+        if (lane == 0) {
+          if (b != cur_b) {
+            const int slot = qn & 1;
+            ok = tc::mbar_wait_bounded(&sm->qempty[slot], ((qn >> 1) & 1) ^ 1, abort);
+            if (ok) {
+              tc::mbar_arrive_expect_tx(&sm->qfull[slot], q_bytes);
+              for (int kb = 0; kb < a.kblk; ++kb)
+                tc::tma_load_2d(q_mem + slot * q_bytes + kb * a.N * 128, &qmap, kb * 64, b * a.qps * a.Ih,
+                                &sm->qfull[slot]);
+              ++qn;
+              cur_b = b;
+            }
+          }
+          if (ok) ok = tc::mbar_wait_bounded(&sm->empty[stage], phase ^ 1, abort);
+          if (ok) {
+            const uint32_t bytes = (uint32_t)((p0 >= 0) + (p1 >= 0)) * a.kblk * (KB_BYTES / 2);
+            uint8_t* st = stage_mem + stage * stage_bytes;
+            tc::mbar_arrive_expect_tx(&sm->full[stage], bytes);
+            for (int kb = 0; kb < a.kblk; ++kb) {
+              if (p0 >= 0) tc::tma_load_2d(st + kb * KB_BYTES, &kmap, kb * 64, p0 * 64, &sm->full[stage]);
+              if (p1 >= 0)
+                tc::tma_load_2d(st + kb * KB_BYTES + KB_BYTES / 2, &kmap, kb * 64, p1 * 64, &sm->full[stage]);
+            }
+            if (++stage == a.stages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          stop = true;
+          break;
+        }
+      }
+    }
+    if (lane == 0) {
+      // drain: every issued load must land before the CTA may exit (a completed phase returns at once)
       for (int s = 0; s < a.stages; ++s) {
-        // the most recent use of stage s completed phase `ph`; waiting on it returns at once when consumed
-        int uses_parity = (s < stage) ? (int)phase : (int)(phase ^ 1);
-        tc::mbar_wait_bounded(&sm->full[s], uses_parity, abort, 100000000ull);
+        const int parity = (s < stage) ? (int)phase : (int)(phase ^ 1);
+        tc::mbar_wait_bounded(&sm->full[s], parity, abort, 100000000ull);
+      }
+      for (int slot = 0; slot < 2; ++slot) {
+        const int last = (qn - 1 - slot) >= 0 ? (qn - 1) - ((qn - 1 - slot) & 1) : -1;  // last load into slot
+        if (last >= 0) tc::mbar_wait_bounded(&sm->qfull[slot], (last >> 1) & 1, abort, 100000000ull);
       }
     }
   } else if (warp == 5) {
     if (lane == 0) {
       // ---------------- MMA issuer
       const uint32_t idesc = tc::idesc_bf16_f32(TILE, a.N);
-      const uint32_t q_addr = tc::smem_addr(q_mem);
-      int stage = 0, acc = 0, cur_b = -1;
-      uint32_t phase = 0, aphase = 0, qphase = 0;
-      int b, tile;
-      for (int it = next_item(a, lo, hi, b, tile); it < hi;) {
-        if (b != cur_b) {
-          if (!tc::mbar_wait_bounded(&sm->qfull, qphase, abort)) break;
-          qphase ^= 1;
-          cur_b = b;
+      int stage = 0, acc = 0, cur_b = -1, qn = 0, slot = 0;
+      uint32_t phase = 0, aphase = 0;
+      ItemIter cur;
+      cur.init(a, lo, hi);
+      while (cur.valid()) {
+        if (cur.b != cur_b) {
+          slot = qn & 1;
+          if (!tc::mbar_wait_bounded(&sm->qfull[slot], (qn >> 1) & 1, abort)) break;
+          ++qn;
+          cur_b = cur.b;
         }
         if (!tc::mbar_wait_bounded(&sm->full[stage], phase, abort)) break;
         if (!tc::mbar_wait_bounded(&sm->dempty[acc], aphase ^ 1, abort)) break;
         tc::tc_fence_after();
-        const uint32_t a_addr = tc::smem_addr(stage_mem + stage * STAGE_BYTES);
+        const uint32_t a_addr = tc::smem_addr(stage_mem + stage * stage_bytes);
+        const uint32_t q_addr = tc::smem_addr(q_mem + slot * q_bytes);
         const uint32_t d_tmem = tmem + (uint32_t)(acc * a.N);
         for (int kb = 0; kb < a.kblk; ++kb) {
 #pragma unroll
@@ -299,20 +412,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc::mma_commit(&sm->empty[stage]);
         tc::mma_commit(&sm->dfull[acc]);
-        int nb, ntile;
-        const int nx = next_item(a, it + 1, hi, nb, ntile);
-        if (nx >= hi || nb != b) tc::mma_commit(&sm->qempty);
+        const int b_now = cur.b;
+        cur.next(a);
+        if (!cur.valid() || cur.b != b_now) tc::mma_commit(&sm->qempty[slot]);
         if (++stage == a.stages) {
           stage = 0;
           phase ^= 1;
         }
-        if (++acc == 2) {
+        if (++acc == a.nacc) {
           acc = 0;
           aphase ^= 1;
         }
-        it = nx;
-        b = nb;
-        tile = ntile;
       }
       tc::mma_commit(&sm->done);
       tc::mbar_wait_bounded(&sm->done, 0, abort, 100000000ull);
@@ -322,11 +432,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int row = warp * 32 + lane;
     int acc = 0, cur_b = -1;
     uint32_t aphase = 0;
-    int b, tile;
-    for (int it = next_item(a, lo, hi, b, tile); it < hi; it = next_item(a, it + 1, hi, b, tile)) {
+    int nc_tok[DSV4_MAX_Q_PER_SEQ] = {0, 0, 0, 0};
+    ItemIter cur;
+    cur.init(a, lo, hi);
+    for (; cur.valid(); cur.next(a)) {
+      const int b = cur.b;
       if (b != cur_b) {
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        flush_hist(a, hist_s, cur_b, row);
         for (int x = row; x < a.N; x += 128) w_s[x] = a.weights[(int64_t)b * a.qps * a.Ih + x];
+#pragma unroll
+        for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q)
+          nc_tok[q] = q < a.qps ? visible_entries(a.positions, b * a.qps + q, a.max_context, a.ratio) : 0;
         asm volatile("bar.sync 1, 128;" ::: "memory");
         cur_b = b;
       }
@@ -334,33 +450,60 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::tc_fence_after();
       float sk[DSV4_MAX_Q_PER_SEQ] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * a.N);
-      for (int c0 = 0; c0 < a.N; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(lane_addr + c0, v);
-        float part = 0.f;
+      for (int c0 = 0; c0 < a.N; c0 += 64) {
+        uint32_t r[64];
+        tc::tmem_ld32_nowait(lane_addr + c0, r);
+        tc::tmem_ld32_nowait(lane_addr + c0 + 32, r + 32);
+        tc::tmem_wait_ld_regs<64>(r);
+        const float4* w4 = reinterpret_cast<const float4*>(w_s + c0);
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) part = fmaf(w_s[c0 + i], fmaxf(v[i], 0.f), part);
-        const int k = c0 / a.Ih;
+        for (int i = 0; i < 16; ++i) {
+          const float4 w = w4[i];
+          p[0] = fmaf(w.x, fmaxf(__uint_as_float(r[4 * i + 0]), 0.f), p[0]);
+          p[1] = fmaf(w.y, fmaxf(__uint_as_float(r[4 * i + 1]), 0.f), p[1]);
+          p[2] = fmaf(w.z, fmaxf(__uint_as_float(r[4 * i + 2]), 0.f), p[2]);
+          p[3] = fmaf(w.w, fmaxf(__uint_as_float(r[4 * i + 3]), 0.f), p[3]);
+        }
+        // n_heads is a multiple of 32: the two 32-column halves may belong to different tokens
+        const int k0 = c0 / a.Ih, k1 = (c0 + 32) / a.Ih;
+        if (k0 == k1) {
 #pragma unroll
-        for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q)
-          if (q == k) sk[q] += part;
+          for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q)
+            if (q == k0) sk[q] += (p[0] + p[1]) + (p[2] + p[3]);
+        } else {
+          // recompute the halves separately (only when a token boundary falls mid-chunk)
+          float h0 = 0.f, h1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) h0 = fmaf(w_s[c0 + i], fmaxf(__uint_as_float(r[i]), 0.f), h0);
+#pragma unroll
+          for (int i = 32; i < 64; ++i) h1 = fmaf(w_s[c0 + i], fmaxf(__uint_as_float(r[i]), 0.f), h1);
+#pragma unroll
+          for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q) {
+            if (q == k0) sk[q] += h0;
+            if (q == k1) sk[q] += h1;
+          }
+        }
       }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->dempty[acc]);
-      const int j = tile * TILE + row;
+      const int j = cur.tile * TILE + row;
 #pragma unroll
       for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q) {
         if (q < a.qps) {
           const int t = b * a.qps + q;
-          if (j < tok_entries(a, t)) a.scores[(int64_t)t * a.nc_stride + j] = sk[q];
+          const bool on = j < nc_tok[q];
+          if (on) a.bufs.scores[(int64_t)t * a.bufs.nc_stride + j] = sk[q];
+          hist_add_warp(hist_s + q * HIST_BINS, order_key(sk[q]) >> HIST_SHIFT, on);
         }
       }
-      if (++acc == 2) {
+      if (++acc == a.nacc) {
         acc = 0;
         aphase ^= 1;
       }
     }
+    flush_hist(a, hist_s, cur_b, row);
   }
   __syncthreads();
   if (threadIdx.x == 0 && sm->abort) atomicOr(&g_flags_ix, FLAG_TIMEOUT);
@@ -375,10 +518,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 static bool use_tc_indexer(const dsv4_indexer_topk_params& p) {
   const int N = p.q_per_seq * p.n_heads;
   return p.k_dtype == DSV4_BF16 && p.q_dtype == DSV4_BF16 && (p.head_dim == 64 || p.head_dim == 128) &&
-         p.n_heads % 32 == 0 && N >= 32 && N <= 256 && p.page_size == 64;
+         p.n_heads % 32 == 0 && N >= 64 && N <= 128 && N % 64 == 0 && p.page_size == 64;
 }
 
-static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, float* scores, int nc_stride,
+static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, const TopkBufs& bufs,
                                            cudaStream_t st) {
   using namespace ixtc;
   const int max_nc = p.max_context / p.ratio;
@@ -386,7 +529,7 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, fl
   a.positions = p.positions;
   a.block_table = p.block_table;
   a.weights = p.weights;
-  a.scores = scores;
+  a.bufs = bufs;
   a.num_pages = p.num_pages;
   a.T = p.T;
   a.B = p.B;
@@ -395,22 +538,26 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, fl
   a.d = p.head_dim;
   a.ratio = p.ratio;
   a.max_pages = p.max_pages_per_seq;
-  a.nc_stride = nc_stride;
   a.tiles_max = (max_nc + TILE - 1) / TILE;
   a.max_context = p.max_context;
   a.N = p.q_per_seq * p.n_heads;
   a.kblk = p.head_dim / 64;
-  a.stages = a.N > 128 ? 4 : 5;
-  a.tmem_cols = a.N <= 16 ? 32 : (2 * a.N <= 64 ? 64 : (2 * a.N <= 128 ? 128 : (2 * a.N <= 256 ? 256 : 512)));
+  a.nacc = 4 * a.N <= 512 ? 4 : 2;  // TMEM accumulators (512 columns available)
+  a.tmem_cols = a.nacc * a.N <= 64 ? 64 : (a.nacc * a.N <= 128 ? 128 : (a.nacc * a.N <= 256 ? 256 : 512));
+  const size_t fixed = 1024 + 2 * (size_t)a.kblk * a.N * 128 + 256 * 4 + (size_t)a.qps * HIST_BINS * 4 + sizeof(Smem);
+  const size_t budget = 227 * 1024;
+  const int stages = (int)((budget - fixed) / ((size_t)a.kblk * KB_BYTES));
+  a.stages = stages > MAX_STAGES ? MAX_STAGES : stages;
+  if (a.stages < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = fixed + (size_t)a.stages * a.kblk * KB_BYTES;
   CUtensorMap kmap, qmap;
   cudaError_t e = make_tmap_2d_bf16(&kmap, p.k_cache, (uint64_t)p.head_dim, (uint64_t)p.num_pages * 64, 64, 64);
   if (e != cudaSuccess) return e;
   e = make_tmap_2d_bf16(&qmap, p.q, (uint64_t)p.head_dim, (uint64_t)p.T * p.n_heads, 64, (uint32_t)a.N);
   if (e != cudaSuccess) return e;
-  const size_t smem = 1024 + (size_t)a.stages * STAGE_BYTES + (size_t)a.kblk * a.N * 128 + 256 * 4 + sizeof(Smem);
   static int attr_done = 0;
   if (!attr_done) {
-    e = cudaFuncSetAttribute(indexer_score_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    e = cudaFuncSetAttribute(indexer_score_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
     if (e != cudaSuccess) return e;
     attr_done = 1;
   }
@@ -423,111 +570,282 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, fl
 }
 
 // ------------------------------------------------------------------------------------------------
-// Top-k: exact radix select, one CTA per token.
+// Top-k selection
 // ------------------------------------------------------------------------------------------------
-constexpr int TK_THREADS = 1024;
+constexpr int COLLECT_THREADS = 256;
+constexpr int COLLECT_PER = 32;                                   // scores per thread
+constexpr int COLLECT_SLICE = COLLECT_THREADS * COLLECT_PER;      // 8192 scores per CTA
+constexpr int FINAL_THREADS = 1024;
+constexpr int CAND_CAP = 4096;                                    // candidates kept in shared memory
+constexpr int J_BITS = 20;                                        // n_c <= 2^20 (checked on the host)
 
-__device__ __forceinline__ uint32_t order_key(float s) {
-  uint32_t u = __float_as_uint(s);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+// Candidate value: (low 20 order-key bits << 20) | (2^20 - 1 - j); larger = better score, then smaller j.
+__device__ __forceinline__ uint64_t cand_value(uint32_t key, int j) {
+  return ((uint64_t)(key & ((1u << HIST_SHIFT) - 1u)) << J_BITS) | (uint64_t)((1u << J_BITS) - 1u - (uint32_t)j);
 }
+__device__ __forceinline__ int cand_j(uint64_t v) { return (int)((1u << J_BITS) - 1u - (uint32_t)(v & ((1u << J_BITS) - 1u))); }
 
-// Exclusive prefix of a 0/1 flag over the CTA (thread order); returns the total in *total.
-__device__ __forceinline__ int block_excl_scan_flag(bool f, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const unsigned bal = __ballot_sync(0xffffffffu, f);
-  const int in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) warp_tot[warp] = __popc(bal);
-  __syncthreads();
-  if (warp == 0) {
-    int v = lane < nw ? warp_tot[lane] : 0;
-    int incl = v;
+// Bin holding the k-th largest score (from the histogram of one token) and the number of scores in
+// the bins above it.  Called by all COLLECT_THREADS threads.
+__device__ void threshold_bin(const uint32_t* hist, int K, int* bin_out, int* above_out) {
+  __shared__ uint32_t part[COLLECT_THREADS];
+  constexpr int PER = HIST_BINS / COLLECT_THREADS;  // thread i owns bins [i*PER, (i+1)*PER)
+  const int tid = threadIdx.x;
+  uint32_t local[PER];
+  uint32_t sum = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += u;
+  for (int i = 0; i < PER; ++i) {
+    local[i] = hist[tid * PER + i];
+    sum += local[i];
+  }
+  part[tid] = sum;
+  __syncthreads();
+  // inclusive suffix sums over the threads' groups (from the top bins down)
+  for (int off = 1; off < COLLECT_THREADS; off <<= 1) {
+    const uint32_t v = (tid + off < COLLECT_THREADS) ? part[tid + off] : 0u;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  const uint32_t incl = part[tid];
+  const uint32_t above_group = incl - sum;  // scores in the groups above this thread's
+  if (above_group < (uint32_t)K && incl >= (uint32_t)K) {
+    uint32_t cum = above_group;
+    for (int i = PER - 1; i >= 0; --i) {
+      if (cum + local[i] >= (uint32_t)K) {
+        *bin_out = tid * PER + i;
+        *above_out = (int)cum;
+        break;
+      }
+      cum += local[i];
     }
-    if (lane < nw) warp_tot[lane] = incl - v;  // exclusive warp offsets
-    if (lane == 31) warp_tot[32] = incl;
   }
   __syncthreads();
-  const int r = warp_tot[warp] + in_warp;
+}
+
+// Appends `val` to a shared-memory list for every lane with `on`, one shared atomic per warp.
+template <typename T>
+__device__ __forceinline__ void warp_append_smem(unsigned* cnt, T* list, T val, bool on) {
+  const unsigned m = __ballot_sync(0xffffffffu, on);
+  if (m == 0) return;
+  const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+  unsigned base = 0;
+  if (lane == leader) base = atomicAdd(cnt, (unsigned)__popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  if (on) list[base + __popc(m & ((1u << lane) - 1u))] = val;
+}
+
+// One CTA per (8192-score slice, token): entries above the threshold bin are selected outright,
+// entries in it become candidates; both are staged in shared memory and appended to the token's
+// global lists with one atomic each.
+__global__ void __launch_bounds__(COLLECT_THREADS) topk_collect(dsv4_indexer_topk_params p, TopkBufs bufs) {
+  extern __shared__ uint64_t csm[];
+  uint64_t* maybe_s = csm;                                        // COLLECT_SLICE
+  int32_t* cert_s = reinterpret_cast<int32_t*>(csm + COLLECT_SLICE);  // COLLECT_SLICE
+  __shared__ unsigned n_cert, n_maybe, base_cert, base_maybe;
+  __shared__ int sh_bin, sh_above;
+  const int t = blockIdx.y;
+  const int n = visible_entries(p, t);
+  const int K = p.topk;
+  const int j0 = blockIdx.x * COLLECT_SLICE;
+  if (n <= K || j0 >= n) return;  // block-uniform
+  const int j1 = min(n, j0 + COLLECT_SLICE);
+  const float* s = bufs.scores + (int64_t)t * bufs.nc_stride;
+  float v[COLLECT_PER];
+#pragma unroll
+  for (int i = 0; i < COLLECT_PER; ++i) {  // all loads in flight first
+    const int j = j0 + i * COLLECT_THREADS + threadIdx.x;
+    v[i] = j < j1 ? s[j] : 0.f;
+  }
+  if (threadIdx.x == 0) {
+    sh_bin = HIST_BINS - 1;
+    n_cert = n_maybe = 0;
+  }
+  __syncthreads();
+  threshold_bin(bufs.hist + (int64_t)t * HIST_BINS, K, &sh_bin, &sh_above);
+  const uint32_t bstar = (uint32_t)sh_bin;
+#pragma unroll
+  for (int i = 0; i < COLLECT_PER; ++i) {
+    const int j = j0 + i * COLLECT_THREADS + threadIdx.x;
+    const uint32_t key = order_key(v[i]);
+    const uint32_t bin = key >> HIST_SHIFT;
+    warp_append_smem<int32_t>(&n_cert, cert_s, j, j < j1 && bin > bstar);
+    warp_append_smem<uint64_t>(&n_maybe, maybe_s, cand_value(key, j), j < j1 && bin == bstar);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    base_cert = n_cert ? atomicAdd(&bufs.cnt[2 * t], n_cert) : 0u;
+    base_maybe = n_maybe ? atomicAdd(&bufs.cnt[2 * t + 1], n_maybe) : 0u;
+  }
+  __syncthreads();
+  int32_t* certain = bufs.certain + (int64_t)t * K;
+  uint64_t* maybe = bufs.maybe + (int64_t)t * bufs.nc_stride;
+  for (unsigned x = threadIdx.x; x < n_cert; x += COLLECT_THREADS)
+    if (base_cert + x < (unsigned)K) certain[base_cert + x] = cert_s[x];
+  for (unsigned x = threadIdx.x; x < n_maybe; x += COLLECT_THREADS)
+    if (base_maybe + x < (unsigned)bufs.nc_stride) maybe[base_maybe + x] = maybe_s[x];
+}
+
+// Digit of the radix bucket holding the rem-th largest element, from a 256-bin histogram: warp 0
+// does it with 8 bins per lane and a shuffle scan.  Writes the digit to *digit and the number of
+// elements in higher buckets to *above.  Called by the whole CTA.
+__device__ __forceinline__ void pick_digit(const unsigned* hist, unsigned rem, int* digit, unsigned* above) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    unsigned c[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c[i] = hist[255 - 8 * lane - i];  // lane 0 owns the top bins
+      sum += c[i];
+    }
+    unsigned incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    const unsigned excl = incl - sum;
+    if (excl < rem && incl >= rem) {
+      unsigned cum = excl;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (cum + c[i] >= rem) {
+          *digit = 255 - 8 * lane - i;
+          *above = cum;
+          break;
+        }
+        cum += c[i];
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Exclusive prefix sum of one value per thread over the CTA; *total gets the sum.
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nw ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += u;
+    }
+    if (lane < nw) warp_tot[lane] = wi - w;
+    if (lane == 31) warp_tot[32] = wi;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + incl - v;
   *total = warp_tot[32];
   __syncthreads();
   return r;
 }
 
-__global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(dsv4_indexer_topk_params p, const float* scores,
-                                                                int nc_stride) {
+// One CTA per token: exact choice of the remaining entries among the candidates (radix select on
+// the candidate values), then the selection written in increasing j through a bitmap over j.
+__global__ void __launch_bounds__(FINAL_THREADS) topk_final(dsv4_indexer_topk_params p, TopkBufs bufs) {
+  extern __shared__ uint64_t fsm[];
+  uint64_t* cand_s = fsm;                                           // CAND_CAP
+  uint32_t* bits = reinterpret_cast<uint32_t*>(fsm + CAND_CAP);    // nc_stride / 32 words
   const int t = blockIdx.x, tid = threadIdx.x;
   const int K = p.topk;
   const int n = visible_entries(p, t);
   int32_t* out = p.topk_idx + (int64_t)t * K;
   float* out_s = p.topk_score ? p.topk_score + (int64_t)t * K : nullptr;
-  const float* s = scores + (int64_t)t * nc_stride;
+  const float* s = bufs.scores + (int64_t)t * bufs.nc_stride;
 
   if (n <= K) {  // short context: every candidate, in order
-    for (int x = tid; x < K; x += TK_THREADS) {
+    for (int x = tid; x < K; x += FINAL_THREADS) {
       out[x] = x < n ? x : -1;
       if (out_s) out_s[x] = x < n ? s[x] : -INFINITY;
     }
     return;
   }
-
-  __shared__ unsigned int hist[256];
-  __shared__ unsigned int sh_prefix, sh_remaining;
+  __shared__ unsigned hist[256];
+  __shared__ unsigned long long sh_prefix;
+  __shared__ unsigned sh_rem, sh_above;
+  __shared__ int sh_digit;
   __shared__ int warp_tot[33];
-  uint32_t prefix = 0, mask = 0;
-  if (tid == 0) sh_remaining = K;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int x = tid; x < 256; x += TK_THREADS) hist[x] = 0;
-    __syncthreads();
-    for (int j = tid; j < n; j += TK_THREADS) {
-      const uint32_t u = order_key(s[j]);
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      unsigned int rem = sh_remaining, cum = 0;
-      int dsel = 0;
-      for (int dd = 255; dd >= 0; --dd) {
-        if (cum + hist[dd] >= rem) {
-          dsel = dd;
-          break;
-        }
-        cum += hist[dd];
+  const int words = (n + 31) >> 5;
+  for (int x = tid; x < words; x += FINAL_THREADS) bits[x] = 0u;
+  const int n_certain = (int)min(bufs.cnt[2 * t], (uint32_t)K);
+  const int m = (int)min(bufs.cnt[2 * t + 1], (uint32_t)bufs.nc_stride);
+  int need = K - n_certain;
+  if (need > m) {  // cannot happen with a complete histogram; keep the output valid
+    if (tid == 0) atomicOr(&g_flags_ix, FLAG_TOPK);
+    need = m;
+  }
+  const uint64_t* maybe_g = bufs.maybe + (int64_t)t * bufs.nc_stride;
+  const bool in_smem = m <= CAND_CAP;
+  if (in_smem)
+    for (int i = tid; i < m; i += FINAL_THREADS) cand_s[i] = maybe_g[i];
+  const uint64_t* cand = in_smem ? cand_s : maybe_g;
+  __syncthreads();
+  for (int x = tid; x < n_certain; x += FINAL_THREADS) {
+    const int j = bufs.certain[(int64_t)t * K + x];
+    if (j >= 0 && j < n) atomicOr(&bits[j >> 5], 1u << (j & 31));
+  }
+  if (need > 0) {
+    // radix select (8-bit digits over the 40-bit values) of the need-th largest candidate
+    unsigned long long prefix = 0, mask = 0;
+    if (tid == 0) sh_rem = (unsigned)need;
+    for (int shift = 32; shift >= 0; shift -= 8) {
+      for (int x = tid; x < 256; x += FINAL_THREADS) hist[x] = 0;
+      __syncthreads();
+      for (int i = tid; i < m; i += FINAL_THREADS) {
+        const unsigned long long v = cand[i];
+        if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255ull], 1u);
       }
-      sh_remaining = rem - cum;
-      sh_prefix = prefix | ((uint32_t)dsel << shift);
+      __syncthreads();
+      const unsigned rem = sh_rem;
+      pick_digit(hist, rem, &sh_digit, &sh_above);
+      if (tid == 0) {
+        sh_rem = rem - sh_above;
+        sh_prefix = prefix | ((unsigned long long)sh_digit << shift);
+      }
+      __syncthreads();
+      prefix = sh_prefix;
+      mask |= 255ull << shift;
     }
-    __syncthreads();
-    prefix = sh_prefix;
-    mask |= 255u << shift;
-  }
-  const uint32_t kth = prefix;             // key of the k-th largest score
-  const int need_eq = (int)sh_remaining;   // how many entries equal to it are taken (lowest j first)
-
-  int base_out = 0, base_eq = 0;
-  for (int j0 = 0; j0 < n; j0 += TK_THREADS) {
-    const int j = j0 + tid;
-    uint32_t u = 0;
-    if (j < n) u = order_key(s[j]);
-    const bool gt = j < n && u > kth;
-    const bool eq = j < n && u == kth;
-    int eq_tot;
-    const int eq_rank = block_excl_scan_flag(eq, warp_tot, &eq_tot);
-    const bool take = gt || (eq && base_eq + eq_rank < need_eq);
-    int take_tot;
-    const int pos = block_excl_scan_flag(take, warp_tot, &take_tot);
-    if (take) {
-      out[base_out + pos] = j;
-      if (out_s) out_s[base_out + pos] = s[j];
+    const unsigned long long kth = prefix;
+    for (int i = tid; i < m; i += FINAL_THREADS) {
+      const unsigned long long v = cand[i];
+      if (v >= kth) {
+        const int j = cand_j(v);
+        if (j < n) atomicOr(&bits[j >> 5], 1u << (j & 31));
+      }
     }
-    base_out += take_tot;
-    base_eq += eq_tot;
   }
-  for (int x = base_out + tid; x < K; x += TK_THREADS) {  // cannot happen when n > K; kept for safety
+  __syncthreads();
+  // compaction of the bitmap in increasing j
+  const int per = (words + FINAL_THREADS - 1) / FINAL_THREADS;
+  const int w0 = tid * per, w1 = min(words, w0 + per);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+  int total;
+  int pos = block_excl_scan(cnt, warp_tot, &total);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t b = bits[w];
+    while (b) {
+      const int j = (w << 5) + __ffs(b) - 1;
+      b &= b - 1;
+      if (pos < K) {
+        out[pos] = j;
+        if (out_s) out_s[pos] = s[j];
+      }
+      ++pos;
+    }
+  }
+  for (int x = total + tid; x < K; x += FINAL_THREADS) {
     out[x] = -1;
     if (out_s) out_s[x] = -INFINITY;
   }
@@ -536,22 +854,47 @@ __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(dsv4_indexer_top
 cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t st) {
   if (p.T == 0) return cudaSuccess;
   IxLayout L = ix_layout(p);
-  float* scores = reinterpret_cast<float*>(reinterpret_cast<char*>(p.workspace) + L.scores_off);
+  char* ws = reinterpret_cast<char*>(p.workspace);
+  TopkBufs bufs;
+  bufs.scores = reinterpret_cast<float*>(ws + L.scores_off);
+  bufs.hist = reinterpret_cast<uint32_t*>(ws + L.hist_off);
+  bufs.cnt = reinterpret_cast<uint32_t*>(ws + L.cnt_off);
+  bufs.certain = reinterpret_cast<int32_t*>(ws + L.certain_off);
+  bufs.maybe = reinterpret_cast<uint64_t*>(ws + L.maybe_off);
+  bufs.nc_stride = (int)L.nc_stride;
+  cudaError_t e = cudaMemsetAsync(ws + L.hist_off, 0, L.certain_off - L.hist_off, st);
+  if (e != cudaSuccess) return e;
   const int max_nc = p.max_context / p.ratio;
   if (max_nc > 0 && use_tc_indexer(p)) {
-    cudaError_t e = launch_indexer_score_tc(p, scores, (int)L.nc_stride, st);
+    e = launch_indexer_score_tc(p, bufs, st);
     if (e != cudaSuccess) return e;
   } else if (max_nc > 0) {
     const int tiles = (max_nc + IX_TILE - 1) / IX_TILE;
     const size_t smem = sizeof(float) * ((size_t)p.q_per_seq * p.n_heads * p.head_dim +
                                          (size_t)p.q_per_seq * p.n_heads + (size_t)(p.head_dim + 1) * (IX_TILE + 1));
-    cudaError_t e = cudaFuncSetAttribute(indexer_score_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(indexer_score_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    indexer_score_simt<<<dim3(tiles, p.B), IX_TILE, smem, st>>>(p, scores, (int)L.nc_stride);
+    indexer_score_simt<<<dim3(tiles, p.B), IX_TILE, smem, st>>>(p, bufs);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  topk_radix_kernel<<<p.T, TK_THREADS, 0, st>>>(p, scores, (int)L.nc_stride);
+  static int attr_done = 0;
+  const size_t csmem = (size_t)COLLECT_SLICE * (sizeof(uint64_t) + sizeof(int32_t));
+  const size_t fsmem = (size_t)CAND_CAP * sizeof(uint64_t) + L.nc_stride / 32 * sizeof(uint32_t);
+  if (!attr_done) {
+    e = cudaFuncSetAttribute(topk_collect, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_final, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_done = 1;
+  }
+  if (max_nc > p.topk) {
+    const int slices = (max_nc + COLLECT_SLICE - 1) / COLLECT_SLICE;
+    topk_collect<<<dim3(slices, p.T), COLLECT_THREADS, csmem, st>>>(p, bufs);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  topk_final<<<p.T, FINAL_THREADS, fsmem, st>>>(p, bufs);
   return cudaGetLastError();
 }
 

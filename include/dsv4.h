@@ -152,7 +152,8 @@ typedef struct dsv4_indexer_topk_params {
   int32_t max_pages_per_seq;
   const int32_t* positions;    /* [T] */
   int32_t T, B, q_per_seq, ratio, n_heads, head_dim, topk, page_size;
-  int32_t max_context;         /* host bound on positions[t] + 1 (sizes the workspace and grid) */
+  int32_t max_context;         /* host bound on positions[t] + 1 (sizes the workspace and grid);
+                                  max_context / ratio <= 2^20 compressed entries */
   int32_t* topk_idx;           /* [T, topk] output */
   float* topk_score;           /* [T, topk] output scores of topk_idx (-inf on padding) or NULL */
   void* workspace;             /* dsv4_indexer_topk_workspace_bytes() bytes, 256-byte aligned */

@@ -106,3 +106,27 @@ def test_bad_block_table_is_flagged_not_faulting(lib):
     assert M.dsv4_read_device_flags() & 1
     assert M.dsv4_read_device_flags() == 0       # flags clear after reading
     assert torch.isfinite(ds.out.float()).all()
+
+
+@pytest.mark.parametrize("mode", ["all_ties", "negative"])
+def test_topk_ties_and_negative_scores(lib, mode):
+    """Every score equal (zero head weights: the lowest indices must win) and all-negative scores."""
+    from deepseek_v4_hybrid_gb300.step import DeviceStep
+    import deepseek_v4_hybrid_gb300 as M
+    st = I.make_step(I.SMALL_CONFIGS["small_c4_bf16"])
+    if mode == "all_ties":
+        st.w_idx = np.zeros_like(st.w_idx)
+    else:
+        st.w_idx = -np.abs(st.w_idx) - 0.01
+    ds = DeviceStep(st)
+    ds.run()
+    torch.cuda.synchronize()
+    assert M.dsv4_read_device_flags() == 0
+    res = O.decode_step(st)
+    CMP.check_step(st, res, gpu_results(ds), where=mode)
+    if mode == "all_ties":
+        got = to_host(ds.topk_idx)
+        for t in range(st.cfg.T):
+            nc = O.n_compressed(int(st.positions[t]), st.cfg.ratio)
+            m = min(nc, st.cfg.topk)
+            assert np.array_equal(got[t][:m], np.arange(m))
