@@ -11,6 +11,8 @@
 // (an index outside [0, n_c(p)) is masked) or j = 0 .. n_c(p) - 1 when no list is given.
 #include "dsv4_common.cuh"
 #include "dsv4_launch.h"
+#include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace dsv4 {
 
@@ -33,9 +35,12 @@ static int max_rows(const dsv4_sparse_mla_decode_params& p) {
   return n_swa + n_cmp;
 }
 
+static bool use_tc_attention(const dsv4_sparse_mla_decode_params& p);
+constexpr int TC_CHUNK = 256;   // rows per CTA of the tensor-core kernel
+
 static AtLayout at_layout(const dsv4_sparse_mla_decode_params& p) {
   AtLayout L;
-  L.chunk_rows = AT_CH;
+  L.chunk_rows = use_tc_attention(p) ? TC_CHUNK : AT_CH;
   L.n_chunks = (max_rows(p) + L.chunk_rows - 1) / L.chunk_rows;
   if (L.n_chunks < 1) L.n_chunks = 1;
   const size_t parts = (size_t)p.T * L.n_chunks * p.H;
@@ -202,6 +207,373 @@ __global__ void __launch_bounds__(AT_THREADS) mla_partial_simt(dsv4_sparse_mla_d
   }
 }
 
+
+// ------------------------------------------------------------------------------------------------
+// Tensor-core partial kernel (bf16 caches and queries).  CTA = (chunk of 256 rows, token, 64-head
+// group x value half).  Heads are the MMA M dimension (M = 128, lanes 64..127 unused), rows the
+// N dimension of S = Q K^T (K = 576 in 9 K-blocks of 64 dims) and the K dimension of
+// O[:, half] += P V[:, half] (N = 256 value dims).
+//
+// Warp 2 (all lanes) gathers 64-row tiles with TMA: one 128-byte box per (row, K-block), 128-byte
+// swizzle, so any row order (window positions, top-k indices, dense runs) lands in the layout the
+// MMA reads; a masked row is loaded from past the end of the tensor, which TMA fills with zeros.
+// Lane 0 of warp 3 issues the MMAs; S goes to one of two TMEM buffers, P (bf16) is written back
+// to TMEM by the softmax warps and read from there as the A operand of the P V product; O stays in
+// TMEM for the whole chunk.  Warps 0-1 (one head per thread, TMEM lanes 0-63) run the online
+// softmax in the log2 domain with a lazy rescale (O is only rescaled when the running max grows
+// by more than 2^8), then write the unnormalised O and (max, sum) of the chunk.
+// ------------------------------------------------------------------------------------------------
+namespace attc {
+constexpr int TILE = 64;
+constexpr int HG = 64;
+constexpr int DVH = 256;
+constexpr int NKB = 9;
+constexpr int KB_BYTES = TILE * 128;          // 8 KB
+constexpr int STAGE_BYTES = NKB * KB_BYTES;   // 72 KB
+constexpr int Q_BYTES = NKB * HG * 128;       // 72 KB
+constexpr int STAGES = 2;
+constexpr int THREADS = 128;
+constexpr uint32_t COL_O = 0, COL_S = 256, COL_P = 384;  // S: 2 x 64 columns, P: 2 x 32 columns
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr uint32_t FLAG_TIMEOUT = 4u;
+
+struct Args {
+  dsv4_sparse_mla_decode_params p;
+  float* o_part;
+  float2* ml_part;
+  int n_chunks;
+  int swa_rows, main_rows;  // rows of the two tensor maps (a masked row loads from this index)
+  float c_log2;             // softmax_scale * log2(e)
+};
+
+struct Smem {
+  uint64_t full[STAGES], empty[STAGES], sfull[2], pfull[2], pvdone[2], qfull, odone;
+  uint64_t mask[STAGES];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// TMA row of entry r of token t's row list: (which map, row index); masked rows get the
+// out-of-range row of the map.
+__device__ __forceinline__ void row_source(const Args& a, int t, int b, int pos, int n_swa, int nc, int n_rows, int r,
+                                           int& use_main, int& y, bool& valid) {
+  const dsv4_sparse_mla_decode_params& p = a.p;
+  use_main = 0;
+  y = a.swa_rows;
+  valid = false;
+  if (r >= n_rows) return;
+  if (r < n_swa) {
+    const int q = pos - n_swa + 1 + r;
+    const int lp = q / p.page_size;
+    const int page = lp < p.swa_max_pages ? p.swa_block_table[(int64_t)b * p.swa_max_pages + lp] : -1;
+    if (page < 0 || page >= p.swa_num_pages) {
+      atomicOr(&g_flags_at, FLAG_PAGE);
+      return;
+    }
+    y = page * p.page_size + q % p.page_size;
+    valid = true;
+    return;
+  }
+  use_main = 1;
+  y = a.main_rows;
+  const int i = r - n_swa;
+  int j = i;
+  if (p.topk_idx != nullptr) {
+    j = p.topk_idx[(int64_t)t * p.topk + i];
+    if (j < 0) return;
+    if (j >= nc) {
+      atomicOr(&g_flags_at, FLAG_TOPK);
+      return;
+    }
+  }
+  const int lp = j / p.page_size;
+  const int page = lp < p.main_max_pages ? p.main_block_table[(int64_t)b * p.main_max_pages + lp] : -1;
+  if (page < 0 || page >= p.main_num_pages) {
+    atomicOr(&g_flags_at, FLAG_PAGE);
+    return;
+  }
+  y = page * p.page_size + j % p.page_size;
+  valid = true;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    mla_partial_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap swamap,
+                   const __grid_constant__ CUtensorMap mainmap, Args a) {
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_mem = base;                     // Q_BYTES (GEMM1 rows 64..127 read the next 8 KB: still smem)
+  uint8_t* stage_mem = base + Q_BYTES;       // STAGES x STAGE_BYTES
+  Smem* sm = reinterpret_cast<Smem*>(stage_mem + STAGES * STAGE_BYTES);
+  volatile int* abort = &sm->abort;
+
+  const dsv4_sparse_mla_decode_params& p = a.p;
+  const int chunk = blockIdx.x, t = blockIdx.y;
+  const int hg = blockIdx.z >> 1, dh = blockIdx.z & 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = t / p.q_per_seq;
+  int pos = p.positions[t];
+  int n_swa, nc, n_cmp;
+  token_rows(p, pos, n_swa, nc, n_cmp);
+  const int n_rows = n_swa + n_cmp;
+  const int r0 = chunk * TC_CHUNK;
+  const int rows = min(TC_CHUNK, n_rows - r0);
+  const int64_t part = ((int64_t)t * a.n_chunks + chunk) * p.H + hg * HG;
+  if (rows <= 0) {  // block-uniform: an empty chunk contributes nothing
+    if (dh == 0 && threadIdx.x < HG) a.ml_part[part + threadIdx.x] = make_float2(-INFINITY, 0.f);
+    return;
+  }
+  const int ntiles = (rows + TILE - 1) / TILE;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&sm->full[s], 1);
+      tc::mbar_init(&sm->empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sm->sfull[i], 1);
+      tc::mbar_init(&sm->pfull[i], 2);
+      tc::mbar_init(&sm->pvdone[i], 1);
+    }
+    tc::mbar_init(&sm->qfull, 1);
+    tc::mbar_init(&sm->odone, 1);
+    sm->abort = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 3) {
+    tc::tmem_alloc(&sm->tmem_base, TMEM_COLS);
+    tc::tmem_relinquish();
+    tc::tc_fence_before();
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == 2) {
+    // ---------------- producer: Q once, then 64-row tiles (lane l gathers rows l and l + 32)
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&qmap);
+      tc::tma_prefetch_desc(&swamap);
+      tc::tma_prefetch_desc(&mainmap);
+      tc::mbar_arrive_expect_tx(&sm->qfull, Q_BYTES);
+      for (int kb = 0; kb < NKB; ++kb)
+        tc::tma_load_2d(q_mem + kb * HG * 128, &qmap, kb * 64, t * p.H + hg * HG, &sm->qfull);
+    }
+    int um0, y0, um1, y1;
+    bool v0, v1;
+    row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + lane, um0, y0, v0);
+    row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + lane + 32, um1, y1, v1);
+    for (int i = 0; i < ntiles; ++i) {
+      const int stage = i % STAGES;
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait_bounded(&sm->empty[stage], ((i / STAGES) & 1) ^ 1, abort);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      // rows beyond the chunk are masked (zero rows)
+      const bool in0 = i * TILE + lane < rows, in1 = i * TILE + lane + 32 < rows;
+      const bool m0 = v0 && in0, m1 = v1 && in1;
+      if (!in0) y0 = um0 ? a.main_rows : a.swa_rows;
+      if (!in1) y1 = um1 ? a.main_rows : a.swa_rows;
+      const unsigned b0 = __ballot_sync(0xffffffffu, m0), b1 = __ballot_sync(0xffffffffu, m1);
+      uint8_t* st = stage_mem + stage * STAGE_BYTES;
+      if (lane == 0) {
+        sm->mask[stage] = (uint64_t)b0 | ((uint64_t)b1 << 32);
+        tc::mbar_arrive_expect_tx(&sm->full[stage], (uint32_t)TILE * NKB * 128);
+      }
+      __syncwarp();
+      const CUtensorMap* map0 = um0 ? &mainmap : &swamap;
+      const CUtensorMap* map1 = um1 ? &mainmap : &swamap;
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb) {
+        tc::tma_load_2d(st + kb * KB_BYTES + lane * 128, map0, kb * 64, y0, &sm->full[stage]);
+        tc::tma_load_2d(st + kb * KB_BYTES + (lane + 32) * 128, map1, kb * 64, y1, &sm->full[stage]);
+      }
+      // look up the next tile's rows while this one is in flight
+      if (i + 1 < ntiles) {
+        row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + (i + 1) * TILE + lane, um0, y0, v0);
+        row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + (i + 1) * TILE + lane + 32, um1, y1, v1);
+      }
+    }
+    if (lane == 0) {
+      // every issued load lands before the CTA may exit
+      tc::mbar_wait_bounded(&sm->qfull, 0, abort, 100000000ull);
+      for (int i = (ntiles > STAGES ? ntiles - STAGES : 0); i < ntiles; ++i)
+        tc::mbar_wait_bounded(&sm->full[i % STAGES], (i / STAGES) & 1, abort, 100000000ull);
+    }
+  } else if (warp == 3) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      const uint32_t idesc_s = tc::idesc_bf16_f32(128, TILE);
+      const uint32_t idesc_o = tc::idesc_bf16_f32_bmn(128, DVH);
+      const uint32_t q_addr = tc::smem_addr(q_mem);
+      bool ok = tc::mbar_wait_bounded(&sm->qfull, 0, abort);
+      auto pv = [&](int j) -> bool {
+        if (!tc::mbar_wait_bounded(&sm->pfull[j & 1], (j >> 1) & 1, abort)) return false;
+        tc::tc_fence_after();
+        const uint32_t v_addr = tc::smem_addr(stage_mem + (j % STAGES) * STAGE_BYTES + (4 * dh) * KB_BYTES);
+#pragma unroll
+        for (int s = 0; s < TILE / 16; ++s) {
+          const uint64_t bd = tc::sdesc_mn_sw128(v_addr + s * 2048, KB_BYTES, 1024);
+          tc::mma_bf16_ts(tmem + COL_O, tmem + COL_P + (j & 1) * 32 + s * 8, bd, idesc_o, (j > 0 || s > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&sm->empty[j % STAGES]);
+        tc::mma_commit(&sm->pvdone[j & 1]);
+        return true;
+      };
+      for (int i = 0; ok && i < ntiles; ++i) {
+        const int stage = i % STAGES;
+        if (!tc::mbar_wait_bounded(&sm->full[stage], (i / STAGES) & 1, abort)) break;
+        tc::tc_fence_after();
+        const uint32_t k_addr = tc::smem_addr(stage_mem + stage * STAGE_BYTES);
+        for (int kb = 0; kb < NKB; ++kb) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint64_t ad = tc::sdesc_k_sw128(q_addr + kb * HG * 128 + s * 32);
+            const uint64_t bd = tc::sdesc_k_sw128(k_addr + kb * KB_BYTES + s * 32);
+            tc::mma_bf16(tmem + COL_S + (i & 1) * TILE, ad, bd, idesc_s, (kb | s) != 0);
+          }
+        }
+        tc::mma_commit(&sm->sfull[i & 1]);
+        if (i >= 1 && !pv(i - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok && !*abort) pv(ntiles - 1);
+      tc::mma_commit(&sm->odone);
+    }
+  } else {
+    // ---------------- softmax + epilogue: warps 0-1, thread = head (TMEM lane)
+    const int h = warp * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < ntiles; ++i) {
+      if (!tc::mbar_wait_bounded(&sm->sfull[i & 1], (i >> 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      // the stage's row mask was published with its full barrier
+      tc::mbar_wait_bounded(&sm->full[i % STAGES], (i / STAGES) & 1, abort);
+      tc::tc_fence_after();
+      uint32_t r[64];
+      tc::tmem_ld32_nowait(lane_base + COL_S + (i & 1) * TILE, r);
+      tc::tmem_ld32_nowait(lane_base + COL_S + (i & 1) * TILE + 32, r + 32);
+      tc::tmem_wait_ld_regs<64>(r);
+      const uint64_t mask = sm->mask[i % STAGES];
+      float z[64];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        z[k] = ((mask >> k) & 1ull) ? __uint_as_float(r[k]) * a.c_log2 : -INFINITY;
+        mt = fmaxf(mt, z[k]);
+      }
+      const float m_new = fmaxf(m_ref, mt);
+      if (m_ref == -INFINITY) {
+        m_ref = m_new;  // nothing accumulated yet that is not zero
+      } else if (m_new > m_ref + RESCALE_LOG2) {
+        // O must be stable (the previous P V done) before it is rescaled in place
+        if (!tc::mbar_wait_bounded(&sm->pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const float f = exp2f(m_ref - m_new);
+        l *= f;
+        for (int c = 0; c < DVH; c += 32) {
+          uint32_t o[32];
+          tc::tmem_ld32_nowait(lane_base + COL_O + c, o);
+          tc::tmem_wait_ld_regs<32>(o);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+          tc::tmem_st32(lane_base + COL_O + c, o);
+        }
+        tc::tmem_wait_st();
+        m_ref = m_new;
+      }
+      uint32_t pk[32];
+      float ls = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float e0 = (m_ref == -INFINITY) ? 0.f : exp2f(z[2 * k] - m_ref);
+        const float e1 = (m_ref == -INFINITY) ? 0.f : exp2f(z[2 * k + 1] - m_ref);
+        ls += e0 + e1;
+        pk[k] = float2_to_bf16x2_bits(e0, e1);
+      }
+      l += ls;
+      // P buffer (i & 1) was last read by the P V product of tile i - 2
+      if (i >= 2 && !tc::mbar_wait_bounded(&sm->pvdone[i & 1], ((i - 2) >> 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      tc::tmem_st32(lane_base + COL_P + (i & 1) * 32, pk);
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm->pfull[i & 1]);
+    }
+    if (ok && tc::mbar_wait_bounded(&sm->odone, 0, abort)) {
+      tc::tc_fence_after();
+      float* dst = a.o_part + (part + h) * DV + dh * DVH;
+      for (int c = 0; c < DVH; c += 32) {
+        uint32_t o[32];
+        tc::tmem_ld32_nowait(lane_base + COL_O + c, o);
+        tc::tmem_wait_ld_regs<32>(o);
+#pragma unroll
+        for (int k = 0; k < 32; k += 4)
+          *reinterpret_cast<float4*>(dst + c + k) = make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]),
+                                                                 __uint_as_float(o[k + 2]), __uint_as_float(o[k + 3]));
+      }
+      if (dh == 0) a.ml_part[part + h] = make_float2(m_ref * 0.69314718055994531f, l);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && sm->abort) atomicOr(&g_flags_at, FLAG_TIMEOUT);
+  if (warp == 3) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+}  // namespace attc
+
+static bool use_tc_attention(const dsv4_sparse_mla_decode_params& p) {
+  return p.cache_dtype == DSV4_BF16 && p.q_dtype == DSV4_BF16 && p.H % attc::HG == 0 && p.page_size == 64;
+}
+
+static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p, const AtLayout& L, float* o_part,
+                                         float2* ml_part, cudaStream_t st) {
+  using namespace attc;
+  Args a;
+  a.p = p;
+  a.o_part = o_part;
+  a.ml_part = ml_part;
+  a.n_chunks = L.n_chunks;
+  a.swa_rows = (int)(p.swa_num_pages * p.page_size);
+  a.main_rows = p.ratio > 0 ? (int)(p.main_num_pages * p.page_size) : a.swa_rows;
+  a.c_log2 = p.softmax_scale * 1.4426950408889634f;
+  CUtensorMap qmap, swamap, mainmap;
+  cudaError_t e = make_tmap_2d_bf16(&qmap, p.q, (uint64_t)D, (uint64_t)p.T * p.H, 64, HG);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_2d_bf16(&swamap, p.swa_cache, (uint64_t)D, (uint64_t)a.swa_rows, 64, 1);
+  if (e != cudaSuccess) return e;
+  if (p.ratio > 0) {
+    e = make_tmap_2d_bf16(&mainmap, p.main_cache, (uint64_t)D, (uint64_t)a.main_rows, 64, 1);
+    if (e != cudaSuccess) return e;
+  } else {
+    mainmap = swamap;
+  }
+  const size_t smem = 1024 + (size_t)Q_BYTES + (size_t)STAGES * STAGE_BYTES + sizeof(Smem);
+  static int attr_done = 0;
+  if (!attr_done) {
+    e = cudaFuncSetAttribute(mla_partial_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = 1;
+  }
+  dim3 grid(L.n_chunks, p.T, (p.H / HG) * 2);
+  mla_partial_tc<<<grid, THREADS, smem, st>>>(qmap, swamap, mainmap, a);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------------------------------------
 // Merge of the chunk partials (m_c, l_c, unnormalised O_c) with the sink: CTA per (token, head).
 // ------------------------------------------------------------------------------------------------
@@ -238,13 +610,19 @@ cudaError_t launch_sparse_mla_decode(const dsv4_sparse_mla_decode_params& p, cud
   char* ws = reinterpret_cast<char*>(p.workspace);
   float* o_part = reinterpret_cast<float*>(ws + L.o_off);
   float2* ml_part = reinterpret_cast<float2*>(ws + L.ml_off);
-  const size_t smem = sizeof(float) * ((size_t)AT_HG * D + (size_t)AT_CH * (D + 1) + (size_t)AT_HG * AT_CH);
-  cudaError_t e = cudaFuncSetAttribute(mla_partial_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  mla_partial_simt<<<dim3(L.n_chunks, p.T, (p.H + AT_HG - 1) / AT_HG), AT_THREADS, smem, st>>>(p, o_part, ml_part,
-                                                                                                 L.n_chunks);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if (use_tc_attention(p)) {
+    e = launch_mla_partial_tc(p, L, o_part, ml_part, st);
+    if (e != cudaSuccess) return e;
+  } else {
+    const size_t smem = sizeof(float) * ((size_t)AT_HG * D + (size_t)AT_CH * (D + 1) + (size_t)AT_HG * AT_CH);
+    e = cudaFuncSetAttribute(mla_partial_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    mla_partial_simt<<<dim3(L.n_chunks, p.T, (p.H + AT_HG - 1) / AT_HG), AT_THREADS, smem, st>>>(p, o_part, ml_part,
+                                                                                                   L.n_chunks);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   mla_merge<<<dim3(p.T, p.H), MERGE_THREADS, 0, st>>>(p, o_part, ml_part, L.n_chunks);
   return cudaGetLastError();
 }
