@@ -240,6 +240,10 @@ def run_ours(args):
         flush.fill_(1.0)
         ds.run()
     torch.cuda.synchronize()
+    import deepseek_v4_hybrid_gb300 as M
+    flags = M.dsv4_read_device_flags()
+    if flags:
+        raise SystemExit(f"kernels raised range/timeout flags {flags:#x} during warm-up; not timing")
     topk_host = ds.topk_idx.cpu().numpy() if ds.has_indexer else None
     alg = algorithmic_bytes(st, topk_host)
 

@@ -214,10 +214,10 @@ __global__ void __launch_bounds__(AT_THREADS) mla_partial_simt(dsv4_sparse_mla_d
 // N dimension of S = Q K^T (K = 576 in 9 K-blocks of 64 dims) and the K dimension of
 // O[:, half] += P V[:, half] (N = 256 value dims).
 //
-// Warp 2 (all lanes) gathers 64-row tiles with TMA: one 128-byte box per (row, K-block), 128-byte
-// swizzle, so any row order (window positions, top-k indices, dense runs) lands in the layout the
-// MMA reads; a masked row is loaded from past the end of the tensor, which TMA fills with zeros.
-// Lane 0 of warp 3 issues the MMAs; S goes to one of two TMEM buffers, P (bf16) is written back
+// Warps 2 and 3 gather 64-row tiles with 16-byte cp.async copies written straight into the 128-byte
+// swizzled K-major layout the MMA reads (one copy instruction = 4 rows x 128 bytes), so any row
+// order (window positions, top-k indices, dense runs) works; a masked row is zero-filled.  Q comes
+// by TMA.  Lane 0 of warp 4 issues the MMAs; S goes to one of two TMEM buffers, P (bf16) is written back
 // to TMEM by the softmax warps and read from there as the A operand of the P V product; O stays in
 // TMEM for the whole chunk.  Warps 0-1 (one head per thread, TMEM lanes 0-63) run the online
 // softmax in the log2 domain with a lazy rescale (O is only rescaled when the running max grows
@@ -232,7 +232,7 @@ constexpr int KB_BYTES = TILE * 128;          // 8 KB
 constexpr int STAGE_BYTES = NKB * KB_BYTES;   // 72 KB
 constexpr int Q_BYTES = NKB * HG * 128;       // 72 KB
 constexpr int STAGES = 2;
-constexpr int THREADS = 128;
+constexpr int THREADS = 160;  // warps 0-1 softmax, 2-3 producers, 4 MMA
 constexpr uint32_t COL_O = 0, COL_S = 256, COL_P = 384;  // S: 2 x 64 columns, P: 2 x 32 columns
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      tc::mbar_init(&sm->full[s], 1);
+      tc::mbar_init(&sm->full[s], 32);  // every producer lane arrives once its copies have landed
       tc::mbar_init(&sm->empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     sm->abort = 0;
     tc::fence_barrier_init();
   }
-  if (warp == 3) {
+  if (warp == 4) {
     tc::tmem_alloc(&sm->tmem_base, TMEM_COLS);
     tc::tmem_relinquish();
     tc::tc_fence_before();
@@ -349,58 +349,69 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc::tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
 
-  if (warp == 2) {
-    // ---------------- producer: Q once, then 64-row tiles (lane l gathers rows l and l + 32)
-    if (lane == 0) {
+  if (warp == 2 || warp == 3) {
+    // ---------------- producers: warp 2 loads Q by TMA and the even tiles, warp 3 the odd tiles
+    // (tile i always uses stage i % 2), each tile by 16-byte cp.async copies; a warp publishes its
+    // tile as soon as the copies have landed, so no tile's issue waits on another's publication.
+    const int wp = warp - 2;
+    if (wp == 0 && lane == 0) {
       tc::tma_prefetch_desc(&qmap);
-      tc::tma_prefetch_desc(&swamap);
-      tc::tma_prefetch_desc(&mainmap);
       tc::mbar_arrive_expect_tx(&sm->qfull, Q_BYTES);
       for (int kb = 0; kb < NKB; ++kb)
         tc::tma_load_2d(q_mem + kb * HG * 128, &qmap, kb * 64, t * p.H + hg * HG, &sm->qfull);
     }
-    int um0, y0, um1, y1;
-    bool v0, v1;
-    row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + lane, um0, y0, v0);
-    row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + lane + 32, um1, y1, v1);
-    for (int i = 0; i < ntiles; ++i) {
+    const uint8_t* swa_base = reinterpret_cast<const uint8_t*>(p.swa_cache);
+    const uint8_t* main_base = p.ratio > 0 ? reinterpret_cast<const uint8_t*>(p.main_cache) : swa_base;
+    // lane l owns rows l and l + 32 of a tile; source row pointers (nullptr = masked row)
+    auto row_ptr = [&](int r) -> const uint8_t* {
+      int um, y;
+      bool v;
+      row_source(a, t, b, pos, n_swa, nc, n_rows, r, um, y, v);
+      if (!v || r >= r0 + rows) return nullptr;
+      return (um ? main_base : swa_base) + (int64_t)y * (D * 2);
+    };
+    const int sub = lane >> 3, chunk16 = lane & 7;  // a copy instruction covers 4 rows x 128 bytes
+    const uint8_t* ptr0 = nullptr;
+    const uint8_t* ptr1 = nullptr;
+    if (wp < ntiles) {
+      ptr0 = row_ptr(r0 + wp * TILE + lane);
+      ptr1 = row_ptr(r0 + wp * TILE + lane + 32);
+    }
+    for (int i = wp; i < ntiles; i += STAGES) {
       const int stage = i % STAGES;
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait_bounded(&sm->empty[stage], ((i / STAGES) & 1) ^ 1, abort);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      // rows beyond the chunk are masked (zero rows)
-      const bool in0 = i * TILE + lane < rows, in1 = i * TILE + lane + 32 < rows;
-      const bool m0 = v0 && in0, m1 = v1 && in1;
-      if (!in0) y0 = um0 ? a.main_rows : a.swa_rows;
-      if (!in1) y1 = um1 ? a.main_rows : a.swa_rows;
-      const unsigned b0 = __ballot_sync(0xffffffffu, m0), b1 = __ballot_sync(0xffffffffu, m1);
+      const unsigned b0 = __ballot_sync(0xffffffffu, ptr0 != nullptr);
+      const unsigned b1 = __ballot_sync(0xffffffffu, ptr1 != nullptr);
+      if (lane == 0) sm->mask[stage] = (uint64_t)b0 | ((uint64_t)b1 << 32);
       uint8_t* st = stage_mem + stage * STAGE_BYTES;
-      if (lane == 0) {
-        sm->mask[stage] = (uint64_t)b0 | ((uint64_t)b1 << 32);
-        tc::mbar_arrive_expect_tx(&sm->full[stage], (uint32_t)TILE * NKB * 128);
-      }
-      __syncwarp();
-      const CUtensorMap* map0 = um0 ? &mainmap : &swamap;
-      const CUtensorMap* map1 = um1 ? &mainmap : &swamap;
+#pragma unroll 4
+      for (int rg = 0; rg < TILE / 4; ++rg) {
+        const int row = rg * 4 + sub;
+        const uint8_t* lo = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, (unsigned long long)ptr0, row & 31));
+        const uint8_t* hi = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, (unsigned long long)ptr1, row & 31));
+        const uint8_t* src = row < 32 ? lo : hi;
+        const uint32_t nbytes = src != nullptr ? 16u : 0u;
+        if (src == nullptr) src = swa_base;  // any valid address; nothing is read
+        uint8_t* dst = st + row * 128 + ((chunk16 ^ (row & 7)) << 4);
 #pragma unroll
-      for (int kb = 0; kb < NKB; ++kb) {
-        tc::tma_load_2d(st + kb * KB_BYTES + lane * 128, map0, kb * 64, y0, &sm->full[stage]);
-        tc::tma_load_2d(st + kb * KB_BYTES + (lane + 32) * 128, map1, kb * 64, y1, &sm->full[stage]);
+        for (int kb = 0; kb < NKB; ++kb)
+          tc::cp_async16(dst + kb * KB_BYTES, src + (nbytes ? kb * 128 + chunk16 * 16 : 0), nbytes);
       }
-      // look up the next tile's rows while this one is in flight
-      if (i + 1 < ntiles) {
-        row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + (i + 1) * TILE + lane, um0, y0, v0);
-        row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + (i + 1) * TILE + lane + 32, um1, y1, v1);
+      tc::cp_async_commit();
+      if (i + STAGES < ntiles) {  // look up this warp's next tile while the copies are in flight
+        ptr0 = row_ptr(r0 + (i + STAGES) * TILE + lane);
+        ptr1 = row_ptr(r0 + (i + STAGES) * TILE + lane + 32);
       }
+      tc::cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&sm->full[stage]);
     }
-    if (lane == 0) {
-      // every issued load lands before the CTA may exit
-      tc::mbar_wait_bounded(&sm->qfull, 0, abort, 100000000ull);
-      for (int i = (ntiles > STAGES ? ntiles - STAGES : 0); i < ntiles; ++i)
-        tc::mbar_wait_bounded(&sm->full[i % STAGES], (i / STAGES) & 1, abort, 100000000ull);
-    }
-  } else if (warp == 3) {
+    tc::cp_async_wait<0>();
+    if (wp == 0 && lane == 0) tc::mbar_wait_bounded(&sm->qfull, 0, abort, 100000000ull);  // Q landed before exit
+  } else if (warp == 4) {
     if (lane == 0) {
       // ---------------- MMA issuer
       const uint32_t idesc_s = tc::idesc_bf16_f32(128, TILE);
@@ -529,7 +540,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   __syncthreads();
   if (threadIdx.x == 0 && sm->abort) atomicOr(&g_flags_at, FLAG_TIMEOUT);
-  if (warp == 3) {
+  if (warp == 4) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }

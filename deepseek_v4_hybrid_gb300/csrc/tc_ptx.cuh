@@ -54,7 +54,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Waits for the phase of `parity` to complete.  Gives up after `limit_ns` (or at once when *abort
 // is already set): then raises *abort and returns false, so every role of the kernel drains out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  uint64_t limit_ns = 2000000000ull) {
+                                                  uint64_t limit_ns = 250000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -221,6 +221,23 @@ __device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo,
 
 // kind::f16 instruction descriptor with bf16 A (K-major), bf16 B (MN-major), fp32 D, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) { return idesc_bf16_f32(M, N) | (1u << 16); }
+
+
+// ---------------------------------------------------------------------------------------------
+// cp.async (16-byte global -> shared copies) feeding tcgen05 operands
+// ---------------------------------------------------------------------------------------------
+// Copies 16 bytes, or writes 16 zero bytes when `src_bytes` is 0.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy (tcgen05) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 }  // namespace tc
 }  // namespace dsv4
