@@ -249,7 +249,23 @@ def run_ours(args):
 
     calls = ["insert", "compress", "indexer", "attention"]
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    # the step (and each call alone) captured once as a CUDA graph: the library never synchronises,
+    # so the four calls replay with no host launch gaps
+    graph_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_step):
+        ds.run()
+    graph_call = {}
+    for c in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            getattr(ds, c)()
+        graph_call[c] = g
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        flush.fill_(1.0)
+        graph_step.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler = ClockSampler(local)
     if world > 1:
         dist.barrier()
@@ -259,35 +275,36 @@ def run_ours(args):
     wall0 = time.perf_counter()
     for k in range(K):
         flush.fill_(float(k))
-        e = ev[k]
-        e[0].record(stream)
-        ds.insert()
-        e[1].record(stream)
-        ds.compress()
-        e[2].record(stream)
-        ds.indexer()
-        e[3].record(stream)
-        ds.attention()
-        e[4].record(stream)
+        ev[k][0].record(stream)
+        graph_step.replay()
+        ev[k][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    per_call = {c: 0.0 for c in calls}
-    total_ms = 0.0
-    for e in ev:
-        total_ms += e[0].elapsed_time(e[4])
-        for i, c in enumerate(calls):
-            per_call[c] += e[i].elapsed_time(e[i + 1])
+    total_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     ms_per_step = total_ms / K
+    # per-call breakdown (each call's graph timed alone, same flushing)
+    Kc = min(K, 200)
+    per_call = {c: 0.0 for c in calls}
+    for k in range(Kc):
+        flush.fill_(float(k))
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        evs[0].record(stream)
+        for i, c in enumerate(calls):
+            graph_call[c].replay()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        for i, c in enumerate(calls):
+            per_call[c] += evs[i].elapsed_time(evs[i + 1])
     if world > 1:
         tt = torch.tensor([ms_per_step], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_per_step = float(tt.item())
     tokens = cfg.T * world
     value = tokens / (ms_per_step * 1e-3)
-    per_call_us = {c: 1e3 * v / K for c, v in per_call.items()}
+    per_call_us = {c: 1e3 * v / Kc for c, v in per_call.items()}
 
     # ---- end to end through host buffers: pinned H2D of the step's inputs, step, D2H of results
     host_in = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in ds.step_input_tensors().items()}

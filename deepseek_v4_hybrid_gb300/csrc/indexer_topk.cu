@@ -96,6 +96,8 @@ __device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool
 // ------------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_params p, TopkBufs bufs) {
   extern __shared__ float smem[];
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.y, tile = blockIdx.x, jj = threadIdx.x;
   const int Ih = p.n_heads, d = p.head_dim, qps = p.q_per_seq;
   const int t0 = b * qps;
@@ -195,7 +197,7 @@ struct Args {
 };
 
 struct Smem {
-  uint64_t full[MAX_STAGES], empty[MAX_STAGES], dfull[4], dempty[4], qfull[2], qempty[2], done;
+  uint64_t full[MAX_STAGES], empty[MAX_STAGES], dfull[4], dempty[4], qfull[2], qempty[2], done, ebar;
   uint32_t tmem_base;
   int abort;
 };
@@ -246,9 +248,11 @@ struct ItemIter {
   __device__ __forceinline__ bool valid() const { return it < hi; }
 };
 
-// Adds the shared histogram of sequence b (if any) to the global one and clears it.
-__device__ __forceinline__ void flush_hist(const Args& a, uint32_t* hist_s, int b, int row) {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+// Adds the shared histogram of sequence b (if any) to the global one and clears it (the four
+// epilogue warps, with bounded group barriers before and after).
+__device__ __forceinline__ bool flush_hist(const Args& a, uint32_t* hist_s, int b, int row, uint64_t* ebar,
+                                           uint32_t* ephase, volatile int* abort) {
+  if (!tc::group_sync(ebar, ephase, abort)) return false;
   if (b >= 0) {
     for (int x = row; x < a.qps * HIST_BINS; x += 128) {
       const uint32_t v = hist_s[x];
@@ -258,7 +262,7 @@ __device__ __forceinline__ void flush_hist(const Args& a, uint32_t* hist_s, int 
       }
     }
   }
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  return tc::group_sync(ebar, ephase, abort);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -293,6 +297,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_init(&sm->qempty[i], 1);
     }
     tc::mbar_init(&sm->done, 1);
+    tc::mbar_init(&sm->ebar, 4);
     sm->abort = 0;
     tc::fence_barrier_init();
   }
@@ -302,6 +307,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tmem_relinquish();
     tc::tc_fence_before();
   }
+  pdl_launch_dependents();
+  pdl_wait();  // the prologue above overlaps the previous kernel
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
@@ -431,19 +438,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- epilogue: warps 0-3, thread = key row (TMEM lane)
     const int row = warp * 32 + lane;
     int acc = 0, cur_b = -1;
-    uint32_t aphase = 0;
+    uint32_t aphase = 0, ephase = 0;
     int nc_tok[DSV4_MAX_Q_PER_SEQ] = {0, 0, 0, 0};
     ItemIter cur;
     cur.init(a, lo, hi);
     for (; cur.valid(); cur.next(a)) {
       const int b = cur.b;
       if (b != cur_b) {
-        flush_hist(a, hist_s, cur_b, row);
+        if (!flush_hist(a, hist_s, cur_b, row, &sm->ebar, &ephase, abort)) break;
         for (int x = row; x < a.N; x += 128) w_s[x] = a.weights[(int64_t)b * a.qps * a.Ih + x];
 #pragma unroll
         for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q)
           nc_tok[q] = q < a.qps ? visible_entries(a.positions, b * a.qps + q, a.max_context, a.ratio) : 0;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (!tc::group_sync(&sm->ebar, &ephase, abort)) break;
         cur_b = b;
       }
       if (!tc::mbar_wait_bounded(&sm->dfull[acc], aphase, abort)) break;
@@ -503,7 +510,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         aphase ^= 1;
       }
     }
-    flush_hist(a, hist_s, cur_b, row);
+    flush_hist(a, hist_s, cur_b, row, &sm->ebar, &ephase, abort);
   }
   __syncthreads();
   if (threadIdx.x == 0 && sm->abort) atomicOr(&g_flags_ix, FLAG_TIMEOUT);
@@ -565,8 +572,7 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   int grid = num_sms();
   if (grid > total) grid = total;
   if (grid <= 0) return cudaSuccess;
-  indexer_score_tc<<<grid, THREADS, smem, st>>>(kmap, qmap, a);
-  return cudaGetLastError();
+  return launch_pdl(indexer_score_tc, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/false, kmap, qmap, a);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -640,6 +646,8 @@ __device__ __forceinline__ void warp_append_smem(unsigned* cnt, T* list, T val, 
 // global lists with one atomic each.
 __global__ void __launch_bounds__(COLLECT_THREADS) topk_collect(dsv4_indexer_topk_params p, TopkBufs bufs) {
   extern __shared__ uint64_t csm[];
+  pdl_launch_dependents();
+  pdl_wait();
   uint64_t* maybe_s = csm;                                        // COLLECT_SLICE
   int32_t* cert_s = reinterpret_cast<int32_t*>(csm + COLLECT_SLICE);  // COLLECT_SLICE
   __shared__ unsigned n_cert, n_maybe, base_cert, base_maybe;
@@ -754,6 +762,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
 // the candidate values), then the selection written in increasing j through a bitmap over j.
 __global__ void __launch_bounds__(FINAL_THREADS) topk_final(dsv4_indexer_topk_params p, TopkBufs bufs) {
   extern __shared__ uint64_t fsm[];
+  pdl_launch_dependents();
+  pdl_wait();
   uint64_t* cand_s = fsm;                                           // CAND_CAP
   uint32_t* bits = reinterpret_cast<uint32_t*>(fsm + CAND_CAP);    // nc_stride / 32 words
   const int t = blockIdx.x, tid = threadIdx.x;
@@ -874,8 +884,7 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
                                          (size_t)p.q_per_seq * p.n_heads + (size_t)(p.head_dim + 1) * (IX_TILE + 1));
     e = cudaFuncSetAttribute(indexer_score_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    indexer_score_simt<<<dim3(tiles, p.B), IX_TILE, smem, st>>>(p, bufs);
-    e = cudaGetLastError();
+    e = launch_pdl(indexer_score_simt, dim3(tiles, p.B), dim3(IX_TILE), smem, st, /*pdl=*/false, p, bufs);
     if (e != cudaSuccess) return e;
   }
   static int attr_done = 0;
@@ -890,12 +899,10 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
   }
   if (max_nc > p.topk) {
     const int slices = (max_nc + COLLECT_SLICE - 1) / COLLECT_SLICE;
-    topk_collect<<<dim3(slices, p.T), COLLECT_THREADS, csmem, st>>>(p, bufs);
-    e = cudaGetLastError();
+    e = launch_pdl(topk_collect, dim3(slices, p.T), dim3(COLLECT_THREADS), csmem, st, /*pdl=*/false, p, bufs);
     if (e != cudaSuccess) return e;
   }
-  topk_final<<<p.T, FINAL_THREADS, fsmem, st>>>(p, bufs);
-  return cudaGetLastError();
+  return launch_pdl(topk_final, dim3(p.T), dim3(FINAL_THREADS), fsmem, st, /*pdl=*/false, p, bufs);
 }
 
 cudaError_t read_flags_indexer(uint32_t* f) {
