@@ -37,11 +37,22 @@ static int max_rows(const dsv4_sparse_mla_decode_params& p) {
 }
 
 static bool use_tc_attention(const dsv4_sparse_mla_decode_params& p);
-constexpr int TC_CHUNK = 256;   // rows per CTA of the tensor-core kernel
+
+// Rows per CTA of the tensor-core kernel: about one wave of CTAs over the SMs (each (token, head
+// group) has two CTAs, one per value half), in whole 64-row tiles.
+static int tc_chunk_rows(const dsv4_sparse_mla_decode_params& p) {
+  const int per_chunk = p.T * (p.H / 64) * 2;
+  int n = per_chunk > 0 ? num_sms() / per_chunk : 1;
+  if (n < 1) n = 1;
+  const int rows = max_rows(p);
+  int c = (rows + n - 1) / n;
+  c = (c + 63) / 64 * 64;
+  return c < 64 ? 64 : c;
+}
 
 static AtLayout at_layout(const dsv4_sparse_mla_decode_params& p) {
   AtLayout L;
-  L.chunk_rows = use_tc_attention(p) ? TC_CHUNK : AT_CH;
+  L.chunk_rows = use_tc_attention(p) ? tc_chunk_rows(p) : AT_CH;
   L.n_chunks = (max_rows(p) + L.chunk_rows - 1) / L.chunk_rows;
   if (L.n_chunks < 1) L.n_chunks = 1;
   const size_t parts = (size_t)p.T * L.n_chunks * p.H;
@@ -212,7 +223,7 @@ __global__ void __launch_bounds__(AT_THREADS) mla_partial_simt(dsv4_sparse_mla_d
 
 
 // ------------------------------------------------------------------------------------------------
-// Tensor-core partial kernel (bf16 caches and queries).  CTA = (chunk of 256 rows, token, 64-head
+// Tensor-core partial kernel (bf16 caches and queries).  CTA = (chunk of rows, token, 64-head
 // group x value half); the two value halves form a 2-CTA cluster and share every load: each CTA
 // issues half of the TMA traffic (Q, gathers, page boxes) with multicast to both, and both CTAs'
 // P V commits release a stage in both.  Heads are the MMA M dimension (M = 128, lanes 64..127 unused), rows the
@@ -247,7 +258,7 @@ struct Args {
   dsv4_sparse_mla_decode_params p;
   float* o_part;
   float2* ml_part;
-  int n_chunks;
+  int n_chunks, chunk_rows;
   int swa_rows, main_rows;  // rows of the two tensor maps (a masked row loads from this index)
   float c_log2;             // softmax_scale * log2(e)
 };
@@ -326,8 +337,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   int n_swa, nc, n_cmp;
   token_rows(p, pos, n_swa, nc, n_cmp);
   const int n_rows = padded_window(n_swa) + n_cmp;
-  const int r0 = chunk * TC_CHUNK;
-  const int rows = min(TC_CHUNK, n_rows - r0);
+  const int r0 = chunk * a.chunk_rows;
+  const int rows = min(a.chunk_rows, n_rows - r0);
   const int64_t part = ((int64_t)t * a.n_chunks + chunk) * p.H + hg * HG;
   pdl_launch_dependents();
   if (rows <= 0) {  // block-uniform: an empty chunk contributes nothing
@@ -619,6 +630,7 @@ static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p,
   a.o_part = o_part;
   a.ml_part = ml_part;
   a.n_chunks = L.n_chunks;
+  a.chunk_rows = L.chunk_rows;
   a.swa_rows = (int)(p.swa_num_pages * p.page_size);
   a.main_rows = p.ratio > 0 ? (int)(p.main_num_pages * p.page_size) : a.swa_rows;
   a.c_log2 = p.softmax_scale * 1.4426950408889634f;

@@ -65,7 +65,7 @@ static IxLayout ix_layout(const dsv4_indexer_topk_params& p) {
   L.scores_off = 0;
   L.hist_off = align_up(L.scores_off + (size_t)p.T * L.nc_stride * sizeof(float), 256);
   L.cnt_off = L.hist_off + (size_t)p.T * HIST_BINS * sizeof(uint32_t);  // zeroed together with hist
-  L.certain_off = align_up(L.cnt_off + (size_t)p.T * 2 * sizeof(uint32_t), 256);
+  L.certain_off = align_up(L.cnt_off + (size_t)p.T * 3 * sizeof(uint32_t), 256);
   L.maybe_off = align_up(L.certain_off + (size_t)p.T * p.topk * sizeof(int32_t), 256);
   L.total = align_up(L.maybe_off + (size_t)p.T * L.nc_stride * sizeof(uint64_t), 256);
   return L;
@@ -76,7 +76,7 @@ size_t indexer_topk_workspace(const dsv4_indexer_topk_params& p) { return ix_lay
 struct TopkBufs {
   float* scores;
   uint32_t* hist;      // [T][HIST_BINS]
-  uint32_t* cnt;       // [T][2]: selected-outright count, candidate count
+  uint32_t* cnt;       // [T][3]: selected-outright count, candidate count, finished collect CTAs
   int32_t* certain;    // [T][topk]
   uint64_t* maybe;     // [T][nc_stride] candidates: (low 20 key bits << 32) | ~j
   int nc_stride;
@@ -581,7 +581,6 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
 constexpr int COLLECT_THREADS = 256;
 constexpr int COLLECT_PER = 32;                                   // scores per thread
 constexpr int COLLECT_SLICE = COLLECT_THREADS * COLLECT_PER;      // 8192 scores per CTA
-constexpr int FINAL_THREADS = 1024;
 constexpr int CAND_CAP = 4096;                                    // candidates kept in shared memory
 constexpr int J_BITS = 20;                                        // n_c <= 2^20 (checked on the host)
 
@@ -644,6 +643,8 @@ __device__ __forceinline__ void warp_append_smem(unsigned* cnt, T* list, T val, 
 // One CTA per (8192-score slice, token): entries above the threshold bin are selected outright,
 // entries in it become candidates; both are staged in shared memory and appended to the token's
 // global lists with one atomic each.
+__device__ void finalize_token(const dsv4_indexer_topk_params& p, const TopkBufs& bufs, int t, int n, uint64_t* dsm);
+
 __global__ void __launch_bounds__(COLLECT_THREADS) topk_collect(dsv4_indexer_topk_params p, TopkBufs bufs) {
   extern __shared__ uint64_t csm[];
   pdl_launch_dependents();
@@ -651,14 +652,25 @@ __global__ void __launch_bounds__(COLLECT_THREADS) topk_collect(dsv4_indexer_top
   uint64_t* maybe_s = csm;                                        // COLLECT_SLICE
   int32_t* cert_s = reinterpret_cast<int32_t*>(csm + COLLECT_SLICE);  // COLLECT_SLICE
   __shared__ unsigned n_cert, n_maybe, base_cert, base_maybe;
-  __shared__ int sh_bin, sh_above;
+  __shared__ int sh_bin, sh_above, sh_last;
   const int t = blockIdx.y;
   const int n = visible_entries(p, t);
   const int K = p.topk;
   const int j0 = blockIdx.x * COLLECT_SLICE;
-  if (n <= K || j0 >= n) return;  // block-uniform
-  const int j1 = min(n, j0 + COLLECT_SLICE);
   const float* s = bufs.scores + (int64_t)t * bufs.nc_stride;
+  if (n <= K) {  // short context: every candidate, in order (slice 0 writes it)
+    if (blockIdx.x == 0) {
+      int32_t* out = p.topk_idx + (int64_t)t * K;
+      float* out_s = p.topk_score ? p.topk_score + (int64_t)t * K : nullptr;
+      for (int x = threadIdx.x; x < K; x += COLLECT_THREADS) {
+        out[x] = x < n ? x : -1;
+        if (out_s) out_s[x] = x < n ? s[x] : -INFINITY;
+      }
+    }
+    return;
+  }
+  if (j0 >= n) return;  // block-uniform: this slice holds no entry of the token
+  const int j1 = min(n, j0 + COLLECT_SLICE);
   float v[COLLECT_PER];
 #pragma unroll
   for (int i = 0; i < COLLECT_PER; ++i) {  // all loads in flight first
@@ -682,8 +694,8 @@ __global__ void __launch_bounds__(COLLECT_THREADS) topk_collect(dsv4_indexer_top
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    base_cert = n_cert ? atomicAdd(&bufs.cnt[2 * t], n_cert) : 0u;
-    base_maybe = n_maybe ? atomicAdd(&bufs.cnt[2 * t + 1], n_maybe) : 0u;
+    base_cert = n_cert ? atomicAdd(&bufs.cnt[3 * t], n_cert) : 0u;
+    base_maybe = n_maybe ? atomicAdd(&bufs.cnt[3 * t + 1], n_maybe) : 0u;
   }
   __syncthreads();
   int32_t* certain = bufs.certain + (int64_t)t * K;
@@ -692,6 +704,17 @@ __global__ void __launch_bounds__(COLLECT_THREADS) topk_collect(dsv4_indexer_top
     if (base_cert + x < (unsigned)K) certain[base_cert + x] = cert_s[x];
   for (unsigned x = threadIdx.x; x < n_maybe; x += COLLECT_THREADS)
     if (base_maybe + x < (unsigned)bufs.nc_stride) maybe[base_maybe + x] = maybe_s[x];
+  // the CTA that finishes the token's collection last makes the final choice (no CTA waits)
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned slices = (unsigned)((n + COLLECT_SLICE - 1) / COLLECT_SLICE);
+    sh_last = atomicAdd(&bufs.cnt[3 * t + 2], 1u) == slices - 1;
+  }
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  finalize_token(p, bufs, t, n, csm);
 }
 
 // Digit of the radix bucket holding the rem-th largest element, from a 256-bin histogram: warp 0
@@ -758,37 +781,27 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
   return r;
 }
 
-// One CTA per token: exact choice of the remaining entries among the candidates (radix select on
-// the candidate values), then the selection written in increasing j through a bitmap over j.
-__global__ void __launch_bounds__(FINAL_THREADS) topk_final(dsv4_indexer_topk_params p, TopkBufs bufs) {
-  extern __shared__ uint64_t fsm[];
-  pdl_launch_dependents();
-  pdl_wait();
-  uint64_t* cand_s = fsm;                                           // CAND_CAP
-  uint32_t* bits = reinterpret_cast<uint32_t*>(fsm + CAND_CAP);    // nc_stride / 32 words
-  const int t = blockIdx.x, tid = threadIdx.x;
+// Exact choice of the remaining entries among the candidates of token t (radix select on the
+// candidate values), then the selection written in increasing j through a bitmap over j.  Run by
+// the whole CTA that finished the token's collection last; `dsm` holds CAND_CAP candidates followed
+// by the bitmap.
+__device__ void finalize_token(const dsv4_indexer_topk_params& p, const TopkBufs& bufs, int t, int n, uint64_t* dsm) {
+  uint64_t* cand_s = dsm;                                           // CAND_CAP
+  uint32_t* bits = reinterpret_cast<uint32_t*>(dsm + CAND_CAP);    // nc_stride / 32 words
+  const int tid = threadIdx.x, nthr = blockDim.x;
   const int K = p.topk;
-  const int n = visible_entries(p, t);
   int32_t* out = p.topk_idx + (int64_t)t * K;
   float* out_s = p.topk_score ? p.topk_score + (int64_t)t * K : nullptr;
   const float* s = bufs.scores + (int64_t)t * bufs.nc_stride;
-
-  if (n <= K) {  // short context: every candidate, in order
-    for (int x = tid; x < K; x += FINAL_THREADS) {
-      out[x] = x < n ? x : -1;
-      if (out_s) out_s[x] = x < n ? s[x] : -INFINITY;
-    }
-    return;
-  }
   __shared__ unsigned hist[256];
   __shared__ unsigned long long sh_prefix;
   __shared__ unsigned sh_rem, sh_above;
   __shared__ int sh_digit;
   __shared__ int warp_tot[33];
   const int words = (n + 31) >> 5;
-  for (int x = tid; x < words; x += FINAL_THREADS) bits[x] = 0u;
-  const int n_certain = (int)min(bufs.cnt[2 * t], (uint32_t)K);
-  const int m = (int)min(bufs.cnt[2 * t + 1], (uint32_t)bufs.nc_stride);
+  for (int x = tid; x < words; x += nthr) bits[x] = 0u;
+  const int n_certain = (int)min(bufs.cnt[3 * t], (uint32_t)K);
+  const int m = (int)min(bufs.cnt[3 * t + 1], (uint32_t)bufs.nc_stride);
   int need = K - n_certain;
   if (need > m) {  // cannot happen with a complete histogram; keep the output valid
     if (tid == 0) atomicOr(&g_flags_ix, FLAG_TOPK);
@@ -797,10 +810,10 @@ __global__ void __launch_bounds__(FINAL_THREADS) topk_final(dsv4_indexer_topk_pa
   const uint64_t* maybe_g = bufs.maybe + (int64_t)t * bufs.nc_stride;
   const bool in_smem = m <= CAND_CAP;
   if (in_smem)
-    for (int i = tid; i < m; i += FINAL_THREADS) cand_s[i] = maybe_g[i];
+    for (int i = tid; i < m; i += nthr) cand_s[i] = maybe_g[i];
   const uint64_t* cand = in_smem ? cand_s : maybe_g;
   __syncthreads();
-  for (int x = tid; x < n_certain; x += FINAL_THREADS) {
+  for (int x = tid; x < n_certain; x += nthr) {
     const int j = bufs.certain[(int64_t)t * K + x];
     if (j >= 0 && j < n) atomicOr(&bits[j >> 5], 1u << (j & 31));
   }
@@ -809,9 +822,9 @@ __global__ void __launch_bounds__(FINAL_THREADS) topk_final(dsv4_indexer_topk_pa
     unsigned long long prefix = 0, mask = 0;
     if (tid == 0) sh_rem = (unsigned)need;
     for (int shift = 32; shift >= 0; shift -= 8) {
-      for (int x = tid; x < 256; x += FINAL_THREADS) hist[x] = 0;
+      for (int x = tid; x < 256; x += nthr) hist[x] = 0;
       __syncthreads();
-      for (int i = tid; i < m; i += FINAL_THREADS) {
+      for (int i = tid; i < m; i += nthr) {
         const unsigned long long v = cand[i];
         if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255ull], 1u);
       }
@@ -827,7 +840,7 @@ __global__ void __launch_bounds__(FINAL_THREADS) topk_final(dsv4_indexer_topk_pa
       mask |= 255ull << shift;
     }
     const unsigned long long kth = prefix;
-    for (int i = tid; i < m; i += FINAL_THREADS) {
+    for (int i = tid; i < m; i += nthr) {
       const unsigned long long v = cand[i];
       if (v >= kth) {
         const int j = cand_j(v);
@@ -837,7 +850,7 @@ __global__ void __launch_bounds__(FINAL_THREADS) topk_final(dsv4_indexer_topk_pa
   }
   __syncthreads();
   // compaction of the bitmap in increasing j
-  const int per = (words + FINAL_THREADS - 1) / FINAL_THREADS;
+  const int per = (words + nthr - 1) / nthr;
   const int w0 = tid * per, w1 = min(words, w0 + per);
   int cnt = 0;
   for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
@@ -855,7 +868,7 @@ __global__ void __launch_bounds__(FINAL_THREADS) topk_final(dsv4_indexer_topk_pa
       ++pos;
     }
   }
-  for (int x = total + tid; x < K; x += FINAL_THREADS) {
+  for (int x = total + tid; x < K; x += nthr) {
     out[x] = -1;
     if (out_s) out_s[x] = -INFINITY;
   }
@@ -888,21 +901,16 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
     if (e != cudaSuccess) return e;
   }
   static int attr_done = 0;
-  const size_t csmem = (size_t)COLLECT_SLICE * (sizeof(uint64_t) + sizeof(int32_t));
-  const size_t fsmem = (size_t)CAND_CAP * sizeof(uint64_t) + L.nc_stride / 32 * sizeof(uint32_t);
+  const size_t stage_smem = (size_t)COLLECT_SLICE * (sizeof(uint64_t) + sizeof(int32_t));
+  const size_t final_smem = (size_t)CAND_CAP * sizeof(uint64_t) + L.nc_stride / 32 * sizeof(uint32_t);
+  const size_t csmem = stage_smem > final_smem ? stage_smem : final_smem;
   if (!attr_done) {
-    e = cudaFuncSetAttribute(topk_collect, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_final, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    e = cudaFuncSetAttribute(topk_collect, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     attr_done = 1;
   }
-  if (max_nc > p.topk) {
-    const int slices = (max_nc + COLLECT_SLICE - 1) / COLLECT_SLICE;
-    e = launch_pdl(topk_collect, dim3(slices, p.T), dim3(COLLECT_THREADS), csmem, st, /*pdl=*/false, p, bufs);
-    if (e != cudaSuccess) return e;
-  }
-  return launch_pdl(topk_final, dim3(p.T), dim3(FINAL_THREADS), fsmem, st, /*pdl=*/false, p, bufs);
+  const int slices = max_nc > 0 ? (max_nc + COLLECT_SLICE - 1) / COLLECT_SLICE : 1;
+  return launch_pdl(topk_collect, dim3(slices, p.T), dim3(COLLECT_THREADS), csmem, st, /*pdl=*/false, p, bufs);
 }
 
 cudaError_t read_flags_indexer(uint32_t* f) {
