@@ -30,24 +30,24 @@ struct AtLayout {
 
 static int max_rows(const dsv4_sparse_mla_decode_params& p) {
   int n_swa = p.window < p.max_context ? p.window : p.max_context;
-  n_swa = (n_swa + 63) / 64 * 64;  // the tensor-core kernel pads the window part to whole tiles
+  // the tensor-core kernel reads whole window pages: at most ceil((window - 1) / 64) + 1 of them
+  n_swa = ((n_swa + 62) / 64 + 1) * 64;
   int n_cmp = 0;
   if (p.ratio > 0) n_cmp = p.topk_idx ? p.topk : p.max_context / p.ratio;
-  return n_swa + n_cmp;
+  return n_swa + (n_cmp + 63) / 64 * 64;
 }
 
 static bool use_tc_attention(const dsv4_sparse_mla_decode_params& p);
 
-// Rows per CTA of the tensor-core kernel: about one wave of CTAs over the SMs (each (token, head
-// group) has two CTAs, one per value half), in whole 64-row tiles.
+// Rows per CTA of the tensor-core kernel: about one wave of CTAs (one per chunk, token and 64-head
+// group) over the SMs, in whole 64-row halves.
 static int tc_chunk_rows(const dsv4_sparse_mla_decode_params& p) {
-  const int per_chunk = p.T * (p.H / 64) * 2;
-  int n = per_chunk > 0 ? num_sms() / per_chunk : 1;
+  const int units = p.T * (p.H / 64);
+  int n = units > 0 ? num_sms() / units : 1;
   if (n < 1) n = 1;
-  const int rows = max_rows(p);
-  int c = (rows + n - 1) / n;
-  c = (c + 63) / 64 * 64;
-  return c < 64 ? 64 : c;
+  const int halves = max_rows(p) / 64;
+  const int c = (halves + n - 1) / n;
+  return (c < 1 ? 1 : c) * 64;
 }
 
 static AtLayout at_layout(const dsv4_sparse_mla_decode_params& p) {
@@ -224,394 +224,517 @@ __global__ void __launch_bounds__(AT_THREADS) mla_partial_simt(dsv4_sparse_mla_d
 
 // ------------------------------------------------------------------------------------------------
 // Tensor-core partial kernel (bf16 caches and queries).  CTA = (chunk of rows, token, 64-head
-// group x value half); the two value halves form a 2-CTA cluster and share every load: each CTA
-// issues half of the TMA traffic (Q, gathers, page boxes) with multicast to both, and both CTAs'
-// P V commits release a stage in both.  Heads are the MMA M dimension (M = 128, lanes 64..127 unused), rows the
-// N dimension of S = Q K^T (K = 576 in 9 K-blocks of 64 dims) and the K dimension of
-// O[:, half] += P V[:, half] (N = 256 value dims).
+// group).  Both products are computed transposed, so that the attended rows, not the heads, fill
+// the 128 lanes of the MMA:
+//   S^T[r, h]  = K[r, :] . Q[h, :]        M = 128 rows, N = 64 heads, K = 576 (9 K-blocks of 64)
+//   O^T[v, h] += V^T[v, r] P^T[r, h]      M = 128 value dims (4 blocks for 512), N = 64 heads,
+//                                         K = the tile's 128 rows
+// O^T takes 4 x 64 TMEM columns and S^T 64 more, so one CTA keeps all 512 value dims and computes
+// each QK^T once.
 //
-// Warp 2 gathers 64-row tiles with TMA gather4 loads (4 rows x one 64-dim K-block each) straight
-// into the 128-byte swizzled K-major layout the MMA reads, so any row order (window positions,
-// top-k indices, dense runs) works; a masked row is loaded from past the end of the tensor (zeros).
-// Lane 0 of warp 3 issues the MMAs; S goes to one of two TMEM buffers, P (bf16) is written back
-// to TMEM by the softmax warps and read from there as the A operand of the P V product; O stays in
-// TMEM for the whole chunk.  Warps 0-1 (one head per thread, TMEM lanes 0-63) run the online
-// softmax in the log2 domain with a lazy rescale (O is only rescaled when the running max grows
-// by more than 2^8), then write the unnormalised O and (max, sum) of the chunk.
+// Shared memory holds Q (72 KB) and one 128-row tile (9 K-block slots of 16 KB = 144 KB) in the
+// 128-byte swizzled layout TMA writes: K-major for QK^T and, read the other way, MN-major for the
+// V^T operand of PV.  P^T (bf16, 128 rows x 64 heads) is written by the softmax warps over slot 8
+// (the rope dims, which PV does not read) once QK^T is done.  Slots are refilled per group as soon
+// as the PV MMAs that read them retire: {0,1} after value block 0, ..., {6,7} and 8 after block 3.
+//
+// Row list of a token: the window pages (whole 64-row pages of the SWA cache covering positions
+// p - n_swa + 1 .. p, rows outside that range masked), then the compressed rows in 64-row halves
+// (top-k indices, or dense pages of the main cache).  Warp 8 loads a window page or a dense page as
+// 9 TMA boxes and top-k rows with TMA gather4 (4 rows x one K-block each; an invalid index loads a
+// row past the end of the tensor, i.e. zeros).  Lane 0 of warp 9 issues the MMAs.  Warps 0-7 run
+// the online softmax in the log2 domain with a lazy rescale (O^T is rescaled only when a head's
+// running max grows by more than 2^8): warp w owns tile rows 32 (w & 3) .. + 31 (its TMEM lane
+// quarter) and heads 32 (w >> 2) .. + 31; a tile's per-head maxima are reduced across lanes by a
+// shuffle transpose-reduce and across the four row quarters in shared memory.  A masked row of a
+// loaded half gets zero V (it may hold anything, and 0 x NaN would poison O); PV skips halves that
+// were not loaded.  At the end the same warps turn O^T into [head][value] rows in the idle tile
+// buffer and store the unnormalised O and the chunk's (max, sum) per head.
 // ------------------------------------------------------------------------------------------------
 namespace attc {
-constexpr int TILE = 64;
-constexpr int HG = 64;
-constexpr int DVH = 256;
-constexpr int NKB = 9;
-constexpr int KB_BYTES = TILE * 128;          // 8 KB
-constexpr int STAGE_BYTES = NKB * KB_BYTES;   // 72 KB
-constexpr int Q_BYTES = NKB * HG * 128;       // 72 KB
-constexpr int STAGES = 2;
-constexpr int THREADS = 192;  // warps 0-1 and 4-5 softmax, 2 producer, 3 MMA
-constexpr uint32_t COL_O = 0, COL_S = 256, COL_P = 384;  // S: 2 x 64 columns, P: 2 x 32 columns
-constexpr uint32_t TMEM_COLS = 512;
+constexpr int TILE = 128;                  // rows per tile
+constexpr int HALF = 64;                   // rows per load unit (one page)
+constexpr int HG = 64;                     // heads per CTA
+constexpr int NKB = 9;                     // 64-dim K-blocks of a 576-dim row
+constexpr int SLOT_BYTES = TILE * 128;     // one K-block of a tile: 16 KB
+constexpr int HALF_BYTES = HALF * 128;     // 8 KB
+constexpr int Q_BYTES = NKB * HG * 128;    // 72 KB
+constexpr int KV_BYTES = NKB * SLOT_BYTES;  // 144 KB
+constexpr int NGROUPS = 5;                 // slot groups {0,1} {2,3} {4,5} {6,7} {8}
+constexpr int THREADS = 320;               // warps 0-7 softmax + epilogue, 8 loads, 9 MMA
+constexpr int W_LOAD = 8, W_MMA = 9;
+constexpr uint32_t COL_O = 0, COL_S = 256, TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr uint32_t FLAG_TIMEOUT = 4u;
+constexpr int K_NONE = 0, K_BOX_SWA = 1, K_BOX_MAIN = 2, K_GATHER = 3;
 
 struct Args {
   dsv4_sparse_mla_decode_params p;
   float* o_part;
   float2* ml_part;
-  int n_chunks, chunk_rows;
-  int swa_rows, main_rows;  // rows of the two tensor maps (a masked row loads from this index)
+  int n_chunks, chunk_halves;
+  int swa_rows, main_rows;  // rows of the two caches (a gather from this row loads zeros)
   float c_log2;             // softmax_scale * log2(e)
 };
 
 struct Smem {
-  uint64_t full[STAGES], empty[STAGES], sfull[2], pfull[2], pvdone[2], qfull, odone;
-  uint64_t mask[STAGES];
-  uint64_t xbar[2], lbar;  // exchanges between the two softmax halves (4 warps arrive)
-  float xmax[2][2][HG];  // [tile parity][half][head] row maxima
-  float lsum[2][HG];     // [half][head] softmax sums
+  uint64_t full[NGROUPS], vfree[4], sfull, pfull, pvdone, qfull, odone, xbar[2][2], ebar;
+  uint32_t mask[2][4];  // [tile parity][row / 32]: valid rows
+  uint32_t loaded[2];   // [tile parity]: bit u = half u was loaded
+  float red[2][2][4][32];  // [tile parity][head half][row quarter][lane]: per-warp maxima
+  float lred[2][4][32];
+  float mrow[8][64];       // per softmax warp: running max and rescale factor of its 32 heads
   uint32_t tmem_base;
   int abort;
 };
+static_assert(1024 + Q_BYTES + KV_BYTES + sizeof(Smem) <= 232448, "shared memory of one CTA");
 
-// Row list of the tensor-core kernel: the window rows, padded with masked rows to a multiple of 64 so
-// that every 64-row tile reads a single cache, then the compressed rows.
-__device__ __forceinline__ int padded_window(int n_swa) { return (n_swa + TILE - 1) / TILE * TILE; }
+struct TokenRows {
+  int pos, lo, first_wp, n_wp, nc, n_cmp, n_halves;
+};
 
-// Source row of entry r (row index into the SWA cache if r is a window row, into the main cache
-// otherwise); a masked row gets the map's out-of-range row, which loads zeros.
-__device__ __forceinline__ int row_source(const Args& a, int t, int b, int pos, int n_swa, int nc, int n_rows, int r,
-                                          bool& valid) {
+__device__ __forceinline__ TokenRows token_plan(const dsv4_sparse_mla_decode_params& p, int t) {
+  TokenRows r;
+  int pos = p.positions[t], n_swa, nc, n_cmp;
+  token_rows(p, pos, n_swa, nc, n_cmp);
+  r.pos = pos;
+  r.nc = nc;
+  r.n_cmp = n_cmp;
+  if (n_swa > 0) {
+    r.lo = pos - n_swa + 1;
+    r.first_wp = r.lo / p.page_size;
+    r.n_wp = pos / p.page_size - r.first_wp + 1;
+  } else {
+    r.lo = 0;
+    r.first_wp = 0;
+    r.n_wp = 0;
+  }
+  r.n_halves = r.n_wp + (n_cmp + HALF - 1) / HALF;
+  return r;
+}
+
+struct HalfPlan {
+  int kind, ybox, y0, y1;
+  bool v0, v1;  // rows lane and lane + 32 of the half are valid
+};
+
+// How half `hh` of the token's row list is loaded, and which of its rows are valid (warp-wide).
+__device__ __forceinline__ HalfPlan plan_half(const Args& a, int t, int b, const TokenRows& tr, int hh, int lane) {
   const dsv4_sparse_mla_decode_params& p = a.p;
-  const int n_win = padded_window(n_swa);
-  valid = false;
-  if (r < n_win) {
-    if (r >= n_swa || r >= n_rows) return a.swa_rows;
-    const int q = pos - n_swa + 1 + r;
-    const int lp = q / p.page_size;
+  HalfPlan h;
+  h.kind = K_NONE;
+  h.ybox = 0;
+  h.y0 = h.y1 = a.main_rows;
+  h.v0 = h.v1 = false;
+  if (hh >= tr.n_halves) return h;
+  if (hh < tr.n_wp) {
+    const int lp = tr.first_wp + hh;
     const int page = lp < p.swa_max_pages ? p.swa_block_table[(int64_t)b * p.swa_max_pages + lp] : -1;
     if (page < 0 || page >= p.swa_num_pages) {
-      atomicOr(&g_flags_at, FLAG_PAGE);
-      return a.swa_rows;
+      if (lane == 0) atomicOr(&g_flags_at, FLAG_PAGE);
+      return h;
     }
-    valid = true;
-    return page * p.page_size + q % p.page_size;
+    const int q0 = lp * p.page_size + lane, q1 = q0 + 32;
+    h.v0 = q0 >= tr.lo && q0 <= tr.pos;
+    h.v1 = q1 >= tr.lo && q1 <= tr.pos;
+    h.kind = K_BOX_SWA;
+    h.ybox = page * p.page_size;
+    return h;
   }
-  if (r >= n_rows) return a.main_rows;
-  const int i = r - n_win;
-  int j = i;
-  if (p.topk_idx != nullptr) {
-    j = p.topk_idx[(int64_t)t * p.topk + i];
-    if (j < 0) return a.main_rows;
-    if (j >= nc) {
-      atomicOr(&g_flags_at, FLAG_TOPK);
-      return a.main_rows;
+  const int j0 = (hh - tr.n_wp) * HALF;
+  if (p.topk_idx == nullptr) {  // dense: the half is logical page j0 / 64 of the main cache
+    const int lp = j0 / p.page_size;
+    const int page = lp < p.main_max_pages ? p.main_block_table[(int64_t)b * p.main_max_pages + lp] : -1;
+    if (page < 0 || page >= p.main_num_pages) {
+      if (lane == 0) atomicOr(&g_flags_at, FLAG_PAGE);
+      return h;
+    }
+    h.v0 = j0 + lane < tr.nc;
+    h.v1 = j0 + lane + 32 < tr.nc;
+    h.kind = K_BOX_MAIN;
+    h.ybox = page * p.page_size;
+    return h;
+  }
+  int y[2];
+  bool v[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = j0 + lane + 32 * u;
+    v[u] = false;
+    y[u] = a.main_rows;
+    if (i < tr.n_cmp) {
+      const int j = p.topk_idx[(int64_t)t * p.topk + i];
+      if (j >= tr.nc) atomicOr(&g_flags_at, FLAG_TOPK);
+      if (j >= 0 && j < tr.nc) {
+        const int lp = j / p.page_size;
+        const int page = lp < p.main_max_pages ? p.main_block_table[(int64_t)b * p.main_max_pages + lp] : -1;
+        if (page < 0 || page >= p.main_num_pages) {
+          atomicOr(&g_flags_at, FLAG_PAGE);
+        } else {
+          v[u] = true;
+          y[u] = page * p.page_size + j % p.page_size;
+        }
+      }
     }
   }
-  const int lp = j / p.page_size;
-  const int page = lp < p.main_max_pages ? p.main_block_table[(int64_t)b * p.main_max_pages + lp] : -1;
-  if (page < 0 || page >= p.main_num_pages) {
-    atomicOr(&g_flags_at, FLAG_PAGE);
-    return a.main_rows;
+  h.y0 = y[0];
+  h.y1 = y[1];
+  h.v0 = v[0];
+  h.v1 = v[1];
+  h.kind = __any_sync(0xffffffffu, v[0] || v[1]) ? K_GATHER : K_NONE;
+  return h;
+}
+
+// Max (or sum) over the 32 lanes of 32 per-lane values, transposed: lane l returns the result for
+// value l.  Five butterfly steps, each halving the values a lane keeps.
+template <bool kMax>
+__device__ __forceinline__ float transpose_reduce32(const float (&x)[32], int lane) {
+  float v[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const bool up = lane & 16;
+    const float send = up ? x[k] : x[k + 16];
+    const float keep = up ? x[k + 16] : x[k];
+    const float o = __shfl_xor_sync(0xffffffffu, send, 16);
+    v[k] = kMax ? fmaxf(keep, o) : keep + o;
   }
-  valid = true;
-  return page * p.page_size + j % p.page_size;
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {  // 16 -> 8 -> 4 -> 2 -> 1 values, lane bits 3, 2, 1, 0
+#pragma unroll
+    for (int k = 0; k < w; ++k) {
+      const bool up = lane & w;
+      const float send = up ? v[k] : v[k + w];
+      const float keep = up ? v[k + w] : v[k];
+      const float o = __shfl_xor_sync(0xffffffffu, send, w);
+      v[k] = kMax ? fmaxf(keep, o) : keep + o;
+    }
+  }
+  return v[0];
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-    mla_partial_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap swamap,
+    mla_partial_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap swamap64,
                    const __grid_constant__ CUtensorMap mainmap, const __grid_constant__ CUtensorMap mainmap64,
                    Args a) {
   extern __shared__ __align__(1024) uint8_t dsm[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_mem = base;                     // Q_BYTES (GEMM1 rows 64..127 read the next 8 KB: still smem)
-  uint8_t* stage_mem = base + Q_BYTES;       // STAGES x STAGE_BYTES
-  Smem* sm = reinterpret_cast<Smem*>(stage_mem + STAGES * STAGE_BYTES);
+  uint8_t* q_mem = base;             // Q_BYTES
+  uint8_t* kv_mem = base + Q_BYTES;  // KV_BYTES: slot kb at kb * SLOT_BYTES
+  Smem* sm = reinterpret_cast<Smem*>(kv_mem + KV_BYTES);
   volatile int* abort = &sm->abort;
-
   const dsv4_sparse_mla_decode_params& p = a.p;
-  const int chunk = blockIdx.x, t = blockIdx.y;
-  const int hg = blockIdx.z >> 1, dh = blockIdx.z & 1;
+  const int chunk = blockIdx.x, t = blockIdx.y, hg = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = t / p.q_per_seq;
-  int pos = p.positions[t];
-  int n_swa, nc, n_cmp;
-  token_rows(p, pos, n_swa, nc, n_cmp);
-  const int n_rows = padded_window(n_swa) + n_cmp;
-  const int r0 = chunk * a.chunk_rows;
-  const int rows = min(a.chunk_rows, n_rows - r0);
+  const TokenRows tr = token_plan(p, t);
+  const int h0 = chunk * a.chunk_halves;
+  const int nh = min(a.chunk_halves, tr.n_halves - h0);
   const int64_t part = ((int64_t)t * a.n_chunks + chunk) * p.H + hg * HG;
   pdl_launch_dependents();
-  if (rows <= 0) {  // block-uniform: an empty chunk contributes nothing
+  if (nh <= 0) {  // block-uniform: an empty chunk contributes nothing
     pdl_wait();
-    if (dh == 0 && threadIdx.x < HG) a.ml_part[part + threadIdx.x] = make_float2(-INFINITY, 0.f);
+    if (threadIdx.x < HG) a.ml_part[part + threadIdx.x] = make_float2(-INFINITY, 0.f);
     return;
   }
-  const int ntiles = (rows + TILE - 1) / TILE;
+  const int ntiles = (nh + 1) / 2;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      tc::mbar_init(&sm->full[s], 1);
-      tc::mbar_init(&sm->empty[s], 2);  // both CTAs of the pair release a stage (multicast commit)
-    }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sm->sfull[i], 1);
-      tc::mbar_init(&sm->pfull[i], 4);
-      tc::mbar_init(&sm->xbar[i], 4);
-      tc::mbar_init(&sm->pvdone[i], 1);
-    }
+    for (int g = 0; g < NGROUPS; ++g) tc::mbar_init(&sm->full[g], 1);
+    for (int m = 0; m < 4; ++m) tc::mbar_init(&sm->vfree[m], 1);
+    tc::mbar_init(&sm->sfull, 1);
+    tc::mbar_init(&sm->pfull, 8);
+    tc::mbar_init(&sm->pvdone, 1);
     tc::mbar_init(&sm->qfull, 1);
     tc::mbar_init(&sm->odone, 1);
-    tc::mbar_init(&sm->lbar, 4);
+    for (int x = 0; x < 4; ++x) tc::mbar_init(&sm->xbar[x >> 1][x & 1], 4);
+    tc::mbar_init(&sm->ebar, 8);
     sm->abort = 0;
     tc::fence_barrier_init();
   }
-  if (warp == 3) {
+  if (warp == W_MMA) {
     tc::tmem_alloc(&sm->tmem_base, TMEM_COLS);
     tc::tmem_relinquish();
     tc::tc_fence_before();
   }
-  tc::cluster_sync_all();  // the partner's barriers exist before any multicast targets them
+  __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
-  const uint32_t crank = tc::cluster_rank();  // 0 or 1: which half of every load this CTA issues
-  if (warp != 2) pdl_wait();
+  if (warp != W_LOAD) pdl_wait();
 
-  if (warp == 2) {
-    // ---------------- producer: Q by TMA, then each 64-row tile by 144 TMA gather4 loads (lane g < 16
-    // loads rows 4g..4g+3 of all 9 K-blocks); the window part of the list is tile-aligned, so a tile
-    // reads one cache
+  if (warp == W_LOAD) {
+    // ---------------- loads
     if (lane == 0) {
       tc::tma_prefetch_desc(&qmap);
-      tc::tma_prefetch_desc(&swamap);
+      tc::tma_prefetch_desc(&swamap64);
       tc::tma_prefetch_desc(&mainmap);
+      tc::tma_prefetch_desc(&mainmap64);
       tc::mbar_arrive_expect_tx(&sm->qfull, Q_BYTES);
-      for (int kb = (int)crank; kb < NKB; kb += 2)
-        tc::tma_load_2d_mc(q_mem + kb * HG * 128, &qmap, kb * 64, t * p.H + hg * HG, &sm->qfull, 0x3);
+      for (int kb = 0; kb < NKB; ++kb)
+        tc::tma_load_2d(q_mem + kb * HG * 128, &qmap, kb * 64, t * p.H + hg * HG, &sm->qfull);
     }
     pdl_wait();  // the caches and the top-k list come from earlier kernels
-    const int n_win = padded_window(n_swa);
-    bool v0, v1;
-    int y0 = row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + lane, v0);
-    int y1 = row_source(a, t, b, pos, n_swa, nc, n_rows, r0 + lane + 32, v1);
-    for (int i = 0; i < ntiles; ++i) {
-      const int stage = i % STAGES;
-      const int tr0 = r0 + i * TILE;
-      const bool in0 = i * TILE + lane < rows, in1 = i * TILE + lane + 32 < rows;
-      const bool use_main = tr0 >= n_win;
-      const int oob = use_main ? a.main_rows : a.swa_rows;
-      if (!(v0 && in0)) y0 = oob;
-      if (!(v1 && in1)) y1 = oob;
-      const unsigned b0 = __ballot_sync(0xffffffffu, v0 && in0), b1 = __ballot_sync(0xffffffffu, v1 && in1);
-      // rows 4g..4g+3 for lane g < 16
-      const int g = lane & 15;
-      const int src_lane = (4 * g) & 31;
+    int armed_tile = -1, armed_groups = 0;
+    bool ok = true;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      HalfPlan hp[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int hh = h0 + 2 * i + u;
+        hp[u] = (2 * i + u < nh) ? plan_half(a, t, b, tr, hh, lane) : plan_half(a, t, b, tr, tr.n_halves, lane);
+      }
+      const uint32_t m0 = __ballot_sync(0xffffffffu, hp[0].v0), m1 = __ballot_sync(0xffffffffu, hp[0].v1);
+      const uint32_t m2 = __ballot_sync(0xffffffffu, hp[1].v0), m3 = __ballot_sync(0xffffffffu, hp[1].v1);
+      const uint32_t ld = (hp[0].kind != K_NONE ? 1u : 0u) | (hp[1].kind != K_NONE ? 2u : 0u);
+      const int nload = __popc(ld);
+      // gather rows: lanes 16u .. 16u + 15 load half u, lane g4 rows 4 g4 .. 4 g4 + 3
+      const int gu = lane >> 4, g4 = lane & 15, src = (4 * g4) & 31;
       int r4[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int ya = __shfl_sync(0xffffffffu, y0, src_lane + u);
-        const int yb = __shfl_sync(0xffffffffu, y1, src_lane + u);
-        r4[u] = g < 8 ? ya : yb;
+      for (int k = 0; k < 4; ++k) {
+        const int a0 = __shfl_sync(0xffffffffu, hp[0].y0, src + k), a1 = __shfl_sync(0xffffffffu, hp[0].y1, src + k);
+        const int b0 = __shfl_sync(0xffffffffu, hp[1].y0, src + k), b1 = __shfl_sync(0xffffffffu, hp[1].y1, src + k);
+        r4[k] = gu == 0 ? (g4 < 8 ? a0 : a1) : (g4 < 8 ? b0 : b1);
       }
-      int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait_bounded(&sm->empty[stage], ((i / STAGES) & 1) ^ 1, abort);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      uint8_t* st = stage_mem + stage * STAGE_BYTES;
-      if (lane == 0) {
-        sm->mask[stage] = (uint64_t)b0 | ((uint64_t)b1 << 32);
-        tc::mbar_arrive_expect_tx(&sm->full[stage], (uint32_t)TILE * NKB * 128);
-      }
-      __syncwarp();
-      // a dense (no top-k list) compressed tile whose 64 rows are all valid is one whole page
-      const int dense_page = (use_main && p.topk_idx == nullptr && (b0 & b1) == 0xffffffffu)
-                                 ? __shfl_sync(0xffffffffu, y0, 0) / p.page_size : -1;
-      if (dense_page >= 0) {
-        if (lane == 0) {
-          for (int kb = (int)crank; kb < NKB; kb += 2)
-            tc::tma_load_2d_mc(st + kb * KB_BYTES, &mainmap64, kb * 64, dense_page * p.page_size, &sm->full[stage], 0x3);
+      const int my_kind = gu == 0 ? hp[0].kind : hp[1].kind;
+      for (int g = 0; g < NGROUPS; ++g) {
+        if (i > 0) {
+          int w = 1;
+          if (lane == 0) w = tc::mbar_wait_bounded(&sm->vfree[g < 4 ? g : 3], (i - 1) & 1, abort);
+          if (!__shfl_sync(0xffffffffu, w, 0)) {
+            ok = false;
+            break;
+          }
         }
-      } else if (lane < 16 && (lane >> 3) == (int)crank) {  // CTA 0 gathers rows 0-31, CTA 1 rows 32-63
-        const CUtensorMap* map = use_main ? &mainmap : &swamap;
+        const int kb0 = 2 * g, nkb = g < 4 ? 2 : 1;
+        if (lane == 0) {
+          if (g == 0) {
+            sm->mask[i & 1][0] = m0;
+            sm->mask[i & 1][1] = m1;
+            sm->mask[i & 1][2] = m2;
+            sm->mask[i & 1][3] = m3;
+            sm->loaded[i & 1] = ld;
+          }
+          tc::mbar_arrive_expect_tx(&sm->full[g], (uint32_t)(nload * nkb * HALF_BYTES));
+        }
+        armed_tile = i;
+        armed_groups = g + 1;
+        __syncwarp();
 #pragma unroll
-        for (int kb = 0; kb < NKB; ++kb)
-          tc::tma_gather4_mc(st + kb * KB_BYTES + 4 * g * 128, map, kb * 64, r4[0], r4[1], r4[2], r4[3], &sm->full[stage],
-                             0x3);
-      }
-      if (i + 1 < ntiles) {  // look up the next tile's rows while this one is in flight
-        y0 = row_source(a, t, b, pos, n_swa, nc, n_rows, tr0 + TILE + lane, v0);
-        y1 = row_source(a, t, b, pos, n_swa, nc, n_rows, tr0 + TILE + lane + 32, v1);
+        for (int u = 0; u < 2; ++u) {
+          const int kind = hp[u].kind;
+          if ((kind == K_BOX_SWA || kind == K_BOX_MAIN) && lane == 0) {
+            const CUtensorMap* map = kind == K_BOX_SWA ? &swamap64 : &mainmap64;
+            for (int kb = kb0; kb < kb0 + nkb; ++kb)
+              tc::tma_load_2d(kv_mem + kb * SLOT_BYTES + u * HALF_BYTES, map, kb * 64, hp[u].ybox, &sm->full[g]);
+          }
+        }
+        if (my_kind == K_GATHER) {
+          for (int kb = kb0; kb < kb0 + nkb; ++kb)
+            tc::tma_gather4(kv_mem + kb * SLOT_BYTES + gu * HALF_BYTES + 4 * g4 * 128, &mainmap, kb * 64, r4[0], r4[1],
+                            r4[2], r4[3], &sm->full[g]);
+        }
       }
     }
     if (lane == 0) {
-      // every load into this CTA has landed, and both CTAs' last stage releases (multicast commits
-      // into this CTA) have arrived, before the closing cluster barrier lets the partner exit
+      // every load into this CTA has landed before it may exit (already true unless it aborted)
       tc::mbar_wait_bounded(&sm->qfull, 0, abort, 100000000ull);
-      for (int i = (ntiles > STAGES ? ntiles - STAGES : 0); i < ntiles; ++i) {
-        tc::mbar_wait_bounded(&sm->full[i % STAGES], (i / STAGES) & 1, abort, 100000000ull);
-        tc::mbar_wait_bounded(&sm->empty[i % STAGES], (i / STAGES) & 1, abort, 100000000ull);
-      }
+      for (int g = 0; g < armed_groups; ++g)
+        tc::mbar_wait_bounded(&sm->full[g], armed_tile & 1, abort, 100000000ull);
     }
-  } else if (warp == 3) {
+  } else if (warp == W_MMA) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      const uint32_t idesc_s = tc::idesc_bf16_f32(128, TILE);
-      const uint32_t idesc_o = tc::idesc_bf16_f32_bmn(128, DVH);
-      const uint32_t q_addr = tc::smem_addr(q_mem);
+      const uint32_t idesc_s = tc::idesc_bf16_f32(TILE, HG);
+      const uint32_t idesc_o = tc::idesc_bf16_f32_amn_bmn(TILE, HG);
+      const uint32_t q_addr = tc::smem_addr(q_mem), kv_addr = tc::smem_addr(kv_mem);
+      const uint64_t a1 = tc::sdesc_k_sw128(kv_addr), b1 = tc::sdesc_k_sw128(q_addr);
+      const uint64_t a2 = tc::sdesc_mn_sw128(kv_addr, SLOT_BYTES, 1024);
+      const uint64_t b2 = tc::sdesc_mn_sw128(kv_addr + 8 * SLOT_BYTES, SLOT_BYTES, 1024);
       bool ok = tc::mbar_wait_bounded(&sm->qfull, 0, abort);
-      // S = Q K^T of tile i needs the tile (full[i]) and a free S buffer (the softmax of tile i - 2
-      // done, i.e. P V of tile i - 2 issued); P V of tile j needs P (pfull[j]).  Each is issued as soon
-      // as it is ready, so a stage is released right after its P V, not one tile load later.
-      int ns = 0, np = 0;  // next S tile, next P V tile
-      uint64_t t_start = 0;
-      while (ok && np < ntiles) {
-        bool progressed = false;
-        if (ns < ntiles && ns <= np + 1 && tc::mbar_try_wait(&sm->full[ns % STAGES], (ns / STAGES) & 1)) {
+      bool o_started = false;
+      for (int i = 0; i < ntiles && ok; ++i) {
+        for (int g = 0; g < NGROUPS && ok; ++g) {
+          ok = tc::mbar_wait_bounded(&sm->full[g], i & 1, abort);
+          if (!ok) break;
           tc::tc_fence_after();
-          const uint32_t k_addr = tc::smem_addr(stage_mem + (ns % STAGES) * STAGE_BYTES);
-          for (int kb = 0; kb < NKB; ++kb) {
+          const int kb0 = 2 * g, nkb = g < 4 ? 2 : 1;
+          for (int kb = kb0; kb < kb0 + nkb; ++kb) {
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              const uint64_t ad = tc::sdesc_k_sw128(q_addr + kb * HG * 128 + s * 32);
-              const uint64_t bd = tc::sdesc_k_sw128(k_addr + kb * KB_BYTES + s * 32);
-              tc::mma_bf16(tmem + COL_S + (ns & 1) * TILE, ad, bd, idesc_s, (kb | s) != 0);
+            for (int s = 0; s < 4; ++s)  // descriptor start addresses advance in 16-byte units
+              tc::mma_bf16(tmem + COL_S, a1 + (uint64_t)((kb * SLOT_BYTES + s * 32) >> 4),
+                           b1 + (uint64_t)((kb * HG * 128 + s * 32) >> 4), idesc_s, (kb | s) != 0);
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(&sm->sfull);
+        ok = tc::mbar_wait_bounded(&sm->pfull, i & 1, abort);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint32_t ld = sm->loaded[i & 1];
+        for (int m = 0; m < 4; ++m) {
+          bool first = !o_started;
+          for (int u = 0; u < 2; ++u) {
+            if (!((ld >> u) & 1u)) continue;
+#pragma unroll
+            for (int s = 4 * u; s < 4 * u + 4; ++s) {
+              tc::mma_bf16(tmem + COL_O + 64 * m, a2 + (uint64_t)((2 * m * SLOT_BYTES + s * 2048) >> 4),
+                           b2 + (uint64_t)((s * 2048) >> 4), idesc_o, first ? 0u : 1u);
+              first = false;
             }
           }
-          tc::mma_commit(&sm->sfull[ns & 1]);
-          ++ns;
-          progressed = true;
+          tc::mma_commit(&sm->vfree[m]);
         }
-        if (np < ns && tc::mbar_try_wait(&sm->pfull[np & 1], (np >> 1) & 1)) {
-          tc::tc_fence_after();
-          const uint32_t v_addr = tc::smem_addr(stage_mem + (np % STAGES) * STAGE_BYTES + (4 * dh) * KB_BYTES);
-#pragma unroll
-          for (int s = 0; s < TILE / 16; ++s) {
-            const uint64_t bd = tc::sdesc_mn_sw128(v_addr + s * 2048, KB_BYTES, 1024);
-            tc::mma_bf16_ts(tmem + COL_O, tmem + COL_P + (np & 1) * 32 + s * 8, bd, idesc_o,
-                            (np > 0 || s > 0) ? 1u : 0u);
-          }
-          tc::mma_commit_mc(&sm->empty[np % STAGES], 0x3);
-          tc::mma_commit(&sm->pvdone[np & 1]);
-          ++np;
-          progressed = true;
-        }
-        if (progressed) {
-          t_start = 0;
-        } else {  // bounded spin, like every other wait
-          if (*abort) ok = false;
-          const uint64_t now = tc::globaltimer_ns();
-          if (t_start == 0) t_start = now;
-          else if (now - t_start > 250000000ull) {
-            *abort = 1;
-            ok = false;
-          }
-        }
+        tc::mma_commit(&sm->pvdone);
+        if (ld) o_started = true;
       }
       tc::mma_commit(&sm->odone);
     }
   } else {
-    // ---------------- softmax + epilogue: warps 0-1 and 4-5, thread = head (TMEM lane); warps 0-1 own
-    // S columns 0-31, O columns 0-127 and P columns 0-15 of the tile, warps 4-5 the other halves
-    const int half = warp >> 2;
-    const int h = (warp & 3) * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t s_col = COL_S + half * 32, o_col = COL_O + half * (DVH / 2), p_col = COL_P + half * 16;
-    float m_ref = -INFINITY, l = 0.f;
+    // ---------------- softmax + epilogue: warps 0-7; warp w owns tile rows R = 32 (w & 3) + lane (TMEM
+    // lane R) and heads 32 hf .. 32 hf + 31 (hf = w >> 2)
+    const int qd = warp & 3, hf = warp >> 2;
+    const int R = qd * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+    float mref = -INFINITY;  // running max (log2 domain) of head 32 hf + lane
+    float lp[32];            // this thread's share of each of the 32 heads' sums
+#pragma unroll
+    for (int k = 0; k < 32; ++k) lp[k] = 0.f;
     bool ok = true;
+    uint8_t* prow = kv_mem + 8 * SLOT_BYTES + (R >> 3) * 1024 + (R & 7) * 128;  // P^T row R
+    float* mrow = sm->mrow[warp];
     for (int i = 0; i < ntiles; ++i) {
-      if (!tc::mbar_wait_bounded(&sm->sfull[i & 1], (i >> 1) & 1, abort)) {
+      if (!tc::mbar_wait_bounded(&sm->sfull, i & 1, abort) ||
+          !tc::mbar_wait_bounded(&sm->full[0], i & 1, abort)) {  // full[0] published the row mask
         ok = false;
         break;
       }
-      // the stage's row mask was published with its full barrier
-      tc::mbar_wait_bounded(&sm->full[i % STAGES], (i / STAGES) & 1, abort);
       tc::tc_fence_after();
       uint32_t r[32];
-      tc::tmem_ld32_nowait(lane_base + s_col + (i & 1) * TILE, r);
+      tc::tmem_ld32_nowait(lane_base + COL_S + 32 * hf, r);
       tc::tmem_wait_ld_regs<32>(r);
-      const uint32_t mask = (uint32_t)(sm->mask[i % STAGES] >> (32 * half));
+      const bool valid = (sm->mask[i & 1][qd] >> lane) & 1u;
+      const bool loaded = (sm->loaded[i & 1] >> (qd >> 1)) & 1u;
       float z[32];
-      float mt = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        z[k] = ((mask >> k) & 1u) ? __uint_as_float(r[k]) * a.c_log2 : -INFINITY;
-        mt = fmaxf(mt, z[k]);
-      }
-      // row max over both halves (an mbarrier, so the wait is bounded like every other one)
-      sm->xmax[i & 1][half][h] = mt;
+      for (int k = 0; k < 32; ++k) z[k] = valid ? __uint_as_float(r[k]) * a.c_log2 : -INFINITY;
+      sm->red[i & 1][hf][qd][lane] = transpose_reduce32<true>(z, lane);
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm->xbar[i & 1]);
-      if (!tc::mbar_wait_bounded(&sm->xbar[i & 1], (i >> 1) & 1, abort)) {
+      if (lane == 0) tc::mbar_arrive(&sm->xbar[i & 1][hf]);
+      if (!tc::mbar_wait_bounded(&sm->xbar[i & 1][hf], (i >> 1) & 1, abort)) {
         ok = false;
         break;
       }
-      mt = fmaxf(mt, sm->xmax[i & 1][half ^ 1][h]);
-      const float m_new = fmaxf(m_ref, mt);
-      if (m_ref == -INFINITY) {
-        m_ref = m_new;  // nothing accumulated yet that is not zero
-      } else if (m_new > m_ref + RESCALE_LOG2) {
-        // O must be stable (the previous P V done) before it is rescaled in place
-        if (!tc::mbar_wait_bounded(&sm->pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, abort)) {
+      float mt = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) mt = fmaxf(mt, sm->red[i & 1][hf][w][lane]);
+      float f = 1.f;
+      if (mref == -INFINITY) {
+        mref = mt;
+      } else if (mt > mref + RESCALE_LOG2) {
+        f = tc::ex2_approx(mref - mt);
+        mref = mt;
+      }
+      // the same decision in the 4 warps of this head half: they computed it from the same maxima
+      const bool resc = __any_sync(0xffffffffu, f != 1.f);
+      mrow[lane] = mref;
+      mrow[32 + lane] = f;
+      __syncwarp();
+      uint32_t pk[16];
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(mrow + k);
+        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        float e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) e[u] = mm[u] == -INFINITY ? 0.f : tc::ex2_approx(z[k + u] - mm[u]);
+        if (resc) {
+          const float4 f4 = *reinterpret_cast<const float4*>(mrow + 32 + k);
+          lp[k] = fmaf(lp[k], f4.x, e[0]);
+          lp[k + 1] = fmaf(lp[k + 1], f4.y, e[1]);
+          lp[k + 2] = fmaf(lp[k + 2], f4.z, e[2]);
+          lp[k + 3] = fmaf(lp[k + 3], f4.w, e[3]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) lp[k + u] += e[u];
+        }
+        pk[k >> 1] = float2_to_bf16x2_bits(e[0], e[1]);
+        pk[(k >> 1) + 1] = float2_to_bf16x2_bits(e[2], e[3]);
+      }
+      // P^T row R, heads 32 hf .. 32 hf + 31 = 16-byte chunks 4 hf .. 4 hf + 3, over slot 8 (QK^T of
+      // this tile is done with it)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(prow + (((4 * hf + c) ^ (R & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      if (!valid && loaded) {  // a masked row that was loaded: zero its V so that 0 x garbage stays 0
+        uint8_t* vrow = kv_mem + (R >> 3) * 1024 + (R & 7) * 128;
+#pragma unroll
+        for (int kb = 4 * hf; kb < 4 * hf + 4; ++kb)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + kb * SLOT_BYTES + c * 16) = make_uint4(0, 0, 0, 0);
+      }
+      tc::fence_proxy_async_smem();
+      if (resc && i > 0) {
+        // O^T must be stable (PV of the previous tile retired) before its columns are rescaled in place
+        if (!tc::mbar_wait_bounded(&sm->pvdone, (i - 1) & 1, abort)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
-        const float f = tc::ex2_approx(m_ref - m_new);
-        l *= f;
-        for (int c = 0; c < DVH / 2; c += 32) {
+        for (int m = 0; m < 4; ++m) {
           uint32_t o[32];
-          tc::tmem_ld32_nowait(lane_base + o_col + c, o);
+          tc::tmem_ld32_nowait(lane_base + COL_O + 64 * m + 32 * hf, o);
           tc::tmem_wait_ld_regs<32>(o);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-          tc::tmem_st32(lane_base + o_col + c, o);
+          for (int k = 0; k < 32; k += 4) {
+            const float4 f4 = *reinterpret_cast<const float4*>(mrow + 32 + k);
+            o[k] = __float_as_uint(__uint_as_float(o[k]) * f4.x);
+            o[k + 1] = __float_as_uint(__uint_as_float(o[k + 1]) * f4.y);
+            o[k + 2] = __float_as_uint(__uint_as_float(o[k + 2]) * f4.z);
+            o[k + 3] = __float_as_uint(__uint_as_float(o[k + 3]) * f4.w);
+          }
+          tc::tmem_st32(lane_base + COL_O + 64 * m + 32 * hf, o);
         }
         tc::tmem_wait_st();
-        m_ref = m_new;
       }
-      uint32_t pk[16];
-      float ls = 0.f;
-      const bool live = m_ref != -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float e0 = live ? tc::ex2_approx(z[2 * k] - m_ref) : 0.f;
-        const float e1 = live ? tc::ex2_approx(z[2 * k + 1] - m_ref) : 0.f;
-        ls += e0 + e1;
-        pk[k] = float2_to_bf16x2_bits(e0, e1);
-      }
-      l += ls;
-      // P buffer (i & 1) was last read by the P V product of tile i - 2
-      if (i >= 2 && !tc::mbar_wait_bounded(&sm->pvdone[i & 1], ((i - 2) >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      tc::tmem_st16(lane_base + p_col + (i & 1) * 32, pk);
-      tc::tmem_wait_st();
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm->pfull[i & 1]);
+      if (lane == 0) tc::mbar_arrive(&sm->pfull);
     }
     if (ok && tc::mbar_wait_bounded(&sm->odone, 0, abort)) {
       tc::tc_fence_after();
-      float* dst = a.o_part + (part + h) * DV + dh * DVH + half * (DVH / 2);
-      for (int c = 0; c < DVH / 2; c += 32) {
+      // O^T (lane R = value dim 128 m + R, column = head) is turned into [head][value] rows in the
+      // now idle tile buffer, then stored with 16-byte writes
+      float* ot = reinterpret_cast<float*>(kv_mem);  // [64 heads][512 values] fp32 = 128 KB
+      for (int m = 0; m < 4; ++m) {
         uint32_t o[32];
-        tc::tmem_ld32_nowait(lane_base + o_col + c, o);
+        tc::tmem_ld32_nowait(lane_base + COL_O + 64 * m + 32 * hf, o);
         tc::tmem_wait_ld_regs<32>(o);
 #pragma unroll
-        for (int k = 0; k < 32; k += 4)
-          *reinterpret_cast<float4*>(dst + c + k) = make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]),
-                                                                 __uint_as_float(o[k + 2]), __uint_as_float(o[k + 3]));
+        for (int k = 0; k < 32; ++k) ot[(32 * hf + k) * DV + 128 * m + R] = __uint_as_float(o[k]);
       }
-      sm->lsum[half][h] = l;  // the two halves' sums
+      sm->lred[hf][qd][lane] = transpose_reduce32<false>(lp, lane);
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm->lbar);
-      if (tc::mbar_wait_bounded(&sm->lbar, 0, abort) && dh == 0 && half == 0)
-        a.ml_part[part + h] = make_float2(m_ref * 0.69314718055994531f, l + sm->lsum[1][h]);
+      if (lane == 0) tc::mbar_arrive(&sm->ebar);
+      if (tc::mbar_wait_bounded(&sm->ebar, 0, abort)) {
+        float4* dst = reinterpret_cast<float4*>(a.o_part + part * DV);
+        const float4* src = reinterpret_cast<const float4*>(ot);
+        for (int x = threadIdx.x; x < HG * DV / 4; x += 256) dst[x] = src[x];
+        if (qd == 0) {
+          float l = 0.f;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) l += sm->lred[hf][w][lane];
+          a.ml_part[part + 32 * hf + lane] = make_float2(mref * 0.69314718055994531f, l);
+        }
+      }
     }
   }
-  tc::cluster_sync_all();  // the partner no longer loads into or releases through this CTA
+  __syncthreads();
   if (threadIdx.x == 0 && sm->abort) atomicOr(&g_flags_at, FLAG_TIMEOUT);
-  if (warp == 3) {
+  if (warp == W_MMA) {
+    // no MMA may still write TMEM when it is released (already true unless the CTA aborted)
+    if (lane == 0) tc::mbar_wait_bounded(&sm->odone, 0, abort, 100000000ull);
+    __syncwarp();
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -630,47 +753,34 @@ static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p,
   a.o_part = o_part;
   a.ml_part = ml_part;
   a.n_chunks = L.n_chunks;
-  a.chunk_rows = L.chunk_rows;
+  a.chunk_halves = L.chunk_rows / HALF;
   a.swa_rows = (int)(p.swa_num_pages * p.page_size);
   a.main_rows = p.ratio > 0 ? (int)(p.main_num_pages * p.page_size) : a.swa_rows;
   a.c_log2 = p.softmax_scale * 1.4426950408889634f;
-  CUtensorMap qmap, swamap, mainmap, mainmap64;
+  CUtensorMap qmap, swamap64, mainmap, mainmap64;
   cudaError_t e = make_tmap_2d_bf16(&qmap, p.q, (uint64_t)D, (uint64_t)p.T * p.H, 64, HG);
   if (e != cudaSuccess) return e;
-  e = make_tmap_2d_bf16(&swamap, p.swa_cache, (uint64_t)D, (uint64_t)a.swa_rows, 64, 1);
+  e = make_tmap_2d_bf16(&swamap64, p.swa_cache, (uint64_t)D, (uint64_t)a.swa_rows, 64, HALF);
   if (e != cudaSuccess) return e;
   if (p.ratio > 0) {
     e = make_tmap_2d_bf16(&mainmap, p.main_cache, (uint64_t)D, (uint64_t)a.main_rows, 64, 1);
     if (e != cudaSuccess) return e;
-    e = make_tmap_2d_bf16(&mainmap64, p.main_cache, (uint64_t)D, (uint64_t)a.main_rows, 64, 64);
+    e = make_tmap_2d_bf16(&mainmap64, p.main_cache, (uint64_t)D, (uint64_t)a.main_rows, 64, HALF);
     if (e != cudaSuccess) return e;
-  } else {
-    mainmap = swamap;
-    mainmap64 = swamap;
+  } else {  // no compressed rows: the main-cache maps are never used (still valid maps)
+    e = make_tmap_2d_bf16(&mainmap, p.swa_cache, (uint64_t)D, (uint64_t)a.swa_rows, 64, 1);
+    if (e != cudaSuccess) return e;
+    mainmap64 = swamap64;
   }
-  const size_t smem = 1024 + (size_t)Q_BYTES + (size_t)STAGES * STAGE_BYTES + sizeof(Smem);
+  const size_t smem = 1024 + (size_t)Q_BYTES + (size_t)KV_BYTES + sizeof(Smem);
   static int attr_done = 0;
   if (!attr_done) {
     e = cudaFuncSetAttribute(mla_partial_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = 1;
   }
-  dim3 grid(L.n_chunks, p.T, (p.H / HG) * 2);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;  // the two value halves of a (chunk, token, head group)
-  attr[1].val.clusterDim.x = 1;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 2;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, mla_partial_tc, qmap, swamap, mainmap, mainmap64, a);
+  return launch_pdl(mla_partial_tc, dim3(L.n_chunks, p.T, p.H / HG), dim3(THREADS), smem, st, true, qmap, swamap64,
+                    mainmap, mainmap64, a);
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -259,6 +259,11 @@ __device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo,
 // kind::f16 instruction descriptor with bf16 A (K-major), bf16 B (MN-major), fp32 D, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) { return idesc_bf16_f32(M, N) | (1u << 16); }
 
+// kind::f16 instruction descriptor with both bf16 operands MN-major, fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_amn_bmn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);
+}
+
 
 // ---------------------------------------------------------------------------------------------
 // cp.async (16-byte global -> shared copies) feeding tcgen05 operands
