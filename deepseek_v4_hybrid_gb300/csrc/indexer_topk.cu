@@ -6,15 +6,16 @@
 // DeepseekV4Indexer.forward (when the candidates fit in top-k, every candidate is selected).
 // Score: s[t][j] = sum_h w[t][h] * ReLU(q[t][h] . k_j) in fp32.
 //
-// Kernels of one call:
+// One call:
 //  1. score: a CTA works on 128-key tiles of one sequence for all of that sequence's query tokens,
 //     so each key row leaves HBM once per step.  bf16 keys run on the tensor cores (tcgen05 MMA,
 //     TMA-fed); fp32 and int8 keys on the CUDA cores.  Besides the score row of each token, the
 //     epilogue builds a 4096-bin histogram of the scores' top 12 order-preserving key bits.
-//  2. collect: from the histogram, the bin B* holding the k-th best score; every entry above B*
-//     is selected outright, every entry inside B* becomes a candidate.
-//  3. final: exact choice among the candidates (larger score first, then smaller j), then the
-//     selection sorted by j.
+//  2. top-k (tk::topk_token, one CTA per token): from the histogram, the bin B* holding the k-th
+//     best score; every entry above B* is selected outright, the k - A best entries inside B* are
+//     chosen exactly (larger score first, then smaller j); the selection is written sorted by j.
+//     On the tensor-core path the CTA that scores the last tile of a sequence runs it at its end
+//     (no further launch); the CUDA-core path launches one CTA per token after scoring.
 #include "dsv4_common.cuh"
 #include "dsv4_launch.h"
 #include "tc_ptx.cuh"
@@ -55,30 +56,28 @@ __device__ __forceinline__ int visible_entries(const dsv4_indexer_topk_params& p
 // ------------------------------------------------------------------------------------------------
 struct IxLayout {
   size_t nc_stride;
-  size_t scores_off, hist_off, cnt_off, certain_off, maybe_off, total;
+  size_t scores_off, hist_off, done_off, cand_off, total;
 };
 
 static IxLayout ix_layout(const dsv4_indexer_topk_params& p) {
   IxLayout L;
   const int64_t max_nc = (int64_t)p.max_context / p.ratio;
-  L.nc_stride = align_up((size_t)(max_nc > 0 ? max_nc : 1), 64);
+  L.nc_stride = align_up((size_t)(max_nc > 0 ? max_nc : 1), 128);  // whole 128-entry scan blocks
   L.scores_off = 0;
   L.hist_off = align_up(L.scores_off + (size_t)p.T * L.nc_stride * sizeof(float), 256);
-  L.cnt_off = L.hist_off + (size_t)p.T * HIST_BINS * sizeof(uint32_t);  // zeroed together with hist
-  L.certain_off = align_up(L.cnt_off + (size_t)p.T * 3 * sizeof(uint32_t), 256);
-  L.maybe_off = align_up(L.certain_off + (size_t)p.T * p.topk * sizeof(int32_t), 256);
-  L.total = align_up(L.maybe_off + (size_t)p.T * L.nc_stride * sizeof(uint64_t), 256);
+  L.done_off = L.hist_off + (size_t)p.T * HIST_BINS * sizeof(uint32_t);  // zeroed together with hist
+  L.cand_off = align_up(L.done_off + (size_t)p.B * sizeof(uint32_t), 256);
+  L.total = align_up(L.cand_off + (size_t)p.T * L.nc_stride * sizeof(uint64_t), 256);
   return L;
 }
 
 size_t indexer_topk_workspace(const dsv4_indexer_topk_params& p) { return ix_layout(p).total; }
 
 struct TopkBufs {
-  float* scores;
-  uint32_t* hist;      // [T][HIST_BINS]
-  uint32_t* cnt;       // [T][3]: selected-outright count, candidate count, finished collect CTAs
-  int32_t* certain;    // [T][topk]
-  uint64_t* maybe;     // [T][nc_stride] candidates: (low 20 key bits << 32) | ~j
+  float* scores;       // [T][nc_stride]
+  uint32_t* hist;      // [T][HIST_BINS] counts of the scores' top 12 order-key bits
+  uint32_t* seq_done;  // [B] key tiles of the sequence scored so far (tensor-core path)
+  uint64_t* cand;      // [T][nc_stride] top-k candidates that do not fit in shared memory
   int nc_stride;
 };
 
@@ -90,6 +89,304 @@ __device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool
   const unsigned peers = __match_any_sync(active, bin);
   if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
 }
+
+// ------------------------------------------------------------------------------------------------
+// Top-k of one token, run by one whole CTA once the token's scores and histogram are complete.
+// The histogram and the score row reach shared memory by bulk (TMA) copies, the row in 16 KB chunks
+// with up to four in flight (plain loads would go through an L1 that the kernels' large shared
+// memory leaves almost no room).
+//  1. From the histogram, the bin B* holding the k-th best score and the count A of scores above it
+//     (256 threads own 16 bins each, a block scan from the top finds the crossing thread).
+//  2. One pass over the scores: lane l of a warp takes entries 4l .. 4l + 3 of a 128-entry block;
+//     their "bin > B*" bits are gathered into the block's four 32-bit words of the selection bitmap
+//     with three shuffles, and entries in B* are appended to a candidate list as (low 20 key bits,
+//     j) values.
+//  3. The k - A largest candidates (larger score first, then smaller j: the values are unique) by a
+//     radix select of 10-bit digits over the 40-bit values, stopping at the first digit whose bin
+//     holds exactly the entries still needed; they are added to the bitmap.
+//  4. The bitmap is compacted in increasing j into the output row; -1 pads it.
+// ------------------------------------------------------------------------------------------------
+namespace tk {
+constexpr int RBINS = 1024;       // radix bins (10-bit digits)
+constexpr int J_BITS = 20;        // n_c <= 2^20 (checked on the host)
+constexpr int CTL_BYTES = 512;
+constexpr int FIND_THREADS = 256;  // threads that own histogram bins in block_find_bin
+constexpr int CHUNK = 4096;       // scores per bulk copy (16 KB)
+constexpr int NBUF = 4;           // chunk buffers (copies in flight)
+
+struct Ctl {
+  uint64_t bar[NBUF + 1];  // chunk buffers, histogram
+  uint32_t bin, above, cnt, ncand;
+  int wt[40];  // block scan scratch
+};
+static_assert(sizeof(Ctl) <= CTL_BYTES, "top-k control block");
+
+// Candidate value: (low 20 order-key bits << 20) | (2^20 - 1 - j); larger = better score, then smaller j.
+__device__ __forceinline__ uint64_t cand_value(uint32_t key, int j) {
+  return ((uint64_t)(key & ((1u << HIST_SHIFT) - 1u)) << J_BITS) | (uint64_t)((1u << J_BITS) - 1u - (uint32_t)j);
+}
+__device__ __forceinline__ int cand_j(uint64_t v) {
+  return (int)((1u << J_BITS) - 1u - (uint32_t)(v & ((1u << J_BITS) - 1u)));
+}
+
+// Offsets in the shared buffer: control, radix bins, bitmap, histogram, chunks, candidates.
+__host__ __device__ inline size_t hist_offset(int n) {
+  return (CTL_BYTES + RBINS * 4 + ((size_t)n + 31) / 32 * 4 + 127) / 128 * 128;
+}
+__host__ __device__ inline size_t fixed_bytes(int n) {
+  return hist_offset(n) + (size_t)HIST_BINS * 4 + (size_t)NBUF * CHUNK * 4;
+}
+
+// Exclusive prefix sum of one value per thread over the CTA; *total gets the sum.
+__device__ __forceinline__ int block_excl_scan(int v, int* wt, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) wt[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nw ? wt[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += u;
+    }
+    if (lane < nw) wt[lane] = wi - w;
+    if (lane == 31) wt[32] = wi;
+  }
+  __syncthreads();
+  const int r = wt[warp] + incl - v;
+  *total = wt[32];
+  __syncthreads();
+  return r;
+}
+
+// The bin of shared histogram h (256 * PER bins) where the count from the top first reaches rem:
+// c->bin, the count in the bins above it: c->above, its own count: c->cnt.  Thread i < 256 owns
+// bins [256 PER - PER (i + 1), 256 PER - PER i) (the top bins first).  Called by the whole CTA.
+template <int PER>
+__device__ __forceinline__ void block_find_bin(const uint32_t* h, uint32_t rem, Ctl* c) {
+  const int tid = threadIdx.x;
+  uint32_t v[PER];
+  uint32_t sum = 0;
+  if (tid < FIND_THREADS) {
+    const uint4* src = reinterpret_cast<const uint4*>(h + FIND_THREADS * PER - PER * (tid + 1));
+#pragma unroll
+    for (int q = 0; q < PER / 4; ++q) {
+      const uint4 u = src[q];
+      v[4 * q] = u.x;
+      v[4 * q + 1] = u.y;
+      v[4 * q + 2] = u.z;
+      v[4 * q + 3] = u.w;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) sum += v[i];
+  }
+  int total;
+  const uint32_t excl = (uint32_t)block_excl_scan((int)sum, c->wt, &total);
+  if (tid < FIND_THREADS && excl < rem && excl + sum >= rem) {
+    uint32_t cum = excl;
+#pragma unroll
+    for (int i = PER - 1; i >= 0; --i) {
+      if (cum < rem && cum + v[i] >= rem) {
+        c->bin = (uint32_t)(FIND_THREADS * PER - PER * (tid + 1) + i);
+        c->above = cum;
+        c->cnt = v[i];
+      }
+      cum += v[i];
+    }
+  }
+  __syncthreads();
+}
+
+// The whole CTA selects the top K of token scores s_g[0, n) (row 16-byte aligned with room for
+// round_up(n, 128) entries; the histogram hist_g of their order keys is complete) into out[0, K) in
+// increasing j (out_s: their scores, may be null); gcand (n entries) holds candidates that do not fit
+// in `buf` (buf_bytes of 128-byte aligned shared memory).  Returns false if a copy timed out.
+__device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int K, int32_t* out, float* out_s,
+                           uint64_t* gcand, uint8_t* buf, size_t buf_bytes, volatile int* abort) {
+  const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31, warp = tid >> 5, NW = NT >> 5;
+  if (n <= K) {  // short context: every entry, in order
+    for (int x = tid; x < K; x += NT) {
+      out[x] = x < n ? x : -1;
+      if (out_s) out_s[x] = x < n ? __ldcg(s_g + x) : -INFINITY;
+    }
+    return true;
+  }
+  const size_t fixed = fixed_bytes(n);
+  if (fixed > buf_bytes) {  // cannot happen for n <= 2^20 with the buffers the kernels pass
+    if (tid == 0) atomicOr(&g_flags_ix, FLAG_TOPK);
+    for (int x = tid; x < K; x += NT) out[x] = -1;
+    return false;
+  }
+  Ctl* c = reinterpret_cast<Ctl*>(buf);
+  uint32_t* rb = reinterpret_cast<uint32_t*>(buf + CTL_BYTES);
+  const int words = (n + 31) >> 5;
+  uint32_t* bits = rb + RBINS;
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(buf + hist_offset(n));
+  uint8_t* chunks = reinterpret_cast<uint8_t*>(hist_s + HIST_BINS);
+  uint64_t* cand_s = reinterpret_cast<uint64_t*>(buf + fixed);
+  const uint32_t cap = (uint32_t)((buf_bytes - fixed) / 8);
+  const int nchunks = (n + CHUNK - 1) / CHUNK;
+  const int n128 = (n + 127) & ~127;  // copy whole 128-entry blocks (the row has room)
+  // the whole row stays in the chunk buffers when it fits (then the output scores come from there)
+  const bool resident = nchunks <= NBUF;
+
+  if (tid == 0) {
+    c->bin = 0;
+    c->above = 0;
+    c->cnt = 0;
+    c->ncand = 0;
+    for (int i = 0; i <= NBUF; ++i) tc::mbar_init(&c->bar[i], 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int cc) {
+    const uint32_t bytes = (uint32_t)min(CHUNK, n128 - cc * CHUNK) * 4u;
+    uint64_t* bar = &c->bar[cc % NBUF];
+    tc::mbar_arrive_expect_tx(bar, bytes);
+    tc::bulk_load(chunks + (size_t)(cc % NBUF) * CHUNK * 4, s_g + (size_t)cc * CHUNK, bytes, bar);
+  };
+  if (tid == 0) {
+    // the scores and counts were written through the generic proxy (possibly by other CTAs): order
+    // them before the bulk copies read them
+    asm volatile("fence.proxy.async;" ::: "memory");
+    tc::mbar_arrive_expect_tx(&c->bar[NBUF], HIST_BINS * 4);
+    tc::bulk_load(hist_s, hist_g, HIST_BINS * 4, &c->bar[NBUF]);
+    for (int cc = 0; cc < min(NBUF, nchunks); ++cc) issue(cc);
+  }
+
+  // 1. threshold bin
+  if (!__syncthreads_and(tc::mbar_wait_bounded(&c->bar[NBUF], 0, abort))) {
+    if (tid == 0)  // copies in flight land before the buffer is given back
+      for (int cc = 0; cc < min(NBUF, nchunks); ++cc) tc::mbar_wait_bounded(&c->bar[cc], 0, abort, 100000000ull);
+    for (int x = tid; x < K; x += NT) out[x] = -1;
+    __syncthreads();
+    return false;
+  }
+  block_find_bin<HIST_BINS / FIND_THREADS>(hist_s, (uint32_t)K, c);
+  const uint32_t bstar = c->bin;
+  const int R = K - (int)c->above;  // still to choose among the candidates
+  const uint32_t C = c->cnt;        // scores in the threshold bin
+  uint64_t* cand = C <= cap ? cand_s : gcand;
+  const uint32_t ccap = C <= cap ? cap : (uint32_t)n;
+
+  // 2. selection bitmap and candidates: in each chunk warp w takes 128-entry blocks w, w + NW, ...
+  int stop = nchunks;  // first chunk not consumed
+  for (int cc = 0; cc < nchunks; ++cc) {
+    if (!__syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc % NBUF], (cc / NBUF) & 1, abort))) {
+      stop = cc;
+      break;
+    }
+    const float4* sb = reinterpret_cast<const float4*>(chunks + (size_t)(cc % NBUF) * CHUNK * 4);
+    const int nb = min(CHUNK, n128 - cc * CHUNK) >> 7;
+    for (int bl = warp; bl < nb; bl += NW) {
+      const float4 v = sb[bl * 32 + lane];
+      const int j0 = cc * CHUNK + bl * 128 + 4 * lane;
+      const float e[4] = {v.x, v.y, v.z, v.w};
+      uint32_t sel = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = j0 + k;
+        const uint32_t key = order_key(e[k]);
+        const uint32_t bin = key >> HIST_SHIFT;
+        if (j < n && bin > bstar) sel |= 1u << k;
+        if (j < n && bin == bstar) {
+          const uint32_t idx = atomicAdd(&c->ncand, 1u);
+          if (idx < ccap) cand[idx] = cand_value(key, j);
+        }
+      }
+      uint32_t w = sel << (4 * (lane & 7));
+      w |= __shfl_xor_sync(0xffffffffu, w, 1);
+      w |= __shfl_xor_sync(0xffffffffu, w, 2);
+      w |= __shfl_xor_sync(0xffffffffu, w, 4);
+      const int wg = ((cc * CHUNK) >> 5) + bl * 4 + (lane >> 3);
+      if ((lane & 7) == 0 && wg < words) bits[wg] = w;
+    }
+    if (cc + NBUF < nchunks) {
+      tc::fence_proxy_async_smem();  // reads of this buffer come before the next copy into it
+      __syncthreads();
+      if (tid == 0) issue(cc + NBUF);
+    }
+  }
+  if (stop < nchunks) {
+    if (tid == 0)  // copies in flight (chunks stop .. stop + NBUF - 1) land before the buffer is given back
+      for (int cc = stop; cc < min(nchunks, stop + NBUF); ++cc)
+        tc::mbar_wait_bounded(&c->bar[cc % NBUF], (cc / NBUF) & 1, abort, 100000000ull);
+    for (int x = tid; x < K; x += NT) out[x] = -1;
+    __syncthreads();
+    return false;
+  }
+  __syncthreads();
+
+  // 3. exact choice among the candidates
+  const uint32_t m = min(c->ncand, ccap);
+  if (R > 0 && (uint32_t)R < m) {
+    uint64_t prefix = 0, thr = 0;
+    uint32_t rem = (uint32_t)R;
+    for (int shift = 30; shift >= 0; shift -= 10) {
+      for (int x = tid; x < RBINS; x += NT) rb[x] = 0u;
+      __syncthreads();
+      const uint64_t hmask = shift == 30 ? 0ull : ((1ull << 40) - 1ull) & ~((1ull << (shift + 10)) - 1ull);
+      for (uint32_t i = tid; i < m; i += NT) {
+        const uint64_t v = cand[i];
+        if ((v & hmask) == prefix) atomicAdd(&rb[(v >> shift) & (RBINS - 1)], 1u);
+      }
+      __syncthreads();
+      block_find_bin<RBINS / FIND_THREADS>(rb, rem, c);
+      prefix |= (uint64_t)c->bin << shift;
+      rem -= c->above;
+      thr = prefix;
+      if (c->cnt == rem) break;  // every candidate of this digit is needed: v >= prefix selects them
+    }
+    for (uint32_t i = tid; i < m; i += NT) {
+      const uint64_t v = cand[i];
+      if (v >= thr) {
+        const int j = cand_j(v);
+        atomicOr(&bits[j >> 5], 1u << (j & 31));
+      }
+    }
+  } else if (R > 0) {
+    for (uint32_t i = tid; i < m; i += NT) {
+      const int j = cand_j(cand[i]);
+      atomicOr(&bits[j >> 5], 1u << (j & 31));
+    }
+  }
+  __syncthreads();
+
+  // 4. compaction in increasing j
+  const float* row_s = reinterpret_cast<const float*>(chunks);
+  const int per = (words + NT - 1) / NT;
+  const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+  int total;
+  int pos = block_excl_scan(cnt, c->wt, &total);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bw = bits[w];
+    while (bw) {
+      const int j = (w << 5) + __ffs(bw) - 1;
+      bw &= bw - 1;
+      if (pos < K) {
+        out[pos] = j;
+        if (out_s) out_s[pos] = resident ? row_s[j] : __ldcg(s_g + j);
+      }
+      ++pos;
+    }
+  }
+  for (int x = total + tid; x < K; x += NT) {
+    out[x] = -1;
+    if (out_s) out_s[x] = -INFINITY;
+  }
+  __syncthreads();  // the buffer may be reused right away
+  return true;
+}
+}  // namespace tk
 
 // ------------------------------------------------------------------------------------------------
 // SIMT score kernel (any key dtype): thread jj of the CTA owns key tile*128 + jj.
@@ -172,32 +469,43 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
 // s_k = sum_h w[k][h] * ReLU(D[key][k*n_heads + h]).
 //
 // Persistent CTAs (one per SM), each owning a contiguous range of (sequence, 128-key tile) items.
-// Warp 4 streams key tiles with TMA (two 64-row pages x d/64 K-blocks of 128 B, 128-byte swizzle)
+// Warp 8 streams key tiles with TMA (two 64-row pages x d/64 K-blocks of 128 B, 128-byte swizzle)
 // into a ring of stages, and each sequence's Q block into one of two Q slots; its 32 lanes look up
-// the block-table pages of 32 items at a time.  One thread of warp 5 issues the tcgen05 MMAs
-// (M = 128, K = 16 steps) into one of two TMEM accumulators; warps 0-3 read their 32 TMEM lanes
-// each (one key per thread), apply ReLU and the head weights, store the scores and count them
-// into a shared-memory histogram that is added to the global one when the sequence changes.
+// the block-table pages of 32 items at a time.  One thread of warp 9 issues the tcgen05 MMAs
+// (M = 128, K = 16 steps) into a ring of TMEM accumulators.  Warps 0-7 are two epilogue groups of
+// four that take alternate tiles: each warp reads its 32 TMEM lanes (one key per thread), applies
+// ReLU and the head weights, stores the scores and counts them into its group's shared-memory
+// histogram, which is added to the global one when the group leaves a sequence.  The group then
+// adds the tiles it scored to the sequence's counter; the group that completes the count records
+// the sequence, and after its tiles the CTA runs the top-k of that sequence's tokens itself.
 // Every wait is bounded; a timeout raises FLAG_TIMEOUT and all roles drain out.
 // ------------------------------------------------------------------------------------------------
 namespace ixtc {
 constexpr int TILE = 128;
 constexpr int KB_BYTES = TILE * 128;         // one 64-dim K-block of a key tile (128 rows x 128 B)
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;
+constexpr int W_LOAD = 8, W_MMA = 9;
 constexpr int MAX_STAGES = 8;
+constexpr int FIN_MAX = 64;  // sequences whose top-k one CTA may have to run
+constexpr int WSEQ = 8;      // sequences whose head weights and entry counts are loaded up front
 
 struct Args {
   const int32_t* positions;
   const int32_t* block_table;
   const float* weights;
   TopkBufs bufs;
+  int32_t* topk_idx;
+  float* topk_score;
   int64_t num_pages;
-  int T, B, qps, Ih, d, ratio, max_pages, tiles_max, max_context;
+  int T, B, qps, Ih, d, ratio, max_pages, tiles_max, max_context, K;
   int N, kblk, stages, tmem_cols, nacc;
 };
 
 struct Smem {
-  uint64_t full[MAX_STAGES], empty[MAX_STAGES], dfull[4], dempty[4], qfull[2], qempty[2], done, ebar;
+  uint64_t full[MAX_STAGES], empty[MAX_STAGES], dfull[4], dempty[4], qfull[2], qempty[2], done, ebar[2];
+  int fin[FIN_MAX];
+  int nc_tab[WSEQ][DSV4_MAX_Q_PER_SEQ];
+  uint32_t nfin;
   uint32_t tmem_base;
   int abort;
 };
@@ -248,21 +556,32 @@ struct ItemIter {
   __device__ __forceinline__ bool valid() const { return it < hi; }
 };
 
-// Adds the shared histogram of sequence b (if any) to the global one and clears it (the four
-// epilogue warps, with bounded group barriers before and after).
-__device__ __forceinline__ bool flush_hist(const Args& a, uint32_t* hist_s, int b, int row, uint64_t* ebar,
+// An epilogue group leaves sequence b after scoring `ntile` of its tiles: its shared histogram is
+// added to the global one and cleared, its writes are made visible device-wide, and its tiles are
+// added to the sequence's counter; the group that completes it records b for the CTA's top-k.
+// Called by the group's four warps, with bounded group barriers.
+__device__ __forceinline__ bool finish_seq(const Args& a, Smem* sm, uint32_t* hist_g, int b, int ntile, int g, int row,
                                            uint32_t* ephase, volatile int* abort) {
-  if (!tc::group_sync(ebar, ephase, abort)) return false;
-  if (b >= 0) {
-    for (int x = row; x < a.qps * HIST_BINS; x += 128) {
-      const uint32_t v = hist_s[x];
-      if (v) {
-        atomicAdd(&a.bufs.hist[(int64_t)(b * a.qps + x / HIST_BINS) * HIST_BINS + (x % HIST_BINS)], v);
-        hist_s[x] = 0;
-      }
+  if (!tc::group_sync(&sm->ebar[g], ephase, abort)) return false;
+  for (int x = row; x < a.qps * HIST_BINS; x += 128) {
+    const uint32_t v = hist_g[x];
+    if (v) {
+      atomicAdd(&a.bufs.hist[(int64_t)(b * a.qps + x / HIST_BINS) * HIST_BINS + (x % HIST_BINS)], v);
+      hist_g[x] = 0;
     }
   }
-  return tc::group_sync(ebar, ephase, abort);
+  __threadfence();  // this thread's scores and histogram counts before the counter below
+  if (!tc::group_sync(&sm->ebar[g], ephase, abort)) return false;
+  if (row == 0) {
+    const uint32_t tiles = (uint32_t)((seq_entries(a, b) + TILE - 1) / TILE);
+    const uint32_t prev = atomicAdd(&a.bufs.seq_done[b], (uint32_t)ntile);
+    if (prev + (uint32_t)ntile == tiles) {
+      const uint32_t i = atomicAdd(&sm->nfin, 1u);
+      if (i < FIN_MAX) sm->fin[i] = b;
+      else atomicOr(&g_flags_ix, FLAG_TOPK);
+    }
+  }
+  return true;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -273,9 +592,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int stage_bytes = a.kblk * KB_BYTES;
   uint8_t* stage_mem = base;                                               // stages x stage_bytes
   uint8_t* q_mem = base + a.stages * stage_bytes;                          // 2 slots x q_bytes
-  float* w_s = reinterpret_cast<float*>(q_mem + 2 * q_bytes);              // 256 floats
-  uint32_t* hist_s = reinterpret_cast<uint32_t*>(w_s + 256);               // qps x HIST_BINS
-  Smem* sm = reinterpret_cast<Smem*>(hist_s + a.qps * HIST_BINS);
+  float* w_s = reinterpret_cast<float*>(q_mem + 2 * q_bytes);              // 2 groups x 256 floats
+  float* w_tab = w_s + 2 * 256;                                            // WSEQ x 128 floats
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(w_tab + WSEQ * 128);      // 2 groups x qps x HIST_BINS
+  Smem* sm = reinterpret_cast<Smem*>(hist_s + 2 * a.qps * HIST_BINS);
   volatile int* abort = &sm->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -297,12 +617,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_init(&sm->qempty[i], 1);
     }
     tc::mbar_init(&sm->done, 1);
-    tc::mbar_init(&sm->ebar, 4);
+    tc::mbar_init(&sm->ebar[0], 4);
+    tc::mbar_init(&sm->ebar[1], 4);
+    sm->nfin = 0;
     sm->abort = 0;
     tc::fence_barrier_init();
   }
-  for (int x = threadIdx.x; x < a.qps * HIST_BINS; x += THREADS) hist_s[x] = 0;
-  if (warp == 5) {
+  for (int x = threadIdx.x; x < 2 * a.qps * HIST_BINS; x += THREADS) hist_s[x] = 0;
+  // head weights and per-token entry counts of the CTA's sequences, when there are few of them
+  const int b_first = lo / a.tiles_max;
+  const int nseq_rng = hi > lo ? (hi - 1) / a.tiles_max - b_first + 1 : 0;
+  const bool pre = nseq_rng <= WSEQ;
+  if (pre) {
+    for (int x = threadIdx.x; x < nseq_rng * a.N; x += THREADS)
+      w_tab[x] = a.weights[(int64_t)b_first * a.qps * a.Ih + x];
+    for (int x = threadIdx.x; x < nseq_rng * a.qps; x += THREADS)
+      sm->nc_tab[x / a.qps][x % a.qps] =
+          visible_entries(a.positions, (b_first + x / a.qps) * a.qps + x % a.qps, a.max_context, a.ratio);
+  }
+  if (warp == W_MMA) {
     tc::tmem_alloc(&sm->tmem_base, a.tmem_cols);
     tc::tmem_relinquish();
     tc::tc_fence_before();
@@ -313,7 +646,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc::tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
 
-  if (warp == 4) {
+  if (warp == W_LOAD) {
     // ---------------- TMA producer (lane 0 issues; all lanes look up pages 32 items at a time)
     if (lane == 0) {
       tc::tma_prefetch_desc(&kmap);
@@ -322,6 +655,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int stage = 0, cur_b = -1, qn = 0;
     uint32_t phase = 0;
     bool stop = false;
+    const uint64_t pol = tc::l2_policy_evict_first();
     for (int base_it = lo; base_it < hi && !stop; base_it += 32) {
       const int it = base_it + lane;
       int vb = -1, pg0 = -1, pg1 = -1;
@@ -359,10 +693,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t bytes = (uint32_t)((p0 >= 0) + (p1 >= 0)) * a.kblk * (KB_BYTES / 2);
             uint8_t* st = stage_mem + stage * stage_bytes;
             tc::mbar_arrive_expect_tx(&sm->full[stage], bytes);
-            for (int kb = 0; kb < a.kblk; ++kb) {
-              if (p0 >= 0) tc::tma_load_2d(st + kb * KB_BYTES, &kmap, kb * 64, p0 * 64, &sm->full[stage]);
+            for (int kb = 0; kb < a.kblk; ++kb) {  // keys are read once: evicted from L2 first
+              if (p0 >= 0) tc::tma_load_2d_hint(st + kb * KB_BYTES, &kmap, kb * 64, p0 * 64, &sm->full[stage], pol);
               if (p1 >= 0)
-                tc::tma_load_2d(st + kb * KB_BYTES + KB_BYTES / 2, &kmap, kb * 64, p1 * 64, &sm->full[stage]);
+                tc::tma_load_2d_hint(st + kb * KB_BYTES + KB_BYTES / 2, &kmap, kb * 64, p1 * 64, &sm->full[stage],
+                                     pol);
             }
             if (++stage == a.stages) {
               stage = 0;
@@ -388,7 +723,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (last >= 0) tc::mbar_wait_bounded(&sm->qfull[slot], (last >> 1) & 1, abort, 100000000ull);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == W_MMA) {
     if (lane == 0) {
       // ---------------- MMA issuer
       const uint32_t idesc = tc::idesc_bf16_f32(TILE, a.N);
@@ -435,25 +770,49 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_wait_bounded(&sm->done, 0, abort, 100000000ull);
     }
   } else {
-    // ---------------- epilogue: warps 0-3, thread = key row (TMEM lane)
-    const int row = warp * 32 + lane;
-    int acc = 0, cur_b = -1;
-    uint32_t aphase = 0, ephase = 0;
+    // ---------------- epilogue: warps 0-7 in two groups of four; group g takes the CTA's items
+    // g, g + 2, ...; thread = key row (TMEM lane)
+    const int g = warp >> 2, row = (warp & 3) * 32 + lane;
+    const float* w_g = w_s + g * 256;
+    uint32_t* hist_g = hist_s + g * a.qps * HIST_BINS;
+    int cur_b = -1, ntile = 0;
+    uint32_t ephase = 0;
+    bool ok = true;
     int nc_tok[DSV4_MAX_Q_PER_SEQ] = {0, 0, 0, 0};
     ItemIter cur;
     cur.init(a, lo, hi);
-    for (; cur.valid(); cur.next(a)) {
+    for (int k = 0; cur.valid(); cur.next(a), ++k) {
+      if ((k & 1) != g) continue;
       const int b = cur.b;
       if (b != cur_b) {
-        if (!flush_hist(a, hist_s, cur_b, row, &sm->ebar, &ephase, abort)) break;
-        for (int x = row; x < a.N; x += 128) w_s[x] = a.weights[(int64_t)b * a.qps * a.Ih + x];
+        if (cur_b >= 0 && !finish_seq(a, sm, hist_g, cur_b, ntile, g, row, &ephase, abort)) {
+          ok = false;
+          break;
+        }
+        if (pre) {
+          w_g = w_tab + (b - b_first) * a.N;
 #pragma unroll
-        for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q)
-          nc_tok[q] = q < a.qps ? visible_entries(a.positions, b * a.qps + q, a.max_context, a.ratio) : 0;
-        if (!tc::group_sync(&sm->ebar, &ephase, abort)) break;
+          for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q) nc_tok[q] = q < a.qps ? sm->nc_tab[b - b_first][q] : 0;
+        } else {
+          float* wl = w_s + g * 256;
+          for (int x = row; x < a.N; x += 128) wl[x] = a.weights[(int64_t)b * a.qps * a.Ih + x];
+#pragma unroll
+          for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q)
+            nc_tok[q] = q < a.qps ? visible_entries(a.positions, b * a.qps + q, a.max_context, a.ratio) : 0;
+          if (!tc::group_sync(&sm->ebar[g], &ephase, abort)) {
+            ok = false;
+            break;
+          }
+        }
         cur_b = b;
+        ntile = 0;
       }
-      if (!tc::mbar_wait_bounded(&sm->dfull[acc], aphase, abort)) break;
+      const int acc = k % a.nacc;
+      const uint32_t aphase = (uint32_t)((k / a.nacc) & 1);
+      if (!tc::mbar_wait_bounded(&sm->dfull[acc], aphase, abort)) {
+        ok = false;
+        break;
+      }
       tc::tc_fence_after();
       float sk[DSV4_MAX_Q_PER_SEQ] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * a.N);
@@ -462,7 +821,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc::tmem_ld32_nowait(lane_addr + c0, r);
         tc::tmem_ld32_nowait(lane_addr + c0 + 32, r + 32);
         tc::tmem_wait_ld_regs<64>(r);
-        const float4* w4 = reinterpret_cast<const float4*>(w_s + c0);
+        const float4* w4 = reinterpret_cast<const float4*>(w_g + c0);
         float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -482,9 +841,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           // recompute the halves separately (only when a token boundary falls mid-chunk)
           float h0 = 0.f, h1 = 0.f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) h0 = fmaf(w_s[c0 + i], fmaxf(__uint_as_float(r[i]), 0.f), h0);
+          for (int i = 0; i < 32; ++i) h0 = fmaf(w_g[c0 + i], fmaxf(__uint_as_float(r[i]), 0.f), h0);
 #pragma unroll
-          for (int i = 32; i < 64; ++i) h1 = fmaf(w_s[c0 + i], fmaxf(__uint_as_float(r[i]), 0.f), h1);
+          for (int i = 32; i < 64; ++i) h1 = fmaf(w_g[c0 + i], fmaxf(__uint_as_float(r[i]), 0.f), h1);
 #pragma unroll
           for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q) {
             if (q == k0) sk[q] += h0;
@@ -502,21 +861,48 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int t = b * a.qps + q;
           const bool on = j < nc_tok[q];
           if (on) a.bufs.scores[(int64_t)t * a.bufs.nc_stride + j] = sk[q];
-          hist_add_warp(hist_s + q * HIST_BINS, order_key(sk[q]) >> HIST_SHIFT, on);
+          hist_add_warp(hist_g + q * HIST_BINS, order_key(sk[q]) >> HIST_SHIFT, on);
         }
       }
-      if (++acc == a.nacc) {
-        acc = 0;
-        aphase ^= 1;
-      }
+      ++ntile;
     }
-    flush_hist(a, hist_s, cur_b, row, &sm->ebar, &ephase, abort);
+    if (ok && cur_b >= 0) finish_seq(a, sm, hist_g, cur_b, ntile, g, row, &ephase, abort);
   }
   __syncthreads();
   if (threadIdx.x == 0 && sm->abort) atomicOr(&g_flags_ix, FLAG_TIMEOUT);
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, a.tmem_cols);
+  }
+  if (sm->abort) return;  // block-uniform
+  // ---------------- top-k of the sequences this CTA completed, in the now idle shared memory
+  __threadfence();
+  uint8_t* tbuf = base;
+  const size_t tbytes = (size_t)(reinterpret_cast<uint8_t*>(sm) - base);
+  const int nfin = min((int)sm->nfin, FIN_MAX);
+  for (int f = 0; f < nfin; ++f) {
+    const int b = sm->fin[f];
+    for (int q = 0; q < a.qps; ++q) {
+      const int t = b * a.qps + q;
+      const int n = visible_entries(a.positions, t, a.max_context, a.ratio);
+      if (!tk::topk_token(a.bufs.scores + (int64_t)t * a.bufs.nc_stride, a.bufs.hist + (int64_t)t * HIST_BINS, n, a.K,
+                          a.topk_idx + (int64_t)t * a.K, a.topk_score ? a.topk_score + (int64_t)t * a.K : nullptr,
+                          a.bufs.cand + (int64_t)t * a.bufs.nc_stride, tbuf, tbytes, abort)) {
+        if (threadIdx.x == 0) atomicOr(&g_flags_ix, FLAG_TIMEOUT);
+        return;
+      }
+    }
+  }
+  // sequences without a visible entry have no tile (nobody completes them): all -1
+  for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+    if (seq_entries(a, b) != 0) continue;
+    for (int q = 0; q < a.qps; ++q) {
+      const int t = b * a.qps + q;
+      for (int x = threadIdx.x; x < a.K; x += THREADS) {
+        a.topk_idx[(int64_t)t * a.K + x] = -1;
+        if (a.topk_score) a.topk_score[(int64_t)t * a.K + x] = -INFINITY;
+      }
+    }
   }
 }
 
@@ -547,11 +933,15 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   a.max_pages = p.max_pages_per_seq;
   a.tiles_max = (max_nc + TILE - 1) / TILE;
   a.max_context = p.max_context;
+  a.K = p.topk;
+  a.topk_idx = p.topk_idx;
+  a.topk_score = p.topk_score;
   a.N = p.q_per_seq * p.n_heads;
   a.kblk = p.head_dim / 64;
   a.nacc = 4 * a.N <= 512 ? 4 : 2;  // TMEM accumulators (512 columns available)
   a.tmem_cols = a.nacc * a.N <= 64 ? 64 : (a.nacc * a.N <= 128 ? 128 : (a.nacc * a.N <= 256 ? 256 : 512));
-  const size_t fixed = 1024 + 2 * (size_t)a.kblk * a.N * 128 + 256 * 4 + (size_t)a.qps * HIST_BINS * 4 + sizeof(Smem);
+  const size_t fixed = 1024 + 2 * (size_t)a.kblk * a.N * 128 + (2 * 256 + WSEQ * 128) * 4 +
+                       2 * (size_t)a.qps * HIST_BINS * 4 + sizeof(Smem);
   const size_t budget = 227 * 1024;
   const int stages = (int)((budget - fixed) / ((size_t)a.kblk * KB_BYTES));
   a.stages = stages > MAX_STAGES ? MAX_STAGES : stages;
@@ -571,307 +961,31 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   const int total = a.B * a.tiles_max;
   int grid = num_sms();
   if (grid > total) grid = total;
+  if (grid < (total + FIN_MAX - 1) / FIN_MAX) grid = (total + FIN_MAX - 1) / FIN_MAX;  // <= FIN_MAX items per CTA
   if (grid <= 0) return cudaSuccess;
   return launch_pdl(indexer_score_tc, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/false, kmap, qmap, a);
 }
 
 // ------------------------------------------------------------------------------------------------
-// Top-k selection
+// Top-k after the CUDA-core score kernel: one CTA per token.
 // ------------------------------------------------------------------------------------------------
-constexpr int COLLECT_THREADS = 256;
-constexpr int COLLECT_PER = 32;                                   // scores per thread
-constexpr int COLLECT_SLICE = COLLECT_THREADS * COLLECT_PER;      // 8192 scores per CTA
-constexpr int CAND_CAP = 4096;                                    // candidates kept in shared memory
-constexpr int J_BITS = 20;                                        // n_c <= 2^20 (checked on the host)
+constexpr int TK_THREADS = 320;
+constexpr size_t TK_SMEM = 220 * 1024;
 
-// Candidate value: (low 20 order-key bits << 20) | (2^20 - 1 - j); larger = better score, then smaller j.
-__device__ __forceinline__ uint64_t cand_value(uint32_t key, int j) {
-  return ((uint64_t)(key & ((1u << HIST_SHIFT) - 1u)) << J_BITS) | (uint64_t)((1u << J_BITS) - 1u - (uint32_t)j);
-}
-__device__ __forceinline__ int cand_j(uint64_t v) { return (int)((1u << J_BITS) - 1u - (uint32_t)(v & ((1u << J_BITS) - 1u))); }
-
-// Bin holding the k-th largest score (from the histogram of one token) and the number of scores in
-// the bins above it.  Called by all COLLECT_THREADS threads.
-__device__ void threshold_bin(const uint32_t* hist, int K, int* bin_out, int* above_out) {
-  __shared__ uint32_t part[COLLECT_THREADS];
-  constexpr int PER = HIST_BINS / COLLECT_THREADS;  // thread i owns bins [i*PER, (i+1)*PER)
-  const int tid = threadIdx.x;
-  uint32_t local[PER];
-  uint32_t sum = 0;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    local[i] = hist[tid * PER + i];
-    sum += local[i];
-  }
-  part[tid] = sum;
-  __syncthreads();
-  // inclusive suffix sums over the threads' groups (from the top bins down)
-  for (int off = 1; off < COLLECT_THREADS; off <<= 1) {
-    const uint32_t v = (tid + off < COLLECT_THREADS) ? part[tid + off] : 0u;
-    __syncthreads();
-    part[tid] += v;
-    __syncthreads();
-  }
-  const uint32_t incl = part[tid];
-  const uint32_t above_group = incl - sum;  // scores in the groups above this thread's
-  if (above_group < (uint32_t)K && incl >= (uint32_t)K) {
-    uint32_t cum = above_group;
-    for (int i = PER - 1; i >= 0; --i) {
-      if (cum + local[i] >= (uint32_t)K) {
-        *bin_out = tid * PER + i;
-        *above_out = (int)cum;
-        break;
-      }
-      cum += local[i];
-    }
-  }
-  __syncthreads();
-}
-
-// Appends `val` to a shared-memory list for every lane with `on`, one shared atomic per warp.
-template <typename T>
-__device__ __forceinline__ void warp_append_smem(unsigned* cnt, T* list, T val, bool on) {
-  const unsigned m = __ballot_sync(0xffffffffu, on);
-  if (m == 0) return;
-  const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
-  unsigned base = 0;
-  if (lane == leader) base = atomicAdd(cnt, (unsigned)__popc(m));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  if (on) list[base + __popc(m & ((1u << lane) - 1u))] = val;
-}
-
-// One CTA per (8192-score slice, token): entries above the threshold bin are selected outright,
-// entries in it become candidates; both are staged in shared memory and appended to the token's
-// global lists with one atomic each.
-__device__ void finalize_token(const dsv4_indexer_topk_params& p, const TopkBufs& bufs, int t, int n, uint64_t* dsm);
-
-__global__ void __launch_bounds__(COLLECT_THREADS) topk_collect(dsv4_indexer_topk_params p, TopkBufs bufs) {
-  extern __shared__ uint64_t csm[];
+__global__ void __launch_bounds__(TK_THREADS) topk_kernel(dsv4_indexer_topk_params p, TopkBufs bufs) {
+  extern __shared__ __align__(128) uint8_t tsm[];
+  __shared__ int abort_s;
   pdl_launch_dependents();
   pdl_wait();
-  uint64_t* maybe_s = csm;                                        // COLLECT_SLICE
-  int32_t* cert_s = reinterpret_cast<int32_t*>(csm + COLLECT_SLICE);  // COLLECT_SLICE
-  __shared__ unsigned n_cert, n_maybe, base_cert, base_maybe;
-  __shared__ int sh_bin, sh_above, sh_last;
-  const int t = blockIdx.y;
+  if (threadIdx.x == 0) abort_s = 0;
+  __syncthreads();
+  const int t = blockIdx.x;
   const int n = visible_entries(p, t);
-  const int K = p.topk;
-  const int j0 = blockIdx.x * COLLECT_SLICE;
-  const float* s = bufs.scores + (int64_t)t * bufs.nc_stride;
-  if (n <= K) {  // short context: every candidate, in order (slice 0 writes it)
-    if (blockIdx.x == 0) {
-      int32_t* out = p.topk_idx + (int64_t)t * K;
-      float* out_s = p.topk_score ? p.topk_score + (int64_t)t * K : nullptr;
-      for (int x = threadIdx.x; x < K; x += COLLECT_THREADS) {
-        out[x] = x < n ? x : -1;
-        if (out_s) out_s[x] = x < n ? s[x] : -INFINITY;
-      }
-    }
-    return;
-  }
-  if (j0 >= n) return;  // block-uniform: this slice holds no entry of the token
-  const int j1 = min(n, j0 + COLLECT_SLICE);
-  float v[COLLECT_PER];
-#pragma unroll
-  for (int i = 0; i < COLLECT_PER; ++i) {  // all loads in flight first
-    const int j = j0 + i * COLLECT_THREADS + threadIdx.x;
-    v[i] = j < j1 ? s[j] : 0.f;
-  }
-  if (threadIdx.x == 0) {
-    sh_bin = HIST_BINS - 1;
-    n_cert = n_maybe = 0;
-  }
-  __syncthreads();
-  threshold_bin(bufs.hist + (int64_t)t * HIST_BINS, K, &sh_bin, &sh_above);
-  const uint32_t bstar = (uint32_t)sh_bin;
-#pragma unroll
-  for (int i = 0; i < COLLECT_PER; ++i) {
-    const int j = j0 + i * COLLECT_THREADS + threadIdx.x;
-    const uint32_t key = order_key(v[i]);
-    const uint32_t bin = key >> HIST_SHIFT;
-    warp_append_smem<int32_t>(&n_cert, cert_s, j, j < j1 && bin > bstar);
-    warp_append_smem<uint64_t>(&n_maybe, maybe_s, cand_value(key, j), j < j1 && bin == bstar);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    base_cert = n_cert ? atomicAdd(&bufs.cnt[3 * t], n_cert) : 0u;
-    base_maybe = n_maybe ? atomicAdd(&bufs.cnt[3 * t + 1], n_maybe) : 0u;
-  }
-  __syncthreads();
-  int32_t* certain = bufs.certain + (int64_t)t * K;
-  uint64_t* maybe = bufs.maybe + (int64_t)t * bufs.nc_stride;
-  for (unsigned x = threadIdx.x; x < n_cert; x += COLLECT_THREADS)
-    if (base_cert + x < (unsigned)K) certain[base_cert + x] = cert_s[x];
-  for (unsigned x = threadIdx.x; x < n_maybe; x += COLLECT_THREADS)
-    if (base_maybe + x < (unsigned)bufs.nc_stride) maybe[base_maybe + x] = maybe_s[x];
-  // the CTA that finishes the token's collection last makes the final choice (no CTA waits)
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned slices = (unsigned)((n + COLLECT_SLICE - 1) / COLLECT_SLICE);
-    sh_last = atomicAdd(&bufs.cnt[3 * t + 2], 1u) == slices - 1;
-  }
-  __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
-  finalize_token(p, bufs, t, n, csm);
-}
-
-// Digit of the radix bucket holding the rem-th largest element, from a 256-bin histogram: warp 0
-// does it with 8 bins per lane and a shuffle scan.  Writes the digit to *digit and the number of
-// elements in higher buckets to *above.  Called by the whole CTA.
-__device__ __forceinline__ void pick_digit(const unsigned* hist, unsigned rem, int* digit, unsigned* above) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    unsigned c[8], sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      c[i] = hist[255 - 8 * lane - i];  // lane 0 owns the top bins
-      sum += c[i];
-    }
-    unsigned incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += u;
-    }
-    const unsigned excl = incl - sum;
-    if (excl < rem && incl >= rem) {
-      unsigned cum = excl;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (cum + c[i] >= rem) {
-          *digit = 255 - 8 * lane - i;
-          *above = cum;
-          break;
-        }
-        cum += c[i];
-      }
-    }
-  }
-  __syncthreads();
-}
-
-// Exclusive prefix sum of one value per thread over the CTA; *total gets the sum.
-__device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = lane < nw ? warp_tot[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += u;
-    }
-    if (lane < nw) warp_tot[lane] = wi - w;
-    if (lane == 31) warp_tot[32] = wi;
-  }
-  __syncthreads();
-  const int r = warp_tot[warp] + incl - v;
-  *total = warp_tot[32];
-  __syncthreads();
-  return r;
-}
-
-// Exact choice of the remaining entries among the candidates of token t (radix select on the
-// candidate values), then the selection written in increasing j through a bitmap over j.  Run by
-// the whole CTA that finished the token's collection last; `dsm` holds CAND_CAP candidates followed
-// by the bitmap.
-__device__ void finalize_token(const dsv4_indexer_topk_params& p, const TopkBufs& bufs, int t, int n, uint64_t* dsm) {
-  uint64_t* cand_s = dsm;                                           // CAND_CAP
-  uint32_t* bits = reinterpret_cast<uint32_t*>(dsm + CAND_CAP);    // nc_stride / 32 words
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  const int K = p.topk;
-  int32_t* out = p.topk_idx + (int64_t)t * K;
-  float* out_s = p.topk_score ? p.topk_score + (int64_t)t * K : nullptr;
-  const float* s = bufs.scores + (int64_t)t * bufs.nc_stride;
-  __shared__ unsigned hist[256];
-  __shared__ unsigned long long sh_prefix;
-  __shared__ unsigned sh_rem, sh_above;
-  __shared__ int sh_digit;
-  __shared__ int warp_tot[33];
-  const int words = (n + 31) >> 5;
-  for (int x = tid; x < words; x += nthr) bits[x] = 0u;
-  const int n_certain = (int)min(bufs.cnt[3 * t], (uint32_t)K);
-  const int m = (int)min(bufs.cnt[3 * t + 1], (uint32_t)bufs.nc_stride);
-  int need = K - n_certain;
-  if (need > m) {  // cannot happen with a complete histogram; keep the output valid
-    if (tid == 0) atomicOr(&g_flags_ix, FLAG_TOPK);
-    need = m;
-  }
-  const uint64_t* maybe_g = bufs.maybe + (int64_t)t * bufs.nc_stride;
-  const bool in_smem = m <= CAND_CAP;
-  if (in_smem)
-    for (int i = tid; i < m; i += nthr) cand_s[i] = maybe_g[i];
-  const uint64_t* cand = in_smem ? cand_s : maybe_g;
-  __syncthreads();
-  for (int x = tid; x < n_certain; x += nthr) {
-    const int j = bufs.certain[(int64_t)t * K + x];
-    if (j >= 0 && j < n) atomicOr(&bits[j >> 5], 1u << (j & 31));
-  }
-  if (need > 0) {
-    // radix select (8-bit digits over the 40-bit values) of the need-th largest candidate
-    unsigned long long prefix = 0, mask = 0;
-    if (tid == 0) sh_rem = (unsigned)need;
-    for (int shift = 32; shift >= 0; shift -= 8) {
-      for (int x = tid; x < 256; x += nthr) hist[x] = 0;
-      __syncthreads();
-      for (int i = tid; i < m; i += nthr) {
-        const unsigned long long v = cand[i];
-        if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255ull], 1u);
-      }
-      __syncthreads();
-      const unsigned rem = sh_rem;
-      pick_digit(hist, rem, &sh_digit, &sh_above);
-      if (tid == 0) {
-        sh_rem = rem - sh_above;
-        sh_prefix = prefix | ((unsigned long long)sh_digit << shift);
-      }
-      __syncthreads();
-      prefix = sh_prefix;
-      mask |= 255ull << shift;
-    }
-    const unsigned long long kth = prefix;
-    for (int i = tid; i < m; i += nthr) {
-      const unsigned long long v = cand[i];
-      if (v >= kth) {
-        const int j = cand_j(v);
-        if (j < n) atomicOr(&bits[j >> 5], 1u << (j & 31));
-      }
-    }
-  }
-  __syncthreads();
-  // compaction of the bitmap in increasing j
-  const int per = (words + nthr - 1) / nthr;
-  const int w0 = tid * per, w1 = min(words, w0 + per);
-  int cnt = 0;
-  for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
-  int total;
-  int pos = block_excl_scan(cnt, warp_tot, &total);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t b = bits[w];
-    while (b) {
-      const int j = (w << 5) + __ffs(b) - 1;
-      b &= b - 1;
-      if (pos < K) {
-        out[pos] = j;
-        if (out_s) out_s[pos] = s[j];
-      }
-      ++pos;
-    }
-  }
-  for (int x = total + tid; x < K; x += nthr) {
-    out[x] = -1;
-    if (out_s) out_s[x] = -INFINITY;
-  }
+  if (!tk::topk_token(bufs.scores + (int64_t)t * bufs.nc_stride, bufs.hist + (int64_t)t * HIST_BINS, n, p.topk,
+                      p.topk_idx + (int64_t)t * p.topk, p.topk_score ? p.topk_score + (int64_t)t * p.topk : nullptr,
+                      bufs.cand + (int64_t)t * bufs.nc_stride, tsm, TK_SMEM, &abort_s) &&
+      threadIdx.x == 0)
+    atomicOr(&g_flags_ix, FLAG_TIMEOUT);
 }
 
 cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t st) {
@@ -881,17 +995,14 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
   TopkBufs bufs;
   bufs.scores = reinterpret_cast<float*>(ws + L.scores_off);
   bufs.hist = reinterpret_cast<uint32_t*>(ws + L.hist_off);
-  bufs.cnt = reinterpret_cast<uint32_t*>(ws + L.cnt_off);
-  bufs.certain = reinterpret_cast<int32_t*>(ws + L.certain_off);
-  bufs.maybe = reinterpret_cast<uint64_t*>(ws + L.maybe_off);
+  bufs.seq_done = reinterpret_cast<uint32_t*>(ws + L.done_off);
+  bufs.cand = reinterpret_cast<uint64_t*>(ws + L.cand_off);
   bufs.nc_stride = (int)L.nc_stride;
-  cudaError_t e = cudaMemsetAsync(ws + L.hist_off, 0, L.certain_off - L.hist_off, st);
+  cudaError_t e = cudaMemsetAsync(ws + L.hist_off, 0, L.cand_off - L.hist_off, st);
   if (e != cudaSuccess) return e;
   const int max_nc = p.max_context / p.ratio;
-  if (max_nc > 0 && use_tc_indexer(p)) {
-    e = launch_indexer_score_tc(p, bufs, st);
-    if (e != cudaSuccess) return e;
-  } else if (max_nc > 0) {
+  if (max_nc > 0 && use_tc_indexer(p)) return launch_indexer_score_tc(p, bufs, st);  // top-k included
+  if (max_nc > 0) {
     const int tiles = (max_nc + IX_TILE - 1) / IX_TILE;
     const size_t smem = sizeof(float) * ((size_t)p.q_per_seq * p.n_heads * p.head_dim +
                                          (size_t)p.q_per_seq * p.n_heads + (size_t)(p.head_dim + 1) * (IX_TILE + 1));
@@ -901,16 +1012,12 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
     if (e != cudaSuccess) return e;
   }
   static int attr_done = 0;
-  const size_t stage_smem = (size_t)COLLECT_SLICE * (sizeof(uint64_t) + sizeof(int32_t));
-  const size_t final_smem = (size_t)CAND_CAP * sizeof(uint64_t) + L.nc_stride / 32 * sizeof(uint32_t);
-  const size_t csmem = stage_smem > final_smem ? stage_smem : final_smem;
   if (!attr_done) {
-    e = cudaFuncSetAttribute(topk_collect, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TK_SMEM);
     if (e != cudaSuccess) return e;
     attr_done = 1;
   }
-  const int slices = max_nc > 0 ? (max_nc + COLLECT_SLICE - 1) / COLLECT_SLICE : 1;
-  return launch_pdl(topk_collect, dim3(slices, p.T), dim3(COLLECT_THREADS), csmem, st, /*pdl=*/false, p, bufs);
+  return launch_pdl(topk_kernel, dim3(p.T), dim3(TK_THREADS), TK_SMEM, st, /*pdl=*/false, p, bufs);
 }
 
 cudaError_t read_flags_indexer(uint32_t* f) {

@@ -97,6 +97,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 // Loads rows y0..y3 (each one 128-byte box row starting at element x) of a 2-D tensor into 4
 // consecutive 128-byte rows of shared memory, with the tensor map's swizzle.  The map's box is one
 // row high.  A row index past the end of the tensor loads zeros.
+// L2 cache policy for data read once (evicted first).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 2D tiled TMA load with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
                                             uint64_t* bar) {
   asm volatile(
@@ -264,6 +281,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_amn_bmn(int M, int N) {
   return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);
 }
 
+
+// Plain (untiled) bulk copy of `bytes` from global to shared memory, completing on `bar`; both
+// addresses 16-byte aligned and `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
 
 // ---------------------------------------------------------------------------------------------
 // cp.async (16-byte global -> shared copies) feeding tcgen05 operands
