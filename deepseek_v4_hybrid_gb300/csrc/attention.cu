@@ -9,6 +9,8 @@
 // Row list of a query at position p: rows 0..n_swa-1 are the window positions
 // p - n_swa + 1 .. p (n_swa = min(window, p + 1)), then the compressed rows: topk_idx[t][i]
 // (an index outside [0, n_c(p)) is masked) or j = 0 .. n_c(p) - 1 when no list is given.
+#include <cstddef>
+
 #include "dsv4_common.cuh"
 #include "dsv4_launch.h"
 #include "tc_ptx.cuh"
@@ -283,11 +285,12 @@ struct Smem {
   uint32_t loaded[2];   // [tile parity]: bit u = half u was loaded
   float red[2][2][4][32];  // [tile parity][head half][row quarter][lane]: per-warp maxima
   float lred[2][4][32];
-  float mrow[8][64];       // per softmax warp: running max and rescale factor of its 32 heads
+  alignas(16) float mrow[8][64];  // per softmax warp: running max and rescale factor of its 32 heads (read as float4)
   uint32_t tmem_base;
   int abort;
 };
 static_assert(1024 + Q_BYTES + KV_BYTES + sizeof(Smem) <= 232448, "shared memory of one CTA");
+static_assert(offsetof(Smem, mrow) % 16 == 0, "mrow is read with 16-byte loads");
 
 struct TokenRows {
   int pos, lo, first_wp, n_wp, nc, n_cmp, n_halves;
