@@ -58,9 +58,41 @@ __global__ void __launch_bounds__(ROW_THREADS) kv_insert_kernel(dsv4_kv_insert_p
 }
 
 
-// RMSNorm * weight of the folded entry j (thread i holds dims 2i, 2i+1), GPT-J RoPE of the rope pairs
-// at position j * ratio, and the encoded store into main-cache row j of sequence b.  All 288 threads.
-__device__ void finish_entry(const dsv4_compress_update_params& p, int b, int j, int i, float x0, float x1,
+// What finishing entry j of sequence b needs, loaded before the fold so that it costs no extra
+// round trip: the RMSNorm weight pair of thread i, its cos/sin pair (rope threads) at position
+// j * ratio and the destination row of the main cache.
+struct EntryCtx {
+  float2 g;
+  float c, s;
+  uint8_t* row;
+};
+
+__device__ __forceinline__ EntryCtx entry_prefetch(const dsv4_compress_update_params& p, int b, int j, int i) {
+  EntryCtx e;
+  e.g = reinterpret_cast<const float2*>(p.norm_weight)[i];
+  e.c = 1.f;
+  e.s = 0.f;
+  if (i >= 256) {
+    int rp = j * p.ratio;
+    if (rp >= p.max_pos) {
+      atomicOr(&g_flags_ic, FLAG_PAGE);
+      rp = 0;
+    }
+    e.c = p.cos_sin[(int64_t)rp * 64 + (i - 256)];
+    e.s = p.cos_sin[(int64_t)rp * 64 + 32 + (i - 256)];
+  }
+  const int lp = j / p.page_size;
+  const int page = (lp < p.max_pages_per_seq) ? p.block_table[(int64_t)b * p.max_pages_per_seq + lp] : -1;
+  e.row = (page >= 0 && page < p.num_pages)
+              ? reinterpret_cast<uint8_t*>(p.main_cache) +
+                    ((int64_t)page * p.page_size + j % p.page_size) * row_bytes(p.cache_dtype, D)
+              : nullptr;
+  return e;
+}
+
+// RMSNorm * weight of the folded entry (thread i holds dims 2i, 2i+1), GPT-J RoPE of the rope pairs
+// and the encoded store into the main-cache row.  All 288 threads (one block reduction).
+__device__ void entry_finish(const dsv4_compress_update_params& p, const EntryCtx& e, int i, float x0, float x1,
                              float* red) {
   float ss = warp_sum(x0 * x0 + x1 * x1);
   if ((i & 31) == 0) red[i >> 5] = ss;
@@ -69,50 +101,58 @@ __device__ void finish_entry(const dsv4_compress_update_params& p, int b, int j,
 #pragma unroll
   for (int w = 0; w < ROW_THREADS / 32; ++w) tot += red[w];
   const float inv = 1.0f / sqrtf(tot / (float)D + p.eps);
-  const float2 g = reinterpret_cast<const float2*>(p.norm_weight)[i];
-  x0 = x0 * inv * g.x;
-  x1 = x1 * inv * g.y;
+  x0 = x0 * inv * e.g.x;
+  x1 = x1 * inv * e.g.y;
   if (i >= 256) {
-    int rp = j * p.ratio;
-    if (rp >= p.max_pos) {
-      atomicOr(&g_flags_ic, FLAG_PAGE);
-      rp = 0;
-    }
-    rope_pair(x0, x1, p.cos_sin + (int64_t)rp * 64, i - 256);
+    const float y0 = x0 * e.c - x1 * e.s;
+    const float y1 = x0 * e.s + x1 * e.c;
+    x0 = y0;
+    x1 = y1;
   }
-  const int lp = j / p.page_size;
-  const int page = (lp < p.max_pages_per_seq) ? p.block_table[(int64_t)b * p.max_pages_per_seq + lp] : -1;
-  if (page < 0 || page >= p.num_pages) {
+  if (e.row == nullptr) {
     if (i == 0) atomicOr(&g_flags_ic, FLAG_PAGE);
   } else {
-    uint8_t* row = reinterpret_cast<uint8_t*>(p.main_cache) +
-                   ((int64_t)page * p.page_size + j % p.page_size) * row_bytes(p.cache_dtype, D);
-    encode_pair_store(p.cache_dtype, row, i, x0, x1);
+    encode_pair_store(p.cache_dtype, e.row, i, x0, x1);
   }
 }
 
-// Stores the fp32 state row of token t (kv half as is, score half + APE); all threads of the CTA.
-__device__ __forceinline__ void store_state_row(const dsv4_compress_update_params& p, float* state_b, int t, int pos,
-                                                int tid, int nthreads) {
-  const int coff = p.coff, r = p.ratio;
-  const int state_w = 2 * coff * D, half = coff * D;
-  const float2* src = reinterpret_cast<const float2*>(p.kv_score + (int64_t)t * state_w);
-  float2* dst = reinterpret_cast<float2*>(state_b + (int64_t)(pos % (coff * r)) * state_w);
-  const float2* ape = p.ape ? reinterpret_cast<const float2*>(p.ape + (int64_t)(pos % r) * half) : nullptr;
-  for (int c = tid; c < state_w / 2; c += nthreads) {
-    float2 v = src[c];
-    if (ape != nullptr && c >= half / 2) {
-      const float2 a = ape[c - half / 2];
-      v.x += a.x;
-      v.y += a.y;
-    }
-    dst[c] = v;
+// Online softmax step of one row of a fold (two channels per thread).
+struct FoldAcc {
+  float m0 = -INFINITY, m1 = -INFINITY, s0 = 0.f, s1 = 0.f, a0 = 0.f, a1 = 0.f;
+  __device__ __forceinline__ void add(float2 kv, float2 sc) {
+    const float n0 = fmaxf(m0, sc.x), n1 = fmaxf(m1, sc.y);
+    const float c0 = expf(m0 - n0), c1 = expf(m1 - n1);
+    const float e0 = expf(sc.x - n0), e1 = expf(sc.y - n1);
+    s0 = s0 * c0 + e0;
+    s1 = s1 * c1 + e1;
+    a0 = a0 * c0 + e0 * kv.x;
+    a1 = a1 * c1 + e1 * kv.y;
+    m0 = n0;
+    m1 = n1;
+  }
+};
+
+// Channel pair i of token t's new state row: kv series `ser` and score series `ser` (+ APE of its
+// position), as stored in the ring.
+__device__ __forceinline__ void new_row_pair(const dsv4_compress_update_params& p, int t, int pos, int ser, int i,
+                                             float2& kv, float2& sc) {
+  const int half = p.coff * D;
+  const float2* src = reinterpret_cast<const float2*>(p.kv_score + (int64_t)t * 2 * half);
+  kv = src[ser * (D / 2) + i];
+  sc = src[half / 2 + ser * (D / 2) + i];
+  if (p.ape != nullptr) {
+    const float2 a = reinterpret_cast<const float2*>(p.ape + (int64_t)(pos % p.ratio) * half)[ser * (D / 2) + i];
+    sc.x += a.x;
+    sc.y += a.y;
   }
 }
 
-// One CTA per sequence; its new tokens are handled in position order so that a fold sees
-// exactly the state a token-by-token decode would have (a later token of the same step can
-// reuse the ring slot of a row the fold still needs).
+// One CTA per sequence; its new tokens are handled in position order, so a fold sees exactly the
+// state a token-by-token decode would have (a later token of the same step may reuse the ring slot
+// of a row an earlier fold reads).  Per token, everything it needs is loaded up front (its new row,
+// the fold's other rows from the ring, the entry's weights and destination); the token's own row
+// enters the fold from registers, so storing it costs no round trip.
+constexpr int FOLD_BATCH = 8;
 __global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compress_update_params p) {
   pdl_launch_dependents();
   pdl_wait();
@@ -131,35 +171,58 @@ __global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compr
       if (i == 0) atomicOr(&g_flags_ic, FLAG_PAGE);
       continue;
     }
-    store_state_row(p, state_b, t, pos, i, ROW_THREADS);  // kv half as is, score half + APE
-    __syncthreads();
-    if ((pos + 1) % r == 0) {
-      const int j = pos / r;
-      // ---- fold: per-channel online softmax over the group's rows
-      float m0 = -INFINITY, m1 = -INFINITY, s0 = 0.f, s1 = 0.f, a0 = 0.f, a1 = 0.f;
-      const int nser = (coff == 2 && j >= 1) ? 2 : 1;
-      for (int ser = 0; ser < nser; ++ser) {
-        const int q0 = (j - ser) * r;  // series A: this group; series B: the previous group
-        const int kv_off = ser * D, sc_off = half + ser * D;
-#pragma unroll 4
-        for (int q = q0; q < q0 + r; ++q) {
+    const bool emit = (pos + 1) % r == 0;
+    const int j = pos / r;
+    float2 kvn[2], scn[2];
+    new_row_pair(p, t, pos, 0, i, kvn[0], scn[0]);
+    if (coff == 2) new_row_pair(p, t, pos, 1, i, kvn[1], scn[1]);
+    EntryCtx ec;
+    // fold rows: series A (kv / score block 0) over this group, then for coff == 2 series B (block 1)
+    // over the previous group (absent for j = 0)
+    const int nser = (coff == 2 && j >= 1) ? 2 : 1;
+    const int nrows = emit ? nser * r : 0;
+    float2 kvb[FOLD_BATCH], scb[FOLD_BATCH];
+    auto load_batch = [&](int base) {
+#pragma unroll
+      for (int u = 0; u < FOLD_BATCH; ++u) {
+        const int idx = base + u;
+        if (idx < nrows) {
+          const int ser = idx / r, q = (j - ser) * r + idx % r;
           const float* rowp = state_b + (int64_t)(q % nslots) * state_w;
-          const float2 kv = reinterpret_cast<const float2*>(rowp + kv_off)[i];
-          const float2 sc = reinterpret_cast<const float2*>(rowp + sc_off)[i];
-          float n0 = fmaxf(m0, sc.x), n1 = fmaxf(m1, sc.y);
-          float c0 = expf(m0 - n0), c1 = expf(m1 - n1);
-          float e0 = expf(sc.x - n0), e1 = expf(sc.y - n1);
-          s0 = s0 * c0 + e0;
-          s1 = s1 * c1 + e1;
-          a0 = a0 * c0 + e0 * kv.x;
-          a1 = a1 * c1 + e1 * kv.y;
-          m0 = n0;
-          m1 = n1;
+          kvb[u] = reinterpret_cast<const float2*>(rowp + ser * D)[i];
+          scb[u] = reinterpret_cast<const float2*>(rowp + half + ser * D)[i];
         }
       }
-      finish_entry(p, b, j, i, a0 / s0, a1 / s1, red);
-      __syncthreads();
+    };
+    if (emit) {
+      ec = entry_prefetch(p, b, j, i);
+      load_batch(0);
     }
+    // this token's row into its ring slot (which holds position pos - nslots, outside the fold)
+    float2* dst = reinterpret_cast<float2*>(state_b + (int64_t)(pos % nslots) * state_w);
+    dst[i] = kvn[0];
+    dst[half / 2 + i] = scn[0];
+    if (coff == 2) {
+      dst[D / 2 + i] = kvn[1];
+      dst[half / 2 + D / 2 + i] = scn[1];
+    }
+    if (emit) {
+      FoldAcc f;
+      for (int base = 0; base < nrows; base += FOLD_BATCH) {
+        if (base > 0) load_batch(base);
+#pragma unroll
+        for (int u = 0; u < FOLD_BATCH; ++u) {
+          const int idx = base + u;
+          if (idx < nrows) {
+            const int ser = idx / r, q = (j - ser) * r + idx % r;
+            if (q == pos) f.add(ser == 0 ? kvn[0] : kvn[1], ser == 0 ? scn[0] : scn[1]);  // own row
+            else f.add(kvb[u], scb[u]);
+          }
+        }
+      }
+      entry_finish(p, ec, i, f.a0 / f.s0, f.a1 / f.s1, red);
+    }
+    __syncthreads();  // the next token's store may reuse a slot this fold read
   }
 }
 
@@ -167,8 +230,10 @@ __global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compr
 // Ratio-128 groups (coff = 1): one 8-CTA cluster per sequence.  Each CTA folds 16 of the group's
 // 128 rows into per-channel partial softmax states (max, sum, weighted kv sum) in its shared memory;
 // CTA 0 combines the eight partial states through distributed shared memory and finishes the entry.
-// The sequence's tokens are still handled in position order (stores up to the emitting token, the
-// fold, then the later tokens' stores).  Cluster barriers are hardware barriers, not flag spins.
+// Rows of this call's tokens up to the emitting one enter the fold straight from kv_score (+ APE),
+// so the fold needs no barrier after CTA 0 stores them; the later tokens' rows, which reuse ring
+// slots of the group, are stored after the fold.  Cluster barriers are hardware barriers, not flag
+// spins.
 constexpr int FOLD_CTAS = 8;
 __global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
     compress_fold_cluster_kernel(dsv4_compress_update_params p) {
@@ -182,31 +247,20 @@ __global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
   float* state_b = p.state + (int64_t)b * nslots * state_w;
   __shared__ float2 pm[ROW_THREADS], ps[ROW_THREADS], pa[ROW_THREADS];
   __shared__ float red[ROW_THREADS / 32];
+  int posk[DSV4_MAX_Q_PER_SEQ];
   int k_emit = -1;
-  for (int k = 0; k < p.q_per_seq; ++k) {
-    const int pos = p.positions[b * p.q_per_seq + k];
-    if (pos >= 0 && (pos + 1) % r == 0) {
-      k_emit = k;
-      break;
-    }
+#pragma unroll
+  for (int k = 0; k < DSV4_MAX_Q_PER_SEQ; ++k) {
+    posk[k] = k < p.q_per_seq ? p.positions[b * p.q_per_seq + k] : -1;
+    if (k < p.q_per_seq && k_emit < 0 && posk[k] >= 0 && (posk[k] + 1) % r == 0) k_emit = k;
   }
   const int k_end = k_emit >= 0 ? k_emit + 1 : p.q_per_seq;
-  if (rank == 0)
-    for (int k = 0; k < k_end; ++k) {
-      const int t = b * p.q_per_seq + k, pos = p.positions[t];
-      if (pos < 0) {
-        if (i == 0) atomicOr(&g_flags_ic, FLAG_PAGE);
-        continue;
-      }
-      store_state_row(p, state_b, t, pos, i, ROW_THREADS);
-      __syncthreads();
-    }
   if (k_emit >= 0) {  // cluster-uniform
-    cluster.sync();   // the stored rows are visible to every CTA of the cluster
-    const int pos = p.positions[b * p.q_per_seq + k_emit];
+    const int pos = posk[k_emit];
     const int j = pos / r;
-    float m0 = -INFINITY, m1 = -INFINITY, s0 = 0.f, s1 = 0.f, a0 = 0.f, a1 = 0.f;
     const int q0 = j * r + rank * (r / FOLD_CTAS);
+    EntryCtx ec;
+    if (rank == 0) ec = entry_prefetch(p, b, j, i);
     float2 kv[16], sc[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) {  // all 32 loads in flight
@@ -214,21 +268,34 @@ __global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
       kv[u] = reinterpret_cast<const float2*>(rowp)[i];
       sc[u] = reinterpret_cast<const float2*>(rowp + D)[i];
     }
+    // rows written by this call's tokens come from kv_score instead of the ring
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const float n0 = fmaxf(m0, sc[u].x), n1 = fmaxf(m1, sc[u].y);
-      const float c0 = expf(m0 - n0), c1 = expf(m1 - n1);
-      const float e0 = expf(sc[u].x - n0), e1 = expf(sc[u].y - n1);
-      s0 = s0 * c0 + e0;
-      s1 = s1 * c1 + e1;
-      a0 = a0 * c0 + e0 * kv[u].x;
-      a1 = a1 * c1 + e1 * kv[u].y;
-      m0 = n0;
-      m1 = n1;
+    for (int k = 0; k < DSV4_MAX_Q_PER_SEQ; ++k) {
+      const int u = posk[k] - q0;
+      if (k <= k_emit && posk[k] >= 0 && u >= 0 && u < 16) {
+#pragma unroll
+        for (int v = 0; v < 16; ++v)
+          if (v == u) new_row_pair(p, b * p.q_per_seq + k, posk[k], 0, i, kv[v], sc[v]);
+      }
     }
-    pm[i] = make_float2(m0, m1);
-    ps[i] = make_float2(s0, s1);
-    pa[i] = make_float2(a0, a1);
+    if (rank == 0)
+      for (int k = 0; k < k_end; ++k) {  // rows of the tokens up to the emitting one, for later calls
+        if (posk[k] < 0) {
+          if (i == 0) atomicOr(&g_flags_ic, FLAG_PAGE);
+          continue;
+        }
+        float2 a, c;
+        new_row_pair(p, b * p.q_per_seq + k, posk[k], 0, i, a, c);
+        float2* dst = reinterpret_cast<float2*>(state_b + (int64_t)(posk[k] % nslots) * state_w);
+        dst[i] = a;
+        dst[D / 2 + i] = c;
+      }
+    FoldAcc f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) f.add(kv[u], sc[u]);
+    pm[i] = make_float2(f.m0, f.m1);
+    ps[i] = make_float2(f.s0, f.s1);
+    pa[i] = make_float2(f.a0, f.a1);
     cluster.sync();  // every CTA's partial state is in its shared memory
     if (rank == 0) {
       float M0 = -INFINITY, M1 = -INFINITY;
@@ -250,16 +317,30 @@ __global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
         A0 += qa[c].x * w0;
         A1 += qa[c].y * w1;
       }
-      finish_entry(p, b, j, i, A0 / S0, A1 / S1, red);
+      entry_finish(p, ec, i, A0 / S0, A1 / S1, red);
     }
-    cluster.sync();  // no CTA leaves while CTA 0 still reads its shared memory
+    cluster.sync();  // the fold has read the ring, and no CTA leaves while CTA 0 reads its shared memory
+  } else if (rank == 0) {
+    for (int k = 0; k < k_end; ++k) {
+      if (posk[k] < 0) {
+        if (i == 0) atomicOr(&g_flags_ic, FLAG_PAGE);
+        continue;
+      }
+      float2 a, c;
+      new_row_pair(p, b * p.q_per_seq + k, posk[k], 0, i, a, c);
+      float2* dst = reinterpret_cast<float2*>(state_b + (int64_t)(posk[k] % nslots) * state_w);
+      dst[i] = a;
+      dst[D / 2 + i] = c;
+    }
   }
   if (rank == 0)
-    for (int k = k_end; k < p.q_per_seq; ++k) {
-      const int t = b * p.q_per_seq + k, pos = p.positions[t];
-      if (pos < 0) continue;
-      __syncthreads();
-      store_state_row(p, state_b, t, pos, i, ROW_THREADS);
+    for (int k = k_end; k < p.q_per_seq; ++k) {  // later tokens (after the fold)
+      if (posk[k] < 0) continue;
+      float2 a, c;
+      new_row_pair(p, b * p.q_per_seq + k, posk[k], 0, i, a, c);
+      float2* dst = reinterpret_cast<float2*>(state_b + (int64_t)(posk[k] % nslots) * state_w);
+      dst[i] = a;
+      dst[D / 2 + i] = c;
     }
 }
 
