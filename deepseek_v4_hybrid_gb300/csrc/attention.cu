@@ -9,12 +9,15 @@
 // Row list of a query at position p: rows 0..n_swa-1 are the window positions
 // p - n_swa + 1 .. p (n_swa = min(window, p + 1)), then the compressed rows: topk_idx[t][i]
 // (an index outside [0, n_c(p)) is masked) or j = 0 .. n_c(p) - 1 when no list is given.
+#include <cooperative_groups.h>
 #include <cstddef>
 
 #include "dsv4_common.cuh"
 #include "dsv4_launch.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
+
+namespace cg = cooperative_groups;
 
 namespace dsv4 {
 
@@ -269,6 +272,7 @@ constexpr uint32_t COL_O = 0, COL_S = 256, TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr uint32_t FLAG_TIMEOUT = 4u;
 constexpr int K_NONE = 0, K_BOX_SWA = 1, K_BOX_MAIN = 2, K_GATHER = 3;
+constexpr int MAX_MERGE_CLUSTER = 8;  // up to this many chunks per token merge inside a (portable) cluster
 
 struct Args {
   dsv4_sparse_mla_decode_params p;
@@ -277,6 +281,7 @@ struct Args {
   int n_chunks, chunk_halves;
   int swa_rows, main_rows;  // rows of the two caches (a gather from this row loads zeros)
   float c_log2;             // softmax_scale * log2(e)
+  int cluster_merge;        // the chunks of a (token, head group) form one cluster and merge in it
 };
 
 struct Smem {
@@ -286,6 +291,7 @@ struct Smem {
   float red[2][2][4][32];  // [tile parity][head half][row quarter][lane]: per-warp maxima
   float lred[2][4][32];
   alignas(16) float mrow[8][64];  // per softmax warp: running max and rescale factor of its 32 heads (read as float4)
+  float2 cml[HG];                 // the chunk's (max in log2 units, sum) per head, read by the cluster
   uint32_t tmem_base;
   int abort;
 };
@@ -434,12 +440,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nh = min(a.chunk_halves, tr.n_halves - h0);
   const int64_t part = ((int64_t)t * a.n_chunks + chunk) * p.H + hg * HG;
   pdl_launch_dependents();
-  if (nh <= 0) {  // block-uniform: an empty chunk contributes nothing
+  if (nh <= 0 && !a.cluster_merge) {  // block-uniform: an empty chunk contributes nothing
     pdl_wait();
     if (threadIdx.x < HG) a.ml_part[part + threadIdx.x] = make_float2(-INFINITY, 0.f);
     return;
   }
-  const int ntiles = (nh + 1) / 2;
+  // (in a merging cluster an empty chunk runs through with no tiles: it joins the cluster's barriers)
+  const int ntiles = nh > 0 ? (nh + 1) / 2 : 0;
 
   if (threadIdx.x == 0) {
     for (int g = 0; g < NGROUPS; ++g) tc::mbar_init(&sm->full[g], 1);
@@ -463,10 +470,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc::tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   if (warp != W_LOAD) pdl_wait();
+  // softmax warps' state, kept past the role split for the epilogue
+  const int qd = warp & 3, hf = warp >> 2;
+  const int R = qd * 32 + lane;
+  const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+  float mref = -INFINITY;  // running max (log2 domain) of head 32 hf + lane
+  float lsum = 0.f;        // this warp's rows' share of the sum of head 32 hf + lane
+  bool have_o = false;     // softmax warps: every PV product has retired
 
   if (warp == W_LOAD) {
     // ---------------- loads
-    if (lane == 0) {
+    if (lane == 0 && ntiles > 0) {
       tc::tma_prefetch_desc(&qmap);
       tc::tma_prefetch_desc(&swamap64);
       tc::tma_prefetch_desc(&mainmap);
@@ -540,7 +554,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (lane == 0) {
       // every load into this CTA has landed before it may exit (already true unless it aborted)
-      tc::mbar_wait_bounded(&sm->qfull, 0, abort, 100000000ull);
+      if (ntiles > 0) tc::mbar_wait_bounded(&sm->qfull, 0, abort, 100000000ull);
       for (int g = 0; g < armed_groups; ++g)
         tc::mbar_wait_bounded(&sm->full[g], armed_tile & 1, abort, 100000000ull);
     }
@@ -553,7 +567,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t a1 = tc::sdesc_k_sw128(kv_addr), b1 = tc::sdesc_k_sw128(q_addr);
       const uint64_t a2 = tc::sdesc_mn_sw128(kv_addr, SLOT_BYTES, 1024);
       const uint64_t b2 = tc::sdesc_mn_sw128(kv_addr + 8 * SLOT_BYTES, SLOT_BYTES, 1024);
-      bool ok = tc::mbar_wait_bounded(&sm->qfull, 0, abort);
+      bool ok = ntiles == 0 || tc::mbar_wait_bounded(&sm->qfull, 0, abort);
       bool o_started = false;
       for (int i = 0; i < ntiles && ok; ++i) {
         for (int g = 0; g < NGROUPS && ok; ++g) {
@@ -595,11 +609,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ---------------- softmax + epilogue: warps 0-7; warp w owns tile rows R = 32 (w & 3) + lane (TMEM
     // lane R) and heads 32 hf .. 32 hf + 31 (hf = w >> 2)
-    const int qd = warp & 3, hf = warp >> 2;
-    const int R = qd * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
-    float mref = -INFINITY;  // running max (log2 domain) of head 32 hf + lane
-    float lp[32];            // this thread's share of each of the 32 heads' sums
+    float lp[32];  // this thread's share of each of the 32 heads' sums
 #pragma unroll
     for (int k = 0; k < 32; ++k) lp[k] = 0.f;
     bool ok = true;
@@ -704,8 +714,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->pfull);
     }
-    if (ok && tc::mbar_wait_bounded(&sm->odone, 0, abort)) {
-      tc::tc_fence_after();
+    lsum = transpose_reduce32<false>(lp, lane);
+    have_o = __all_sync(0xffffffffu, ok && tc::mbar_wait_bounded(&sm->odone, 0, abort));
+    if (have_o) tc::tc_fence_after();
+    if (have_o && !a.cluster_merge) {
       // O^T (lane R = value dim 128 m + R, column = head) is turned into [head][value] rows in the
       // now idle tile buffer, then stored with 16-byte writes
       float* ot = reinterpret_cast<float*>(kv_mem);  // [64 heads][512 values] fp32 = 128 KB
@@ -716,7 +728,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int k = 0; k < 32; ++k) ot[(32 * hf + k) * DV + 128 * m + R] = __uint_as_float(o[k]);
       }
-      sm->lred[hf][qd][lane] = transpose_reduce32<false>(lp, lane);
+      sm->lred[hf][qd][lane] = lsum;
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->ebar);
       if (tc::mbar_wait_bounded(&sm->ebar, 0, abort)) {
@@ -734,6 +746,76 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   __syncthreads();
   if (threadIdx.x == 0 && sm->abort) atomicOr(&g_flags_at, FLAG_TIMEOUT);
+  if (a.cluster_merge) {
+    // ---------------- merge of the chunks inside the cluster (every thread of every CTA reaches the
+    // three cluster barriers, whatever happened before: nothing here waits on a flag)
+    cg::cluster_group cl = cg::this_cluster();
+    const int nc = a.n_chunks, crank = (int)cl.block_rank();
+    const bool smx = warp < 8;
+    if (smx) sm->lred[hf][qd][lane] = lsum;
+    __syncthreads();
+    if (smx && qd == 0) {
+      float l = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) l += sm->lred[hf][w][lane];
+      sm->cml[32 * hf + lane] = make_float2(have_o ? mref : -INFINITY, l);
+    }
+    cl.sync();  // every chunk's (max, sum) per head is in its shared memory
+    float* ot = reinterpret_cast<float*>(kv_mem);  // [64 heads][512 values] fp32 = 128 KB
+    if (smx) {
+      const int h = 32 * hf + lane;
+      float M = p.sink ? p.sink[hg * HG + h] * 1.4426950408889634f : -INFINITY;
+      for (int c = 0; c < nc; ++c) M = fmaxf(M, cl.map_shared_rank(sm->cml, c)[h].x);
+      float L = (M == -INFINITY || p.sink == nullptr) ? 0.f : tc::ex2_approx(p.sink[hg * HG + h] * 1.4426950408889634f - M);
+      for (int c = 0; c < nc; ++c) {
+        const float2 ml = cl.map_shared_rank(sm->cml, c)[h];
+        if (ml.x != -INFINITY) L += ml.y * tc::ex2_approx(ml.x - M);
+      }
+      const float mine = sm->cml[h].x;
+      sm->mrow[warp][lane] = (mine == -INFINITY || !(L > 0.f)) ? 0.f : tc::ex2_approx(mine - M) / L;
+      if (crank == 0 && qd == 0 && p.lse)
+        p.lse[(int64_t)t * p.H + hg * HG + h] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+      __syncwarp();
+      // this chunk's O^T scaled by its weight, as [head][value] rows in the idle tile buffer
+      for (int m = 0; m < 4; ++m) {
+        uint32_t o[32];
+        if (have_o) {
+          tc::tmem_ld32_nowait(lane_base + COL_O + 64 * m + 32 * hf, o);
+          tc::tmem_wait_ld_regs<32>(o);
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float f = sm->mrow[warp][k];
+          ot[(32 * hf + k) * DV + 128 * m + R] = (f == 0.f || !have_o) ? 0.f : __uint_as_float(o[k]) * f;
+        }
+      }
+    }
+    cl.sync();  // every chunk's scaled partial is staged
+    {
+      // this CTA sums its share of the 64 x 512 block over the cluster and writes the output
+      constexpr int TOTAL4 = HG * DV / 4;
+      const int per = (TOTAL4 + nc - 1) / nc;
+      const int x0 = crank * per, x1 = min(TOTAL4, x0 + per);
+      const int64_t obase = ((int64_t)t * p.H + hg * HG) * DV;
+      for (int x = x0 + (int)threadIdx.x; x < x1; x += THREADS) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < nc; ++c) {
+          const float4 v = reinterpret_cast<const float4*>(cl.map_shared_rank(ot, c))[x];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        if (p.out_dtype == DSV4_F32) {
+          reinterpret_cast<float4*>(p.out)[obase / 4 + x] = acc;
+        } else {
+          reinterpret_cast<uint2*>(p.out)[obase / 4 + x] =
+              make_uint2(float2_to_bf16x2_bits(acc.x, acc.y), float2_to_bf16x2_bits(acc.z, acc.w));
+        }
+      }
+    }
+    cl.sync();  // no CTA leaves while another still reads its shared memory
+  }
   if (warp == W_MMA) {
     // no MMA may still write TMEM when it is released (already true unless the CTA aborted)
     if (lane == 0) tc::mbar_wait_bounded(&sm->odone, 0, abort, 100000000ull);
@@ -760,6 +842,7 @@ static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p,
   a.swa_rows = (int)(p.swa_num_pages * p.page_size);
   a.main_rows = p.ratio > 0 ? (int)(p.main_num_pages * p.page_size) : a.swa_rows;
   a.c_log2 = p.softmax_scale * 1.4426950408889634f;
+  a.cluster_merge = L.n_chunks <= MAX_MERGE_CLUSTER ? 1 : 0;
   CUtensorMap qmap, swamap64, mainmap, mainmap64;
   cudaError_t e = make_tmap_2d_bf16(&qmap, p.q, (uint64_t)D, (uint64_t)p.T * p.H, 64, HG);
   if (e != cudaSuccess) return e;
@@ -782,8 +865,21 @@ static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p,
     if (e != cudaSuccess) return e;
     attr_done = 1;
   }
-  return launch_pdl(mla_partial_tc, dim3(L.n_chunks, p.T, p.H / HG), dim3(THREADS), smem, st, true, qmap, swamap64,
-                    mainmap, mainmap64, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.n_chunks, p.T, p.H / HG);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // the chunks of one (token, head group)
+  attr[1].val.clusterDim.x = a.cluster_merge ? L.n_chunks : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, mla_partial_tc, qmap, swamap64, mainmap, mainmap64, a);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -828,6 +924,7 @@ cudaError_t launch_sparse_mla_decode(const dsv4_sparse_mla_decode_params& p, cud
   if (use_tc_attention(p)) {
     e = launch_mla_partial_tc(p, L, o_part, ml_part, st);
     if (e != cudaSuccess) return e;
+    if (L.n_chunks <= attc::MAX_MERGE_CLUSTER) return cudaSuccess;  // merged inside the kernel's clusters
   } else {
     const size_t smem = sizeof(float) * ((size_t)AT_HG * D + (size_t)AT_CH * (D + 1) + (size_t)AT_HG * AT_CH);
     e = cudaFuncSetAttribute(mla_partial_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
