@@ -44,21 +44,26 @@ static int max_rows(const dsv4_sparse_mla_decode_params& p) {
 
 static bool use_tc_attention(const dsv4_sparse_mla_decode_params& p);
 
-// Rows per CTA of the tensor-core kernel: about one wave of CTAs (one per chunk, token and 64-head
-// group) over the SMs, in whole 64-row halves.
-static int tc_chunk_rows(const dsv4_sparse_mla_decode_params& p) {
+// Chunks per (token, head group) of the tensor-core kernel: about one wave of CTAs over the SMs.
+// Chunk c takes the 64-row halves c, c + n_chunks, c + 2 n_chunks, ... of the token's row list, so
+// window pages and gathered rows spread evenly over the chunks.
+static int tc_chunks(const dsv4_sparse_mla_decode_params& p) {
   const int units = p.T * (p.H / 64);
   int n = units > 0 ? num_sms() / units : 1;
   if (n < 1) n = 1;
   const int halves = max_rows(p) / 64;
-  const int c = (halves + n - 1) / n;
-  return (c < 1 ? 1 : c) * 64;
+  return n < halves ? n : (halves > 0 ? halves : 1);
 }
 
 static AtLayout at_layout(const dsv4_sparse_mla_decode_params& p) {
   AtLayout L;
-  L.chunk_rows = use_tc_attention(p) ? tc_chunk_rows(p) : AT_CH;
-  L.n_chunks = (max_rows(p) + L.chunk_rows - 1) / L.chunk_rows;
+  if (use_tc_attention(p)) {
+    L.n_chunks = tc_chunks(p);
+    L.chunk_rows = (max_rows(p) / 64 + L.n_chunks - 1) / L.n_chunks * 64;  // rows of the largest chunk
+  } else {
+    L.chunk_rows = AT_CH;
+    L.n_chunks = (max_rows(p) + L.chunk_rows - 1) / L.chunk_rows;
+  }
   if (L.n_chunks < 1) L.n_chunks = 1;
   const size_t parts = (size_t)p.T * L.n_chunks * p.H;
   L.o_off = 0;
@@ -278,7 +283,7 @@ struct Args {
   dsv4_sparse_mla_decode_params p;
   float* o_part;
   float2* ml_part;
-  int n_chunks, chunk_halves;
+  int n_chunks;             // chunk c takes halves c, c + n_chunks, ... of a token's row list
   int swa_rows, main_rows;  // rows of the two caches (a gather from this row loads zeros)
   float c_log2;             // softmax_scale * log2(e)
   int cluster_merge;        // the chunks of a (token, head group) form one cluster and merge in it
@@ -436,8 +441,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = t / p.q_per_seq;
   const TokenRows tr = token_plan(p, t);
-  const int h0 = chunk * a.chunk_halves;
-  const int nh = min(a.chunk_halves, tr.n_halves - h0);
+  const int nh = chunk < tr.n_halves ? (tr.n_halves - chunk + a.n_chunks - 1) / a.n_chunks : 0;  // halves of this chunk
   const int64_t part = ((int64_t)t * a.n_chunks + chunk) * p.H + hg * HG;
   pdl_launch_dependents();
   if (nh <= 0 && !a.cluster_merge) {  // block-uniform: an empty chunk contributes nothing
@@ -496,7 +500,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       HalfPlan hp[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int hh = h0 + 2 * i + u;
+        const int hh = chunk + (2 * i + u) * a.n_chunks;
         hp[u] = (2 * i + u < nh) ? plan_half(a, t, b, tr, hh, lane) : plan_half(a, t, b, tr, tr.n_halves, lane);
       }
       const uint32_t m0 = __ballot_sync(0xffffffffu, hp[0].v0), m1 = __ballot_sync(0xffffffffu, hp[0].v1);
@@ -838,7 +842,6 @@ static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p,
   a.o_part = o_part;
   a.ml_part = ml_part;
   a.n_chunks = L.n_chunks;
-  a.chunk_halves = L.chunk_rows / HALF;
   a.swa_rows = (int)(p.swa_num_pages * p.page_size);
   a.main_rows = p.ratio > 0 ? (int)(p.main_num_pages * p.page_size) : a.swa_rows;
   a.c_log2 = p.softmax_scale * 1.4426950408889634f;
