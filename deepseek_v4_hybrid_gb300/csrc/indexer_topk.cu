@@ -30,6 +30,7 @@ constexpr int HIST_BITS = 12;
 constexpr int HIST_BINS = 1 << HIST_BITS;
 constexpr int HIST_SHIFT = 32 - HIST_BITS;
 constexpr uint32_t FLAG_TIMEOUT = 4u;
+constexpr int TOPK_FUSED_MAX = 32768;  // longer rows: top-k spread over CTAs by topk_slice_kernel
 
 // Order-preserving map of an fp32 score to uint32 (larger score -> larger key).
 __device__ __forceinline__ uint32_t order_key(float s) {
@@ -56,7 +57,7 @@ __device__ __forceinline__ int visible_entries(const dsv4_indexer_topk_params& p
 // ------------------------------------------------------------------------------------------------
 struct IxLayout {
   size_t nc_stride;
-  size_t scores_off, hist_off, done_off, cand_off, total;
+  size_t scores_off, hist_off, done_off, tcnt_off, cand_off, bits_off, total;
 };
 
 static IxLayout ix_layout(const dsv4_indexer_topk_params& p) {
@@ -66,8 +67,10 @@ static IxLayout ix_layout(const dsv4_indexer_topk_params& p) {
   L.scores_off = 0;
   L.hist_off = align_up(L.scores_off + (size_t)p.T * L.nc_stride * sizeof(float), 256);
   L.done_off = L.hist_off + (size_t)p.T * HIST_BINS * sizeof(uint32_t);  // zeroed together with hist
-  L.cand_off = align_up(L.done_off + (size_t)p.B * sizeof(uint32_t), 256);
-  L.total = align_up(L.cand_off + (size_t)p.T * L.nc_stride * sizeof(uint64_t), 256);
+  L.tcnt_off = L.done_off + (size_t)p.B * sizeof(uint32_t);                // zeroed together with hist
+  L.cand_off = align_up(L.tcnt_off + (size_t)p.T * 2 * sizeof(uint32_t), 256);
+  L.bits_off = align_up(L.cand_off + (size_t)p.T * L.nc_stride * sizeof(uint64_t), 256);
+  L.total = align_up(L.bits_off + (size_t)p.T * (L.nc_stride / 32) * sizeof(uint32_t), 256);
   return L;
 }
 
@@ -78,6 +81,8 @@ struct TopkBufs {
   uint32_t* hist;      // [T][HIST_BINS] counts of the scores' top 12 order-key bits
   uint32_t* seq_done;  // [B] key tiles of the sequence scored so far (tensor-core path)
   uint64_t* cand;      // [T][nc_stride] top-k candidates that do not fit in shared memory
+  uint32_t* tcnt;      // [T][2] sliced top-k: candidates appended, slices finished
+  uint32_t* bits;      // [T][nc_stride / 32] sliced top-k: selection bitmap
   int nc_stride;
 };
 
@@ -113,6 +118,8 @@ constexpr int CTL_BYTES = 512;
 constexpr int FIND_THREADS = 256;  // threads that own histogram bins in block_find_bin
 constexpr int CHUNK = 4096;       // scores per bulk copy (16 KB)
 constexpr int NBUF = 4;           // chunk buffers (copies in flight)
+constexpr int SCAN_WARPS_MIN = 8;  // the kernels run top-k with at least 8 warps
+constexpr int SCAN_U = (CHUNK / 128 + SCAN_WARPS_MIN - 1) / SCAN_WARPS_MIN;  // blocks of a chunk per warp
 
 struct Ctl {
   uint64_t bar[NBUF + 1];  // chunk buffers, histogram
@@ -204,13 +211,149 @@ __device__ __forceinline__ void block_find_bin(const uint32_t* h, uint32_t rem, 
   __syncthreads();
 }
 
+// Bitmap words and candidates of one chunk of scores in shared memory: sb holds entries j_base ..
+// j_base + 128 nblocks - 1 (entries >= n are ignored).  Entries with bin > bstar set their bit in
+// `bits` (word j / 32; every word of the chunk is written), entries in bstar are appended to `cand`
+// (capacity ccap) through the counter *ncand, one atomic per warp.  bits, cand and ncand may be in
+// shared or global memory.  Warp w takes 128-entry blocks w, w + NW, ... side by side.
+__device__ __forceinline__ void scan_chunk(const float4* sb, int nblocks, int j_base, int n, uint32_t bstar,
+                                           uint32_t* bits, int words, uint64_t* cand, uint32_t ccap,
+                                           uint32_t* ncand) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
+  float4 v[SCAN_U];
+#pragma unroll
+  for (int u = 0; u < SCAN_U; ++u) {
+    const int bl = warp + u * NW;
+    v[u] = bl < nblocks ? sb[bl * 32 + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  }
+  uint32_t sel[SCAN_U], cm[SCAN_U];
+  int mycnt = 0;
+#pragma unroll
+  for (int u = 0; u < SCAN_U; ++u) {
+    const int j0 = j_base + (warp + u * NW) * 128 + 4 * lane;
+    const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+    sel[u] = 0u;
+    cm[u] = 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t bin = order_key(e[k]) >> HIST_SHIFT;
+      const bool in = j0 + k < n;
+      if (in && bin > bstar) sel[u] |= 1u << k;
+      if (in && bin == bstar) cm[u] |= 1u << k;
+    }
+    mycnt += __popc(cm[u]);
+  }
+  int incl = mycnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int tt = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += tt;
+  }
+  const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+  if (wtot) {
+    uint32_t base = 0;
+    if (lane == 31) base = atomicAdd(ncand, (uint32_t)wtot);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    if (mycnt) {
+      uint32_t idx = base + (uint32_t)(incl - mycnt);
+#pragma unroll
+      for (int u = 0; u < SCAN_U; ++u) {
+        const int j0 = j_base + (warp + u * NW) * 128 + 4 * lane;
+        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if ((cm[u] >> k) & 1u) {
+            if (idx < ccap) cand[idx] = cand_value(order_key(e[k]), j0 + k);
+            ++idx;
+          }
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < SCAN_U; ++u) {
+    const int bl = warp + u * NW;
+    uint32_t w = sel[u] << (4 * (lane & 7));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    w |= __shfl_xor_sync(0xffffffffu, w, 4);
+    const int wg = (j_base >> 5) + bl * 4 + (lane >> 3);
+    if ((lane & 7) == 0 && bl < nblocks && wg < words) bits[wg] = w;
+  }
+}
+
+// Exact choice of the R largest of m candidate values (unique), OR-ed into the bitmap: a radix
+// select of 10-bit digits that stops at the first digit whose bin holds exactly the entries still
+// needed.  rb: RBINS shared bins.  Whole CTA.
+__device__ void select_candidates(const uint64_t* cand, uint32_t m, int R, uint32_t* rb, Ctl* c, uint32_t* bits) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  if (R <= 0) return;
+  uint64_t thr = 0;
+  if ((uint32_t)R < m) {
+    uint64_t prefix = 0;
+    uint32_t rem = (uint32_t)R;
+    for (int shift = 30; shift >= 0; shift -= 10) {
+      for (int x = tid; x < RBINS; x += NT) rb[x] = 0u;
+      __syncthreads();
+      const uint64_t hmask = shift == 30 ? 0ull : ((1ull << 40) - 1ull) & ~((1ull << (shift + 10)) - 1ull);
+      for (uint32_t i = tid; i < m; i += NT) {
+        const uint64_t v = cand[i];
+        if ((v & hmask) == prefix) atomicAdd(&rb[(v >> shift) & (RBINS - 1)], 1u);
+      }
+      __syncthreads();
+      block_find_bin<RBINS / FIND_THREADS>(rb, rem, c);
+      prefix |= (uint64_t)c->bin << shift;
+      rem -= c->above;
+      thr = prefix;
+      if (c->cnt == rem) break;  // every candidate of this digit is needed: v >= prefix selects them
+    }
+  }
+  for (uint32_t i = tid; i < m; i += NT) {
+    const uint64_t v = cand[i];
+    if (v >= thr) {
+      const int j = cand_j(v);
+      atomicOr(&bits[j >> 5], 1u << (j & 31));
+    }
+  }
+}
+
+// The selection in increasing j from the bitmap (words written by this CTA or, for a global bitmap,
+// by others before a fence), -1 padding; then the scores of the selected entries, read with many
+// loads in flight (from `row_s` when the row is in shared memory, else from global s_g).  Whole CTA.
+__device__ void write_selection(const uint32_t* bits, bool bits_global, int words, int K, int32_t* out, float* out_s,
+                                const float* row_s, const float* s_g, Ctl* c) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int per = (words + NT - 1) / NT;
+  const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bits_global ? __ldcg(bits + w) : bits[w]);
+  int total;
+  int pos = block_excl_scan(cnt, c->wt, &total);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bw = bits_global ? __ldcg(bits + w) : bits[w];
+    while (bw) {
+      const int j = (w << 5) + __ffs(bw) - 1;
+      bw &= bw - 1;
+      if (pos < K) out[pos] = j;
+      ++pos;
+    }
+  }
+  for (int x = total + tid; x < K; x += NT) out[x] = -1;
+  if (out_s) {
+    __syncthreads();  // out[] is complete (global writes of this CTA are visible to it after the barrier)
+    for (int x = tid; x < K; x += NT) {
+      const int j = out[x];
+      out_s[x] = j < 0 ? -INFINITY : (row_s ? row_s[j] : __ldcg(s_g + j));
+    }
+  }
+}
+
 // The whole CTA selects the top K of token scores s_g[0, n) (row 16-byte aligned with room for
 // round_up(n, 128) entries; the histogram hist_g of their order keys is complete) into out[0, K) in
 // increasing j (out_s: their scores, may be null); gcand (n entries) holds candidates that do not fit
 // in `buf` (buf_bytes of 128-byte aligned shared memory).  Returns false if a copy timed out.
 __device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int K, int32_t* out, float* out_s,
                            uint64_t* gcand, uint8_t* buf, size_t buf_bytes, volatile int* abort) {
-  const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31, warp = tid >> 5, NW = NT >> 5;
+  const int tid = threadIdx.x, NT = blockDim.x;
   if (n <= K) {  // short context: every entry, in order
     for (int x = tid; x < K; x += NT) {
       out[x] = x < n ? x : -1;
@@ -276,7 +419,7 @@ __device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int 
   uint64_t* cand = C <= cap ? cand_s : gcand;
   const uint32_t ccap = C <= cap ? cap : (uint32_t)n;
 
-  // 2. selection bitmap and candidates: in each chunk warp w takes 128-entry blocks w, w + NW, ...
+  // 2. selection bitmap and candidates, chunk by chunk
   int stop = nchunks;  // first chunk not consumed
   for (int cc = 0; cc < nchunks; ++cc) {
     if (!__syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc % NBUF], (cc / NBUF) & 1, abort))) {
@@ -284,30 +427,7 @@ __device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int 
       break;
     }
     const float4* sb = reinterpret_cast<const float4*>(chunks + (size_t)(cc % NBUF) * CHUNK * 4);
-    const int nb = min(CHUNK, n128 - cc * CHUNK) >> 7;
-    for (int bl = warp; bl < nb; bl += NW) {
-      const float4 v = sb[bl * 32 + lane];
-      const int j0 = cc * CHUNK + bl * 128 + 4 * lane;
-      const float e[4] = {v.x, v.y, v.z, v.w};
-      uint32_t sel = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int j = j0 + k;
-        const uint32_t key = order_key(e[k]);
-        const uint32_t bin = key >> HIST_SHIFT;
-        if (j < n && bin > bstar) sel |= 1u << k;
-        if (j < n && bin == bstar) {
-          const uint32_t idx = atomicAdd(&c->ncand, 1u);
-          if (idx < ccap) cand[idx] = cand_value(key, j);
-        }
-      }
-      uint32_t w = sel << (4 * (lane & 7));
-      w |= __shfl_xor_sync(0xffffffffu, w, 1);
-      w |= __shfl_xor_sync(0xffffffffu, w, 2);
-      w |= __shfl_xor_sync(0xffffffffu, w, 4);
-      const int wg = ((cc * CHUNK) >> 5) + bl * 4 + (lane >> 3);
-      if ((lane & 7) == 0 && wg < words) bits[wg] = w;
-    }
+    scan_chunk(sb, min(CHUNK, n128 - cc * CHUNK) >> 7, cc * CHUNK, n, bstar, bits, words, cand, ccap, &c->ncand);
     if (cc + NBUF < nchunks) {
       tc::fence_proxy_async_smem();  // reads of this buffer come before the next copy into it
       __syncthreads();
@@ -324,65 +444,11 @@ __device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int 
   }
   __syncthreads();
 
-  // 3. exact choice among the candidates
-  const uint32_t m = min(c->ncand, ccap);
-  if (R > 0 && (uint32_t)R < m) {
-    uint64_t prefix = 0, thr = 0;
-    uint32_t rem = (uint32_t)R;
-    for (int shift = 30; shift >= 0; shift -= 10) {
-      for (int x = tid; x < RBINS; x += NT) rb[x] = 0u;
-      __syncthreads();
-      const uint64_t hmask = shift == 30 ? 0ull : ((1ull << 40) - 1ull) & ~((1ull << (shift + 10)) - 1ull);
-      for (uint32_t i = tid; i < m; i += NT) {
-        const uint64_t v = cand[i];
-        if ((v & hmask) == prefix) atomicAdd(&rb[(v >> shift) & (RBINS - 1)], 1u);
-      }
-      __syncthreads();
-      block_find_bin<RBINS / FIND_THREADS>(rb, rem, c);
-      prefix |= (uint64_t)c->bin << shift;
-      rem -= c->above;
-      thr = prefix;
-      if (c->cnt == rem) break;  // every candidate of this digit is needed: v >= prefix selects them
-    }
-    for (uint32_t i = tid; i < m; i += NT) {
-      const uint64_t v = cand[i];
-      if (v >= thr) {
-        const int j = cand_j(v);
-        atomicOr(&bits[j >> 5], 1u << (j & 31));
-      }
-    }
-  } else if (R > 0) {
-    for (uint32_t i = tid; i < m; i += NT) {
-      const int j = cand_j(cand[i]);
-      atomicOr(&bits[j >> 5], 1u << (j & 31));
-    }
-  }
+  // 3. exact choice among the candidates, 4. the selection in increasing j
+  select_candidates(cand, min(c->ncand, ccap), R, rb, c, bits);
   __syncthreads();
-
-  // 4. compaction in increasing j
-  const float* row_s = reinterpret_cast<const float*>(chunks);
-  const int per = (words + NT - 1) / NT;
-  const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
-  int cnt = 0;
-  for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
-  int total;
-  int pos = block_excl_scan(cnt, c->wt, &total);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bw = bits[w];
-    while (bw) {
-      const int j = (w << 5) + __ffs(bw) - 1;
-      bw &= bw - 1;
-      if (pos < K) {
-        out[pos] = j;
-        if (out_s) out_s[pos] = resident ? row_s[j] : __ldcg(s_g + j);
-      }
-      ++pos;
-    }
-  }
-  for (int x = total + tid; x < K; x += NT) {
-    out[x] = -1;
-    if (out_s) out_s[x] = -INFINITY;
-  }
+  write_selection(bits, false, words, K, out, out_s, resident ? reinterpret_cast<const float*>(chunks) : nullptr,
+                  s_g, c);
   __syncthreads();  // the buffer may be reused right away
   return true;
 }
@@ -484,6 +550,7 @@ namespace ixtc {
 constexpr int TILE = 128;
 constexpr int KB_BYTES = TILE * 128;         // one 64-dim K-block of a key tile (128 rows x 128 B)
 constexpr int THREADS = 320;
+static_assert(THREADS / 32 >= tk::SCAN_WARPS_MIN, "the top-k scan covers a chunk with this many warps");
 constexpr int W_LOAD = 8, W_MMA = 9;
 constexpr int MAX_STAGES = 8;
 constexpr int FIN_MAX = 64;  // sequences whose top-k one CTA may have to run
@@ -498,6 +565,7 @@ struct Args {
   float* topk_score;
   int64_t num_pages;
   int T, B, qps, Ih, d, ratio, max_pages, tiles_max, max_context, K;
+  int fuse_topk;  // the CTA completing a sequence runs its top-k (else a separate sliced launch)
   int N, kblk, stages, tmem_cols, nacc;
 };
 
@@ -874,7 +942,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, a.tmem_cols);
   }
-  if (sm->abort) return;  // block-uniform
+  if (sm->abort || !a.fuse_topk) return;  // block-uniform
   // ---------------- top-k of the sequences this CTA completed, in the now idle shared memory
   __threadfence();
   uint8_t* tbuf = base;
@@ -934,6 +1002,7 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   a.tiles_max = (max_nc + TILE - 1) / TILE;
   a.max_context = p.max_context;
   a.K = p.topk;
+  a.fuse_topk = max_nc <= TOPK_FUSED_MAX;
   a.topk_idx = p.topk_idx;
   a.topk_score = p.topk_score;
   a.N = p.q_per_seq * p.n_heads;
@@ -970,6 +1039,7 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
 // Top-k after the CUDA-core score kernel: one CTA per token.
 // ------------------------------------------------------------------------------------------------
 constexpr int TK_THREADS = 320;
+static_assert(TK_THREADS / 32 >= tk::SCAN_WARPS_MIN, "the top-k scan covers a chunk with this many warps");
 constexpr size_t TK_SMEM = 220 * 1024;
 
 __global__ void __launch_bounds__(TK_THREADS) topk_kernel(dsv4_indexer_topk_params p, TopkBufs bufs) {
@@ -988,6 +1058,107 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(dsv4_indexer_topk_para
     atomicOr(&g_flags_ix, FLAG_TIMEOUT);
 }
 
+// ------------------------------------------------------------------------------------------------
+// Top-k of long rows, spread over CTAs: CTA (slice, token) takes SLICE scores of the token.  Each
+// finds the threshold bin from the complete histogram, writes its words of the token's selection
+// bitmap and appends its candidates to the token's list; the CTA that finishes the token's last
+// slice chooses among the candidates and writes the selection (no CTA waits for another).
+// ------------------------------------------------------------------------------------------------
+constexpr int SLICE_CHUNKS = tk::NBUF;
+constexpr int SLICE = SLICE_CHUNKS * tk::CHUNK;  // 16384 scores
+
+__global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_topk_params p, TopkBufs bufs) {
+  using namespace tk;
+  extern __shared__ __align__(128) uint8_t tsm[];
+  __shared__ int abort_s, last_s;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.y, sl = blockIdx.x, tid = threadIdx.x;
+  const int n = visible_entries(p, t), K = p.topk;
+  const float* s_g = bufs.scores + (int64_t)t * bufs.nc_stride;
+  int32_t* out = p.topk_idx + (int64_t)t * K;
+  float* out_s = p.topk_score ? p.topk_score + (int64_t)t * K : nullptr;
+  if (n <= K) {  // short context: slice 0 writes every entry, in order
+    if (sl == 0)
+      for (int x = tid; x < K; x += TK_THREADS) {
+        out[x] = x < n ? x : -1;
+        if (out_s) out_s[x] = x < n ? __ldcg(s_g + x) : -INFINITY;
+      }
+    return;
+  }
+  const int nsl = (n + SLICE - 1) / SLICE;
+  if (sl >= nsl) return;  // block-uniform
+  Ctl* c = reinterpret_cast<Ctl*>(tsm);
+  uint32_t* rb = reinterpret_cast<uint32_t*>(tsm + CTL_BYTES);
+  uint32_t* hist_s = rb + RBINS;
+  uint8_t* chunks = reinterpret_cast<uint8_t*>(hist_s + HIST_BINS);
+  uint64_t* cand_s = reinterpret_cast<uint64_t*>(chunks + (size_t)SLICE * 4);
+  const size_t fixed = CTL_BYTES + RBINS * 4 + HIST_BINS * 4 + (size_t)SLICE * 4;
+  const uint32_t cap = (uint32_t)((TK_SMEM - fixed) / 8);
+  const int words = (n + 31) >> 5;
+  uint32_t* bits_g = bufs.bits + (int64_t)t * (bufs.nc_stride / 32);
+  uint64_t* cand_g = bufs.cand + (int64_t)t * bufs.nc_stride;
+  const int j_lo = sl * SLICE;
+  const int n128 = (n + 127) & ~127;
+  const int nch = min(SLICE_CHUNKS, (n128 - j_lo + CHUNK - 1) / CHUNK);
+  if (tid == 0) {
+    abort_s = 0;
+    c->bin = 0;
+    c->above = 0;
+    c->cnt = 0;
+    for (int i = 0; i <= NBUF; ++i) tc::mbar_init(&c->bar[i], 1);
+    tc::fence_barrier_init();
+    asm volatile("fence.proxy.async;" ::: "memory");  // scores and counts came through the generic proxy
+    tc::mbar_arrive_expect_tx(&c->bar[NBUF], HIST_BINS * 4);
+    tc::bulk_load(hist_s, bufs.hist + (int64_t)t * HIST_BINS, HIST_BINS * 4, &c->bar[NBUF]);
+    for (int cc = 0; cc < nch; ++cc) {
+      const uint32_t bytes = (uint32_t)min(CHUNK, n128 - j_lo - cc * CHUNK) * 4u;
+      tc::mbar_arrive_expect_tx(&c->bar[cc], bytes);
+      tc::bulk_load(chunks + (size_t)cc * CHUNK * 4, s_g + j_lo + (size_t)cc * CHUNK, bytes, &c->bar[cc]);
+    }
+  }
+  __syncthreads();
+  bool ok = __syncthreads_and(tc::mbar_wait_bounded(&c->bar[NBUF], 0, &abort_s));
+  if (ok) {
+    block_find_bin<HIST_BINS / FIND_THREADS>(hist_s, (uint32_t)K, c);
+    const uint32_t bstar = c->bin;
+    for (int cc = 0; cc < nch && ok; ++cc) {
+      ok = __syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc], 0, &abort_s));
+      if (ok)
+        scan_chunk(reinterpret_cast<const float4*>(chunks + (size_t)cc * CHUNK * 4),
+                   min(CHUNK, n128 - j_lo - cc * CHUNK) >> 7, j_lo + cc * CHUNK, n, bstar, bits_g, words, cand_g,
+                   (uint32_t)n, &bufs.tcnt[2 * t]);
+    }
+  }
+  if (!ok) {
+    if (tid == 0) {  // copies in flight land before the CTA leaves
+      tc::mbar_wait_bounded(&c->bar[NBUF], 0, &abort_s, 100000000ull);
+      for (int cc = 0; cc < nch; ++cc) tc::mbar_wait_bounded(&c->bar[cc], 0, &abort_s, 100000000ull);
+      atomicOr(&g_flags_ix, FLAG_TIMEOUT);
+    }
+    return;  // the token's count never completes: its output stays as it was (flagged)
+  }
+  // the CTA that finishes the token's last slice makes the final choice
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last_s = atomicAdd(&bufs.tcnt[2 * t + 1], 1u) == (uint32_t)(nsl - 1);
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  const int R = K - (int)c->above;
+  const uint32_t m = min(__ldcg(&bufs.tcnt[2 * t]), (uint32_t)n);
+  const uint64_t* cand = cand_g;
+  if (m <= cap) {
+    for (uint32_t i = tid; i < m; i += TK_THREADS) cand_s[i] = __ldcg(cand_g + i);
+    __syncthreads();
+    cand = cand_s;
+  }
+  select_candidates(cand, m, R, rb, c, bits_g);
+  __threadfence();
+  __syncthreads();
+  write_selection(bits_g, true, words, K, out, out_s, nullptr, s_g, c);
+}
+
 cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t st) {
   if (p.T == 0) return cudaSuccess;
   IxLayout L = ix_layout(p);
@@ -996,13 +1167,18 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
   bufs.scores = reinterpret_cast<float*>(ws + L.scores_off);
   bufs.hist = reinterpret_cast<uint32_t*>(ws + L.hist_off);
   bufs.seq_done = reinterpret_cast<uint32_t*>(ws + L.done_off);
+  bufs.tcnt = reinterpret_cast<uint32_t*>(ws + L.tcnt_off);
   bufs.cand = reinterpret_cast<uint64_t*>(ws + L.cand_off);
+  bufs.bits = reinterpret_cast<uint32_t*>(ws + L.bits_off);
   bufs.nc_stride = (int)L.nc_stride;
-  cudaError_t e = cudaMemsetAsync(ws + L.hist_off, 0, L.cand_off - L.hist_off, st);
+  cudaError_t e = cudaMemsetAsync(ws + L.hist_off, 0, L.tcnt_off + (size_t)p.T * 2 * sizeof(uint32_t) - L.hist_off, st);
   if (e != cudaSuccess) return e;
   const int max_nc = p.max_context / p.ratio;
-  if (max_nc > 0 && use_tc_indexer(p)) return launch_indexer_score_tc(p, bufs, st);  // top-k included
-  if (max_nc > 0) {
+  const bool fused = max_nc <= TOPK_FUSED_MAX;
+  if (max_nc > 0 && use_tc_indexer(p)) {
+    e = launch_indexer_score_tc(p, bufs, st);  // includes the top-k when the rows are short
+    if (e != cudaSuccess || fused) return e;
+  } else if (max_nc > 0) {
     const int tiles = (max_nc + IX_TILE - 1) / IX_TILE;
     const size_t smem = sizeof(float) * ((size_t)p.q_per_seq * p.n_heads * p.head_dim +
                                          (size_t)p.q_per_seq * p.n_heads + (size_t)(p.head_dim + 1) * (IX_TILE + 1));
@@ -1015,9 +1191,13 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
   if (!attr_done) {
     e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TK_SMEM);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_slice_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TK_SMEM);
+    if (e != cudaSuccess) return e;
     attr_done = 1;
   }
-  return launch_pdl(topk_kernel, dim3(p.T), dim3(TK_THREADS), TK_SMEM, st, /*pdl=*/false, p, bufs);
+  if (fused) return launch_pdl(topk_kernel, dim3(p.T), dim3(TK_THREADS), TK_SMEM, st, /*pdl=*/false, p, bufs);
+  const int slices = (max_nc + SLICE - 1) / SLICE;
+  return launch_pdl(topk_slice_kernel, dim3(slices, p.T), dim3(TK_THREADS), TK_SMEM, st, /*pdl=*/false, p, bufs);
 }
 
 cudaError_t read_flags_indexer(uint32_t* f) {
