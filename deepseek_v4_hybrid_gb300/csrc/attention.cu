@@ -271,8 +271,9 @@ constexpr int HALF_BYTES = HALF * 128;     // 8 KB
 constexpr int Q_BYTES = NKB * HG * 128;    // 72 KB
 constexpr int KV_BYTES = NKB * SLOT_BYTES;  // 144 KB
 constexpr int NGROUPS = 5;                 // slot groups {0,1} {2,3} {4,5} {6,7} {8}
-constexpr int THREADS = 320;               // warps 0-7 softmax + epilogue, 8 loads, 9 MMA
+constexpr int THREADS = 384;               // warps 0-7 softmax + epilogue, 8, 10, 11 loads, 9 MMA
 constexpr int W_LOAD = 8, W_MMA = 9;
+constexpr int NPROD = 3;                   // loading warps: K-block kb of every tile is loaded by warp kb % 3
 constexpr uint32_t COL_O = 0, COL_S = 256, TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr uint32_t FLAG_TIMEOUT = 4u;
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int ntiles = nh > 0 ? (nh + 1) / 2 : 0;
 
   if (threadIdx.x == 0) {
-    for (int g = 0; g < NGROUPS; ++g) tc::mbar_init(&sm->full[g], 1);
+    for (int g = 0; g < NGROUPS; ++g) tc::mbar_init(&sm->full[g], NPROD);
     for (int m = 0; m < 4; ++m) tc::mbar_init(&sm->vfree[m], 1);
     tc::mbar_init(&sm->sfull, 1);
     tc::mbar_init(&sm->pfull, 8);
@@ -473,7 +474,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
-  if (warp != W_LOAD) pdl_wait();
+  const bool loader = warp == W_LOAD || warp > W_MMA;
+  const int pidx = warp == W_LOAD ? 0 : warp - W_MMA;  // loader index (warps 8, 10, 11)
+  if (!loader) pdl_wait();
   // softmax warps' state, kept past the role split for the epilogue
   const int qd = warp & 3, hf = warp >> 2;
   const int R = qd * 32 + lane;
@@ -482,9 +485,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   float lsum = 0.f;        // this warp's rows' share of the sum of head 32 hf + lane
   bool have_o = false;     // softmax warps: every PV product has retired
 
-  if (warp == W_LOAD) {
-    // ---------------- loads
-    if (lane == 0 && ntiles > 0) {
+  if (loader) {
+    // ---------------- loads: three warps (the TMA issue rate is per issuing warp); loader pidx
+    // issues K-blocks kb with kb % 3 == pidx of every tile, and arrives on each group's barrier with
+    // the bytes it issued there
+    if (pidx == 0 && lane == 0 && ntiles > 0) {
       tc::tma_prefetch_desc(&qmap);
       tc::tma_prefetch_desc(&swamap64);
       tc::tma_prefetch_desc(&mainmap);
@@ -527,30 +532,32 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         const int kb0 = 2 * g, nkb = g < 4 ? 2 : 1;
+        int mine = 0;  // K-blocks of this group that this loader issues
+        for (int kb = kb0; kb < kb0 + nkb; ++kb) mine += kb % NPROD == pidx;
         if (lane == 0) {
-          if (g == 0) {
+          if (g == 0 && pidx == 0) {
             sm->mask[i & 1][0] = m0;
             sm->mask[i & 1][1] = m1;
             sm->mask[i & 1][2] = m2;
             sm->mask[i & 1][3] = m3;
             sm->loaded[i & 1] = ld;
           }
-          tc::mbar_arrive_expect_tx(&sm->full[g], (uint32_t)(nload * nkb * HALF_BYTES));
+          tc::mbar_arrive_expect_tx(&sm->full[g], (uint32_t)(nload * mine * HALF_BYTES));
         }
         armed_tile = i;
         armed_groups = g + 1;
         __syncwarp();
+        for (int kb = kb0; kb < kb0 + nkb; ++kb) {
+          if (kb % NPROD != pidx) continue;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int kind = hp[u].kind;
-          if ((kind == K_BOX_SWA || kind == K_BOX_MAIN) && lane == 0) {
-            const CUtensorMap* map = kind == K_BOX_SWA ? &swamap64 : &mainmap64;
-            for (int kb = kb0; kb < kb0 + nkb; ++kb)
+          for (int u = 0; u < 2; ++u) {
+            const int kind = hp[u].kind;
+            if ((kind == K_BOX_SWA || kind == K_BOX_MAIN) && lane == 0) {
+              const CUtensorMap* map = kind == K_BOX_SWA ? &swamap64 : &mainmap64;
               tc::tma_load_2d(kv_mem + kb * SLOT_BYTES + u * HALF_BYTES, map, kb * 64, hp[u].ybox, &sm->full[g]);
+            }
           }
-        }
-        if (my_kind == K_GATHER) {
-          for (int kb = kb0; kb < kb0 + nkb; ++kb)
+          if (my_kind == K_GATHER)
             tc::tma_gather4(kv_mem + kb * SLOT_BYTES + gu * HALF_BYTES + 4 * g4 * 128, &mainmap, kb * 64, r4[0], r4[1],
                             r4[2], r4[3], &sm->full[g]);
         }
@@ -558,7 +565,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (lane == 0) {
       // every load into this CTA has landed before it may exit (already true unless it aborted)
-      if (ntiles > 0) tc::mbar_wait_bounded(&sm->qfull, 0, abort, 100000000ull);
+      if (ntiles > 0 && pidx == 0) tc::mbar_wait_bounded(&sm->qfull, 0, abort, 100000000ull);
       for (int g = 0; g < armed_groups; ++g)
         tc::mbar_wait_bounded(&sm->full[g], armed_tile & 1, abort, 100000000ull);
     }
