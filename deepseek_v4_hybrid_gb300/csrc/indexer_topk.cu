@@ -549,9 +549,10 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
 namespace ixtc {
 constexpr int TILE = 128;
 constexpr int KB_BYTES = TILE * 128;         // one 64-dim K-block of a key tile (128 rows x 128 B)
-constexpr int THREADS = 320;
+constexpr int THREADS = 384;
 static_assert(THREADS / 32 >= tk::SCAN_WARPS_MIN, "the top-k scan covers a chunk with this many warps");
-constexpr int W_LOAD = 8, W_MMA = 9;
+constexpr int W_LOAD = 8, W_MMA = 9;  // warps 10-11 expand int8 keys to bf16 (int8 caches only)
+constexpr int SCALE_RING = 16;        // int8 keys: row scales of the last 16 tiles (> stages + accumulators)
 constexpr int MAX_STAGES = 8;
 constexpr int FIN_MAX = 64;  // sequences whose top-k one CTA may have to run
 constexpr int WSEQ = 8;      // sequences whose head weights and entry counts are loaded up front
@@ -566,11 +567,15 @@ struct Args {
   int64_t num_pages;
   int T, B, qps, Ih, d, ratio, max_pages, tiles_max, max_context, K;
   int fuse_topk;  // the CTA completing a sequence runs its top-k (else a separate sliced launch)
+  int i8;         // keys are int8 records (d bytes + fp32 scale): bulk-copied pages, expanded in shared memory
+  int nqs;        // query slots (2, or 1 when shared memory is short)
+  const uint8_t* k_raw;  // int8 key cache
   int N, kblk, stages, tmem_cols, nacc;
 };
 
 struct Smem {
   uint64_t full[MAX_STAGES], empty[MAX_STAGES], dfull[4], dempty[4], qfull[2], qempty[2], done, ebar[2];
+  uint64_t raw_full[2], raw_empty[2], sready[SCALE_RING];  // int8 keys
   int fin[FIN_MAX];
   int nc_tab[WSEQ][DSV4_MAX_Q_PER_SEQ];
   uint32_t nfin;
@@ -659,8 +664,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int q_bytes = a.kblk * a.N * 128;
   const int stage_bytes = a.kblk * KB_BYTES;
   uint8_t* stage_mem = base;                                               // stages x stage_bytes
-  uint8_t* q_mem = base + a.stages * stage_bytes;                          // 2 slots x q_bytes
-  float* w_s = reinterpret_cast<float*>(q_mem + 2 * q_bytes);              // 2 groups x 256 floats
+  uint8_t* q_mem = base + a.stages * stage_bytes;                          // nqs slots x q_bytes
+  const int raw_page = 64 * (a.d + 4), raw_stage = 2 * raw_page;          // int8 records: d bytes + fp32 scale
+  uint8_t* raw_mem = q_mem + a.nqs * q_bytes;                              // int8: 2 raw stages
+  float* scale_s = reinterpret_cast<float*>(raw_mem + (a.i8 ? 2 * raw_stage : 0));  // int8: SCALE_RING x 128
+  float* w_s = scale_s + (a.i8 ? SCALE_RING * TILE : 0);                  // 2 groups x 256 floats
   float* w_tab = w_s + 2 * 256;                                            // WSEQ x 128 floats
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(w_tab + WSEQ * 128);      // 2 groups x qps x HIST_BINS
   Smem* sm = reinterpret_cast<Smem*>(hist_s + 2 * a.qps * HIST_BINS);
@@ -673,9 +681,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
-      tc::mbar_init(&sm->full[s], 1);
+      tc::mbar_init(&sm->full[s], a.i8 ? 2 : 1);  // int8: the two expanding warps; else the loader (+ bytes)
       tc::mbar_init(&sm->empty[s], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sm->raw_full[i], 1);
+      tc::mbar_init(&sm->raw_empty[i], 2);
+    }
+    for (int i = 0; i < SCALE_RING; ++i) tc::mbar_init(&sm->sready[i], 2);
     for (int i = 0; i < 4; ++i) {
       tc::mbar_init(&sm->dfull[i], 1);
       tc::mbar_init(&sm->dempty[i], 4);
@@ -720,7 +733,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::tma_prefetch_desc(&kmap);
       tc::tma_prefetch_desc(&qmap);
     }
-    int stage = 0, cur_b = -1, qn = 0;
+    int stage = 0, cur_b = -1, qn = 0, rn = 0;
     uint32_t phase = 0;
     bool stop = false;
     const uint64_t pol = tc::l2_policy_evict_first();
@@ -745,8 +758,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int ok = 1;
         if (lane == 0) {
           if (b != cur_b) {
-            const int slot = qn & 1;
-            ok = tc::mbar_wait_bounded(&sm->qempty[slot], ((qn >> 1) & 1) ^ 1, abort);
+            const int slot = qn % a.nqs;
+            ok = tc::mbar_wait_bounded(&sm->qempty[slot], ((qn / a.nqs) & 1) ^ 1, abort);
             if (ok) {
               tc::mbar_arrive_expect_tx(&sm->qfull[slot], q_bytes);
               for (int kb = 0; kb < a.kblk; ++kb)
@@ -756,8 +769,21 @@ __global__ void __launch_bounds__(THREADS, 1)
               cur_b = b;
             }
           }
-          if (ok) ok = tc::mbar_wait_bounded(&sm->empty[stage], phase ^ 1, abort);
-          if (ok) {
+          if (ok && a.i8) {
+            // raw int8 pages (whole records, untiled bulk copies) into raw stage rn % 2
+            const int rs = rn & 1;
+            ok = tc::mbar_wait_bounded(&sm->raw_empty[rs], ((rn >> 1) & 1) ^ 1, abort);
+            if (ok) {
+              tc::mbar_arrive_expect_tx(&sm->raw_full[rs], (uint32_t)((p0 >= 0) + (p1 >= 0)) * (uint32_t)raw_page);
+              if (p0 >= 0)
+                tc::bulk_load(raw_mem + rs * raw_stage, a.k_raw + (int64_t)p0 * raw_page, raw_page, &sm->raw_full[rs]);
+              if (p1 >= 0)
+                tc::bulk_load(raw_mem + rs * raw_stage + raw_page, a.k_raw + (int64_t)p1 * raw_page, raw_page,
+                              &sm->raw_full[rs]);
+              ++rn;
+            }
+          } else if (ok) ok = tc::mbar_wait_bounded(&sm->empty[stage], phase ^ 1, abort);
+          if (ok && !a.i8) {
             const uint32_t bytes = (uint32_t)((p0 >= 0) + (p1 >= 0)) * a.kblk * (KB_BYTES / 2);
             uint8_t* st = stage_mem + stage * stage_bytes;
             tc::mbar_arrive_expect_tx(&sm->full[stage], bytes);
@@ -782,14 +808,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (lane == 0) {
       // drain: every issued load must land before the CTA may exit (a completed phase returns at once)
-      for (int s = 0; s < a.stages; ++s) {
-        const int parity = (s < stage) ? (int)phase : (int)(phase ^ 1);
-        tc::mbar_wait_bounded(&sm->full[s], parity, abort, 100000000ull);
+      if (a.i8) {
+        for (int r = (rn > 2 ? rn - 2 : 0); r < rn; ++r)
+          tc::mbar_wait_bounded(&sm->raw_full[r & 1], (r >> 1) & 1, abort, 100000000ull);
+      } else {
+        for (int s = 0; s < a.stages; ++s) {
+          const int parity = (s < stage) ? (int)phase : (int)(phase ^ 1);
+          tc::mbar_wait_bounded(&sm->full[s], parity, abort, 100000000ull);
+        }
       }
-      for (int slot = 0; slot < 2; ++slot) {
-        const int last = (qn - 1 - slot) >= 0 ? (qn - 1) - ((qn - 1 - slot) & 1) : -1;  // last load into slot
-        if (last >= 0) tc::mbar_wait_bounded(&sm->qfull[slot], (last >> 1) & 1, abort, 100000000ull);
-      }
+      for (int q = (qn > a.nqs ? qn - a.nqs : 0); q < qn; ++q)  // the last load into each query slot
+        tc::mbar_wait_bounded(&sm->qfull[q % a.nqs], (q / a.nqs) & 1, abort, 100000000ull);
     }
   } else if (warp == W_MMA) {
     if (lane == 0) {
@@ -801,8 +830,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       cur.init(a, lo, hi);
       while (cur.valid()) {
         if (cur.b != cur_b) {
-          slot = qn & 1;
-          if (!tc::mbar_wait_bounded(&sm->qfull[slot], (qn >> 1) & 1, abort)) break;
+          slot = qn % a.nqs;
+          if (!tc::mbar_wait_bounded(&sm->qfull[slot], (qn / a.nqs) & 1, abort)) break;
           ++qn;
           cur_b = cur.b;
         }
@@ -836,6 +865,52 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc::mma_commit(&sm->done);
       tc::mbar_wait_bounded(&sm->done, 0, abort, 100000000ull);
+    }
+  } else if (warp > W_MMA) {
+    // ---------------- int8 keys: warps 10-11 expand each tile's raw records into the bf16 stage
+    // (K-major, 128-byte swizzle, as TMA would write it; an int8 value is exact in bf16) and keep the
+    // row scales for the epilogue (s = scale * sum_h w_h ReLU(q_h . code), since ReLU(c x) = c ReLU(x)
+    // for c > 0)
+    if (a.i8) {
+      const int x = threadIdx.x - (W_MMA + 1) * 32;  // 0..63: rows x and x + 64 of each tile
+      const int rec = a.d + 4;
+      ItemIter cur;
+      cur.init(a, lo, hi);
+      for (int k = 0; cur.valid(); cur.next(a), ++k) {
+        const int rs = k & 1, st = k % a.stages;
+        if (!tc::mbar_wait_bounded(&sm->raw_full[rs], (k >> 1) & 1, abort) ||
+            !tc::mbar_wait_bounded(&sm->empty[st], ((k / a.stages) & 1) ^ 1, abort))
+          break;
+        const int j0 = cur.tile * TILE;
+        uint8_t* stg = stage_mem + st * stage_bytes;
+        float* sc = scale_s + (k % SCALE_RING) * TILE;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = x + 64 * h;
+          if (j0 + r >= cur.nc) continue;  // no key: its D row is never used
+          const uint8_t* src = raw_mem + rs * raw_stage + h * raw_page + (r & 63) * rec;
+          for (int g8 = 0; g8 < a.d / 8; ++g8) {  // 8 codes -> one 16-byte chunk of 8 bf16
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(src + 8 * g8);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(src + 8 * g8 + 4);
+            const int8_t* c0 = reinterpret_cast<const int8_t*>(&w0);
+            const int8_t* c1 = reinterpret_cast<const int8_t*>(&w1);
+            const uint4 out = make_uint4(float2_to_bf16x2_bits((float)c0[0], (float)c0[1]),
+                                         float2_to_bf16x2_bits((float)c0[2], (float)c0[3]),
+                                         float2_to_bf16x2_bits((float)c1[0], (float)c1[1]),
+                                         float2_to_bf16x2_bits((float)c1[2], (float)c1[3]));
+            const int kb = g8 >> 3, ch = g8 & 7;
+            *reinterpret_cast<uint4*>(stg + kb * KB_BYTES + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4)) = out;
+          }
+          sc[r] = *reinterpret_cast<const float*>(src + a.d);
+        }
+        tc::fence_proxy_async_smem();  // the expanded tile is read by the tensor cores
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(&sm->raw_empty[rs]);
+          tc::mbar_arrive(&sm->full[st]);
+          tc::mbar_arrive(&sm->sready[k % SCALE_RING]);
+        }
+      }
     }
   } else {
     // ---------------- epilogue: warps 0-7 in two groups of four; group g takes the CTA's items
@@ -882,8 +957,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc::tc_fence_after();
+      float kscale = 1.f;
+      if (a.i8) {
+        if (!tc::mbar_wait_bounded(&sm->sready[k % SCALE_RING], (k / SCALE_RING) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        kscale = scale_s[(k % SCALE_RING) * TILE + row];
+      }
       float sk[DSV4_MAX_Q_PER_SEQ] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * a.N);
+      const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(acc * a.N);
       for (int c0 = 0; c0 < a.N; c0 += 64) {
         uint32_t r[64];
         tc::tmem_ld32_nowait(lane_addr + c0, r);
@@ -926,6 +1009,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q) {
         if (q < a.qps) {
+          sk[q] *= kscale;  // 1 for bf16 keys
           const int t = b * a.qps + q;
           const bool on = j < nc_tok[q];
           if (on) a.bufs.scores[(int64_t)t * a.bufs.nc_stride + j] = sk[q];
@@ -978,8 +1062,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 static bool use_tc_indexer(const dsv4_indexer_topk_params& p) {
   const int N = p.q_per_seq * p.n_heads;
-  return p.k_dtype == DSV4_BF16 && p.q_dtype == DSV4_BF16 && (p.head_dim == 64 || p.head_dim == 128) &&
-         p.n_heads % 32 == 0 && N >= 64 && N <= 128 && N % 64 == 0 && p.page_size == 64;
+  return (p.k_dtype == DSV4_BF16 || p.k_dtype == DSV4_I8_ROWSCALE) && p.q_dtype == DSV4_BF16 &&
+         (p.head_dim == 64 || p.head_dim == 128) && p.n_heads % 32 == 0 && N >= 64 && N <= 128 && N % 64 == 0 &&
+         p.page_size == 64;
 }
 
 static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, const TopkBufs& bufs,
@@ -1008,19 +1093,31 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   a.N = p.q_per_seq * p.n_heads;
   a.kblk = p.head_dim / 64;
   a.nacc = 4 * a.N <= 512 ? 4 : 2;  // TMEM accumulators (512 columns available)
+  a.i8 = p.k_dtype == DSV4_I8_ROWSCALE;
+  a.k_raw = reinterpret_cast<const uint8_t*>(p.k_cache);
   a.tmem_cols = a.nacc * a.N <= 64 ? 64 : (a.nacc * a.N <= 128 ? 128 : (a.nacc * a.N <= 256 ? 256 : 512));
-  const size_t fixed = 1024 + 2 * (size_t)a.kblk * a.N * 128 + (2 * 256 + WSEQ * 128) * 4 +
-                       2 * (size_t)a.qps * HIST_BINS * 4 + sizeof(Smem);
   const size_t budget = 227 * 1024;
+  auto fixed_for = [&](int nqs) {
+    return 1024 + (size_t)nqs * a.kblk * a.N * 128 +
+           (a.i8 ? 2 * 2 * 64 * (size_t)(a.d + 4) + (size_t)SCALE_RING * TILE * 4 : 0) +
+           (2 * 256 + WSEQ * 128) * 4 + 2 * (size_t)a.qps * HIST_BINS * 4 + sizeof(Smem);
+  };
+  a.nqs = 2;  // a second query slot lets the next sequence's queries load early, if there is room
+  if ((budget - fixed_for(2)) / ((size_t)a.kblk * KB_BYTES) < 2) a.nqs = 1;
+  const size_t fixed = fixed_for(a.nqs);
   const int stages = (int)((budget - fixed) / ((size_t)a.kblk * KB_BYTES));
   a.stages = stages > MAX_STAGES ? MAX_STAGES : stages;
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + (size_t)a.stages * a.kblk * KB_BYTES;
   CUtensorMap kmap, qmap;
-  cudaError_t e = make_tmap_2d_bf16(&kmap, p.k_cache, (uint64_t)p.head_dim, (uint64_t)p.num_pages * 64, 64, 64);
+  cudaError_t e = make_tmap_2d_bf16(&qmap, p.q, (uint64_t)p.head_dim, (uint64_t)p.T * p.n_heads, 64, (uint32_t)a.N);
   if (e != cudaSuccess) return e;
-  e = make_tmap_2d_bf16(&qmap, p.q, (uint64_t)p.head_dim, (uint64_t)p.T * p.n_heads, 64, (uint32_t)a.N);
-  if (e != cudaSuccess) return e;
+  if (a.i8) {
+    kmap = qmap;  // int8 records are bulk-copied: the key map is not used
+  } else {
+    e = make_tmap_2d_bf16(&kmap, p.k_cache, (uint64_t)p.head_dim, (uint64_t)p.num_pages * 64, 64, 64);
+    if (e != cudaSuccess) return e;
+  }
   static int attr_done = 0;
   if (!attr_done) {
     e = cudaFuncSetAttribute(indexer_score_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
