@@ -549,13 +549,14 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
 namespace ixtc {
 constexpr int TILE = 128;
 constexpr int KB_BYTES = TILE * 128;         // one 64-dim K-block of a key tile (128 rows x 128 B)
-constexpr int THREADS = 384;
-static_assert(THREADS / 32 >= tk::SCAN_WARPS_MIN, "the top-k scan covers a chunk with this many warps");
+constexpr int THREADS = 384;  // bf16 keys launch 320 (no expanding warps)
+static_assert((THREADS - 64) / 32 >= tk::SCAN_WARPS_MIN, "the top-k scan covers a chunk with this many warps");
 constexpr int W_LOAD = 8, W_MMA = 9;  // warps 10-11 expand int8 keys to bf16 (int8 caches only)
 constexpr int SCALE_RING = 16;        // int8 keys: row scales of the last 16 tiles (> stages + accumulators)
 constexpr int MAX_STAGES = 8;
 constexpr int FIN_MAX = 64;  // sequences whose top-k one CTA may have to run
 constexpr int WSEQ = 8;      // sequences whose head weights and entry counts are loaded up front
+constexpr int PRE_MAX = 1024;  // batches up to this size split the key tiles evenly over the CTAs
 
 struct Args {
   const int32_t* positions;
@@ -578,6 +579,8 @@ struct Smem {
   uint64_t raw_full[2], raw_empty[2], sready[SCALE_RING];  // int8 keys
   int fin[FIN_MAX];
   int nc_tab[WSEQ][DSV4_MAX_Q_PER_SEQ];
+  int pre[PRE_MAX];  // exclusive prefix of the sequences' key tiles (balanced item ranges)
+  int range[2];      // this CTA's [lo, hi) of the (sequence, tile) grid
   uint32_t nfin;
   uint32_t tmem_base;
   int abort;
@@ -657,6 +660,10 @@ __device__ __forceinline__ bool finish_seq(const Args& a, Smem* sm, uint32_t* hi
   return true;
 }
 
+// One instance per key format: the bf16 one has no expanding warps (320 threads) and none of the
+// int8 branches. Both keep the 384-thread register cap: three warps of a sub-partition share its
+// 16K registers, so 168 a thread.
+template <bool I8>
 __global__ void __launch_bounds__(THREADS, 1)
     indexer_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, Args a) {
   extern __shared__ __align__(1024) uint8_t dsm[];
@@ -667,8 +674,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* q_mem = base + a.stages * stage_bytes;                          // nqs slots x q_bytes
   const int raw_page = 64 * (a.d + 4), raw_stage = 2 * raw_page;          // int8 records: d bytes + fp32 scale
   uint8_t* raw_mem = q_mem + a.nqs * q_bytes;                              // int8: 2 raw stages
-  float* scale_s = reinterpret_cast<float*>(raw_mem + (a.i8 ? 2 * raw_stage : 0));  // int8: SCALE_RING x 128
-  float* w_s = scale_s + (a.i8 ? SCALE_RING * TILE : 0);                  // 2 groups x 256 floats
+  float* scale_s = reinterpret_cast<float*>(raw_mem + (I8 ? 2 * raw_stage : 0));  // int8: SCALE_RING x 128
+  float* w_s = scale_s + (I8 ? SCALE_RING * TILE : 0);                  // 2 groups x 256 floats
   float* w_tab = w_s + 2 * 256;                                            // WSEQ x 128 floats
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(w_tab + WSEQ * 128);      // 2 groups x qps x HIST_BINS
   Smem* sm = reinterpret_cast<Smem*>(hist_s + 2 * a.qps * HIST_BINS);
@@ -676,12 +683,52 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = a.B * a.tiles_max;
-  const int lo = (int)((int64_t)blockIdx.x * total / gridDim.x);
-  const int hi = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
+  // this CTA's range [lo, hi) of the (sequence, tile) grid: an even share of the sequences' valid
+  // tiles (grid positions past a sequence's entries are skipped by every role), worked out by the
+  // loading warp from a prefix over the sequences' tile counts while the others set up
+  if (warp == W_LOAD) {
+    int r0 = (int)((int64_t)blockIdx.x * total / gridDim.x), r1 = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
+    if (a.B <= PRE_MAX) {
+      // the tile counts first (independent loads, all in flight together), then the scan
+#pragma unroll 4
+      for (int b = lane; b < a.B; b += 32) sm->pre[b] = (seq_entries(a, b) + TILE - 1) / TILE;
+      __syncwarp();
+      int running = 0;
+      for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int v = b < a.B ? sm->pre[b] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        if (b < a.B) sm->pre[b] = running + incl - v;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncwarp();
+      auto dense = [&](int x) {  // grid position of valid tile number x
+        if (x >= running) return total;
+        int l = 0, r = a.B - 1;  // last b with pre[b] <= x (it has a tile, since x < pre[b + 1])
+        while (l < r) {
+          const int m = (l + r + 1) >> 1;
+          if (sm->pre[m] <= x) l = m;
+          else r = m - 1;
+        }
+        return l * a.tiles_max + (x - sm->pre[l]);
+      };
+      r0 = dense((int)((int64_t)blockIdx.x * running / gridDim.x));
+      r1 = dense((int)((int64_t)(blockIdx.x + 1) * running / gridDim.x));
+    }
+    if (lane == 0) {
+      sm->range[0] = r0;
+      sm->range[1] = r1;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
-      tc::mbar_init(&sm->full[s], a.i8 ? 2 : 1);  // int8: the two expanding warps; else the loader (+ bytes)
+      tc::mbar_init(&sm->full[s], I8 ? 2 : 1);  // int8: the two expanding warps; else the loader (+ bytes)
       tc::mbar_init(&sm->empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -704,22 +751,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     sm->abort = 0;
     tc::fence_barrier_init();
   }
-  for (int x = threadIdx.x; x < 2 * a.qps * HIST_BINS; x += THREADS) hist_s[x] = 0;
+  for (int x = threadIdx.x; x < 2 * a.qps * HIST_BINS; x += blockDim.x) hist_s[x] = 0;
+  if (warp == W_MMA) {
+    tc::tmem_alloc(&sm->tmem_base, a.tmem_cols);
+    tc::tmem_relinquish();
+    tc::tc_fence_before();
+  }
+  __syncthreads();
+  const int lo = sm->range[0], hi = sm->range[1];
   // head weights and per-token entry counts of the CTA's sequences, when there are few of them
   const int b_first = lo / a.tiles_max;
   const int nseq_rng = hi > lo ? (hi - 1) / a.tiles_max - b_first + 1 : 0;
   const bool pre = nseq_rng <= WSEQ;
   if (pre) {
-    for (int x = threadIdx.x; x < nseq_rng * a.N; x += THREADS)
+    for (int x = threadIdx.x; x < nseq_rng * a.N; x += blockDim.x)
       w_tab[x] = a.weights[(int64_t)b_first * a.qps * a.Ih + x];
-    for (int x = threadIdx.x; x < nseq_rng * a.qps; x += THREADS)
+    for (int x = threadIdx.x; x < nseq_rng * a.qps; x += blockDim.x)
       sm->nc_tab[x / a.qps][x % a.qps] =
           visible_entries(a.positions, (b_first + x / a.qps) * a.qps + x % a.qps, a.max_context, a.ratio);
-  }
-  if (warp == W_MMA) {
-    tc::tmem_alloc(&sm->tmem_base, a.tmem_cols);
-    tc::tmem_relinquish();
-    tc::tc_fence_before();
   }
   pdl_launch_dependents();
   pdl_wait();  // the prologue above overlaps the previous kernel
@@ -769,7 +818,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               cur_b = b;
             }
           }
-          if (ok && a.i8) {
+          if (ok && I8) {
             // raw int8 pages (whole records, untiled bulk copies) into raw stage rn % 2
             const int rs = rn & 1;
             ok = tc::mbar_wait_bounded(&sm->raw_empty[rs], ((rn >> 1) & 1) ^ 1, abort);
@@ -783,7 +832,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               ++rn;
             }
           } else if (ok) ok = tc::mbar_wait_bounded(&sm->empty[stage], phase ^ 1, abort);
-          if (ok && !a.i8) {
+          if (ok && !I8) {
             const uint32_t bytes = (uint32_t)((p0 >= 0) + (p1 >= 0)) * a.kblk * (KB_BYTES / 2);
             uint8_t* st = stage_mem + stage * stage_bytes;
             tc::mbar_arrive_expect_tx(&sm->full[stage], bytes);
@@ -808,7 +857,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (lane == 0) {
       // drain: every issued load must land before the CTA may exit (a completed phase returns at once)
-      if (a.i8) {
+      if (I8) {
         for (int r = (rn > 2 ? rn - 2 : 0); r < rn; ++r)
           tc::mbar_wait_bounded(&sm->raw_full[r & 1], (r >> 1) & 1, abort, 100000000ull);
       } else {
@@ -871,7 +920,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // (K-major, 128-byte swizzle, as TMA would write it; an int8 value is exact in bf16) and keep the
     // row scales for the epilogue (s = scale * sum_h w_h ReLU(q_h . code), since ReLU(c x) = c ReLU(x)
     // for c > 0)
-    if (a.i8) {
+    if (I8) {
       const int x = threadIdx.x - (W_MMA + 1) * 32;  // 0..63: rows x and x + 64 of each tile
       const int rec = a.d + 4;
       ItemIter cur;
@@ -890,16 +939,22 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (j0 + r >= cur.nc) continue;  // no key: its D row is never used
           const uint8_t* src = raw_mem + rs * raw_stage + h * raw_page + (r & 63) * rec;
           for (int g8 = 0; g8 < a.d / 8; ++g8) {  // 8 codes -> one 16-byte chunk of 8 bf16
-            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(src + 8 * g8);
-            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(src + 8 * g8 + 4);
-            const int8_t* c0 = reinterpret_cast<const int8_t*>(&w0);
-            const int8_t* c1 = reinterpret_cast<const int8_t*>(&w1);
-            const uint4 out = make_uint4(float2_to_bf16x2_bits((float)c0[0], (float)c0[1]),
-                                         float2_to_bf16x2_bits((float)c0[2], (float)c0[3]),
-                                         float2_to_bf16x2_bits((float)c1[0], (float)c1[1]),
-                                         float2_to_bf16x2_bits((float)c1[2], (float)c1[3]));
+            uint32_t o[4];
+#pragma unroll
+            for (int h4 = 0; h4 < 2; ++h4) {
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(src + 8 * g8 + 4 * h4) ^ 0x80808080u;
+              // code c as the float 2^23 + (c + 128), minus 2^23 + 128: exact; a small integer's bf16
+              // bits are the top half of its fp32 bits
+              float f[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                f[k] = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)k)) - 8388736.0f;
+              o[2 * h4] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
+              o[2 * h4 + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
+            }
+            const uint4 outv = make_uint4(o[0], o[1], o[2], o[3]);
             const int kb = g8 >> 3, ch = g8 & 7;
-            *reinterpret_cast<uint4*>(stg + kb * KB_BYTES + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4)) = out;
+            *reinterpret_cast<uint4*>(stg + kb * KB_BYTES + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4)) = outv;
           }
           sc[r] = *reinterpret_cast<const float*>(src + a.d);
         }
@@ -958,7 +1013,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc::tc_fence_after();
       float kscale = 1.f;
-      if (a.i8) {
+      if (I8) {
         if (!tc::mbar_wait_bounded(&sm->sready[k % SCALE_RING], (k / SCALE_RING) & 1, abort)) {
           ok = false;
           break;
@@ -1050,7 +1105,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (seq_entries(a, b) != 0) continue;
     for (int q = 0; q < a.qps; ++q) {
       const int t = b * a.qps + q;
-      for (int x = threadIdx.x; x < a.K; x += THREADS) {
+      for (int x = threadIdx.x; x < a.K; x += blockDim.x) {
         a.topk_idx[(int64_t)t * a.K + x] = -1;
         if (a.topk_score) a.topk_score[(int64_t)t * a.K + x] = -INFINITY;
       }
@@ -1120,7 +1175,9 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   }
   static int attr_done = 0;
   if (!attr_done) {
-    e = cudaFuncSetAttribute(indexer_score_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+    e = cudaFuncSetAttribute(indexer_score_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(indexer_score_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
     if (e != cudaSuccess) return e;
     attr_done = 1;
   }
@@ -1129,7 +1186,10 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   if (grid > total) grid = total;
   if (grid < (total + FIN_MAX - 1) / FIN_MAX) grid = (total + FIN_MAX - 1) / FIN_MAX;  // <= FIN_MAX items per CTA
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(indexer_score_tc, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/false, kmap, qmap, a);
+  // the two expanding warps exist only for int8 keys
+  if (a.i8)
+    return launch_pdl(indexer_score_tc<true>, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/false, kmap, qmap, a);
+  return launch_pdl(indexer_score_tc<false>, dim3(grid), dim3(THREADS - 64), smem, st, /*pdl=*/false, kmap, qmap, a);
 }
 
 // ------------------------------------------------------------------------------------------------
