@@ -260,6 +260,15 @@ __global__ void __launch_bounds__(AT_THREADS) mla_partial_simt(dsv4_sparse_mla_d
 // loaded half gets zero V (it may hold anything, and 0 x NaN would poison O); PV skips halves that
 // were not loaded.  At the end the same warps turn O^T into [head][value] rows in the idle tile
 // buffer and store the unnormalised O and the chunk's (max, sum) per head.
+//
+// fp8_ds_mla caches (656-byte records: 512 e4m3 codes, 64 bf16 rope dims, 8 UE8M0 block exponents)
+// run the same kernel with the tile converted in shared memory: the codes of K-block kb < 8 (64 B
+// a row) are loaded by TMA, untiled, into the upper 8 KB of slot kb, and softmax warp kb (idle
+// between handing over P^T and the next tile's S^T) expands them in place into bf16
+// code x 2^(e - 127) in the swizzled K-major layout (exact: an e4m3 value times a power of two has
+// at most 4 significant bits).  The rope dims are bf16 already and go by TMA straight into slot 8.
+// The tile's block exponents (8 bytes a row) come by cp.async with the first group's loads.
+// Everything after the expansion is the bf16 kernel's.
 // ------------------------------------------------------------------------------------------------
 namespace attc {
 constexpr int TILE = 128;                  // rows per tile
@@ -279,6 +288,8 @@ constexpr float RESCALE_LOG2 = 8.0f;
 constexpr uint32_t FLAG_TIMEOUT = 4u;
 constexpr int K_NONE = 0, K_BOX_SWA = 1, K_BOX_MAIN = 2, K_GATHER = 3;
 constexpr int MAX_MERGE_CLUSTER = 8;  // up to this many chunks per token merge inside a (portable) cluster
+constexpr int RAW_OFF = SLOT_BYTES / 2;  // fp8: the codes of K-block kb (128 rows x 64 B) staged in slot kb from here
+constexpr int RAW_HALF = HALF * 64;      // fp8: codes of one K-block of a 64-row half (4 KB)
 
 struct Args {
   dsv4_sparse_mla_decode_params p;
@@ -292,6 +303,9 @@ struct Args {
 
 struct Smem {
   uint64_t full[NGROUPS], vfree[4], sfull, pfull, pvdone, qfull, odone, xbar[2][2], ebar;
+  uint64_t rawb[NPROD][4];  // fp8: codes of loader p's K-blocks in group g have landed
+  uint64_t sbar;            // fp8: the tile's block exponents and row masks are in
+  uint2 scl[TILE];          // fp8: UE8M0 bytes of the tile's rows (byte kb: K-block kb)
   uint32_t mask[2][4];  // [tile parity][row / 32]: valid rows
   uint32_t loaded[2];   // [tile parity]: bit u = half u was loaded
   float red[2][2][4][32];  // [tile parity][head half][row quarter][lane]: per-warp maxima
@@ -427,10 +441,72 @@ __device__ __forceinline__ float transpose_reduce32(const float (&x)[32], int la
   return v[0];
 }
 
+// Four e4m3 codes (byte k = code k) times 2^(e - 127) as bf16, with integer and fp32 arithmetic only.
+// With code k in the top byte, an arithmetic shift by 4 and a mask leave the sign, the 4 exponent
+// bits as the low bits of the fp32 exponent field and the 3 mantissa bits at its top: the float
+// code x 2^-120 for every code, subnormal codes included.  Multiplying by s1 = 2^120 (only when
+// s2 alone would overflow) and s2 scales it exactly, and the bf16 is the product's upper half, also
+// exact (at most 4 significant bits; e in 3 .. 246 keeps every product inside bf16's range).
+__device__ __forceinline__ uint2 e4m3x4_scaled_bf16(uint32_t codes, float s1, float s2) {
+  float f[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int y = (int)__byte_perm(codes, 0u, 0x0444u | ((uint32_t)k << 12));
+    f[k] = __int_as_float((y >> 4) & (int)0x87F00000u) * s1 * s2;
+  }
+  return make_uint2(__byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u),
+                    __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u));
+}
+
+// fp8: expands K-block kb of the tile's loaded halves (bit u of `ld` = half u), staged as
+// [128 rows][64 codes] from RAW_OFF of the slot, into bf16 in the slot's K-major 128-byte-swizzled
+// layout, with the rows' UE8M0 bytes in scl.  Lane L owns rows L, 32 + L, 64 + L, 96 + L.  The bf16
+// rows 0-63 lie below the staged codes, rows 64-95 over the staged codes of half 0 and rows 96-127
+// over those of half 1: so half 0 goes first, then row 64 + L while the codes of row 96 + L are held
+// in registers, then row 96 + L.  Reads rotate the lanes' word order (lane pairs apart by 16 banks)
+// and the 8-byte writes land on 16 distinct bank pairs per half-warp.  One loop body serves the
+// four rows, so the code the warp streams through stays small.
+__device__ __forceinline__ void expand_fp8_kblock(uint8_t* slot, uint32_t ld, const uint2* scl, int kb, int lane) {
+  const uint32_t* raw = reinterpret_cast<const uint32_t*>(slot + RAW_OFF);
+  const int rot = lane >> 1;
+  uint32_t held[16];
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    if (i == 2) {
+      if (ld & 2u) {
+#pragma unroll
+        for (int w = 0; w < 16; ++w) held[w] = raw[(96 + lane) * 16 + ((w + rot) & 15)];
+      }
+      __syncwarp();  // half 0's codes are all read
+    }
+    if (i == 3) __syncwarp();  // the codes of rows 64-95 are all read
+    if (!((ld >> (i >> 1)) & 1u)) continue;
+    const int r = 32 * i + lane;
+    const uint2 b = scl[r];
+    const uint32_t e = ((kb < 4 ? b.x : b.y) >> (8 * (kb & 3))) & 0xFFu;
+    const float s1 = e <= 134u ? 1.0f : 0x1p120f;
+    const float s2 = e <= 134u ? __uint_as_float((e + 120u) << 23) : ue8m0_scale((uint8_t)e);  // s1 s2 = 2^(e - 7)
+    uint32_t c[16];
+#pragma unroll
+    for (int w = 0; w < 16; ++w) c[w] = i == 3 ? held[w] : raw[r * 16 + ((w + rot) & 15)];
+    uint8_t* row = slot + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+    for (int w = 0; w < 16; ++w) {
+      const int wr = (w + rot) & 15;  // the word's codes are dims 4 wr .. 4 wr + 3 of the K-block
+      *reinterpret_cast<uint2*>(row + ((((wr >> 1) ^ (lane & 7)) << 4) | ((wr & 1) << 3))) =
+          e4m3x4_scaled_bf16(c[w], s1, s2);
+    }
+  }
+}
+
+// FP8: the caches hold fp8_ds_mla records (swamap64 / mainmap / mainmap64 then map their codes as
+// bytes, and the rope maps their bf16 rope dims); else bf16 rows (the rope maps are unused).
+template <bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
     mla_partial_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap swamap64,
                    const __grid_constant__ CUtensorMap mainmap, const __grid_constant__ CUtensorMap mainmap64,
-                   Args a) {
+                   const __grid_constant__ CUtensorMap ropeswa64, const __grid_constant__ CUtensorMap ropemain,
+                   const __grid_constant__ CUtensorMap ropemain64, Args a) {
   extern __shared__ __align__(1024) uint8_t dsm[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   uint8_t* q_mem = base;             // Q_BYTES
@@ -454,7 +530,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int ntiles = nh > 0 ? (nh + 1) / 2 : 0;
 
   if (threadIdx.x == 0) {
-    for (int g = 0; g < NGROUPS; ++g) tc::mbar_init(&sm->full[g], NPROD);
+    // fp8: groups 0-3 are released by the two softmax warps that expand their K-blocks
+    for (int g = 0; g < NGROUPS; ++g) tc::mbar_init(&sm->full[g], FP8 && g < NGROUPS - 1 ? 2 : NPROD);
+    for (int x = 0; x < NPROD * 4; ++x) tc::mbar_init(&sm->rawb[x / 4][x % 4], 1);
+    tc::mbar_init(&sm->sbar, 33);  // fp8: loader 0's 32 lanes' exponent copies + its row masks
     for (int m = 0; m < 4; ++m) tc::mbar_init(&sm->vfree[m], 1);
     tc::mbar_init(&sm->sfull, 1);
     tc::mbar_init(&sm->pfull, 8);
@@ -494,6 +573,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::tma_prefetch_desc(&swamap64);
       tc::tma_prefetch_desc(&mainmap);
       tc::tma_prefetch_desc(&mainmap64);
+      if (FP8) {
+        tc::tma_prefetch_desc(&ropeswa64);
+        tc::tma_prefetch_desc(&ropemain);
+        tc::tma_prefetch_desc(&ropemain64);
+      }
       tc::mbar_arrive_expect_tx(&sm->qfull, Q_BYTES);
       for (int kb = 0; kb < NKB; ++kb)
         tc::tma_load_2d(q_mem + kb * HG * 128, &qmap, kb * 64, t * p.H + hg * HG, &sm->qfull);
@@ -534,6 +618,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int kb0 = 2 * g, nkb = g < 4 ? 2 : 1;
         int mine = 0;  // K-blocks of this group that this loader issues
         for (int kb = kb0; kb < kb0 + nkb; ++kb) mine += kb % NPROD == pidx;
+        if (FP8 && g == 0 && pidx == 0) {
+          // the tile's block exponents (rows 64 u + 32 v + lane), now that the previous tile's
+          // expansion is over (its S^T is done: vfree[0] has passed)
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const bool swa = hp[u].kind == K_BOX_SWA;
+            const uint8_t* cache = reinterpret_cast<const uint8_t*>(swa ? p.swa_cache : p.main_cache);
+            const int rows = swa ? a.swa_rows : a.main_rows;
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              const int y = hp[u].kind == K_GATHER ? (v ? hp[u].y1 : hp[u].y0) : hp[u].ybox + 32 * v + lane;
+              const bool in = hp[u].kind != K_NONE && y >= 0 && y < rows;
+              // (a row with no record reads nothing and gets zeros; the address is still a valid one)
+              const uint8_t* src = in ? cache + (int64_t)y * FP8_REC + FP8_SCALE_OFF
+                                      : reinterpret_cast<const uint8_t*>(p.swa_cache);
+              tc::cp_async8(&sm->scl[64 * u + 32 * v + lane], src, in ? 8u : 0u);
+            }
+          }
+          tc::cp_async_mbar_arrive(&sm->sbar);
+        }
         if (lane == 0) {
           if (g == 0 && pidx == 0) {
             sm->mask[i & 1][0] = m0;
@@ -541,25 +645,36 @@ __global__ void __launch_bounds__(THREADS, 1)
             sm->mask[i & 1][2] = m2;
             sm->mask[i & 1][3] = m3;
             sm->loaded[i & 1] = ld;
+            if (FP8) tc::mbar_arrive(&sm->sbar);
           }
-          tc::mbar_arrive_expect_tx(&sm->full[g], (uint32_t)(nload * mine * HALF_BYTES));
+          if (!FP8 || g == NGROUPS - 1)  // bf16 rows (fp8: the rope slot) land on the group's barrier
+            tc::mbar_arrive_expect_tx(&sm->full[g], (uint32_t)(nload * mine * HALF_BYTES));
+          else if (mine > 0)  // fp8 codes land on the loader's own barrier, to be expanded first
+            tc::mbar_arrive_expect_tx(&sm->rawb[pidx][g], (uint32_t)(nload * mine * RAW_HALF));
         }
         armed_tile = i;
         armed_groups = g + 1;
         __syncwarp();
         for (int kb = kb0; kb < kb0 + nkb; ++kb) {
           if (kb % NPROD != pidx) continue;
+          const bool codes = FP8 && kb < NKB - 1;  // fp8 code bytes: staged, expanded once they land
+          const bool rope = FP8 && !codes;         // fp8 rope dims: bf16 already
+          uint8_t* dst = kv_mem + kb * SLOT_BYTES + (codes ? RAW_OFF : 0);
+          const int hstride = codes ? RAW_HALF : HALF_BYTES, rstride = codes ? 64 : 128;
+          uint64_t* bar = codes ? &sm->rawb[pidx][g] : &sm->full[g];
+          const int x = rope ? 0 : kb * 64;
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int kind = hp[u].kind;
             if ((kind == K_BOX_SWA || kind == K_BOX_MAIN) && lane == 0) {
-              const CUtensorMap* map = kind == K_BOX_SWA ? &swamap64 : &mainmap64;
-              tc::tma_load_2d(kv_mem + kb * SLOT_BYTES + u * HALF_BYTES, map, kb * 64, hp[u].ybox, &sm->full[g]);
+              const CUtensorMap* map = kind == K_BOX_SWA ? (rope ? &ropeswa64 : &swamap64)
+                                                         : (rope ? &ropemain64 : &mainmap64);
+              tc::tma_load_2d(dst + u * hstride, map, x, hp[u].ybox, bar);
             }
           }
           if (my_kind == K_GATHER)
-            tc::tma_gather4(kv_mem + kb * SLOT_BYTES + gu * HALF_BYTES + 4 * g4 * 128, &mainmap, kb * 64, r4[0], r4[1],
-                            r4[2], r4[3], &sm->full[g]);
+            tc::tma_gather4(dst + gu * hstride + 4 * g4 * rstride, rope ? &ropemain : &mainmap, x, r4[0], r4[1], r4[2],
+                            r4[3], bar);
         }
       }
     }
@@ -568,6 +683,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (ntiles > 0 && pidx == 0) tc::mbar_wait_bounded(&sm->qfull, 0, abort, 100000000ull);
       for (int g = 0; g < armed_groups; ++g)
         tc::mbar_wait_bounded(&sm->full[g], armed_tile & 1, abort, 100000000ull);
+      if (FP8)
+        for (int g = 0; g < armed_groups && g < NGROUPS - 1; ++g)
+          if ((2 * g) % NPROD == pidx || (2 * g + 1) % NPROD == pidx)
+            tc::mbar_wait_bounded(&sm->rawb[pidx][g], armed_tile & 1, abort, 100000000ull);
     }
   } else if (warp == W_MMA) {
     if (lane == 0) {
@@ -627,6 +746,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* prow = kv_mem + 8 * SLOT_BYTES + (R >> 3) * 1024 + (R & 7) * 128;  // P^T row R
     float* mrow = sm->mrow[warp];
     for (int i = 0; i < ntiles; ++i) {
+      if (FP8) {
+        // K-block `warp` of this tile (8 warps, 8 code K-blocks): expanded once its codes and the
+        // tile's block exponents are in, then its half of the group is released to the MMAs
+        const int kb = warp, g = kb >> 1;
+        if (!tc::mbar_wait_bounded(&sm->sbar, i & 1, abort) ||
+            !tc::mbar_wait_bounded(&sm->rawb[kb % NPROD][g], i & 1, abort)) {
+          ok = false;
+          break;
+        }
+        expand_fp8_kblock(kv_mem + kb * SLOT_BYTES, sm->loaded[i & 1], sm->scl, kb, lane);
+        tc::fence_proxy_async_smem();  // the MMAs read the expanded rows
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm->full[g]);
+      }
       if (!tc::mbar_wait_bounded(&sm->sfull, i & 1, abort) ||
           !tc::mbar_wait_bounded(&sm->full[0], i & 1, abort)) {  // full[0] published the row mask
         ok = false;
@@ -838,7 +971,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace attc
 
 static bool use_tc_attention(const dsv4_sparse_mla_decode_params& p) {
-  return p.cache_dtype == DSV4_BF16 && p.q_dtype == DSV4_BF16 && p.H % attc::HG == 0 && p.page_size == 64;
+  return (p.cache_dtype == DSV4_BF16 || p.cache_dtype == DSV4_FP8_DS_MLA) && p.q_dtype == DSV4_BF16 &&
+         p.H % attc::HG == 0 && p.page_size == 64;
 }
 
 static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p, const AtLayout& L, float* o_part,
@@ -853,25 +987,42 @@ static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p,
   a.main_rows = p.ratio > 0 ? (int)(p.main_num_pages * p.page_size) : a.swa_rows;
   a.c_log2 = p.softmax_scale * 1.4426950408889634f;
   a.cluster_merge = L.n_chunks <= MAX_MERGE_CLUSTER ? 1 : 0;
-  CUtensorMap qmap, swamap64, mainmap, mainmap64;
+  const bool fp8 = p.cache_dtype == DSV4_FP8_DS_MLA;
+  CUtensorMap qmap, swamap64, mainmap, mainmap64, ropeswa64, ropemain, ropemain64;
   cudaError_t e = make_tmap_2d_bf16(&qmap, p.q, (uint64_t)D, (uint64_t)p.T * p.H, 64, HG);
   if (e != cudaSuccess) return e;
-  e = make_tmap_2d_bf16(&swamap64, p.swa_cache, (uint64_t)D, (uint64_t)a.swa_rows, 64, HALF);
+  // a cache's maps: bf16 rows (K-blocks of 64 dims, swizzled), or for fp8_ds_mla records their
+  // 512 code bytes (64-byte boxes, untiled) and their 64 bf16 rope dims (swizzled)
+  auto cache_maps = [&](const void* cache, int rows, uint32_t box_rows, CUtensorMap* codes, CUtensorMap* rope) {
+    if (!fp8) {
+      *rope = qmap;  // unused
+      return make_tmap_2d_bf16(codes, cache, (uint64_t)D, (uint64_t)rows, 64, box_rows);
+    }
+    cudaError_t r = make_tmap_2d(codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, cache, (uint64_t)DV, (uint64_t)rows,
+                                 (uint64_t)FP8_REC, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r != cudaSuccess) return r;
+    return make_tmap_2d(rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, reinterpret_cast<const uint8_t*>(cache) + FP8_ROPE_OFF,
+                        (uint64_t)(D - DV), (uint64_t)rows, (uint64_t)FP8_REC, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  };
+  e = cache_maps(p.swa_cache, a.swa_rows, HALF, &swamap64, &ropeswa64);
   if (e != cudaSuccess) return e;
   if (p.ratio > 0) {
-    e = make_tmap_2d_bf16(&mainmap, p.main_cache, (uint64_t)D, (uint64_t)a.main_rows, 64, 1);
+    e = cache_maps(p.main_cache, a.main_rows, 1, &mainmap, &ropemain);
     if (e != cudaSuccess) return e;
-    e = make_tmap_2d_bf16(&mainmap64, p.main_cache, (uint64_t)D, (uint64_t)a.main_rows, 64, HALF);
+    e = cache_maps(p.main_cache, a.main_rows, HALF, &mainmap64, &ropemain64);
     if (e != cudaSuccess) return e;
   } else {  // no compressed rows: the main-cache maps are never used (still valid maps)
-    e = make_tmap_2d_bf16(&mainmap, p.swa_cache, (uint64_t)D, (uint64_t)a.swa_rows, 64, 1);
+    e = cache_maps(p.swa_cache, a.swa_rows, 1, &mainmap, &ropemain);
     if (e != cudaSuccess) return e;
     mainmap64 = swamap64;
+    ropemain64 = ropeswa64;
   }
   const size_t smem = 1024 + (size_t)Q_BYTES + (size_t)KV_BYTES + sizeof(Smem);
   static int attr_done = 0;
   if (!attr_done) {
-    e = cudaFuncSetAttribute(mla_partial_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(mla_partial_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mla_partial_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = 1;
   }
@@ -889,7 +1040,11 @@ static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, mla_partial_tc, qmap, swamap64, mainmap, mainmap64, a);
+  if (fp8)
+    return cudaLaunchKernelEx(&cfg, mla_partial_tc<true>, qmap, swamap64, mainmap, mainmap64, ropeswa64, ropemain,
+                              ropemain64, a);
+  return cudaLaunchKernelEx(&cfg, mla_partial_tc<false>, qmap, swamap64, mainmap, mainmap64, ropeswa64, ropemain,
+                            ropemain64, a);
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -13,6 +13,12 @@ namespace dsv4 {
 cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                               uint32_t box_rows);
 
+// 2-D tensor of `rows` rows of `cols` elements of type `dt`, consecutive rows `row_bytes` apart (a
+// row may be wider than the mapped columns: a column range of packed records), box
+// [box_rows, box_cols], swizzle `sw`.  Out-of-range rows read as zeros.
+cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                         uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+
 // Multiprocessor count of the current device.
 int num_sms();
 
