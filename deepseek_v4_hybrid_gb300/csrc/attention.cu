@@ -441,21 +441,44 @@ __device__ __forceinline__ float transpose_reduce32(const float (&x)[32], int la
   return v[0];
 }
 
-// Four e4m3 codes (byte k = code k) times 2^(e - 127) as bf16, with integer and fp32 arithmetic only.
-// With code k in the top byte, an arithmetic shift by 4 and a mask leave the sign, the 4 exponent
-// bits as the low bits of the fp32 exponent field and the 3 mantissa bits at its top: the float
-// code x 2^-120 for every code, subnormal codes included.  Multiplying by s1 = 2^120 (only when
-// s2 alone would overflow) and s2 scales it exactly, and the bf16 is the product's upper half, also
-// exact (at most 4 significant bits; e in 3 .. 246 keeps every product inside bf16's range).
-__device__ __forceinline__ uint2 e4m3x4_scaled_bf16(uint32_t codes, float s1, float s2) {
-  float f[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int y = (int)__byte_perm(codes, 0u, 0x0444u | ((uint32_t)k << 12));
-    f[k] = __int_as_float((y >> 4) & (int)0x87F00000u) * s1 * s2;
+// Codes b0..b3 of w (b0 the lowest dim) -> bf16 pairs [b0 b1] and [b2 b3] of code x s1 x s2 x 2^-120.
+// With a code in the top byte of a 16-bit lane, its sign and its 7 exponent and mantissa bits masked
+// into place give the bf16 code x 2^-120 exactly (the 4 exponent bits become the low bits of the bf16
+// exponent and the 3 mantissa bits the top of its mantissa; e4m3 subnormals become bf16 subnormals).
+// Multiplying by powers of two keeps every value exact while the product stays inside bf16's range,
+// which holds for block exponents e in 3 .. 246.  Integer and bf16x2 arithmetic only: the conversion
+// unit is shared by the SM and would bound the expansion.
+template <bool TWO>
+__device__ __forceinline__ uint2 e4m3x4_to_bf16(uint32_t w, __nv_bfloat162 s1, __nv_bfloat162 s2) {
+  uint32_t m01 = __byte_perm(w, 0u, 0x1404u), m23 = __byte_perm(w, 0u, 0x3424u);  // b << 8 in each half
+  m01 = ((m01 >> 4) & 0x07F007F0u) | (m01 & 0x80008000u);
+  m23 = ((m23 >> 4) & 0x07F007F0u) | (m23 & 0x80008000u);
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&m01), b = *reinterpret_cast<__nv_bfloat162*>(&m23);
+  if (TWO) {
+    a = __hmul2(a, s1);
+    b = __hmul2(b, s1);
   }
-  return make_uint2(__byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u),
-                    __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u));
+  a = __hmul2(a, s2);
+  b = __hmul2(b, s2);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+}
+
+// One row of a K-block: v[j] holds the row's codes 16 jr .. 16 jr + 15 (jr = (j + g) & 3), written as
+// the bf16 chunks 2 jr and 2 jr + 1 of the swizzled row (r7 = row & 7), the one of index h first.
+template <bool TWO>
+__device__ __forceinline__ void expand_row16(uint8_t* row, const uint4 (&v)[4], int g, int h, int r7,
+                                             __nv_bfloat162 s1, __nv_bfloat162 s2) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int jr = (j + g) & 3;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int half = e ^ h;  // dims 16 jr + 8 half .. + 7: chunk 2 jr + half
+      const uint2 o0 = e4m3x4_to_bf16<TWO>(half ? v[j].z : v[j].x, s1, s2);
+      const uint2 o1 = e4m3x4_to_bf16<TWO>(half ? v[j].w : v[j].y, s1, s2);
+      *reinterpret_cast<uint4*>(row + (((2 * jr + half) ^ r7) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+    }
+  }
 }
 
 // fp8: expands K-block kb of the tile's loaded halves (bit u of `ld` = half u), staged as
@@ -463,19 +486,21 @@ __device__ __forceinline__ uint2 e4m3x4_scaled_bf16(uint32_t codes, float s1, fl
 // layout, with the rows' UE8M0 bytes in scl.  Lane L owns rows L, 32 + L, 64 + L, 96 + L.  The bf16
 // rows 0-63 lie below the staged codes, rows 64-95 over the staged codes of half 0 and rows 96-127
 // over those of half 1: so half 0 goes first, then row 64 + L while the codes of row 96 + L are held
-// in registers, then row 96 + L.  Reads rotate the lanes' word order (lane pairs apart by 16 banks)
-// and the 8-byte writes land on 16 distinct bank pairs per half-warp.  One loop body serves the
-// four rows, so the code the warp streams through stays small.
+// in registers, then row 96 + L.  Reads and writes move 16 bytes; the order in which lane L takes its
+// row's four 16-code vectors (offset g) and each vector's two output chunks (first h) depends on
+// L & 7 and makes every quarter-warp's reads and writes hit 8 distinct bank groups.  One loop body
+// serves the four rows, so the code the warp streams through stays small.
 __device__ __forceinline__ void expand_fp8_kblock(uint8_t* slot, uint32_t ld, const uint2* scl, int kb, int lane) {
-  const uint32_t* raw = reinterpret_cast<const uint32_t*>(slot + RAW_OFF);
-  const int rot = lane >> 1;
-  uint32_t held[16];
+  const uint4* raw = reinterpret_cast<const uint4*>(slot + RAW_OFF);  // row r: raw[4 r .. 4 r + 3]
+  const int l7 = lane & 7;
+  const int g = (0x27D8 >> (2 * l7)) & 3, h = (0x66 >> l7) & 1;  // g = 0 2 1 3 3 1 2 0, h = 0 1 1 0 0 1 1 0
+  uint4 held[4];
 #pragma unroll 1
   for (int i = 0; i < 4; ++i) {
     if (i == 2) {
       if (ld & 2u) {
 #pragma unroll
-        for (int w = 0; w < 16; ++w) held[w] = raw[(96 + lane) * 16 + ((w + rot) & 15)];
+        for (int j = 0; j < 4; ++j) held[j] = raw[4 * (96 + lane) + ((j + g) & 3)];
       }
       __syncwarp();  // half 0's codes are all read
     }
@@ -484,17 +509,18 @@ __device__ __forceinline__ void expand_fp8_kblock(uint8_t* slot, uint32_t ld, co
     const int r = 32 * i + lane;
     const uint2 b = scl[r];
     const uint32_t e = ((kb < 4 ? b.x : b.y) >> (8 * (kb & 3))) & 0xFFu;
-    const float s1 = e <= 134u ? 1.0f : 0x1p120f;
-    const float s2 = e <= 134u ? __uint_as_float((e + 120u) << 23) : ue8m0_scale((uint8_t)e);  // s1 s2 = 2^(e - 7)
-    uint32_t c[16];
+    uint4 v[4];
 #pragma unroll
-    for (int w = 0; w < 16; ++w) c[w] = i == 3 ? held[w] : raw[r * 16 + ((w + rot) & 15)];
-    uint8_t* row = slot + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-    for (int w = 0; w < 16; ++w) {
-      const int wr = (w + rot) & 15;  // the word's codes are dims 4 wr .. 4 wr + 3 of the K-block
-      *reinterpret_cast<uint2*>(row + ((((wr >> 1) ^ (lane & 7)) << 4) | ((wr & 1) << 3))) =
-          e4m3x4_scaled_bf16(c[w], s1, s2);
+    for (int j = 0; j < 4; ++j) v[j] = i == 3 ? held[j] : raw[4 * r + ((j + g) & 3)];
+    uint8_t* row = slot + (r >> 3) * 1024 + l7 * 128;
+    if (e <= 134u) {  // 2^(e - 7) is a bf16
+      const uint32_t s = ((e + 120u) << 7) * 0x00010001u;
+      const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s);
+      expand_row16<false>(row, v, g, h, l7, s2, s2);
+    } else {  // 2^120, then 2^(e - 127)
+      const uint32_t s1u = (247u << 7) * 0x00010001u, s2u = (e << 7) * 0x00010001u;
+      expand_row16<true>(row, v, g, h, l7, *reinterpret_cast<const __nv_bfloat162*>(&s1u),
+                         *reinterpret_cast<const __nv_bfloat162*>(&s2u));
     }
   }
 }
