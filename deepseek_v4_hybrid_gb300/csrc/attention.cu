@@ -934,13 +934,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     float* ot = reinterpret_cast<float*>(kv_mem);  // [64 heads][512 values] fp32 = 128 KB
     if (smx) {
       const int h = 32 * hf + lane;
-      float M = p.sink ? p.sink[hg * HG + h] * 1.4426950408889634f : -INFINITY;
-      for (int c = 0; c < nc; ++c) M = fmaxf(M, cl.map_shared_rank(sm->cml, c)[h].x);
-      float L = (M == -INFINITY || p.sink == nullptr) ? 0.f : tc::ex2_approx(p.sink[hg * HG + h] * 1.4426950408889634f - M);
-      for (int c = 0; c < nc; ++c) {
-        const float2 ml = cl.map_shared_rank(sm->cml, c)[h];
-        if (ml.x != -INFINITY) L += ml.y * tc::ex2_approx(ml.x - M);
-      }
+      const float sink_l2 = p.sink ? p.sink[hg * HG + h] * 1.4426950408889634f : -INFINITY;
+      // every chunk's (max, sum) of head h read at once: a remote read's latency is paid once, not nc times
+      float2 ml[MAX_MERGE_CLUSTER];
+#pragma unroll
+      for (int c = 0; c < MAX_MERGE_CLUSTER; ++c)
+        ml[c] = c < nc ? cl.map_shared_rank(sm->cml, c)[h] : make_float2(-INFINITY, 0.f);
+      float M = sink_l2;
+#pragma unroll
+      for (int c = 0; c < MAX_MERGE_CLUSTER; ++c) M = fmaxf(M, ml[c].x);
+      float L = (M == -INFINITY || p.sink == nullptr) ? 0.f : tc::ex2_approx(sink_l2 - M);
+#pragma unroll
+      for (int c = 0; c < MAX_MERGE_CLUSTER; ++c)
+        if (ml[c].x != -INFINITY) L += ml[c].y * tc::ex2_approx(ml[c].x - M);
       const float mine = sm->cml[h].x;
       sm->mrow[warp][lane] = (mine == -INFINITY || !(L > 0.f)) ? 0.f : tc::ex2_approx(mine - M) / L;
       if (crank == 0 && qd == 0 && p.lse)
@@ -967,20 +973,38 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int per = (TOTAL4 + nc - 1) / nc;
       const int x0 = crank * per, x1 = min(TOTAL4, x0 + per);
       const int64_t obase = ((int64_t)t * p.H + hg * HG) * DV;
-      for (int x = x0 + (int)threadIdx.x; x < x1; x += THREADS) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < nc; ++c) {
-          const float4 v = reinterpret_cast<const float4*>(cl.map_shared_rank(ot, c))[x];
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
+      // XB outputs a thread at a time: all their remote reads (from every CTA of the cluster) are
+      // issued before any is summed or stored, so their latencies overlap
+      constexpr int XB = 2;
+      for (int xb = x0 + (int)threadIdx.x; xb < x1; xb += XB * THREADS) {
+        float4 v[XB][MAX_MERGE_CLUSTER];
+#pragma unroll
+        for (int c = 0; c < MAX_MERGE_CLUSTER; ++c) {
+          const float4* src = reinterpret_cast<const float4*>(cl.map_shared_rank(ot, c < nc ? c : 0));
+#pragma unroll
+          for (int j = 0; j < XB; ++j) {
+            const int x = xb + j * THREADS;
+            v[j][c] = (c < nc && x < x1) ? src[x] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
-        if (p.out_dtype == DSV4_F32) {
-          reinterpret_cast<float4*>(p.out)[obase / 4 + x] = acc;
-        } else {
-          reinterpret_cast<uint2*>(p.out)[obase / 4 + x] =
-              make_uint2(float2_to_bf16x2_bits(acc.x, acc.y), float2_to_bf16x2_bits(acc.z, acc.w));
+#pragma unroll
+        for (int j = 0; j < XB; ++j) {
+          const int x = xb + j * THREADS;
+          if (x >= x1) break;
+          float4 acc = v[j][0];
+#pragma unroll
+          for (int c = 1; c < MAX_MERGE_CLUSTER; ++c) {
+            acc.x += v[j][c].x;
+            acc.y += v[j][c].y;
+            acc.z += v[j][c].z;
+            acc.w += v[j][c].w;
+          }
+          if (p.out_dtype == DSV4_F32) {
+            reinterpret_cast<float4*>(p.out)[obase / 4 + x] = acc;
+          } else {
+            reinterpret_cast<uint2*>(p.out)[obase / 4 + x] =
+                make_uint2(float2_to_bf16x2_bits(acc.x, acc.y), float2_to_bf16x2_bits(acc.z, acc.w));
+          }
         }
       }
     }
