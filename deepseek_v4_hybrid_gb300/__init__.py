@@ -25,18 +25,19 @@ def _stream(stream=None):
 
 
 def dsv4_kv_insert(kv_new, kv_dtype, slot_mapping, cache, cache_dtype, page_size, positions=None, cos_sin=None,
-                   stream=None):
-    """Writes kv_new[T, 576] into the paged SWA cache at slot_mapping[T] (int64, -1 skips)."""
+                   stream=None, after_independent=False):
+    """Writes kv_new[T, 576] into the paged SWA cache at slot_mapping[T] (int64, -1 skips).
+    after_independent: see include/dsv4.h (the kernel before it on the stream touches nothing this call does)."""
     T = slot_mapping.shape[0]
     p = _abi.make(_abi.KvInsertParams, kv_new=_ptr(kv_new), kv_dtype=kv_dtype, slot_mapping=_ptr(slot_mapping),
                   cache=_ptr(cache), cache_dtype=cache_dtype, T=T, page_size=page_size,
                   num_pages=cache.shape[0], positions=_ptr(positions), cos_sin=_ptr(cos_sin),
-                  max_pos=0 if cos_sin is None else cos_sin.shape[0])
+                  max_pos=0 if cos_sin is None else cos_sin.shape[0], after_independent=int(after_independent))
     _abi.check("dsv4_kv_insert", _lib.dsv4_kv_insert(p, _stream(stream)))
 
 
 def dsv4_compress_update(kv_score, positions, q_per_seq, ratio, coff, state, ape, norm_weight, eps, cos_sin,
-                         main_cache, cache_dtype, block_table, page_size, stream=None):
+                         main_cache, cache_dtype, block_table, page_size, stream=None, after_independent=False):
     """Compressor state store + fold of the new tokens (see include/dsv4.h)."""
     T = positions.shape[0]
     p = _abi.make(_abi.CompressUpdateParams, kv_score=_ptr(kv_score), positions=_ptr(positions), T=T,
@@ -44,7 +45,7 @@ def dsv4_compress_update(kv_score, positions, q_per_seq, ratio, coff, state, ape
                   norm_weight=_ptr(norm_weight), eps=eps, cos_sin=_ptr(cos_sin), max_pos=cos_sin.shape[0],
                   main_cache=_ptr(main_cache), cache_dtype=cache_dtype, page_size=page_size,
                   num_pages=main_cache.shape[0], block_table=_ptr(block_table),
-                  max_pages_per_seq=block_table.shape[1])
+                  max_pages_per_seq=block_table.shape[1], after_independent=int(after_independent))
     _abi.check("dsv4_compress_update", _lib.dsv4_compress_update(p, _stream(stream)))
 
 

@@ -21,7 +21,7 @@ vp, i32, i64, u32, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint32, C.c_float
 class KvInsertParams(C.Structure):
     _fields_ = [("struct_size", u32), ("kv_new", vp), ("kv_dtype", i32), ("slot_mapping", vp), ("cache", vp),
                 ("cache_dtype", i32), ("T", i32), ("page_size", i32), ("num_pages", i64), ("positions", vp),
-                ("cos_sin", vp), ("max_pos", i32)]
+                ("cos_sin", vp), ("max_pos", i32), ("after_independent", i32)]
 
 
 class CompressUpdateParams(C.Structure):
@@ -29,7 +29,7 @@ class CompressUpdateParams(C.Structure):
                 ("q_per_seq", i32), ("ratio", i32), ("coff", i32), ("state", vp), ("ape", vp),
                 ("norm_weight", vp), ("eps", f32), ("cos_sin", vp), ("max_pos", i32), ("main_cache", vp),
                 ("cache_dtype", i32), ("page_size", i32), ("num_pages", i64), ("block_table", vp),
-                ("max_pages_per_seq", i32)]
+                ("max_pages_per_seq", i32), ("after_independent", i32)]
 
 
 class IndexerTopkParams(C.Structure):

@@ -29,9 +29,7 @@ __device__ __forceinline__ void rope_pair(float& x0, float& x1, const float* cs,
   x1 = y1;
 }
 
-__global__ void __launch_bounds__(ROW_THREADS) kv_insert_kernel(dsv4_kv_insert_params p) {
-  pdl_launch_dependents();
-  pdl_wait();
+__device__ __forceinline__ void kv_insert_body(const dsv4_kv_insert_params& p) {
   const int t = blockIdx.x, i = threadIdx.x;
   const int64_t slot = p.slot_mapping[t];
   if (slot < 0) return;
@@ -55,6 +53,13 @@ __global__ void __launch_bounds__(ROW_THREADS) kv_insert_kernel(dsv4_kv_insert_p
   }
   uint8_t* row = reinterpret_cast<uint8_t*>(p.cache) + slot * row_bytes(p.cache_dtype, D);
   encode_pair_store(p.cache_dtype, row, i, x.x, x.y);
+}
+
+__global__ void __launch_bounds__(ROW_THREADS) kv_insert_kernel(dsv4_kv_insert_params p) {
+  pdl_launch_dependents();
+  if (!p.after_independent) pdl_wait();
+  kv_insert_body(p);
+  if (p.after_independent) pdl_wait();  // completes only after the kernel before it
 }
 
 
@@ -153,9 +158,7 @@ __device__ __forceinline__ void new_row_pair(const dsv4_compress_update_params& 
 // the fold's other rows from the ring, the entry's weights and destination); the token's own row
 // enters the fold from registers, so storing it costs no round trip.
 constexpr int FOLD_BATCH = 8;
-__global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compress_update_params p) {
-  pdl_launch_dependents();
-  pdl_wait();
+__device__ __forceinline__ void compress_update_body(const dsv4_compress_update_params& p) {
   const int b = blockIdx.x, i = threadIdx.x;
   const int coff = p.coff, r = p.ratio;
   const int nslots = coff * r;
@@ -226,6 +229,13 @@ __global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compr
   }
 }
 
+__global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compress_update_params p) {
+  pdl_launch_dependents();
+  if (!p.after_independent) pdl_wait();
+  compress_update_body(p);
+  if (p.after_independent) pdl_wait();  // completes only after the kernel before it
+}
+
 
 // Ratio-128 groups (coff = 1): one 8-CTA cluster per sequence.  Each CTA folds 16 of the group's
 // 128 rows into per-channel partial softmax states (max, sum, weighted kv sum) in its shared memory;
@@ -235,10 +245,7 @@ __global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compr
 // slots of the group, are stored after the fold.  Cluster barriers are hardware barriers, not flag
 // spins.
 constexpr int FOLD_CTAS = 8;
-__global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
-    compress_fold_cluster_kernel(dsv4_compress_update_params p) {
-  pdl_launch_dependents();
-  pdl_wait();
+__device__ __forceinline__ void compress_fold_cluster_body(const dsv4_compress_update_params& p) {
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.y, i = threadIdx.x;
@@ -342,6 +349,14 @@ __global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
       dst[i] = a;
       dst[D / 2 + i] = c;
     }
+}
+
+__global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
+    compress_fold_cluster_kernel(dsv4_compress_update_params p) {
+  pdl_launch_dependents();
+  if (!p.after_independent) pdl_wait();
+  compress_fold_cluster_body(p);
+  if (p.after_independent) pdl_wait();  // completes only after the kernel before it
 }
 
 cudaError_t launch_kv_insert(const dsv4_kv_insert_params& p, cudaStream_t s) {

@@ -92,16 +92,16 @@ class DeviceStep:
         self.at_params.workspace_bytes = self.at_ws.numel()
         self.eps = st.eps
 
-    def insert(self, stream=None):
+    def insert(self, stream=None, after_independent=False):
         dsv4_kv_insert(self.kv_new, self.cfg.act_dtype, self.slot_mapping, self.swa_cache, self.cfg.cache_dtype,
-                       PAGE, stream=stream)
+                       PAGE, stream=stream, after_independent=after_independent)
 
-    def compress(self, stream=None):
+    def compress(self, stream=None, after_independent=False):
         if self.has_compress:
             cfg = self.cfg
             dsv4_compress_update(self.kv_score, self.positions, cfg.q_per_seq, cfg.ratio, cfg.coff, self.state,
                                  self.ape, self.norm_w, self.eps, self.cos_sin, self.main_cache, cfg.cache_dtype,
-                                 self.main_bt, PAGE, stream=stream)
+                                 self.main_bt, PAGE, stream=stream, after_independent=after_independent)
 
     def indexer(self, stream=None):
         if self.has_indexer:
@@ -111,10 +111,19 @@ class DeviceStep:
         dsv4_sparse_mla_decode(self.at_params, stream=stream)
 
     def run(self, stream=None):
-        """One decode step: insert -> compress -> indexer + top-k -> attention."""
-        self.insert(stream)
-        self.compress(stream)
-        self.indexer(stream)
+        """One decode step.  With an indexer: indexer + top-k -> insert -> compress -> attention.  The
+        indexer reads none of what insert and compress write and they read none of its outputs, so
+        those two start at once (they wait for the kernel before them only before exiting) and run
+        on the SMs the indexer's CTAs leave during its top-k; attention, which needs all three,
+        waits for compress, whose completion implies the others'.  Without an indexer: insert ->
+        compress -> attention, each waiting for the one before."""
+        if self.has_indexer:
+            self.indexer(stream)
+            self.insert(stream, after_independent=True)
+            self.compress(stream, after_independent=True)
+        else:
+            self.insert(stream)
+            self.compress(stream)
         self.attention(stream)
 
     def step_input_tensors(self):

@@ -95,6 +95,12 @@ typedef struct dsv4_kv_insert_params {
   const int32_t* positions;    /* [T] RoPE positions; only read when cos_sin != NULL */
   const float* cos_sin;        /* [max_pos, 64] (32 cos | 32 sin) or NULL = rows already rotated */
   int32_t max_pos;
+  int32_t after_independent;   /* 0: the kernel waits for the kernel before it on `stream` before it
+                                  starts its work (always safe).  1: the caller guarantees that the
+                                  kernel before it on `stream` neither reads nor writes anything this
+                                  call reads or writes (as the indexer call of the same step); the
+                                  kernel then does its work at once and waits for that kernel only
+                                  before it exits, so its completion still implies the earlier one's */
 } dsv4_kv_insert_params;
 
 int dsv4_kv_insert(const dsv4_kv_insert_params* p, dsv4_stream_t stream);
@@ -128,6 +134,7 @@ typedef struct dsv4_compress_update_params {
   int64_t num_pages;
   const int32_t* block_table;  /* [B, max_pages_per_seq] main-cache pages of each sequence */
   int32_t max_pages_per_seq;
+  int32_t after_independent;   /* as in dsv4_kv_insert_params */
 } dsv4_compress_update_params;
 
 int dsv4_compress_update(const dsv4_compress_update_params* p, dsv4_stream_t stream);
