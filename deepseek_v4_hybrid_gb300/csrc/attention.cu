@@ -975,7 +975,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t obase = ((int64_t)t * p.H + hg * HG) * DV;
       // XB outputs a thread at a time: all their remote reads (from every CTA of the cluster) are
       // issued before any is summed or stored, so their latencies overlap
-      constexpr int XB = 2;
+      constexpr int XB = 3;
       for (int xb = x0 + (int)threadIdx.x; xb < x1; xb += XB * THREADS) {
         float4 v[XB][MAX_MERGE_CLUSTER];
 #pragma unroll
