@@ -250,9 +250,11 @@ __global__ void __launch_bounds__(AT_THREADS) mla_partial_simt(dsv4_sparse_mla_d
 //
 // Row list of a token: the window pages (whole 64-row pages of the SWA cache covering positions
 // p - n_swa + 1 .. p, rows outside that range masked), then the compressed rows in 64-row halves
-// (top-k indices, or dense pages of the main cache).  Warp 8 loads a window page or a dense page as
-// 9 TMA boxes and top-k rows with TMA gather4 (4 rows x one K-block each; an invalid index loads a
-// row past the end of the tensor, i.e. zeros).  Lane 0 of warp 9 issues the MMAs.  Warps 0-7 run
+// (top-k indices, or dense pages of the main cache).  Warps 8, 10 and 11 load (the TMA issue rate
+// is per issuing warp: K-block kb of every tile is loaded by the kb mod 3-th of them): a window
+// page or a dense page as TMA boxes, top-k rows with TMA gather4 (4 rows x one K-block each; an
+// invalid index loads a row past the end of the tensor, i.e. zeros).  Lane 0 of warp 9 issues the
+// MMAs.  Warps 0-7 run
 // the online softmax in the log2 domain with a lazy rescale (O^T is rescaled only when a head's
 // running max grows by more than 2^8): warp w owns tile rows 32 (w & 3) .. + 31 (its TMEM lane
 // quarter) and heads 32 (w >> 2) .. + 31; a tile's per-head maxima are reduced across lanes by a

@@ -530,14 +530,17 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
 }
 
 // ------------------------------------------------------------------------------------------------
-// Tensor-core score kernel (bf16 keys and queries): D[128 keys x N] = K_tile[128 x d] * Q[N x d]^T
-// with N = q_per_seq * n_heads (every query head of the sequence), then per key
-// s_k = sum_h w[k][h] * ReLU(D[key][k*n_heads + h]).
+// Tensor-core score kernel (bf16 queries; bf16 keys, or int8 row-scale keys expanded to bf16 in
+// shared memory): D[128 keys x N] = K_tile[128 x d] * Q[N x d]^T with N = q_per_seq * n_heads
+// (every query head of the sequence), then per key s_k = sum_h w[k][h] * ReLU(D[key][k*n_heads + h])
+// (times the key's row scale for int8 keys).
 //
-// Persistent CTAs (one per SM), each owning a contiguous range of (sequence, 128-key tile) items.
-// Warp 8 streams key tiles with TMA (two 64-row pages x d/64 K-blocks of 128 B, 128-byte swizzle)
-// into a ring of stages, and each sequence's Q block into one of two Q slots; its 32 lanes look up
-// the block-table pages of 32 items at a time.  One thread of warp 9 issues the tcgen05 MMAs
+// Persistent CTAs (one per SM), each owning a contiguous range of (sequence, 128-key tile) items: an
+// even share of the valid tiles.  Warp 8 streams key tiles with TMA (two 64-row pages x d/64
+// K-blocks of 128 B, 128-byte swizzle) into a ring of stages (int8 keys: the two record pages by
+// bulk copy into a ring of two raw stages, which warps 10-11 expand into the stages), and each
+// sequence's Q block into one of two Q slots (one when shared memory is short); its 32 lanes look
+// up the block-table pages of 32 items at a time.  One thread of warp 9 issues the tcgen05 MMAs
 // (M = 128, K = 16 steps) into a ring of TMEM accumulators.  Warps 0-7 are two epilogue groups of
 // four that take alternate tiles: each warp reads its 32 TMEM lanes (one key per thread), applies
 // ReLU and the head weights, stores the scores and counts them into its group's shared-memory
