@@ -153,3 +153,30 @@ def test_after_independent_gives_the_same_caches(lib, name):
                      if getattr(ds, k, None) is not None}
     for k, v in out[False].items():
         assert np.array_equal(v, out[True][k]), k
+
+
+def test_fp8_block_exponents_on_both_scaling_paths(lib):
+    """fp8_ds_mla caches whose UE8M0 block exponents span 126..142: the attention kernel scales the
+    codes with one bf16x2 multiply by 2^(e - 7) up to e = 134 and with two (2^120, then 2^(e - 127))
+    above, so both paths meet rows of the same tile; the result must still match the oracle."""
+    from deepseek_v4_hybrid_gb300.step import DeviceStep
+    import deepseek_v4_hybrid_gb300 as M
+    st = I.make_step(I.SMALL_CONFIGS["small_c4_fp8"])
+    rng = np.random.default_rng(0xE8)
+    for cache in (st.swa_cache, st.main_cache):
+        sc = cache[..., I.FP8_SCALE_OFF:I.FP8_SCALE_OFF + 8]
+        cache[..., I.FP8_SCALE_OFF:I.FP8_SCALE_OFF + 8] = rng.integers(126, 143, size=sc.shape, dtype=np.uint8)
+    ds = DeviceStep(st, topk_override=st.given_topk)
+    ds.run()
+    torch.cuda.synchronize()
+    assert M.dsv4_read_device_flags() == 0
+    res = O.decode_step(st, topk_override=st.given_topk)
+    g = gpu_results(ds)
+    lse = g.pop("lse")
+    CMP.check_step(st, res, g, where="fp8 exponents 126..142")
+    # the logits reach about 1e5 here, and fp32 scores (576-term dot products) carry an absolute
+    # error proportional to their size: the log-sum-exp is held to 2^-14 of its magnitude on top of
+    # the usual 2e-3
+    for t in res["tokens"]:
+        ref = np.asarray(res["lse"][t], np.float64)
+        assert np.all(np.abs(lse[t] - ref) <= 2e-3 + 2.0 ** -14 * np.abs(ref)), f"lse of token {t}"
