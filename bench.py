@@ -47,6 +47,28 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def rank_config(cfg, rank):
+    """Replicas: every rank decodes its own batch of the workload, drawn with the seed offset by the
+    rank (sequences are independent, so no data crosses ranks)."""
+    return dataclasses.replace(cfg, seed=cfg.seed + 1000 * rank)
+
+
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values of x, on every rank (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms_per_step):
+    """Whole-job throughput: the tokens of every rank's step over the (slowest rank's) step time."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -229,8 +251,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     from deepseek_v4_hybrid_gb300.step import DeviceStep
-    cfg = I.ALL_CONFIGS[args.config]
-    cfg = dataclasses.replace(cfg, seed=cfg.seed + 1000 * rank)
+    cfg = rank_config(I.ALL_CONFIGS[args.config], rank)
     st = I.make_step(cfg)
     ds = DeviceStep(st)
     stream = torch.cuda.current_stream()
@@ -298,12 +319,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         for i, c in enumerate(calls):
             per_call[c] += evs[i].elapsed_time(evs[i + 1])
-    if world > 1:
-        tt = torch.tensor([ms_per_step], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_per_step = float(tt.item())
-    tokens = cfg.T * world
-    value = tokens / (ms_per_step * 1e-3)
+    ms_per_step = max_over_ranks(ms_per_step, world, "cuda")
+    value = job_tokens_per_s(cfg.T, world, ms_per_step)
     per_call_us = {c: 1e3 * v / Kc for c, v in per_call.items()}
 
     # ---- end to end through host buffers: pinned H2D of the step's inputs, step, D2H of results
@@ -330,10 +347,7 @@ def run_ours(args):
         bnd.synchronize()
         e2e_ms += a.elapsed_time(bnd)
     e2e_ms /= Ke
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
 
     # ---- roofline of the dominant call
     dom = max((c for c in calls if c in alg), key=lambda c: per_call_us[c])
@@ -353,7 +367,7 @@ def run_ours(args):
                    "context": list(map(int, (st.ctx_len.min(), st.ctx_len.max()))), "heads": cfg.H,
                    "ratio": cfg.ratio, "indexer": [cfg.I_h, cfg.d_I], "topk": cfg.topk, "page": 64,
                    "l2": "flushed between steps (512 MB write)", "parallelism": f"replicas x{world} (per-sequence)"},
-        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": job_tokens_per_s(cfg.T, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "gpu_launches": int(K * launches_per_step(ds)),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
