@@ -101,6 +101,6 @@ def dsv4_read_device_flags() -> int:
     """Synchronises and returns (and clears) the kernels' range-check flags."""
     f = _abi.u32(0)
     st = _lib.dsv4_read_device_flags(f)
-    if st not in (_abi.OK, _abi.ERR_BOUNDS):
+    if st not in (_abi.OK, _abi.ERR_BOUNDS, _abi.ERR_TIMEOUT):
         _abi.check("dsv4_read_device_flags", st)
     return int(f.value)

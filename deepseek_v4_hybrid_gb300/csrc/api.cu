@@ -43,7 +43,7 @@ const char* dsv4_status_string(int s) {
     case DSV4_ERR_UNSUPPORTED: return "unsupported dtype or shape";
     case DSV4_ERR_CUDA: return "CUDA error";
     case DSV4_ERR_BOUNDS: return "a kernel skipped an out-of-range index";
-    case DSV4_ERR_TIMEOUT: return "timeout";
+    case DSV4_ERR_TIMEOUT: return "a kernel gave up a bounded wait (outputs unspecified)";
   }
   return "unknown status";
 }
@@ -61,6 +61,7 @@ int dsv4_read_device_flags(uint32_t* flags) {
   if (st != DSV4_OK) return st;
   st = cuda_status(read_flags_attention(flags));
   if (st != DSV4_OK) return st;
+  if (*flags & 4u) return DSV4_ERR_TIMEOUT;
   return *flags ? DSV4_ERR_BOUNDS : DSV4_OK;
 }
 

@@ -1070,14 +1070,9 @@ static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p,
     ropemain64 = ropeswa64;
   }
   const size_t smem = 1024 + (size_t)Q_BYTES + (size_t)KV_BYTES + sizeof(Smem);
-  static int attr_done = 0;
-  if (!attr_done) {
-    e = cudaFuncSetAttribute(mla_partial_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mla_partial_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = 1;
-  }
+  e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(mla_partial_tc<false>), (int)smem);
+  if (e == cudaSuccess) e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(mla_partial_tc<true>), (int)smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.n_chunks, p.T, p.H / HG);
   cfg.blockDim = dim3(THREADS);

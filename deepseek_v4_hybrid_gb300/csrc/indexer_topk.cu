@@ -1176,14 +1176,9 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
     e = make_tmap_2d_bf16(&kmap, p.k_cache, (uint64_t)p.head_dim, (uint64_t)p.num_pages * 64, 64, 64);
     if (e != cudaSuccess) return e;
   }
-  static int attr_done = 0;
-  if (!attr_done) {
-    e = cudaFuncSetAttribute(indexer_score_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(indexer_score_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
-    if (e != cudaSuccess) return e;
-    attr_done = 1;
-  }
+  e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(indexer_score_tc<false>), (int)budget);
+  if (e == cudaSuccess) e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(indexer_score_tc<true>), (int)budget);
+  if (e != cudaSuccess) return e;
   const int total = a.B * a.tiles_max;
   int grid = num_sms();
   if (grid > total) grid = total;
@@ -1342,19 +1337,15 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
     const int tiles = (max_nc + IX_TILE - 1) / IX_TILE;
     const size_t smem = sizeof(float) * ((size_t)p.q_per_seq * p.n_heads * p.head_dim +
                                          (size_t)p.q_per_seq * p.n_heads + (size_t)(p.head_dim + 1) * (IX_TILE + 1));
-    e = cudaFuncSetAttribute(indexer_score_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(indexer_score_simt), (int)smem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(indexer_score_simt, dim3(tiles, p.B), dim3(IX_TILE), smem, st, /*pdl=*/false, p, bufs);
     if (e != cudaSuccess) return e;
   }
-  static int attr_done = 0;
-  if (!attr_done) {
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TK_SMEM);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_slice_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TK_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = 1;
-  }
+  e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(topk_kernel), (int)TK_SMEM);
+  if (e != cudaSuccess) return e;
+  e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(topk_slice_kernel), (int)TK_SMEM);
+  if (e != cudaSuccess) return e;
   if (fused) return launch_pdl(topk_kernel, dim3(p.T), dim3(TK_THREADS), TK_SMEM, st, /*pdl=*/false, p, bufs);
   const int slices = (max_nc + SLICE - 1) / SLICE;
   return launch_pdl(topk_slice_kernel, dim3(slices, p.T), dim3(TK_THREADS), TK_SMEM, st, /*pdl=*/false, p, bufs);

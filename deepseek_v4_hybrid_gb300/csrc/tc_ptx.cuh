@@ -107,9 +107,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Loads rows y0..y3 (each one 128-byte box row starting at element x) of a 2-D tensor into 4
-// consecutive 128-byte rows of shared memory, with the tensor map's swizzle.  The map's box is one
-// row high.  A row index past the end of the tensor loads zeros.
 // L2 cache policy for data read once (evicted first).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
@@ -127,6 +124,9 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Loads rows y0..y3 (each one 128-byte box row starting at element x) of a 2-D tensor into 4
+// consecutive 128-byte rows of shared memory, with the tensor map's swizzle.  The map's box is one
+// row high.  A row index past the end of the tensor loads zeros.
 __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
                                             uint64_t* bar) {
   asm volatile(
@@ -332,7 +332,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.p
 
 
 // ---------------------------------------------------------------------------------------------
-// Thread-block clusters: multicast TMA and cross-CTA commits
+// Thread-block clusters
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -342,30 +342,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 // Hardware barrier over every thread of every CTA of the cluster (no spin on a flag).
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// tma_load_2d delivered to the same shared-memory offset (and mbarrier) of every CTA in `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-// tma_gather4 delivered to every CTA in `mask`.
-__device__ __forceinline__ void tma_gather4_mc(void* dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
-                                               uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-// tcgen05.commit arriving on the mbarrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               ::"r"(smem_addr(bar)), "h"(mask)
-               : "memory");
 }
 
 }  // namespace tc

@@ -49,16 +49,49 @@ cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* b
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr int kMaxKernels = 16;
+std::mutex g_dev_mutex;
+int g_sms[kMaxDevices] = {0};
+struct SmemAttr {
+  const void* fn;
+  int bytes;
+};
+SmemAttr g_smem_attr[kMaxDevices][kMaxKernels] = {};
+}  // namespace
+
 int num_sms() {
-  static int cache[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (cache[dev] == 0) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_sms[dev] == 0) {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = n > 0 ? n : 1;
+    g_sms[dev] = n > 0 ? n : 1;
   }
-  return cache[dev];
+  return g_sms[dev];
+}
+
+cudaError_t ensure_max_dynamic_smem(const void* fn, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  SmemAttr* tab = g_smem_attr[dev];
+  int i = 0;
+  for (; i < kMaxKernels && tab[i].fn != nullptr; ++i)
+    if (tab[i].fn == fn && tab[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  for (int k = 0; k < kMaxKernels; ++k)
+    if (tab[k].fn == fn) {
+      tab[k].bytes = bytes;
+      return cudaSuccess;
+    }
+  if (i < kMaxKernels) tab[i] = SmemAttr{fn, bytes};
+  return cudaSuccess;
 }
 
 }  // namespace dsv4

@@ -22,4 +22,8 @@ cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* b
 // Multiprocessor count of the current device.
 int num_sms();
 
+// Sets the maximum dynamic shared memory of kernel `fn` to `bytes` on the current device, once per
+// device (function attributes belong to each device's context); thread safe.
+cudaError_t ensure_max_dynamic_smem(const void* fn, int bytes);
+
 }  // namespace dsv4

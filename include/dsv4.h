@@ -34,6 +34,12 @@
  *    sizes over the limits) returns an error before anything is launched.  Device-side range
  *    checks (block-table pages, slots, top-k indices) skip the bad access and raise a flag that
  *    dsv4_read_device_flags() returns; no kernel traps or faults on bad indices.
+ *  - Inside a kernel, warps hand work to each other through shared-memory barriers (TMA and tensor
+ *    core completions, producer/consumer rings) and the CTAs of a cluster meet at cluster
+ *    barriers.  Every such wait is bounded in time (about 0.25 s): a wait that runs out makes the
+ *    kernel's roles drain and exit, leaves the affected outputs unspecified and raises the
+ *    timeout flag (bit 2 of dsv4_read_device_flags()).  No kernel waits on another kernel or on
+ *    the host.
  */
 #ifndef DSV4_H
 #define DSV4_H
@@ -58,7 +64,7 @@ typedef enum dsv4_status {
   DSV4_ERR_UNSUPPORTED = -2,  /* dtype or shape combination not implemented */
   DSV4_ERR_CUDA = -3,         /* a CUDA call failed; dsv4_last_cuda_error() has the code */
   DSV4_ERR_BOUNDS = -4,       /* returned by dsv4_read_device_flags() when a kernel skipped a bad index */
-  DSV4_ERR_TIMEOUT = -5       /* reserved: no kernel of this library waits on another */
+  DSV4_ERR_TIMEOUT = -5       /* returned by dsv4_read_device_flags() when a kernel gave up a bounded wait */
 } dsv4_status;
 
 /* Storage formats of rows and activations. */
@@ -181,7 +187,9 @@ int dsv4_indexer_topk(const dsv4_indexer_topk_params* p, dsv4_stream_t stream);
  * The call allocates nothing.  Problems whose dsv4_indexer_topk_workspace_bytes() exceeds
  * DSV4_NOALLOC_SCRATCH_BYTES are rejected with DSV4_ERR_INVALID before any launch.
  * The first call on a device (made with that device current) looks up the array's device address
- * once; make that first call outside any CUDA stream capture.  Every call on a device shares the
+ * once and keeps it for the life of the process; make that first call outside any CUDA stream
+ * capture, and do not use this call on a device after cudaDeviceReset() there (the address kept
+ * belongs to the torn-down context).  Every call on a device shares the
  * one array and leaves its contents behind, so calls whose kernels overlap on the GPU (different
  * streams, or graph replays that run concurrently) race on it: order them on one stream.
  * ------------------------------------------------------------------------------------------- */
@@ -237,9 +245,13 @@ int dsv4_abi_version(void);
 const char* dsv4_status_string(int status);
 /* The cudaError_t of the last failed CUDA call made by this thread inside the library. */
 int dsv4_last_cuda_error(void);
-/* Synchronises the current device, returns the OR of the range-check flags the kernels raised
- * since the previous call in *flags (bit 0: page/slot out of range, bit 1: top-k index out of
- * range) and clears them.  Returns DSV4_ERR_BOUNDS if any flag was set, else DSV4_OK. */
+/* Synchronises the current device, returns the OR of the flags the kernels raised since the
+ * previous call in *flags and clears them:
+ *   bit 0 (1): a block-table page, slot or position out of range (the access was skipped),
+ *   bit 1 (2): a top-k index out of range, or a top-k whose candidates did not fit,
+ *   bit 2 (4): a bounded wait inside a kernel ran out (that call's outputs are unspecified).
+ * Returns DSV4_ERR_TIMEOUT if bit 2 was set, else DSV4_ERR_BOUNDS if another bit was set, else
+ * DSV4_OK (or DSV4_ERR_CUDA if the synchronisation failed). */
 int dsv4_read_device_flags(uint32_t* flags);
 
 #ifdef __cplusplus
