@@ -1,0 +1,147 @@
+"""Pins of the oracle's compositions (no GPU needed): the value of one compressed entry, and which
+rows one decode step's attention sees.
+
+Both are recomputed here element by element with Python scalars (math.fsum, math.exp, math.sqrt)
+in the order "DeepSeek V4 Attention: Code Reading Map", "How Does Compression Actually Work?"
+gives the steps: softmax of the gate scores over the group's tokens per channel, the weighted sum
+of kv, RMSNorm times its weight, then GPT-J RoPE of dims 512..575 at the group's position.  The
+rotary table is built here from math.cos / math.sin, not taken from the input generator.  The
+decode-step pin assembles the attended rows by hand (the window including this step's new row,
+the selected compressed rows including the entry folded this step) and applies
+scipy.special.softmax / logsumexp to them.
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp, softmax
+
+import dsv4_inputs as I
+from oracle import dsv4_oracle as O
+
+D, DV = 576, 512
+
+
+def rotary_table(max_pos, theta=10000.0):
+    """[max_pos, 64]: cos of the 32 pair angles then their sin; pair i turns by pos * theta^(-2i/64)."""
+    t = np.zeros((max_pos, 64))
+    for pos in range(max_pos):
+        for i in range(32):
+            a = pos * theta ** (-2.0 * i / 64.0)
+            t[pos, i] = math.cos(a)
+            t[pos, 32 + i] = math.sin(a)
+    return t
+
+
+def scalar_entry(state_b, j, ratio, coff, gamma, eps, table):
+    """Compressed entry j of one sequence from its fp32 state ring, one channel at a time."""
+    nslots = coff * ratio
+    members = []  # (slot, kv column offset, score column offset) of every row in the group
+    for pos in range(j * ratio, (j + 1) * ratio):
+        members.append((pos % nslots, 0, coff * D))
+    if coff == 2 and j >= 1:  # overlapping series B: the previous block's tokens
+        for pos in range((j - 1) * ratio, j * ratio):
+            members.append((pos % nslots, D, coff * D + D))
+    e = [0.0] * D
+    for c in range(D):
+        scores = [float(state_b[s][so + c]) for s, _, so in members]
+        kvs = [float(state_b[s][ko + c]) for s, ko, _ in members]
+        top = max(scores)
+        w = [math.exp(x - top) for x in scores]
+        z = math.fsum(w)
+        e[c] = math.fsum(wi * kv for wi, kv in zip(w, kvs)) / z
+    inv = 1.0 / math.sqrt(math.fsum(x * x for x in e) / D + eps)
+    n = [e[c] * inv * float(gamma[c]) for c in range(D)]
+    row = table[j * ratio]
+    for i in range(32):
+        a, b = n[512 + 2 * i], n[512 + 2 * i + 1]
+        cs, sn = float(row[i]), float(row[32 + i])
+        n[512 + 2 * i] = a * cs - b * sn
+        n[512 + 2 * i + 1] = a * sn + b * cs
+    return np.array(n)
+
+
+@pytest.mark.parametrize("ratio,coff,j", [(4, 2, 5), (4, 2, 1), (4, 2, 0), (128, 1, 3)])
+def test_compressed_entry_matches_scalar_recomputation(ratio, coff, j):
+    rng = np.random.default_rng(100 + ratio + j)
+    nslots = coff * ratio
+    state_b = rng.standard_normal((nslots, 2 * coff * D)).astype(np.float32)
+    gamma = (1.0 + 0.5 * rng.standard_normal(D)).astype(np.float32)   # far from 1 on purpose
+    table = rotary_table((j + 1) * ratio + 1)
+    want = scalar_entry(state_b, j, ratio, coff, gamma, 1e-6, table)
+    got = O.compressed_entry(state_b, j, ratio, coff, gamma, 1e-6, table)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_compressed_entry_rope_uses_group_position_row():
+    """Entry j takes the rotary row j * ratio: swapping in row j changes the rope dims only."""
+    ratio, coff, j = 4, 2, 6
+    rng = np.random.default_rng(7)
+    state_b = rng.standard_normal((coff * ratio, 2 * coff * D)).astype(np.float32)
+    gamma = (1.0 + 0.5 * rng.standard_normal(D)).astype(np.float32)
+    table = rotary_table(64)
+    got = O.compressed_entry(state_b, j, ratio, coff, gamma, 1e-6, table)
+    shifted = table.copy()
+    shifted[j * ratio] = table[j]
+    other = O.compressed_entry(state_b, j, ratio, coff, gamma, 1e-6, shifted)
+    assert np.array_equal(got[:512], other[:512])
+    assert np.max(np.abs(got[512:] - other[512:])) > 1e-3
+
+
+def _emitting_step(ctx, topk_sel):
+    cfg = dataclasses.replace(I.CONFIGS["tiny_c4_f32"], name="pin_emit", B=1, H=4, topk=8,
+                              explicit_lens=(ctx,))
+    st = I.make_step(cfg)
+    st.cos_sin = rotary_table(ctx + 1).astype(np.float32)
+    sel = np.full((1, cfg.topk), -1, np.int32)
+    sel[0, :len(topk_sel)] = topk_sel
+    return cfg, st, sel
+
+
+@pytest.mark.parametrize("ctx,sel", [(300, [3, 10, 50, 74]), (256, [0, 63, 12]), (300, [74])])
+def test_decode_step_attends_this_steps_row_and_entry(ctx, sel):
+    """One sequence whose new token completes a group: the attention of decode_step must equal a
+    softmax over rows put together by hand -- the window ending at this step's own new row, then
+    the selected entries, where the entry folded this step comes from the updated state ring."""
+    cfg, st, given = _emitting_step(ctx, sel)
+    p = ctx - 1
+    assert (p + 1) % cfg.ratio == 0
+    j_new = p // cfg.ratio
+    res = O.decode_step(st, topk_override=given)
+
+    # the state ring after this step's store: the new token's row, with APE on the score half (fp32)
+    ring = np.array(st.state[0], np.float32, copy=True)
+    new_row = np.array(st.kv_score[0], np.float32, copy=True)
+    coff = cfg.coff
+    new_row[coff * D:] = (new_row[coff * D:] + st.ape[p % cfg.ratio]).astype(np.float32)
+    ring[p % (coff * cfg.ratio)] = new_row
+
+    rows = []
+    for pos in range(max(0, p - 127), p + 1):
+        if pos == p:
+            rows.append(np.asarray(st.kv_new[0], np.float64))        # inserted this step
+        else:
+            page = st.swa_bt[0][pos // 64]
+            rows.append(np.asarray(st.swa_cache[page, pos % 64], np.float64))
+    for j in given[0]:
+        if j < 0 or j >= (p + 1) // cfg.ratio:
+            continue
+        if j == j_new:                                                   # folded this step
+            e = scalar_entry(ring, j, cfg.ratio, coff, st.norm_w, st.eps, st.cos_sin)
+            rows.append(e.astype(np.float32).astype(np.float64))        # stored as fp32
+        else:
+            page = st.main_bt[0][j // 64]
+            rows.append(np.asarray(st.main_cache[page, j % 64], np.float64))
+    R = np.stack(rows)
+    if j_new in given[0]:
+        assert R.shape[0] == min(p + 1, 128) + len(sel)
+
+    q = np.asarray(st.q[0], np.float64)
+    for h in range(cfg.H):
+        z = st.softmax_scale * (R @ q[h])
+        logits = np.concatenate([z, [float(st.sink[h])]])
+        w = softmax(logits)[:-1]
+        want = (w[:, None] * R[:, :DV]).sum(axis=0)
+        np.testing.assert_allclose(res["out"][0][h], want, rtol=1e-9, atol=1e-12)
+        assert abs(res["lse"][0][h] - logsumexp(logits)) <= 1e-10 * max(1.0, abs(logsumexp(logits)))
