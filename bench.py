@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-extra", action="store_true", help="time the headline workload only")
     return ap.parse_args()
 
 
@@ -220,10 +221,6 @@ def oracle_throughput(st, seconds):
 
 # ------------------------------------------------------------------------------------------------
 
-def flush_buffer(torch):
-    return torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
-
-
 def kernel_source_hash(files):
     h = hashlib.sha256()
     for f in files:
@@ -247,6 +244,170 @@ def traffic_from_profiles(config, kernel_file, units):
         return None
 
 
+L2_BYTES = 129 * 1024 * 1024  # GB300 L2 (bench uses the device's own figure when it can read it)
+
+
+def replica_count(step_bytes, l2_bytes):
+    """Device replicas of a workload to rotate so that, between two uses of one replica's inputs, at
+    least twice the L2 of other inputs is read (every step then starts from a cold L2 without a
+    flush kernel, whose dirty lines would be written back during the timed kernels)."""
+    need = int(np.ceil(2.0 * l2_bytes / max(step_bytes, 1))) + 1
+    return int(min(8, max(4, need)))
+
+
+def rotating_call_us(torch, replays, reps):
+    """GPU time of one call: the replicas' graphs of that call replayed back to back in rotation,
+    `reps` rounds, between two CUDA events on the launching stream, divided by the calls made (the
+    host stays ahead of the GPU, so no host launch gap enters)."""
+    stream = torch.cuda.current_stream()
+    for f in replays:
+        f()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        for f in replays:
+            f()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (reps * len(replays))
+
+
+def measure_workload(cfg, K, warmup, world, local, want_e2e):
+    """Times one workload's decode step on this GPU: the step (CUDA-graph replay, CUDA events), each
+    call alone, the end-to-end path through host buffers, and the roofline of the dominant call.
+    L2: the step's inputs live in R device replicas used in rotation (R chosen so that each step's
+    inputs were last touched R - 1 steps, at least twice the L2 of other inputs, earlier).
+    Returns a dict of the JSON fields."""
+    import torch
+    import dsv4_inputs as I
+    import deepseek_v4_hybrid_gb300 as M
+    from deepseek_v4_hybrid_gb300.step import DeviceStep
+    st = I.make_step(cfg)
+    ds0 = DeviceStep(st)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(warmup, 3)):
+        ds0.run()
+    torch.cuda.synchronize()
+    flags = M.dsv4_read_device_flags()
+    if flags:
+        raise SystemExit(f"kernels raised range/timeout flags {flags:#x} during warm-up of {cfg.name}; not timing")
+    topk_host = ds0.topk_idx.cpu().numpy() if ds0.has_indexer else None
+    alg = algorithmic_bytes(st, topk_host)
+    try:
+        l2 = int(torch.cuda.get_device_properties(local).L2_cache_size)
+    except Exception:
+        l2 = L2_BYTES
+    R = replica_count(sum(alg.values()), l2)
+    reps_ds = [ds0] + [DeviceStep(st) for _ in range(R - 1)]
+    ctx_range = list(map(int, (st.ctx_len.min(), st.ctx_len.max())))
+    del st
+
+    calls = ["insert", "compress", "indexer", "attention"]
+    # each replica's step (and each call alone) captured once as a CUDA graph: the library never
+    # synchronises, so the calls replay with no host launch gaps
+    graph_step, graph_call = [], {c: [] for c in calls}
+    for ds in reps_ds:
+        for _ in range(max(warmup, 3)):
+            ds.run()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            ds.run()
+        graph_step.append(g)
+        for c in calls:
+            gc = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gc):
+                getattr(ds, c)()
+            graph_call[c].append(gc)
+    for _ in range(3):
+        for g in graph_step:
+            g.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    wall0 = time.perf_counter()
+    for k in range(K):
+        ev[k][0].record(stream)
+        graph_step[k % R].replay()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_per_step = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    ms_per_step = max_over_ranks(ms_per_step, world, "cuda")
+    # per-call breakdown: each call's graphs, replicas in rotation
+    rounds = max(1, min(K, 400) // R)
+    per_call_us = {c: rotating_call_us(torch, [g.replay for g in graph_call[c]], rounds) for c in calls}
+
+    res = {"ms_per_step": ms_per_step, "value": job_tokens_per_s(cfg.T, world, ms_per_step), "calls_us": per_call_us,
+           "clocks": clocks, "wall_s_timed": wall, "gpu_launches": int(K * launches_per_step(ds0)),
+           "step_algorithmic_gbs": sum(alg.values()) / (ms_per_step * 1e-3) / 1e9,
+           "config": {"workload": cfg.name, "batch_per_gpu": cfg.B, "q_per_seq": cfg.q_per_seq,
+                      "context": ctx_range,
+                      "heads": cfg.H, "ratio": cfg.ratio, "indexer": [cfg.I_h, cfg.d_I], "topk": cfg.topk, "page": 64,
+                      "l2": (f"inputs larger than L2: {R} device replicas of the step's inputs used in rotation, "
+                             f"so each step's inputs were last read {R - 1} steps earlier with >= 2x L2 "
+                             f"({l2 // 2**20} MiB) of other inputs read since; no flush kernel")},
+           "dtype": {0: "f32", 1: "bf16"}[cfg.act_dtype] + "/" + I.DTYPE_NAMES[cfg.cache_dtype]}
+
+    if want_e2e:
+        # end to end through host buffers: pinned H2D of the step's inputs, step, D2H of results
+        host_in = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in ds0.step_input_tensors().items()}
+        for k, v in ds0.step_input_tensors().items():
+            host_in[k].copy_(v)
+        host_out = torch.empty_like(ds0.out, device="cpu").pin_memory()
+        host_topk = torch.empty_like(ds0.topk_idx, device="cpu").pin_memory() if ds0.has_indexer else None
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = host_out.numel() * host_out.element_size() + (host_topk.numel() * 4 if host_topk is not None else 0)
+        Ke = max(20, min(K, 400))
+        e2e_ms = 0.0
+        for k in range(Ke):
+            ds = reps_ds[k % R]
+            a, bnd = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for name, dev in ds.step_input_tensors().items():
+                dev.copy_(host_in[name], non_blocking=True)
+            ds.run()
+            host_out.copy_(ds.out, non_blocking=True)
+            if host_topk is not None:
+                host_topk.copy_(ds.topk_idx, non_blocking=True)
+            bnd.record(stream)
+            bnd.synchronize()
+            e2e_ms += a.elapsed_time(bnd)
+        e2e_ms /= Ke
+        e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
+        res["e2e"] = {"value": job_tokens_per_s(cfg.T, world, e2e_ms), "unit": "tokens/s",
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+    # roofline of the dominant call
+    dom = max((c for c in calls if c in alg), key=lambda c: per_call_us[c])
+    peak, peak_kind = peaks()
+    achieved = alg[dom] / (per_call_us[dom] * 1e-6) / 1e9
+    dom_file = {"indexer": "indexer_topk.cu", "attention": "attention.cu", "compress": "insert_compress.cu",
+                "insert": "insert_compress.cu"}[dom]
+    res["roofline"] = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                       "frac": achieved / peak, "peak_kind": peak_kind,
+                       "traffic": traffic_from_profiles(cfg.name, dom_file, cfg.T),
+                       "algorithmic_bytes": int(alg[dom]), "us_per_launch": per_call_us[dom]}
+    res["calls_roofline"] = {c: {"algorithmic_bytes": int(alg[c]), "us": per_call_us[c],
+                                 "frac": alg[c] / (per_call_us[c] * 1e-6) / 1e9 / peak if per_call_us[c] > 0 else None}
+                             for c in calls if c in alg}
+    del reps_ds, ds0, graph_step, graph_call
+    torch.cuda.empty_cache()
+    return res
+
+
+EXTRA_WORKLOADS = ("hca_c128_bf16", "csa_c4_fp8", "csa_c4_1m")
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -255,142 +416,60 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    from deepseek_v4_hybrid_gb300.step import DeviceStep
     cfg = rank_config(I.ALL_CONFIGS[args.config], rank)
-    st = I.make_step(cfg)
-    ds = DeviceStep(st)
-    stream = torch.cuda.current_stream()
-    flush = flush_buffer(torch)
-
-    for _ in range(max(args.warmup, 3)):
-        flush.fill_(1.0)
-        ds.run()
-    torch.cuda.synchronize()
-    import deepseek_v4_hybrid_gb300 as M
-    flags = M.dsv4_read_device_flags()
-    if flags:
-        raise SystemExit(f"kernels raised range/timeout flags {flags:#x} during warm-up; not timing")
-    topk_host = ds.topk_idx.cpu().numpy() if ds.has_indexer else None
-    alg = algorithmic_bytes(st, topk_host)
-
-    calls = ["insert", "compress", "indexer", "attention"]
     K = args.steps
-    # the step (and each call alone) captured once as a CUDA graph: the library never synchronises,
-    # so the four calls replay with no host launch gaps
-    graph_step = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_step):
-        ds.run()
-    graph_call = {}
-    for c in calls:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            getattr(ds, c)()
-        graph_call[c] = g
-    stream = torch.cuda.current_stream()
-    for _ in range(3):
-        flush.fill_(1.0)
-        graph_step.replay()
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    sampler = ClockSampler(local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.2)
-    wall0 = time.perf_counter()
-    for k in range(K):
-        flush.fill_(float(k))
-        ev[k][0].record(stream)
-        graph_step.replay()
-        ev[k][1].record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    total_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
-    ms_per_step = total_ms / K
-    # per-call breakdown (each call's graph timed alone, same flushing)
-    Kc = min(K, 200)
-    per_call = {c: 0.0 for c in calls}
-    for k in range(Kc):
-        flush.fill_(float(k))
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
-        evs[0].record(stream)
-        for i, c in enumerate(calls):
-            graph_call[c].replay()
-            evs[i + 1].record(stream)
-        torch.cuda.synchronize()
-        for i, c in enumerate(calls):
-            per_call[c] += evs[i].elapsed_time(evs[i + 1])
-    ms_per_step = max_over_ranks(ms_per_step, world, "cuda")
-    value = job_tokens_per_s(cfg.T, world, ms_per_step)
-    per_call_us = {c: 1e3 * v / Kc for c, v in per_call.items()}
-
-    # ---- end to end through host buffers: pinned H2D of the step's inputs, step, D2H of results
-    host_in = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in ds.step_input_tensors().items()}
-    for k, v in ds.step_input_tensors().items():
-        host_in[k].copy_(v)
-    host_out = torch.empty_like(ds.out, device="cpu").pin_memory()
-    host_topk = torch.empty_like(ds.topk_idx, device="cpu").pin_memory() if ds.has_indexer else None
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = host_out.numel() * host_out.element_size() + (host_topk.numel() * 4 if host_topk is not None else 0)
-    Ke = max(20, min(K, 400))
-    e2e_ms = 0.0
-    for k in range(Ke):
-        flush.fill_(float(k))
-        a, bnd = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for name, dev in ds.step_input_tensors().items():
-            dev.copy_(host_in[name], non_blocking=True)
-        ds.run()
-        host_out.copy_(ds.out, non_blocking=True)
-        if host_topk is not None:
-            host_topk.copy_(ds.topk_idx, non_blocking=True)
-        bnd.record(stream)
-        bnd.synchronize()
-        e2e_ms += a.elapsed_time(bnd)
-    e2e_ms /= Ke
-    e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
-
-    # ---- roofline of the dominant call
-    dom = max((c for c in calls if c in alg), key=lambda c: per_call_us[c])
-    peak, peak_kind = peaks()
-    achieved = alg[dom] / (per_call_us[dom] * 1e-6) / 1e9
-    dom_file = {"indexer": "indexer_topk.cu", "attention": "attention.cu", "compress": "insert_compress.cu",
-                "insert": "insert_compress.cu"}[dom]
-    units = cfg.T
-    traffic = traffic_from_profiles(args.config, dom_file, units)
-
+    head = measure_workload(cfg, K, args.warmup, world, local, want_e2e=True)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {0: "f32", 1: "bf16"}[cfg.act_dtype] + "/" + I.DTYPE_NAMES[cfg.cache_dtype],
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": head["dtype"],
         "data": "synthetic (seeded N(0,1)*0.1 rows, shuffled paged block tables)",
-        "config": {"workload": cfg.name, "batch_per_gpu": cfg.B, "q_per_seq": cfg.q_per_seq,
-                   "context": list(map(int, (st.ctx_len.min(), st.ctx_len.max()))), "heads": cfg.H,
-                   "ratio": cfg.ratio, "indexer": [cfg.I_h, cfg.d_I], "topk": cfg.topk, "page": 64,
-                   "l2": "flushed between steps (512 MB write)", "parallelism": f"replicas x{world} (per-sequence)"},
-        "e2e": {"value": job_tokens_per_s(cfg.T, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
-        "gpu_launches": int(K * launches_per_step(ds)),
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes": int(alg[dom]), "us_per_launch": per_call_us[dom]},
-        "calls_us": per_call_us,
-        "step_algorithmic_gbs": sum(alg.values()) / (ms_per_step * 1e-3) / 1e9,
-        "clocks": clocks,
-        "wall_s_timed": wall,
+        "config": dict(head["config"], parallelism=f"replicas x{world} (per-sequence)"),
+        "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "roofline": head["roofline"],
+        "calls_us": head["calls_us"], "calls_roofline": head["calls_roofline"],
+        "step_algorithmic_gbs": head["step_algorithmic_gbs"], "clocks": head["clocks"],
+        "wall_s_timed": head["wall_s_timed"],
     }
+    if world == 1 and not args.no_extra:
+        # the other full-size workloads on the same GPU (the headline stays `config.workload`)
+        extra = {}
+        for name in EXTRA_WORKLOADS:
+            if name == cfg.name:
+                continue
+            r = measure_workload(I.ALL_CONFIGS[name], min(K, 500), args.warmup, 1, local, want_e2e=False)
+            extra[name] = {k: r[k] for k in ("value", "ms_per_step", "dtype", "config", "roofline", "calls_us",
+                                             "calls_roofline", "step_algorithmic_gbs", "clocks", "gpu_launches")}
+            extra[name]["unit"] = "tokens/s"
+            extra[name]["steps"] = min(K, 500)
+        line["extra_workloads"] = extra
     if rank == 0 and not args.no_cpu_baseline:
+        st = I.make_step(cfg)
         v, sample = oracle_throughput(st, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                                 "sample": sample}
+        one = oracle_single_core(args.config, args.cpu_seconds)
+        if one is not None:
+            line["cpu_baseline"]["single_core"] = one
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def oracle_single_core(config, seconds):
+    """The same oracle sample in a child process limited to one core (BLAS threads 1, CPU affinity
+    one core)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import os, sys, json; sys.path.insert(0, %r); os.sched_setaffinity(0, {min(os.sched_getaffinity(0))}); "
+            "import bench, dsv4_inputs as I; st = I.make_step(I.ALL_CONFIGS[%r]); "
+            "v, s = bench.oracle_throughput(st, %r); print(json.dumps({'value': v, 'sample': s}))"
+            % (ROOT, config, float(seconds)))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"value": d["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": d["sample"]}
+    except Exception:
+        return None
 
 
 def launches_per_step(ds):

@@ -82,7 +82,7 @@ struct TopkBufs {
   uint32_t* seq_done;  // [B] key tiles of the sequence scored so far (tensor-core path)
   uint64_t* cand;      // [T][nc_stride] top-k candidates that do not fit in shared memory
   uint32_t* tcnt;      // [T][2] sliced top-k: candidates appended, slices finished
-  uint32_t* bits;      // [T][nc_stride / 32] sliced top-k: selection bitmap
+  uint32_t* bits;      // [T][nc_stride / 32] sliced top-k: selection bitmap (layout of bitmap_words)
   int nc_stride;
 };
 
@@ -103,9 +103,9 @@ __device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool
 //  1. From the histogram, the bin B* holding the k-th best score and the count A of scores above it
 //     (256 threads own 16 bins each, a block scan from the top finds the crossing thread).
 //  2. One pass over the scores: lane l of a warp takes entries 4l .. 4l + 3 of a 128-entry block;
-//     their "bin > B*" bits are gathered into the block's four 32-bit words of the selection bitmap
-//     with three shuffles, and entries in B* are appended to a candidate list as (low 20 key bits,
-//     j) values.
+//     the four ballots of "bin > B*" are the block's four words of the selection bitmap (bit l of
+//     word c = entry 4l + c), and entries in B* are appended to a candidate list as (low 20 key
+//     bits, j) values.
 //  3. The k - A largest candidates (larger score first, then smaller j: the values are unique) by a
 //     radix select of 10-bit digits over the 40-bit values, stopping at the first digit whose bin
 //     holds exactly the entries still needed; they are added to the bitmap.
@@ -119,7 +119,6 @@ constexpr int FIND_THREADS = 256;  // threads that own histogram bins in block_f
 constexpr int CHUNK = 4096;       // scores per bulk copy (16 KB)
 constexpr int NBUF = 4;           // chunk buffers (copies in flight)
 constexpr int SCAN_WARPS_MIN = 8;  // the kernels run top-k with at least 8 warps
-constexpr int SCAN_U = (CHUNK / 128 + SCAN_WARPS_MIN - 1) / SCAN_WARPS_MIN;  // blocks of a chunk per warp
 
 struct Ctl {
   uint64_t bar[NBUF + 1];  // chunk buffers, histogram
@@ -137,8 +136,15 @@ __device__ __forceinline__ int cand_j(uint64_t v) {
 }
 
 // Offsets in the shared buffer: control, radix bins, bitmap, histogram, chunks, candidates.
+// Selection bitmap layout: 128-entry block b has the four words 4 b + c, and bit l of word 4 b + c
+// stands for entry 128 b + 4 l + c (lane l of a warp reads entries 4 l .. 4 l + 3 of a block as one
+// float4, so each of the four ballots of a block is one word).
+__host__ __device__ inline int bitmap_words(int n) { return (n + 127) / 128 * 4; }
+__device__ __forceinline__ int bit_word(int j) { return ((j >> 7) << 2) | (j & 3); }
+__device__ __forceinline__ uint32_t bit_mask(int j) { return 1u << ((j >> 2) & 31); }
+
 __host__ __device__ inline size_t hist_offset(int n) {
-  return (CTL_BYTES + RBINS * 4 + ((size_t)n + 31) / 32 * 4 + 127) / 128 * 128;
+  return (CTL_BYTES + RBINS * 4 + (size_t)bitmap_words(n) * 4 + 127) / 128 * 128;
 }
 __host__ __device__ inline size_t fixed_bytes(int n) {
   return hist_offset(n) + (size_t)HIST_BINS * 4 + (size_t)NBUF * CHUNK * 4;
@@ -212,72 +218,71 @@ __device__ __forceinline__ void block_find_bin(const uint32_t* h, uint32_t rem, 
 }
 
 // Bitmap words and candidates of one chunk of scores in shared memory: sb holds entries j_base ..
-// j_base + 128 nblocks - 1 (entries >= n are ignored).  Entries with bin > bstar set their bit in
-// `bits` (word j / 32; every word of the chunk is written), entries in bstar are appended to `cand`
-// (capacity ccap) through the counter *ncand, one atomic per warp.  bits, cand and ncand may be in
-// shared or global memory.  Warp w takes 128-entry blocks w, w + NW, ... side by side.
-__device__ __forceinline__ void scan_chunk(const float4* sb, int nblocks, int j_base, int n, uint32_t bstar,
+// j_base + 128 nblocks - 1 (j_base a multiple of 128, nblocks <= CHUNK / 128; entries >= n are
+// ignored).  Entries with bin > bstar set their bit in `bits` (every word of the chunk's blocks
+// below `words` is written, 16 bytes at a time), entries in bstar are appended to `cand` (capacity
+// ccap) through the counter *ncand.  bits (16-byte aligned), cand and ncand may be in shared or
+// global memory.  Warp w owns the consecutive blocks w P .. w P + P - 1 (P <= SCAN_B); lane l reads
+// entries 4 l .. 4 l + 3 of a block as one float4, and the four ballots of "bin > bstar" are the
+// block's four bitmap words.  Candidates are rare: each lane counts its own, the warp takes its slots
+// with one atomic, and each lane writes its candidates to consecutive slots.
+constexpr int SCAN_B = CHUNK / 128 / SCAN_WARPS_MIN;  // 128-entry blocks of a chunk per warp (4)
+__device__ __forceinline__ void scan_chunk(const float* sb, int nblocks, int j_base, int n, uint32_t bstar,
                                            uint32_t* bits, int words, uint64_t* cand, uint32_t ccap,
                                            uint32_t* ncand) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
-  float4 v[SCAN_U];
+  const float4* sb4 = reinterpret_cast<const float4*>(sb);
+  const int per = (nblocks + NW - 1) / NW;  // <= SCAN_B since NW >= SCAN_WARPS_MIN
+  const int b0 = warp * per;
+  float4 v[SCAN_B];
 #pragma unroll
-  for (int u = 0; u < SCAN_U; ++u) {
-    const int bl = warp + u * NW;
-    v[u] = bl < nblocks ? sb[bl * 32 + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  for (int i = 0; i < SCAN_B; ++i) {
+    const int blk = b0 + i;
+    v[i] = (i < per && blk < nblocks) ? sb4[blk * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  uint32_t sel[SCAN_U], cm[SCAN_U];
-  int mycnt = 0;
+  int lc = 0;  // this lane's candidates
 #pragma unroll
-  for (int u = 0; u < SCAN_U; ++u) {
-    const int j0 = j_base + (warp + u * NW) * 128 + 4 * lane;
-    const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-    sel[u] = 0u;
-    cm[u] = 0u;
+  for (int i = 0; i < SCAN_B; ++i) {
+    const int blk = b0 + i;
+    const bool live = i < per && blk < nblocks;  // warp-uniform
+    const int nv = live ? n - (j_base + blk * 128 + 4 * lane) : 0;  // entries c < nv of the lane are valid
+    const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t sw[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t bin = order_key(e[k]) >> HIST_SHIFT;
-      const bool in = j0 + k < n;
-      if (in && bin > bstar) sel[u] |= 1u << k;
-      if (in && bin == bstar) cm[u] |= 1u << k;
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t bin = order_key(e[c]) >> HIST_SHIFT;
+      sw[c] = __ballot_sync(0xffffffffu, c < nv && bin > bstar);
+      lc += (c < nv && bin == bstar) ? 1 : 0;
     }
-    mycnt += __popc(cm[u]);
+    const int wg = ((j_base >> 7) + blk) * 4;
+    if (lane == 0 && live && wg < words) *reinterpret_cast<uint4*>(bits + wg) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
   }
-  int incl = mycnt;
+  const int wtot = __reduce_add_sync(0xffffffffu, lc);
+  if (wtot == 0) return;  // warp-uniform
+  int incl = lc;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int tt = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += tt;
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
   }
-  const int wtot = __shfl_sync(0xffffffffu, incl, 31);
-  if (wtot) {
-    uint32_t base = 0;
-    if (lane == 31) base = atomicAdd(ncand, (uint32_t)wtot);
-    base = __shfl_sync(0xffffffffu, base, 31);
-    if (mycnt) {
-      uint32_t idx = base + (uint32_t)(incl - mycnt);
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(ncand, (uint32_t)wtot);
+  uint32_t idx = __shfl_sync(0xffffffffu, base, 0) + (uint32_t)(incl - lc);
+  if (lc == 0) return;
 #pragma unroll
-      for (int u = 0; u < SCAN_U; ++u) {
-        const int j0 = j_base + (warp + u * NW) * 128 + 4 * lane;
-        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+  for (int i = 0; i < SCAN_B; ++i) {
+    const int blk = b0 + i;
+    const int j0 = j_base + blk * 128 + 4 * lane;
+    const int nv = (i < per && blk < nblocks) ? n - j0 : 0;
+    const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if ((cm[u] >> k) & 1u) {
-            if (idx < ccap) cand[idx] = cand_value(order_key(e[k]), j0 + k);
-            ++idx;
-          }
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t key = order_key(e[c]);
+      if (c < nv && (key >> HIST_SHIFT) == bstar) {
+        if (idx < ccap) cand[idx] = cand_value(key, j0 + c);
+        ++idx;
       }
     }
-  }
-#pragma unroll
-  for (int u = 0; u < SCAN_U; ++u) {
-    const int bl = warp + u * NW;
-    uint32_t w = sel[u] << (4 * (lane & 7));
-    w |= __shfl_xor_sync(0xffffffffu, w, 1);
-    w |= __shfl_xor_sync(0xffffffffu, w, 2);
-    w |= __shfl_xor_sync(0xffffffffu, w, 4);
-    const int wg = (j_base >> 5) + bl * 4 + (lane >> 3);
-    if ((lane & 7) == 0 && bl < nblocks && wg < words) bits[wg] = w;
   }
 }
 
@@ -311,39 +316,52 @@ __device__ void select_candidates(const uint64_t* cand, uint32_t m, int R, uint3
     const uint64_t v = cand[i];
     if (v >= thr) {
       const int j = cand_j(v);
-      atomicOr(&bits[j >> 5], 1u << (j & 31));
+      atomicOr(&bits[bit_word(j)], bit_mask(j));
     }
   }
 }
 
 // The selection in increasing j from the bitmap (words written by this CTA or, for a global bitmap,
-// by others before a fence), -1 padding; then the scores of the selected entries, read with many
-// loads in flight (from `row_s` when the row is in shared memory, else from global s_g).  Whole CTA.
+// by others before a fence), listed first in sel_s (K ints of shared memory), then written out with
+// -1 padding together with the scores of the selected entries (from `row_s` when the row is in
+// shared memory, else from global s_g).  Thread i takes a run of 128-entry blocks; within a block
+// the entries of lane position l come in the order c = 0..3, which is increasing j.  Whole CTA.
 __device__ void write_selection(const uint32_t* bits, bool bits_global, int words, int K, int32_t* out, float* out_s,
-                                const float* row_s, const float* s_g, Ctl* c) {
+                                const float* row_s, const float* s_g, Ctl* c, int* sel_s) {
   const int tid = threadIdx.x, NT = blockDim.x;
-  const int per = (words + NT - 1) / NT;
-  const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+  const int nblk = words >> 2;
+  const int per = (nblk + NT - 1) / NT;
+  const int k0 = min(nblk, tid * per), k1 = min(nblk, k0 + per);
+  auto block = [&](int b) {
+    const uint4* p4 = reinterpret_cast<const uint4*>(bits) + b;
+    return bits_global ? __ldcg(p4) : *p4;
+  };
   int cnt = 0;
-  for (int w = w0; w < w1; ++w) cnt += __popc(bits_global ? __ldcg(bits + w) : bits[w]);
+  for (int b = k0; b < k1; ++b) {
+    const uint4 w = block(b);
+    cnt += __popc(w.x) + __popc(w.y) + __popc(w.z) + __popc(w.w);
+  }
   int total;
   int pos = block_excl_scan(cnt, c->wt, &total);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bw = bits_global ? __ldcg(bits + w) : bits[w];
-    while (bw) {
-      const int j = (w << 5) + __ffs(bw) - 1;
-      bw &= bw - 1;
-      if (pos < K) out[pos] = j;
-      ++pos;
+  for (int b = k0; b < k1 && pos < K; ++b) {
+    const uint4 w = block(b);
+    uint32_t any = w.x | w.y | w.z | w.w;
+    while (any && pos < K) {
+      const int l = __ffs(any) - 1;
+      any &= any - 1;
+      const int j = b * 128 + 4 * l;
+      if ((w.x >> l) & 1u && pos < K) sel_s[pos++] = j;
+      if ((w.y >> l) & 1u && pos < K) sel_s[pos++] = j + 1;
+      if ((w.z >> l) & 1u && pos < K) sel_s[pos++] = j + 2;
+      if ((w.w >> l) & 1u && pos < K) sel_s[pos++] = j + 3;
     }
   }
-  for (int x = total + tid; x < K; x += NT) out[x] = -1;
-  if (out_s) {
-    __syncthreads();  // out[] is complete (global writes of this CTA are visible to it after the barrier)
-    for (int x = tid; x < K; x += NT) {
-      const int j = out[x];
-      out_s[x] = j < 0 ? -INFINITY : (row_s ? row_s[j] : __ldcg(s_g + j));
-    }
+  __syncthreads();
+  const int m = min(total, K);
+  for (int x = tid; x < K; x += NT) {
+    const int j = x < m ? sel_s[x] : -1;
+    out[x] = j;
+    if (out_s) out_s[x] = j < 0 ? -INFINITY : (row_s ? row_s[j] : __ldcg(s_g + j));
   }
 }
 
@@ -369,12 +387,18 @@ __device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int 
   }
   Ctl* c = reinterpret_cast<Ctl*>(buf);
   uint32_t* rb = reinterpret_cast<uint32_t*>(buf + CTL_BYTES);
-  const int words = (n + 31) >> 5;
+  const int words = bitmap_words(n);
   uint32_t* bits = rb + RBINS;
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(buf + hist_offset(n));
   uint8_t* chunks = reinterpret_cast<uint8_t*>(hist_s + HIST_BINS);
   uint64_t* cand_s = reinterpret_cast<uint64_t*>(buf + fixed);
   const uint32_t cap = (uint32_t)((buf_bytes - fixed) / 8);
+  if ((size_t)K > 2 * (size_t)cap) {  // the selection is listed over the candidate area (never short for
+                                      // the buffers the kernels pass)
+    if (tid == 0) atomicOr(&g_flags_ix, FLAG_TOPK);
+    for (int x = tid; x < K; x += NT) out[x] = -1;
+    return false;
+  }
   const int nchunks = (n + CHUNK - 1) / CHUNK;
   const int n128 = (n + 127) & ~127;  // copy whole 128-entry blocks (the row has room)
   // the whole row stays in the chunk buffers when it fits (then the output scores come from there)
@@ -426,7 +450,7 @@ __device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int 
       stop = cc;
       break;
     }
-    const float4* sb = reinterpret_cast<const float4*>(chunks + (size_t)(cc % NBUF) * CHUNK * 4);
+    const float* sb = reinterpret_cast<const float*>(chunks + (size_t)(cc % NBUF) * CHUNK * 4);
     scan_chunk(sb, min(CHUNK, n128 - cc * CHUNK) >> 7, cc * CHUNK, n, bstar, bits, words, cand, ccap, &c->ncand);
     if (cc + NBUF < nchunks) {
       tc::fence_proxy_async_smem();  // reads of this buffer come before the next copy into it
@@ -444,11 +468,12 @@ __device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int 
   }
   __syncthreads();
 
-  // 3. exact choice among the candidates, 4. the selection in increasing j
+  // 3. exact choice among the candidates, 4. the selection in increasing j, listed over the candidate
+  // area (its candidates are no longer needed; it holds at least 2 cap >= K ints)
   select_candidates(cand, min(c->ncand, ccap), R, rb, c, bits);
   __syncthreads();
   write_selection(bits, false, words, K, out, out_s, resident ? reinterpret_cast<const float*>(chunks) : nullptr,
-                  s_g, c);
+                  s_g, c, reinterpret_cast<int*>(cand_s));
   __syncthreads();  // the buffer may be reused right away
   return true;
 }
@@ -686,10 +711,41 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = a.B * a.tiles_max;
-  // this CTA's range [lo, hi) of the (sequence, tile) grid: an even share of the sequences' valid
-  // tiles (grid positions past a sequence's entries are skipped by every role), worked out by the
-  // loading warp from a prefix over the sequences' tile counts while the others set up
+  pdl_launch_dependents();
+  pdl_wait();  // nothing below runs before the kernels ahead of this one have finished
+  // Set-up, arranged so that the loading warp issues its first copies as early as possible: it
+  // initialises the mbarriers and works out the CTA's range [lo, hi) of the (sequence, tile) grid (an
+  // even share of the sequences' valid tiles, from a prefix over their tile counts), announces both on
+  // named barrier BAR_SETUP and goes straight on to loading.  The MMA warp allocates TMEM and announces
+  // it on BAR_TMEM to the epilogue warps, which meanwhile clear their histograms and load the head
+  // weights and entry counts of the CTA's sequences.
+  constexpr uint32_t BAR_SETUP = 1, BAR_TMEM = 2, BAR_EPI = 3;
   if (warp == W_LOAD) {
+    if (lane == 0) {
+      for (int s = 0; s < a.stages; ++s) {
+        tc::mbar_init(&sm->full[s], I8 ? 2 : 1);  // int8: the two expanding warps; else the loader (+ bytes)
+        tc::mbar_init(&sm->empty[s], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        tc::mbar_init(&sm->raw_full[i], 1);
+        tc::mbar_init(&sm->raw_empty[i], 2);
+      }
+      for (int i = 0; i < SCALE_RING; ++i) tc::mbar_init(&sm->sready[i], 2);
+      for (int i = 0; i < 4; ++i) {
+        tc::mbar_init(&sm->dfull[i], 1);
+        tc::mbar_init(&sm->dempty[i], 4);
+      }
+      for (int i = 0; i < 2; ++i) {
+        tc::mbar_init(&sm->qfull[i], 1);
+        tc::mbar_init(&sm->qempty[i], 1);
+      }
+      tc::mbar_init(&sm->done, 1);
+      tc::mbar_init(&sm->ebar[0], 4);
+      tc::mbar_init(&sm->ebar[1], 4);
+      sm->nfin = 0;
+      sm->abort = 0;
+      tc::fence_barrier_init();
+    }
     int r0 = (int)((int64_t)blockIdx.x * total / gridDim.x), r1 = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
     if (a.B <= PRE_MAX) {
       // the tile counts first (independent loads, all in flight together), then the scan
@@ -727,57 +783,39 @@ __global__ void __launch_bounds__(THREADS, 1)
       sm->range[0] = r0;
       sm->range[1] = r1;
     }
-  }
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < a.stages; ++s) {
-      tc::mbar_init(&sm->full[s], I8 ? 2 : 1);  // int8: the two expanding warps; else the loader (+ bytes)
-      tc::mbar_init(&sm->empty[s], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sm->raw_full[i], 1);
-      tc::mbar_init(&sm->raw_empty[i], 2);
-    }
-    for (int i = 0; i < SCALE_RING; ++i) tc::mbar_init(&sm->sready[i], 2);
-    for (int i = 0; i < 4; ++i) {
-      tc::mbar_init(&sm->dfull[i], 1);
-      tc::mbar_init(&sm->dempty[i], 4);
-    }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sm->qfull[i], 1);
-      tc::mbar_init(&sm->qempty[i], 1);
-    }
-    tc::mbar_init(&sm->done, 1);
-    tc::mbar_init(&sm->ebar[0], 4);
-    tc::mbar_init(&sm->ebar[1], 4);
-    sm->nfin = 0;
-    sm->abort = 0;
-    tc::fence_barrier_init();
-  }
-  for (int x = threadIdx.x; x < 2 * a.qps * HIST_BINS; x += blockDim.x) hist_s[x] = 0;
-  if (warp == W_MMA) {
+    __syncwarp();
+    tc::named_bar_arrive(BAR_SETUP, blockDim.x);
+  } else if (warp == W_MMA) {
     tc::tmem_alloc(&sm->tmem_base, a.tmem_cols);
     tc::tmem_relinquish();
     tc::tc_fence_before();
+    tc::named_bar_arrive(BAR_TMEM, 32 + 256);
+    tc::named_bar_sync(BAR_SETUP, blockDim.x);
+  } else if (warp < W_LOAD) {
+    const int g = warp >> 2;
+    for (int x = threadIdx.x & 127; x < a.qps * HIST_BINS; x += 128) hist_s[g * a.qps * HIST_BINS + x] = 0;
+    tc::named_bar_sync(BAR_SETUP, blockDim.x);
+  } else {
+    tc::named_bar_sync(BAR_SETUP, blockDim.x);
   }
-  __syncthreads();
   const int lo = sm->range[0], hi = sm->range[1];
   // head weights and per-token entry counts of the CTA's sequences, when there are few of them
+  // (epilogue warps only)
   const int b_first = lo / a.tiles_max;
   const int nseq_rng = hi > lo ? (hi - 1) / a.tiles_max - b_first + 1 : 0;
   const bool pre = nseq_rng <= WSEQ;
-  if (pre) {
-    for (int x = threadIdx.x; x < nseq_rng * a.N; x += blockDim.x)
-      w_tab[x] = a.weights[(int64_t)b_first * a.qps * a.Ih + x];
-    for (int x = threadIdx.x; x < nseq_rng * a.qps; x += blockDim.x)
-      sm->nc_tab[x / a.qps][x % a.qps] =
-          visible_entries(a.positions, (b_first + x / a.qps) * a.qps + x % a.qps, a.max_context, a.ratio);
+  if (warp < W_LOAD) {
+    if (pre) {
+      for (int x = threadIdx.x; x < nseq_rng * a.N; x += 256) w_tab[x] = a.weights[(int64_t)b_first * a.qps * a.Ih + x];
+      for (int x = threadIdx.x; x < nseq_rng * a.qps; x += 256)
+        sm->nc_tab[x / a.qps][x % a.qps] =
+            visible_entries(a.positions, (b_first + x / a.qps) * a.qps + x % a.qps, a.max_context, a.ratio);
+    }
+    tc::named_bar_sync(BAR_EPI, 256);
+    tc::named_bar_sync(BAR_TMEM, 32 + 256);
   }
-  pdl_launch_dependents();
-  pdl_wait();  // the prologue above overlaps the previous kernel
-  __syncthreads();
   tc::tc_fence_after();
-  const uint32_t tmem = sm->tmem_base;
+  const uint32_t tmem = sm->tmem_base;  // read by the MMA and epilogue warps only
 
   if (warp == W_LOAD) {
     // ---------------- TMA producer (lane 0 issues; all lanes look up pages 32 items at a time)
@@ -1250,8 +1288,8 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
   uint64_t* cand_s = reinterpret_cast<uint64_t*>(chunks + (size_t)SLICE * 4);
   const size_t fixed = CTL_BYTES + RBINS * 4 + HIST_BINS * 4 + (size_t)SLICE * 4;
   const uint32_t cap = (uint32_t)((TK_SMEM - fixed) / 8);
-  const int words = (n + 31) >> 5;
-  uint32_t* bits_g = bufs.bits + (int64_t)t * (bufs.nc_stride / 32);
+  const int words = bitmap_words(n);
+  uint32_t* bits_g = bufs.bits + (int64_t)t * (bufs.nc_stride / 32);  // nc_stride / 32 >= bitmap_words(n)
   uint64_t* cand_g = bufs.cand + (int64_t)t * bufs.nc_stride;
   const int j_lo = sl * SLICE;
   const int n128 = (n + 127) & ~127;
@@ -1280,7 +1318,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
     for (int cc = 0; cc < nch && ok; ++cc) {
       ok = __syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc], 0, &abort_s));
       if (ok)
-        scan_chunk(reinterpret_cast<const float4*>(chunks + (size_t)cc * CHUNK * 4),
+        scan_chunk(reinterpret_cast<const float*>(chunks + (size_t)cc * CHUNK * 4),
                    min(CHUNK, n128 - j_lo - cc * CHUNK) >> 7, j_lo + cc * CHUNK, n, bstar, bits_g, words, cand_g,
                    (uint32_t)n, &bufs.tcnt[2 * t]);
     }
@@ -1311,7 +1349,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
   select_candidates(cand, m, R, rb, c, bits_g);
   __threadfence();
   __syncthreads();
-  write_selection(bits_g, true, words, K, out, out_s, nullptr, s_g, c);
+  write_selection(bits_g, true, words, K, out, out_s, nullptr, s_g, c, reinterpret_cast<int*>(cand_s));
 }
 
 cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t st) {

@@ -91,6 +91,16 @@ __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t* phase, volat
   return ok;
 }
 
+// Named CTA barriers (ids 1..15; id 0 is __syncthreads): `count` threads (a multiple of 32) take
+// part; arrive does not wait, sync waits for the count.  Shared-memory writes made before the arrive
+// or sync are visible to the threads that complete the sync.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------------------------
