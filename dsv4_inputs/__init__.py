@@ -17,7 +17,8 @@ Workload shapes follow the five decode configurations of the hot path:
 plus small variants (``small_*``) of the same dtypes and head counts that the
 oracle finishes in seconds while still spanning several tiles and ragged tails.
 
-Value recipe: q, kv_new, indexer queries, cache rows ~ N(0,1)*0.1; kv_score
+Value recipe: q, kv_new, indexer queries, cache rows ~ N(0,1)*0.1; query RMSNorm weight
+1 + N(0,1)*0.1; kv_score
 ~ N(0,1); indexer weights ~ N(0,1)*0.1; RMSNorm weight 1 + N(0,1)*0.1; APE
 ~ N(0,1)*0.1; sink ~ N(0,1); RoPE table theta = 10000.  Large bf16 buffers are
 drawn by inverse-CDF lookup: a uniform 16-bit integer indexes a table of the
@@ -63,10 +64,17 @@ class Config:
     out_dtype: int        # attention output dtype
     seed: int = 0xD5E4
     explicit_lens: tuple = ()
+    q_prep: bool = True   # queries arrive un-normed and un-rotated: the fused insert norms, rotates and pads them
 
     @property
     def T(self) -> int:
         return self.B * self.q_per_seq
+
+    @property
+    def H_pad(self) -> int:
+        """Query heads of the attention's input and output buffers: a multiple of 64 for bf16 and
+        fp8_ds_mla caches (the tensor-core attention takes heads in groups of 64), else H."""
+        return self.H if self.cache_dtype == F32 else (self.H + 63) // 64 * 64
 
     @property
     def coff(self) -> int:
@@ -104,6 +112,9 @@ SMALL_CONFIGS = {
                                           d_I=0, topk=0, explicit_lens=(300, 7)),
     "edge_first_token": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="edge_first_token", B=2,
                                             explicit_lens=(1, 4)),
+    # 32 query heads padded to 64 by the fused query preparation
+    "small_c4_h32pad": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_c4_h32pad", B=3, H=32,
+                                           explicit_lens=(3000, 700, 129)),
 }
 
 ALL_CONFIGS = {**CONFIGS, **SMALL_CONFIGS}
@@ -223,12 +234,13 @@ class StepInputs:
     q: np.ndarray                # [T, H, D]
     sink: np.ndarray             # [H] f32
     softmax_scale: float
+    q_norm_w: np.ndarray = None  # [D] f32 per-channel weight of the per-head query RMSNorm
+    cos_sin: np.ndarray = None   # [max_pos, 64] f32: 32 cos | 32 sin (RoPE of q, kv and compressed entries)
     kv_score: np.ndarray = None  # [T, 2*coff*D] f32
     state: np.ndarray = None     # [B, coff*ratio, 2*coff*D] f32
     ape: np.ndarray = None       # [ratio, coff*D] f32
     norm_w: np.ndarray = None    # [D] f32
     eps: float = 1e-6
-    cos_sin: np.ndarray = None   # [max_pos, 64] f32: 32 cos | 32 sin
     main_cache: np.ndarray = None
     main_bt: np.ndarray = None   # [B, main_max_pages] int32
     idx_cache: np.ndarray = None
@@ -298,6 +310,8 @@ def make_step(cfg: Config, with_given_topk: bool = True) -> StepInputs:
     sink = draw.normal_f32("sink", (H,), 1.0)
     st = StepInputs(cfg=cfg, ctx_len=L, positions=positions, kv_new=kv_new, slot_mapping=slot,
                     swa_cache=swa_cache, swa_bt=swa_bt, q=q, sink=sink, softmax_scale=float(D) ** -0.5)
+    st.cos_sin = rope_table(max_ctx + 1)
+    st.q_norm_w = draw.normal_f32("q_norm_w", (D,), 0.1, 1.0)
     if cfg.ratio == 0:
         return st
 
@@ -307,7 +321,6 @@ def make_step(cfg: Config, with_given_topk: bool = True) -> StepInputs:
     st.state = draw.normal_f32("state", (B, coff * r, 2 * coff * D), 1.0)
     st.ape = draw.normal_f32("ape", (r, coff * D), 0.1)
     st.norm_w = draw.normal_f32("norm_w", (D,), 0.1, 1.0)
-    st.cos_sin = rope_table(max_ctx + 1)
 
     # ---- main (compressed) cache: rows j < floor(L/r) exist after the step
     nc_after = L // r

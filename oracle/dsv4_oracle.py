@@ -268,6 +268,26 @@ def rope_gptj(x, cos, sin) -> np.ndarray:
     return out
 
 
+def qnorm_rope(q_t, p: int, cos_sin, norm_w, eps, apply_norm: bool, apply_rope: bool, h_pad: int) -> np.ndarray:
+    """The query heads one token hands to the attention ([MAP] "Phase 2", default stream, item 2:
+    per-head RMSNorm of every query head, GPT-J RoPE of the last 64 dims of each head; [API]
+    DeepseekV4Attention._fused_qnorm_rope_kv_insert: the query is zero-padded to the backend's
+    padded head count).  q_t [H, 576] values -> [h_pad, 576]: each head x becomes
+    x / sqrt(mean(x^2) + eps) * w (w = 1 when norm_w is None) when apply_norm, then dims 512..575
+    are rotated by the cos/sin row of position p when apply_rope; heads H .. h_pad-1 are zero."""
+    q = np.asarray(q_t, np.float64)
+    H = q.shape[0]
+    out = np.zeros((h_pad, D), np.float64)
+    w = np.ones(D) if norm_w is None else np.asarray(norm_w, np.float64)
+    cs = np.asarray(cos_sin[int(p)], np.float64) if apply_rope else None
+    for h in range(H):
+        x = rms_norm(q[h], w, eps) if apply_norm else q[h].copy()
+        if apply_rope:
+            x[D_NOPE:] = rope_gptj(x[D_NOPE:], cs[:32], cs[32:])
+        out[h] = x
+    return out
+
+
 def kv_insert(swa: Paged, kv_new, kv_dtype: int, slot_mapping, cache_dtype: int,
               positions=None, cos_sin=None):
     """Write each token's latent row into the paged SWA cache at its slot ([MAP] "4.
@@ -463,9 +483,24 @@ def decode_step(st, seqs=None, topk_override=None):
     sel = np.zeros(cfg.T, bool)
     sel[toks] = True
     slots = np.where(sel, st.slot_mapping, -1)
-    kv_insert(swa, st.kv_new, cfg.act_dtype, slots, cfg.cache_dtype)
+    q_prep = getattr(cfg, "q_prep", False)
+    if q_prep:  # the fused insert also rotates the new kv rows at their positions
+        kv_insert(swa, st.kv_new, cfg.act_dtype, slots, cfg.cache_dtype, st.positions, st.cos_sin)
+    else:
+        kv_insert(swa, st.kv_new, cfg.act_dtype, slots, cfg.cache_dtype)
 
     res = {"swa_written": dict(swa.written), "tokens": toks}
+    # the queries the attention reads: as given, or normed, rotated and padded by the fused insert and
+    # stored in the activation format
+    q_att, q_out = {}, {}
+    for t in toks:
+        q_t = decode_rows(st.q[t], cfg.act_dtype)
+        if q_prep:
+            qv = qnorm_rope(q_t, int(st.positions[t]), st.cos_sin, st.q_norm_w, st.eps, True, True, cfg.H_pad)
+            q_out[t] = encode_row(qv, cfg.act_dtype)
+            q_t = decode_rows(q_out[t], cfg.act_dtype)[:cfg.H]
+        q_att[t] = q_t
+    res["q_out"] = q_out
     main = None
     if cfg.ratio > 0:
         main = Paged(st.main_cache)
@@ -496,7 +531,6 @@ def decode_step(st, seqs=None, topk_override=None):
         if cfg.ratio > 0 and cfg.topk > 0:
             krow = topk_override[t] if topk_override is not None else topk[t]
         rows = attention_rows(p, b, swa, st.swa_bt, cfg.cache_dtype, main, st.main_bt, cfg.ratio, krow)
-        q_t = decode_rows(st.q[t], cfg.act_dtype)
-        out[t], lse[t] = mqa_decode(q_t, rows, st.sink, st.softmax_scale)
+        out[t], lse[t] = mqa_decode(q_att[t], rows, st.sink, st.softmax_scale)
     res["out"], res["lse"] = out, lse
     return res

@@ -89,9 +89,17 @@ def test_compressed_entry_rope_uses_group_position_row():
     assert np.max(np.abs(got[512:] - other[512:])) > 1e-3
 
 
-def _emitting_step(ctx, topk_sel):
+def scalar_rotate(y, p, table):
+    """GPT-J RoPE of dims 512..575 of a list of values as complex multiplication, in place."""
+    for k in range(32):
+        z = complex(y[512 + 2 * k], y[513 + 2 * k]) * complex(float(table[p][k]), float(table[p][32 + k]))
+        y[512 + 2 * k], y[513 + 2 * k] = z.real, z.imag
+    return y
+
+
+def _emitting_step(ctx, topk_sel, q_prep):
     cfg = dataclasses.replace(I.CONFIGS["tiny_c4_f32"], name="pin_emit", B=1, H=4, topk=8,
-                              explicit_lens=(ctx,))
+                              explicit_lens=(ctx,), q_prep=q_prep)
     st = I.make_step(cfg)
     st.cos_sin = rotary_table(ctx + 1).astype(np.float32)
     sel = np.full((1, cfg.topk), -1, np.int32)
@@ -99,12 +107,15 @@ def _emitting_step(ctx, topk_sel):
     return cfg, st, sel
 
 
+@pytest.mark.parametrize("q_prep", [False, True])
 @pytest.mark.parametrize("ctx,sel", [(300, [3, 10, 50, 74]), (256, [0, 63, 12]), (300, [74])])
-def test_decode_step_attends_this_steps_row_and_entry(ctx, sel):
+def test_decode_step_attends_this_steps_row_and_entry(ctx, sel, q_prep):
     """One sequence whose new token completes a group: the attention of decode_step must equal a
     softmax over rows put together by hand -- the window ending at this step's own new row, then
-    the selected entries, where the entry folded this step comes from the updated state ring."""
-    cfg, st, given = _emitting_step(ctx, sel)
+    the selected entries, where the entry folded this step comes from the updated state ring.  With
+    the query preparation on, the new row is rotated at its position and every query head is
+    RMS-normed (times its weight), rotated and stored as fp32 before the attention reads it."""
+    cfg, st, given = _emitting_step(ctx, sel, q_prep)
     p = ctx - 1
     assert (p + 1) % cfg.ratio == 0
     j_new = p // cfg.ratio
@@ -119,8 +130,11 @@ def test_decode_step_attends_this_steps_row_and_entry(ctx, sel):
 
     rows = []
     for pos in range(max(0, p - 127), p + 1):
-        if pos == p:
-            rows.append(np.asarray(st.kv_new[0], np.float64))        # inserted this step
+        if pos == p:                                                     # inserted this step
+            row = [float(x) for x in st.kv_new[0]]
+            if q_prep:
+                row = scalar_rotate(row, p, st.cos_sin)
+            rows.append(np.asarray(row, np.float32).astype(np.float64))  # stored as fp32
         else:
             page = st.swa_bt[0][pos // 64]
             rows.append(np.asarray(st.swa_cache[page, pos % 64], np.float64))
@@ -138,6 +152,12 @@ def test_decode_step_attends_this_steps_row_and_entry(ctx, sel):
         assert R.shape[0] == min(p + 1, 128) + len(sel)
 
     q = np.asarray(st.q[0], np.float64)
+    if q_prep:
+        for h in range(cfg.H):
+            inv = 1.0 / math.sqrt(math.fsum(x * x for x in q[h]) / D + st.eps)
+            y = scalar_rotate([q[h][c] * inv * float(st.q_norm_w[c]) for c in range(D)], p, st.cos_sin)
+            q[h] = np.asarray(y, np.float32)                             # stored as fp32
+        np.testing.assert_allclose(np.asarray(res["q_out"][0])[:cfg.H].astype(np.float64), q, rtol=2.0 ** -23, atol=0)
     for h in range(cfg.H):
         z = st.softmax_scale * (R @ q[h])
         logits = np.concatenate([z, [float(st.sink[h])]])
@@ -145,3 +165,50 @@ def test_decode_step_attends_this_steps_row_and_entry(ctx, sel):
         want = (w[:, None] * R[:, :DV]).sum(axis=0)
         np.testing.assert_allclose(res["out"][0][h], want, rtol=1e-9, atol=1e-12)
         assert abs(res["lse"][0][h] - logsumexp(logits)) <= 1e-10 * max(1.0, abs(logsumexp(logits)))
+
+
+# ------------------------------------------------------------------------------------------------
+# query preparation: per-head RMSNorm, GPT-J RoPE of dims 512..575, zero padding
+# ------------------------------------------------------------------------------------------------
+
+def test_qnorm_rope_against_scalar_recomputation():
+    """Every head: RMSNorm over its 576 dims (weight far from 1), then each GPT-J pair of the rope
+    dims turned as the complex number x_2k + i x_2k+1 times e^(i p theta^(-2k/64)), the angle taken
+    from math.cos / math.sin here; heads past H are zero."""
+    rng = np.random.default_rng(11)
+    H, h_pad, p = 5, 8, 777
+    q = rng.standard_normal((H, D)) * 0.3
+    w = 1.0 + 0.5 * rng.standard_normal(D)
+    table = rotary_table(p + 1)
+    got = O.qnorm_rope(q, p, table, w, 1e-6, True, True, h_pad)
+    for h in range(H):
+        inv = 1.0 / math.sqrt(math.fsum(x * x for x in q[h]) / D + 1e-6)
+        y = [q[h][c] * inv * w[c] for c in range(D)]
+        for k in range(32):
+            ang = p * 10000.0 ** (-2.0 * k / 64.0)
+            z = complex(y[512 + 2 * k], y[513 + 2 * k]) * complex(math.cos(ang), math.sin(ang))
+            y[512 + 2 * k], y[513 + 2 * k] = z.real, z.imag
+        np.testing.assert_allclose(got[h], y, rtol=1e-12, atol=1e-12)
+    assert np.all(got[H:] == 0.0)
+
+
+def test_qnorm_invariants_and_switches():
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((3, D))
+    table = rotary_table(40)
+    # unit weight, no rope: every head's mean square is ms / (ms + eps); a head scaled by c > 0 maps
+    # to (nearly) the same output
+    y = O.qnorm_rope(q, 30, table, None, 1e-6, True, False, 3)
+    for h in range(3):
+        ms = np.mean(q[h] ** 2)
+        assert abs(np.mean(y[h] ** 2) - ms / (ms + 1e-6)) < 1e-12
+    y2 = O.qnorm_rope(q * 7.5, 30, table, None, 1e-6, True, False, 3)
+    np.testing.assert_allclose(y2, y, rtol=1e-6)
+    # rope only: the no-pe dims are untouched, each rope pair keeps its length, position 0 is the identity
+    r = O.qnorm_rope(q, 30, table, None, 1e-6, False, True, 3)
+    assert np.array_equal(r[:, :512], q[:, :512])
+    np.testing.assert_allclose(np.hypot(r[:, 512::2], r[:, 513::2]), np.hypot(q[:, 512::2], q[:, 513::2]), rtol=1e-12)
+    assert np.array_equal(O.qnorm_rope(q, 0, table, None, 1e-6, False, True, 3), q)
+    # neither switch: a copy, zero padded
+    z = O.qnorm_rope(q, 5, table, None, 1e-6, False, False, 6)
+    assert np.array_equal(z[:3], q) and np.all(z[3:] == 0.0)
