@@ -99,6 +99,10 @@ def algorithmic_bytes(st, topk_idx=None):
     qps = cfg.q_per_seq
     b = {}
     b["insert"] = T * 576 * act + T * 8 + T * rb
+    H_att = H
+    if getattr(cfg, "q_prep", False):  # the fused insert also reads the raw queries and writes the padded ones
+        H_att = cfg.H_pad
+        b["insert"] += T * H * 576 * act + T * H_att * 576 * act
     if cfg.ratio:
         coff = cfg.coff
         sw = 2 * coff * 576 * 4
@@ -126,7 +130,7 @@ def algorithmic_bytes(st, topk_idx=None):
             else:
                 rows += (p_last + 1) // cfg.ratio
     out_b = 4 if cfg.out_dtype == I.F32 else 2
-    b["attention"] = rows * rb + T * H * 576 * act + T * H * 512 * out_b + T * H * 4
+    b["attention"] = rows * rb + T * H_att * 576 * act + T * H_att * 512 * out_b + T * H_att * 4
     return b
 
 

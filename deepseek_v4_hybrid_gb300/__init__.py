@@ -36,6 +36,30 @@ def dsv4_kv_insert(kv_new, kv_dtype, slot_mapping, cache, cache_dtype, page_size
     _abi.check("dsv4_kv_insert", _lib.dsv4_kv_insert(p, _stream(stream)))
 
 
+def dsv4_qnorm_rope_kv_insert(q, q_out, act_dtype, kv_new, slot_mapping, cache, cache_dtype, page_size, positions,
+                              cos_sin, q_norm_weight=None, eps=1e-6, apply_q_norm=True, apply_q_rope=True,
+                              apply_kv_rope=True, stream=None, after_independent=False):
+    """Per-head RMSNorm + GPT-J RoPE of q[T, H, 576] into q_out[T, H_pad, 576] (heads >= H zero) and the
+    kv rows' RoPE + store into the paged SWA cache, in one launch (see include/dsv4.h)."""
+    T, H, _ = q.shape
+    p = _abi.make(_abi.QnormRopeKvInsertParams, q=_ptr(q), q_out=_ptr(q_out), H=H, H_pad=q_out.shape[1],
+                  q_norm_weight=_ptr(q_norm_weight), apply_q_norm=int(apply_q_norm), apply_q_rope=int(apply_q_rope),
+                  eps=eps, kv_new=_ptr(kv_new), slot_mapping=_ptr(slot_mapping), cache=_ptr(cache),
+                  cache_dtype=cache_dtype, page_size=page_size, num_pages=cache.shape[0],
+                  apply_kv_rope=int(apply_kv_rope), act_dtype=act_dtype, T=T, positions=_ptr(positions),
+                  cos_sin=_ptr(cos_sin), max_pos=0 if cos_sin is None else cos_sin.shape[0],
+                  after_independent=int(after_independent))
+    _abi.check("dsv4_qnorm_rope_kv_insert", _lib.dsv4_qnorm_rope_kv_insert(p, _stream(stream)))
+
+
+def dsv4_padded_num_q_heads(H, cache_dtype) -> int:
+    """Query heads the attention's q and output buffers hold for H heads with this cache dtype."""
+    n = int(_lib.dsv4_padded_num_q_heads(int(H), int(cache_dtype)))
+    if n < 0:
+        raise ValueError(f"no padded head count for H={H}, cache dtype {cache_dtype}")
+    return n
+
+
 def dsv4_compress_update(kv_score, positions, q_per_seq, ratio, coff, state, ape, norm_weight, eps, cos_sin,
                          main_cache, cache_dtype, block_table, page_size, stream=None, after_independent=False):
     """Compressor state store + fold of the new tokens (see include/dsv4.h)."""

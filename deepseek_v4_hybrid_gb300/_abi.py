@@ -24,6 +24,14 @@ class KvInsertParams(C.Structure):
                 ("cos_sin", vp), ("max_pos", i32), ("after_independent", i32)]
 
 
+class QnormRopeKvInsertParams(C.Structure):
+    _fields_ = [("struct_size", u32), ("q", vp), ("q_out", vp), ("H", i32), ("H_pad", i32), ("q_norm_weight", vp),
+                ("apply_q_norm", i32), ("apply_q_rope", i32), ("eps", f32), ("kv_new", vp), ("slot_mapping", vp),
+                ("cache", vp), ("cache_dtype", i32), ("page_size", i32), ("num_pages", i64),
+                ("apply_kv_rope", i32), ("act_dtype", i32), ("T", i32), ("positions", vp), ("cos_sin", vp),
+                ("max_pos", i32), ("after_independent", i32)]
+
+
 class CompressUpdateParams(C.Structure):
     _fields_ = [("struct_size", u32), ("kv_score", vp), ("positions", vp), ("T", i32), ("B", i32),
                 ("q_per_seq", i32), ("ratio", i32), ("coff", i32), ("state", vp), ("ape", vp),
@@ -52,7 +60,8 @@ class SparseMlaDecodeParams(C.Structure):
 
 EXPORTS = ["dsv4_kv_insert", "dsv4_compress_update", "dsv4_indexer_topk_workspace_bytes", "dsv4_indexer_topk",
            "dsv4_sparse_mla_decode_workspace_bytes", "dsv4_sparse_mla_decode", "dsv4_abi_version",
-           "dsv4_status_string", "dsv4_last_cuda_error", "dsv4_read_device_flags", "dsv4_indexer_topk_noalloc"]
+           "dsv4_status_string", "dsv4_last_cuda_error", "dsv4_read_device_flags", "dsv4_indexer_topk_noalloc",
+           "dsv4_qnorm_rope_kv_insert", "dsv4_padded_num_q_heads"]
 
 # bytes of the scratch array built into the library for dsv4_indexer_topk_noalloc
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -70,6 +79,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                            "python -m deepseek_v4_hybrid_gb300.build")
     lib = C.CDLL(path)
     for name, st in (("dsv4_kv_insert", KvInsertParams), ("dsv4_compress_update", CompressUpdateParams),
+                     ("dsv4_qnorm_rope_kv_insert", QnormRopeKvInsertParams),
                      ("dsv4_indexer_topk", IndexerTopkParams), ("dsv4_sparse_mla_decode", SparseMlaDecodeParams),
                      ("dsv4_indexer_topk_noalloc", IndexerTopkParams)):
         fn = getattr(lib, name)
@@ -80,6 +90,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [C.POINTER(st)]
         fn.restype = C.c_size_t
+    lib.dsv4_padded_num_q_heads.argtypes = [C.c_int, C.c_int]
+    lib.dsv4_padded_num_q_heads.restype = C.c_int
     lib.dsv4_abi_version.restype = C.c_int
     lib.dsv4_status_string.argtypes = [C.c_int]
     lib.dsv4_status_string.restype = C.c_char_p

@@ -77,6 +77,32 @@ int dsv4_kv_insert(const dsv4_kv_insert_params* p, dsv4_stream_t stream) {
   return cuda_status(launch_kv_insert(*p, (cudaStream_t)stream));
 }
 
+int dsv4_qnorm_rope_kv_insert(const dsv4_qnorm_rope_kv_insert_params* p, dsv4_stream_t stream) {
+  CHECK(p != nullptr && p->struct_size == sizeof(dsv4_qnorm_rope_kv_insert_params), DSV4_ERR_INVALID);
+  CHECK(p->T >= 0 && p->page_size > 0 && p->num_pages >= 0, DSV4_ERR_INVALID);
+  CHECK(p->H >= 1 && p->H_pad >= p->H && p->H_pad <= 1024, DSV4_ERR_INVALID);
+  CHECK(act_dtype(p->act_dtype), DSV4_ERR_UNSUPPORTED);
+  CHECK(latent_cache_dtype(p->cache_dtype), DSV4_ERR_UNSUPPORTED);
+  if (p->T == 0) return DSV4_OK;
+  CHECK(p->q && p->q_out && p->kv_new && p->slot_mapping && p->cache, DSV4_ERR_INVALID);
+  CHECK(aligned(p->q, 16) && aligned(p->q_out, 16) && aligned(p->kv_new, 8) && aligned(p->cache, 16) &&
+            aligned(p->slot_mapping, 8) && aligned(p->q_norm_weight, 4),
+        DSV4_ERR_INVALID);
+  const bool rope = p->apply_q_rope || p->apply_kv_rope;
+  CHECK(!rope || (p->positions != nullptr && p->cos_sin != nullptr && p->max_pos > 0), DSV4_ERR_INVALID);
+  // q_out is q itself (in place, same head count) or a separate buffer
+  const size_t esz = p->act_dtype == DSV4_F32 ? 4 : 2;
+  const uintptr_t q0 = reinterpret_cast<uintptr_t>(p->q), q1 = q0 + (size_t)p->T * p->H * D * esz;
+  const uintptr_t o0 = reinterpret_cast<uintptr_t>(p->q_out), o1 = o0 + (size_t)p->T * p->H_pad * D * esz;
+  CHECK((q0 == o0 && p->H_pad == p->H) || o1 <= q0 || q1 <= o0, DSV4_ERR_INVALID);
+  return cuda_status(launch_qnorm_rope_kv_insert(*p, (cudaStream_t)stream));
+}
+
+int dsv4_padded_num_q_heads(int H, int cache_dtype) {
+  if (H < 1 || !latent_cache_dtype(cache_dtype)) return -1;
+  return cache_dtype == DSV4_F32 ? H : (H + 63) / 64 * 64;
+}
+
 int dsv4_compress_update(const dsv4_compress_update_params* p, dsv4_stream_t stream) {
   CHECK(p != nullptr && p->struct_size == sizeof(dsv4_compress_update_params), DSV4_ERR_INVALID);
   CHECK(p->B >= 0 && p->q_per_seq >= 1 && p->q_per_seq <= DSV4_MAX_Q_PER_SEQ, DSV4_ERR_INVALID);

@@ -12,6 +12,7 @@
 namespace dsv4 {
 
 cudaError_t launch_kv_insert(const dsv4_kv_insert_params& p, cudaStream_t s);
+cudaError_t launch_qnorm_rope_kv_insert(const dsv4_qnorm_rope_kv_insert_params& p, cudaStream_t s);
 cudaError_t launch_compress_update(const dsv4_compress_update_params& p, cudaStream_t s);
 
 size_t indexer_topk_workspace(const dsv4_indexer_topk_params& p);

@@ -62,6 +62,150 @@ __global__ void __launch_bounds__(ROW_THREADS) kv_insert_kernel(dsv4_kv_insert_p
   if (p.after_independent) pdl_wait();  // completes only after the kernel before it
 }
 
+// ------------------------------------------------------------------------------------------------
+// Fused query preparation + KV insert.  CTA (t, y): for y < ceil(H_pad / 8) warp w < 8 prepares
+// query head 8 y + w of token t; CTA (t, ngroups) stores the token's kv row (kv_insert_body).  A
+// warp holds its head in registers: with 16-byte vectors of E elements (8 bf16 or 4 fp32), lane l
+// takes no-pe vectors l + 32 v (512 / E / 32 of them) and, when l < 64 / E, rope vector 512 / E + l,
+// whose GPT-J pairs lie inside it.  All loads come before any store, so q_out may be q itself.
+// ------------------------------------------------------------------------------------------------
+constexpr int QP_HEADS = 8;
+
+template <bool BF>
+struct QVec {
+  static constexpr int E = BF ? 8 : 4;  // elements per 16-byte vector
+  static __device__ __forceinline__ void load(const uint8_t* src, int vec, float (&x)[E]) {
+    const uint4 u = reinterpret_cast<const uint4*>(src)[vec];
+    if (BF) {
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        x[2 * k] = __uint_as_float(w[k] << 16);
+        x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+    } else {
+      x[0] = __uint_as_float(u.x);
+      x[1] = __uint_as_float(u.y);
+      x[2] = __uint_as_float(u.z);
+      x[3] = __uint_as_float(u.w);
+    }
+  }
+  static __device__ __forceinline__ void store(uint8_t* dst, int vec, const float (&x)[E]) {
+    uint4 u;
+    if (BF) {
+      u = make_uint4(float2_to_bf16x2_bits(x[0], x[1]), float2_to_bf16x2_bits(x[2], x[3]),
+                     float2_to_bf16x2_bits(x[4], x[5]), float2_to_bf16x2_bits(x[6], x[7]));
+    } else {
+      u = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
+    }
+    reinterpret_cast<uint4*>(dst)[vec] = u;
+  }
+};
+
+// One query head (576 elements at src) -> dst, by one warp.  cs: the cos/sin row of the token's
+// position, or nullptr for no RoPE; w: the RMSNorm weight or nullptr (= 1).
+template <bool BF>
+__device__ __forceinline__ void qprep_head(const uint8_t* src, uint8_t* dst, bool norm, const float* w, float eps,
+                                           const float* cs, int lane) {
+  using V = QVec<BF>;
+  constexpr int E = V::E, NV = D_NOPE / E / 32, RV = D_ROPE / E;
+  float x[NV][E], r[E];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) V::load(src, lane + 32 * v, x[v]);
+  const bool rl = lane < RV;
+  if (rl) V::load(src, D_NOPE / E + lane, r);
+  float ss = 0.f;
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(x[v][e], x[v][e], ss);
+  if (rl)
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(r[e], r[e], ss);
+  if (norm) {
+    const float inv = 1.0f / sqrtf(warp_sum(ss) / (float)D + eps);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int d0 = (lane + 32 * v) * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[v][e] *= inv * (w ? __ldg(w + d0 + e) : 1.f);
+    }
+    if (rl) {
+      const int d0 = D_NOPE + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) r[e] *= inv * (w ? __ldg(w + d0 + e) : 1.f);
+    }
+  }
+  if (rl && cs != nullptr) {
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) {
+      const int pr = lane * (E / 2) + k;  // GPT-J pair of dims 512 + 2 pr, 512 + 2 pr + 1
+      const float c = __ldg(cs + pr), s = __ldg(cs + 32 + pr);
+      const float y0 = r[2 * k] * c - r[2 * k + 1] * s;
+      const float y1 = r[2 * k] * s + r[2 * k + 1] * c;
+      r[2 * k] = y0;
+      r[2 * k + 1] = y1;
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < NV; ++v) V::store(dst, lane + 32 * v, x[v]);
+  if (rl) V::store(dst, D_NOPE / E + lane, r);
+}
+
+__global__ void __launch_bounds__(ROW_THREADS) qnorm_rope_kv_insert_kernel(dsv4_qnorm_rope_kv_insert_params p) {
+  pdl_launch_dependents();
+  if (!p.after_independent) pdl_wait();
+  const int t = blockIdx.x, y = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngroups = (p.H_pad + QP_HEADS - 1) / QP_HEADS;
+  if (y < ngroups) {
+    const int h = y * QP_HEADS + warp;
+    if (warp < QP_HEADS && h < p.H_pad) {
+      const int esz = p.act_dtype == DSV4_F32 ? 4 : 2;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.q_out) + ((int64_t)t * p.H_pad + h) * D * esz;
+      if (h >= p.H) {  // padding head: zeros
+        for (int v = lane; v < D * esz / 16; v += 32) reinterpret_cast<uint4*>(dst)[v] = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) + ((int64_t)t * p.H + h) * D * esz;
+        const float* cs = nullptr;
+        if (p.apply_q_rope) {
+          int pos = p.positions[t];
+          if (pos < 0 || pos >= p.max_pos) {
+            if (lane == 0) atomicOr(&g_flags_ic, FLAG_PAGE);
+            pos = 0;
+          }
+          cs = p.cos_sin + (int64_t)pos * 64;
+        }
+        if (p.act_dtype == DSV4_F32)
+          qprep_head<false>(src, dst, p.apply_q_norm != 0, p.q_norm_weight, p.eps, cs, lane);
+        else
+          qprep_head<true>(src, dst, p.apply_q_norm != 0, p.q_norm_weight, p.eps, cs, lane);
+      }
+    }
+  } else {
+    dsv4_kv_insert_params k;
+    k.struct_size = sizeof(k);
+    k.kv_new = p.kv_new;
+    k.kv_dtype = p.act_dtype;
+    k.slot_mapping = p.slot_mapping;
+    k.cache = p.cache;
+    k.cache_dtype = p.cache_dtype;
+    k.T = p.T;
+    k.page_size = p.page_size;
+    k.num_pages = p.num_pages;
+    k.positions = p.positions;
+    k.cos_sin = p.apply_kv_rope ? p.cos_sin : nullptr;
+    k.max_pos = p.max_pos;
+    k.after_independent = p.after_independent;
+    kv_insert_body(k);
+  }
+  if (p.after_independent) pdl_wait();  // completes only after the kernel before it
+}
+
+cudaError_t launch_qnorm_rope_kv_insert(const dsv4_qnorm_rope_kv_insert_params& p, cudaStream_t s) {
+  if (p.T == 0) return cudaSuccess;
+  const int ngroups = (p.H_pad + QP_HEADS - 1) / QP_HEADS;
+  return launch_pdl(qnorm_rope_kv_insert_kernel, dim3(p.T, ngroups + 1), dim3(ROW_THREADS), 0, s, true, p);
+}
 
 // What finishing entry j of sequence b needs, loaded before the fold so that it costs no extra
 // round trip: the RMSNorm weight pair of thread i, its cos/sin pair (rope threads) at position

@@ -10,8 +10,8 @@ import numpy as np
 import torch
 
 from . import (BF16, F32, dsv4_compress_update, dsv4_indexer_topk, dsv4_indexer_topk_workspace_bytes,
-               dsv4_kv_insert, dsv4_sparse_mla_decode, dsv4_sparse_mla_decode_workspace_bytes, indexer_topk_params,
-               sparse_mla_params, _abi)
+               dsv4_kv_insert, dsv4_padded_num_q_heads, dsv4_qnorm_rope_kv_insert, dsv4_sparse_mla_decode,
+               dsv4_sparse_mla_decode_workspace_bytes, indexer_topk_params, sparse_mla_params, _abi)
 
 PAGE = 64
 WINDOW = 128
@@ -44,16 +44,29 @@ class DeviceStep:
         self.slot_mapping = dev(st.slot_mapping.astype(np.int64))
         self.swa_cache = dev(st.swa_cache)
         self.swa_bt = dev(st.swa_bt)
-        self.q = dev(st.q)
-        self.sink = dev(st.sink)
         self.max_context = int(st.ctx_len.max())
         T, H = cfg.T, cfg.H
+        # with query preparation, the fused insert turns the raw queries q_in [T, H, 576] into the
+        # attention's q [T, H_pad, 576]; the sink of the padding heads is -inf
+        self.q_prep = bool(getattr(cfg, "q_prep", False))
+        self.H_pad = dsv4_padded_num_q_heads(H, cfg.cache_dtype) if self.q_prep else H
+        self.cos_sin = dev(st.cos_sin)
+        if self.q_prep:
+            self.q_in = dev(st.q)
+            self.q = torch.empty((T, self.H_pad, 576), dtype=self.q_in.dtype, device=device)
+            self.q_norm_w = dev(st.q_norm_w)
+            sink = np.full(self.H_pad, -np.inf, np.float32)
+            sink[:H] = st.sink
+            self.sink = dev(sink)
+        else:
+            self.q = dev(st.q)
+            self.sink = dev(st.sink)
         odt = torch.float32 if cfg.out_dtype == F32 else torch.bfloat16
-        self.out = torch.empty((T, H, 512), dtype=odt, device=device)
-        self.lse = torch.empty((T, H), dtype=torch.float32, device=device)
+        self.out = torch.empty((T, self.H_pad, 512), dtype=odt, device=device)
+        self.lse = torch.empty((T, self.H_pad), dtype=torch.float32, device=device)
         self.has_compress = cfg.ratio > 0
         self.has_indexer = cfg.ratio > 0 and cfg.topk > 0
-        self.kv_score = self.state = self.ape = self.norm_w = self.cos_sin = None
+        self.kv_score = self.state = self.ape = self.norm_w = None
         self.main_cache = self.main_bt = None
         self.q_idx = self.w_idx = None
         if self.has_compress:
@@ -61,7 +74,6 @@ class DeviceStep:
             self.state = dev(st.state)
             self.ape = dev(st.ape)
             self.norm_w = dev(st.norm_w)
-            self.cos_sin = dev(st.cos_sin)
             self.main_cache = dev(st.main_cache)
             self.main_bt = dev(st.main_bt)
         self.topk_idx = None
@@ -93,8 +105,14 @@ class DeviceStep:
         self.eps = st.eps
 
     def insert(self, stream=None, after_independent=False):
-        dsv4_kv_insert(self.kv_new, self.cfg.act_dtype, self.slot_mapping, self.swa_cache, self.cfg.cache_dtype,
-                       PAGE, stream=stream, after_independent=after_independent)
+        if self.q_prep:
+            dsv4_qnorm_rope_kv_insert(self.q_in, self.q, self.cfg.act_dtype, self.kv_new, self.slot_mapping,
+                                      self.swa_cache, self.cfg.cache_dtype, PAGE, self.positions, self.cos_sin,
+                                      q_norm_weight=self.q_norm_w, eps=self.eps, stream=stream,
+                                      after_independent=after_independent)
+        else:
+            dsv4_kv_insert(self.kv_new, self.cfg.act_dtype, self.slot_mapping, self.swa_cache, self.cfg.cache_dtype,
+                           PAGE, stream=stream, after_independent=after_independent)
 
     def compress(self, stream=None, after_independent=False):
         if self.has_compress:
@@ -127,4 +145,8 @@ class DeviceStep:
         self.attention(stream)
 
     def step_input_tensors(self):
-        return {k: getattr(self, k) for k in self.STEP_INPUTS if getattr(self, k, None) is not None}
+        """The tensors a caller fills every step (the raw queries under the name "q")."""
+        d = {k: getattr(self, k) for k in self.STEP_INPUTS if getattr(self, k, None) is not None}
+        if self.q_prep:
+            d["q"] = self.q_in
+        return d

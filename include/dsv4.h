@@ -112,6 +112,51 @@ typedef struct dsv4_kv_insert_params {
 int dsv4_kv_insert(const dsv4_kv_insert_params* p, dsv4_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * dsv4_qnorm_rope_kv_insert: the query heads made ready for the attention and the new KV rows
+ * stored, in one launch (MAP "Phase 2", default stream, item 2: per-head RMSNorm of every query
+ * head, GPT-J RoPE of the last 64 dims of each query head and of kv, kv stored into the SWA cache;
+ * API DeepseekV4Attention._fused_qnorm_rope_kv_insert: the query zero-padded to the padded head
+ * count the attention backend allocates, see dsv4_padded_num_q_heads).
+ * For token t at position p = positions[t] and head h < H:
+ *   x = q[t][h];  if apply_q_norm: x = x / sqrt(mean(x^2) + eps) * q_norm_weight  (over 576 dims,
+ *   fp32);  if apply_q_rope: dims 512..575 of x turned by GPT-J RoPE with cos_sin[p];
+ *   q_out[t][h] = x in act_dtype (bf16: round to nearest even);  q_out[t][h] = 0 for H <= h < H_pad.
+ * and kv_new[t] is stored at slot_mapping[t] exactly as dsv4_kv_insert does (RoPE at p when
+ * apply_kv_rope).
+ * ------------------------------------------------------------------------------------------- */
+typedef struct dsv4_qnorm_rope_kv_insert_params {
+  uint32_t struct_size;
+  const void* q;               /* [T, H, 576] in act_dtype, 16-byte aligned */
+  void* q_out;                 /* [T, H_pad, 576] in act_dtype, 16-byte aligned; may be q itself only
+                                  when H_pad == H (in place), else must not overlap q */
+  int32_t H, H_pad;            /* 1 <= H <= H_pad <= 1024 */
+  const float* q_norm_weight;  /* [576] per-channel weight of the query RMSNorm, or NULL (= 1) */
+  int32_t apply_q_norm, apply_q_rope;
+  float eps;
+  const void* kv_new;          /* [T, 576] in act_dtype */
+  const int64_t* slot_mapping; /* [T] SWA slot = page * page_size + offset; -1 skips the token's kv */
+  void* cache;                 /* [num_pages, page_size, row] in cache_dtype (F32, BF16, FP8_DS_MLA) */
+  int32_t cache_dtype;
+  int32_t page_size;
+  int64_t num_pages;
+  int32_t apply_kv_rope;
+  int32_t act_dtype;           /* DSV4_F32 or DSV4_BF16: q, q_out and kv_new */
+  int32_t T;                   /* tokens, >= 0 */
+  const int32_t* positions;    /* [T] (read when some RoPE is applied; outside [0, max_pos) is flagged) */
+  const float* cos_sin;        /* [max_pos, 64] (32 cos | 32 sin, GPT-J pairs); needed for any RoPE */
+  int32_t max_pos;
+  int32_t after_independent;   /* as in dsv4_kv_insert_params */
+} dsv4_qnorm_rope_kv_insert_params;
+
+int dsv4_qnorm_rope_kv_insert(const dsv4_qnorm_rope_kv_insert_params* p, dsv4_stream_t stream);
+
+/* Query heads the attention's q and output buffers must hold for H real heads with caches of
+ * cache_dtype (API get_padded_num_q_heads): the tensor-core attention of bf16 and fp8_ds_mla caches
+ * takes heads in groups of 64, so H rounded up to 64; fp32 caches take H as it is.  A pure host
+ * function; returns -1 for H < 1 or an unknown dtype. */
+int dsv4_padded_num_q_heads(int H, int cache_dtype);
+
+/* ---------------------------------------------------------------------------------------------
  * dsv4_compress_update: compressor state store and fold (MAP "What Are the Gate Scores?",
  * "How Does Compression Actually Work?", "Phase 2" compressor stream items 1-4).
  * For each sequence, for each of its new tokens in position order:

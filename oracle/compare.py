@@ -67,14 +67,37 @@ def topk_sets_match(gpu_idx, oracle_scores, k):
     return bool(all(abs(float(s[j]) - float(kth)) <= TIE_EPS for j in diff)), False
 
 
+def q_out_ok(stored_gpu, stored_oracle, act_dtype):
+    """Prepared query heads: padding heads exactly zero; the others within one unit in the last place
+    of the activation format (the device normalises in fp32, the oracle in fp64) plus 1e-6 of the
+    head's largest value."""
+    g = O.decode_rows(stored_gpu, act_dtype)
+    o = O.decode_rows(stored_oracle, act_dtype)
+    rel = 2.0 ** -7 if act_dtype == O.BF16 else 1e-5
+    amax = np.max(np.abs(o), axis=-1, keepdims=True)
+    return bool(np.all(np.abs(g - o) <= rel * np.abs(o) + 1e-6 * amax))
+
+
 def check_step(st, res, gpu, where=""):
     """Asserts parity of every device result in `gpu` (numpy arrays) with the oracle's `res`.
     Returns a small report dict."""
     cfg = st.cfg
     rep = {"tokens": len(res["tokens"]), "max_rel_err": 0.0, "tie_tokens": 0}
-    # a1: inserted SWA rows, bit-exact
+    # a1: inserted SWA rows (rotated in fp32 when the insert applies RoPE: within one storage ulp of the
+    # oracle's row, else bit-exact)
+    rotated = bool(getattr(cfg, "q_prep", False))
     for (page, off), row in res["swa_written"].items():
-        assert np.array_equal(gpu["swa_cache"][page, off], row), f"{where} SWA row {(page, off)}"
+        if rotated:
+            ok, _ = entry_error_ok(gpu["swa_cache"][page, off], O.decode_rows(row, cfg.cache_dtype), cfg.cache_dtype)
+            assert ok, f"{where} SWA row {(page, off)}"
+        else:
+            assert np.array_equal(gpu["swa_cache"][page, off], row), f"{where} SWA row {(page, off)}"
+    # the prepared queries
+    for t, qo in res.get("q_out", {}).items():
+        if "q_out" in gpu:
+            H = cfg.H
+            assert np.all(O.decode_rows(gpu["q_out"][t][H:], cfg.act_dtype) == 0.0), f"{where} padded heads of {t}"
+            assert q_out_ok(gpu["q_out"][t][:H], qo[:H], cfg.act_dtype), f"{where} prepared query of token {t}"
     if cfg.ratio:
         # a2: fp32 state ring, bit-exact; emitted entries within one storage ulp
         for b, stb in res["state"].items():
@@ -100,12 +123,13 @@ def check_step(st, res, gpu, where=""):
     for t in res["tokens"]:
         if same_sel.get(t, True) is False:
             continue  # a near-tie changed the selected rows: attention is checked on given selections
-        ref, out = res["out"][t], gpu["out"][t].astype(np.float64)
+        ref = res["out"][t]
+        out = gpu["out"][t][:ref.shape[0]].astype(np.float64)  # the padding heads are not compared
         amax = float(np.max(np.abs(ref)))
         err = float(np.max(np.abs(out - ref)))
         rep["max_rel_err"] = max(rep["max_rel_err"], err / amax)
         assert err <= tol * amax, f"{where} attention of token {t}: err {err:.3e} vs {tol} * {amax:.3e}"
         if "lse" in gpu:
-            lerr = float(np.max(np.abs(gpu["lse"][t] - res["lse"][t])))
+            lerr = float(np.max(np.abs(gpu["lse"][t][:ref.shape[0]] - res["lse"][t])))
             assert lerr <= (1e-5 if cfg.cache_dtype == O.F32 else 2e-3), f"{where} lse of token {t}: {lerr:.3e}"
     return rep

@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(abi):
     names = declared_functions()
-    assert len(names) == 11
+    assert len(names) == 13
     out = subprocess.run(["nm", "-D", "--defined-only", abi.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (dsv4_\w+)", out))
     assert set(names) <= exported, set(names) - exported
@@ -39,6 +39,7 @@ def test_exports_every_declared_symbol(abi):
 def test_struct_layout_matches_header(abi, tmp_path):
     """Compile a C program that prints sizeof/offsetof of every field and compare with ctypes."""
     structs = {"dsv4_kv_insert_params": abi.KvInsertParams, "dsv4_compress_update_params": abi.CompressUpdateParams,
+               "dsv4_qnorm_rope_kv_insert_params": abi.QnormRopeKvInsertParams,
                "dsv4_indexer_topk_params": abi.IndexerTopkParams,
                "dsv4_sparse_mla_decode_params": abi.SparseMlaDecodeParams}
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', 'int main(void){']
@@ -72,6 +73,24 @@ def test_host_validation_rejects_bad_arguments(abi):
     p = abi.make(abi.KvInsertParams, T=2, page_size=64, kv_dtype=abi.BF16, cache_dtype=abi.BF16, kv_new=0x1001,
                  slot_mapping=0x1000, cache=0x1000)
     assert lib.dsv4_kv_insert(p, None) == abi.ERR_INVALID             # misaligned kv_new
+
+    qp = abi.make(abi.QnormRopeKvInsertParams, T=2, H=64, H_pad=64, page_size=64, act_dtype=abi.BF16,
+                  cache_dtype=abi.BF16)
+    assert lib.dsv4_qnorm_rope_kv_insert(qp, None) == abi.ERR_INVALID   # null pointers
+    for k in ("q", "kv_new", "slot_mapping", "cache"):
+        setattr(qp, k, 0x100000)
+    qp.q_out = 0x100000 + 64 * 576 * 2                                  # overlaps q, different layout
+    assert lib.dsv4_qnorm_rope_kv_insert(qp, None) == abi.ERR_INVALID
+    qp.H_pad = 32
+    assert lib.dsv4_qnorm_rope_kv_insert(qp, None) == abi.ERR_INVALID   # H_pad < H
+    qp.H_pad, qp.q_out, qp.apply_q_rope = 64, 0x100000, 1
+    assert lib.dsv4_qnorm_rope_kv_insert(qp, None) == abi.ERR_INVALID   # RoPE without a table
+    qp.apply_q_rope, qp.act_dtype = 0, abi.FP8_DS_MLA
+    assert lib.dsv4_qnorm_rope_kv_insert(qp, None) == abi.ERR_UNSUPPORTED
+    assert lib.dsv4_padded_num_q_heads(32, abi.BF16) == 64
+    assert lib.dsv4_padded_num_q_heads(64, abi.FP8_DS_MLA) == 64
+    assert lib.dsv4_padded_num_q_heads(16, abi.F32) == 16
+    assert lib.dsv4_padded_num_q_heads(0, abi.BF16) == -1
 
     c = abi.make(abi.CompressUpdateParams, T=2, B=1, q_per_seq=2, ratio=8, coff=1, page_size=64,
                  max_pages_per_seq=1, max_pos=10, cache_dtype=abi.BF16)

@@ -32,6 +32,8 @@ def gpu_results(ds):
     g = {"swa_cache": to_host(ds.swa_cache), "out": to_host(ds.out), "lse": to_host(ds.lse)}
     if g["out"].dtype == np.uint16:
         g["out"] = O.bf16_decode(g["out"])
+    if ds.q_prep:
+        g["q_out"] = to_host(ds.q)
     if ds.has_compress:
         g["state"] = to_host(ds.state)
         g["main_cache"] = to_host(ds.main_cache)
@@ -180,3 +182,53 @@ def test_fp8_block_exponents_on_both_scaling_paths(lib):
     for t in res["tokens"]:
         ref = np.asarray(res["lse"][t], np.float64)
         assert np.all(np.abs(lse[t] - ref) <= 2e-3 + 2.0 ** -14 * np.abs(ref)), f"lse of token {t}"
+
+
+@pytest.mark.parametrize("name", ["small_c4_bf16", "small_c4_fp8", "small_c4_f32"])
+def test_kv_insert_with_rope(lib, name):
+    """dsv4_kv_insert with a rotary table: each new row's dims 512..575 turned at its position, then
+    encoded into the SWA cache (oracle kv_insert with positions and cos_sin)."""
+    import deepseek_v4_hybrid_gb300 as M
+    from deepseek_v4_hybrid_gb300.step import to_device
+    st = I.make_step(I.SMALL_CONFIGS[name])
+    cfg = st.cfg
+    cache = to_device(st.swa_cache, "cuda")
+    M.dsv4_kv_insert(to_device(st.kv_new, "cuda"), cfg.act_dtype, to_device(st.slot_mapping.astype(np.int64), "cuda"),
+                     cache, cfg.cache_dtype, 64, positions=to_device(st.positions.astype(np.int32), "cuda"),
+                     cos_sin=to_device(st.cos_sin, "cuda"))
+    torch.cuda.synchronize()
+    assert M.dsv4_read_device_flags() == 0
+    swa = O.Paged(st.swa_cache)
+    O.kv_insert(swa, st.kv_new, cfg.act_dtype, st.slot_mapping, cfg.cache_dtype, st.positions, st.cos_sin)
+    got = to_host(cache)
+    assert len(swa.written) == cfg.T
+    for (page, off), row in swa.written.items():
+        ok, _ = CMP.entry_error_ok(got[page, off], O.decode_rows(row, cfg.cache_dtype), cfg.cache_dtype)
+        assert ok, (page, off)
+
+
+def test_qprep_in_place_and_without_switches(lib):
+    """The fused call with q_out = q (same head count) gives what it gives into a separate buffer, and
+    with every switch off it copies the heads and zero-pads."""
+    import deepseek_v4_hybrid_gb300 as M
+    from deepseek_v4_hybrid_gb300.step import to_device
+    st = I.make_step(I.SMALL_CONFIGS["small_c4_bf16"])
+    cfg = st.cfg
+    dev = lambda a: to_device(a, "cuda")  # noqa: E731
+    q = dev(st.q)
+    slots = dev(np.full(cfg.T, -1, np.int64))            # no kv stored
+    cache = dev(st.swa_cache)
+    sep = torch.empty_like(q)
+    args = (cfg.act_dtype, dev(st.kv_new), slots, cache, cfg.cache_dtype, 64, dev(st.positions.astype(np.int32)),
+            dev(st.cos_sin))
+    M.dsv4_qnorm_rope_kv_insert(q, sep, *args, q_norm_weight=dev(st.q_norm_w))
+    M.dsv4_qnorm_rope_kv_insert(q, q, *args, q_norm_weight=dev(st.q_norm_w))
+    torch.cuda.synchronize()
+    assert torch.equal(q.view(torch.int16), sep.view(torch.int16))
+    padded = torch.empty((cfg.T, 96, 576), dtype=torch.bfloat16, device="cuda")
+    q0 = dev(st.q)
+    M.dsv4_qnorm_rope_kv_insert(q0, padded, *args, apply_q_norm=False, apply_q_rope=False, apply_kv_rope=False)
+    torch.cuda.synchronize()
+    assert M.dsv4_read_device_flags() == 0
+    assert torch.equal(padded[:, :cfg.H].view(torch.int16), q0.view(torch.int16))
+    assert torch.count_nonzero(padded[:, cfg.H:].float()) == 0
