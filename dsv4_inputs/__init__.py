@@ -17,8 +17,8 @@ Workload shapes follow the five decode configurations of the hot path:
 plus small variants (``small_*``) of the same dtypes and head counts that the
 oracle finishes in seconds while still spanning several tiles and ragged tails.
 
-Value recipe: q, kv_new, indexer queries, cache rows ~ N(0,1)*0.1; query RMSNorm weight
-1 + N(0,1)*0.1; kv_score
+Value recipe: q, kv_new, indexer queries, cache rows ~ N(0,1)*0.1; query and index-key RMSNorm
+weights 1 + N(0,1)*0.1; latent -> index key projection N(0,1)*0.1 (bf16); kv_score
 ~ N(0,1); indexer weights ~ N(0,1)*0.1; RMSNorm weight 1 + N(0,1)*0.1; APE
 ~ N(0,1)*0.1; sink ~ N(0,1); RoPE table theta = 10000.  Large bf16 buffers are
 drawn by inverse-CDF lookup: a uniform 16-bit integer indexes a table of the
@@ -65,6 +65,7 @@ class Config:
     seed: int = 0xD5E4
     explicit_lens: tuple = ()
     q_prep: bool = True   # queries arrive un-normed and un-rotated: the fused insert norms, rotates and pads them
+    ik_store: bool = True  # the compressor also writes each new entry's index key (CSA layers with an indexer)
 
     @property
     def T(self) -> int:
@@ -235,6 +236,8 @@ class StepInputs:
     sink: np.ndarray             # [H] f32
     softmax_scale: float
     q_norm_w: np.ndarray = None  # [D] f32 per-channel weight of the per-head query RMSNorm
+    wk: np.ndarray = None        # [d_I, D] bf16 bits: latent -> index key projection (CSA layers)
+    ik_norm_w: np.ndarray = None # [d_I] f32 weight of the index key's RMSNorm
     cos_sin: np.ndarray = None   # [max_pos, 64] f32: 32 cos | 32 sin (RoPE of q, kv and compressed entries)
     kv_score: np.ndarray = None  # [T, 2*coff*D] f32
     state: np.ndarray = None     # [B, coff*ratio, 2*coff*D] f32
@@ -337,6 +340,9 @@ def make_step(cfg: Config, with_given_topk: bool = True) -> StepInputs:
             (idx_pages, PAGE) + ir_shape)
         st.q_idx = draw.act("q_idx", (T, cfg.I_h, cfg.d_I), cfg.act_dtype)
         st.w_idx = draw.normal_f32("w_idx", (T, cfg.I_h), 0.1)
+        if cfg.ik_store:
+            st.wk = draw.bf16("wk", (cfg.d_I, D))
+            st.ik_norm_w = draw.normal_f32("ik_norm_w", (cfg.d_I,), 0.1, 1.0)
 
     if cfg.topk > 0 and with_given_topk:
         # an arbitrary valid selection (distinct visible indices, ascending, -1 padded) for attention-only cases

@@ -353,25 +353,59 @@ def fold_entry(kv: np.ndarray, sc: np.ndarray) -> np.ndarray:
     return (w * kv).sum(axis=0)
 
 
+def entry_latent(state_b, j, ratio, coff, norm_w, eps) -> np.ndarray:
+    """The compressor's latent of entry j: fold, then RMSNorm * weight, before the RoPE ([MAP] "How
+    Does Compression Actually Work?", steps 1-4)."""
+    kv, sc = fold_group(state_b, j, ratio, coff)
+    return rms_norm(fold_entry(kv, sc), norm_w, eps)
+
+
 def compressed_entry(state_b, j, ratio, coff, norm_w, eps, cos_sin) -> np.ndarray:
     """Value of compressed entry j before encoding: fold, RMSNorm * weight, GPT-J RoPE of the last
     64 dims at position j*ratio ([MAP] "How Does Compression Actually Work?", steps 1-5)."""
-    kv, sc = fold_group(state_b, j, ratio, coff)
-    e = rms_norm(fold_entry(kv, sc), norm_w, eps)
+    e = entry_latent(state_b, j, ratio, coff, norm_w, eps)
     cs = np.asarray(cos_sin[j * ratio], np.float64)
     e[D_NOPE:] = rope_gptj(e[D_NOPE:], cs[:32], cs[32:])
     return e
 
 
+def index_key(latent, wk, kn_w, eps, cos_sin, pos: int) -> np.ndarray:
+    """Index key of a compressed entry ([API] DeepseekV4Indexer (V4.1): the index key is derived from
+    the compressor's latent, k = k_norm(wk(latent)); _produce_k: at group-boundary tokens, RoPE'd at
+    the group position, then quantised into the indexer K cache; wk maps the main compressor's
+    pre-RoPE latent to index keys).  latent [576] (entry_latent), wk [d, 576], kn_w [d]: k = wk latent,
+    RMSNorm over its d dims times kn_w, then GPT-J RoPE of its last 64 dims at `pos` (reading: the
+    key's rope dims are its last 64, as in the latent)."""
+    k = np.asarray(wk, np.float64) @ np.asarray(latent, np.float64)
+    k = rms_norm(k, kn_w, eps)
+    cs = np.asarray(cos_sin[int(pos)], np.float64)
+    k[-D_ROPE:] = rope_gptj(k[-D_ROPE:], cs[:32], cs[32:])
+    return k
+
+
+def encode_key(k, dtype: int) -> np.ndarray:
+    """One index key -> its stored form in indexer-cache format `dtype` (F32, BF16, I8_ROWSCALE)."""
+    if dtype == F32:
+        return np.asarray(k, np.float64).astype(np.float32)
+    if dtype == BF16:
+        return bf16_encode(k)
+    if dtype == I8_ROWSCALE:
+        return i8_rowscale_encode(np.asarray(k, np.float64).astype(np.float32))
+    raise ValueError(dtype)
+
+
 def compress_update(state, kv_score, positions, q_per_seq, ratio, coff, ape, norm_w, eps, cos_sin,
-                    main: Paged, main_bt, cache_dtype, seqs=None):
+                    main: Paged, main_bt, cache_dtype, seqs=None, ik=None):
     """Per sequence, per new token in position order: store the token's state row, and when the
     token completes a group, fold the group and store the encoded entry into the main cache row
-    j = p // ratio ([MAP] "Phase 2", compressor stream, items 1-4).
-    Returns (new state for the processed sequences {b: array}, {(b, j): entry value})."""
+    j = p // ratio ([MAP] "Phase 2", compressor stream, items 1-4).  With `ik` (a dict: wk, kn_w,
+    eps, cache: Paged, bt, dtype) the entry's index key (index_key, at the entry's RoPE position
+    j * ratio) is also stored into row j of the indexer cache.
+    Returns (new state for the processed sequences {b: array}, {(b, j): entry value},
+    {(b, j): index key value})."""
     B = state.shape[0]
     seqs = range(B) if seqs is None else seqs
-    new_state, entries = {}, {}
+    new_state, entries, keys = {}, {}, {}
     for b in seqs:
         st = np.array(state[b], np.float32, copy=True)
         for i in range(q_per_seq):
@@ -383,8 +417,13 @@ def compress_update(state, kv_score, positions, q_per_seq, ratio, coff, ape, nor
                 e = compressed_entry(st, j, ratio, coff, norm_w, eps, cos_sin)
                 entries[(b, j)] = e
                 main.put(main_bt[b][j // PAGE], j % PAGE, encode_row(e, cache_dtype))
+                if ik is not None:
+                    k = index_key(entry_latent(st, j, ratio, coff, norm_w, eps), ik["wk"], ik["kn_w"], ik["eps"],
+                                  cos_sin, j * ratio)
+                    keys[(b, j)] = k
+                    ik["cache"].put(ik["bt"][b][j // PAGE], j % PAGE, encode_key(k, ik["dtype"]))
         new_state[b] = st
-    return new_state, entries
+    return new_state, entries, keys
 
 
 # ----------------------------------------------------------------------------------------------
@@ -502,18 +541,24 @@ def decode_step(st, seqs=None, topk_override=None):
         q_att[t] = q_t
     res["q_out"] = q_out
     main = None
+    idx = Paged(st.idx_cache) if (cfg.ratio > 0 and cfg.topk > 0) else None
     if cfg.ratio > 0:
         main = Paged(st.main_cache)
-        new_state, entries = compress_update(st.state, st.kv_score, st.positions, qps, cfg.ratio, cfg.coff,
-                                             st.ape, st.norm_w, st.eps, st.cos_sin, main, st.main_bt,
-                                             cfg.cache_dtype, seqs=seqs)
+        ik = None
+        if idx is not None and getattr(st, "wk", None) is not None:  # the compressor also stores index keys
+            ik = {"wk": bf16_decode(st.wk), "kn_w": st.ik_norm_w, "eps": st.eps, "cache": idx, "bt": st.idx_bt,
+                  "dtype": cfg.idx_dtype}
+        new_state, entries, keys = compress_update(st.state, st.kv_score, st.positions, qps, cfg.ratio, cfg.coff,
+                                                   st.ape, st.norm_w, st.eps, st.cos_sin, main, st.main_bt,
+                                                   cfg.cache_dtype, seqs=seqs, ik=ik)
         res["state"] = new_state
         res["entries"] = entries
         res["main_written"] = dict(main.written)
+        res["keys"] = keys
+        res["idx_written"] = dict(idx.written) if idx is not None else {}
 
     topk, scores = {}, {}
     if cfg.ratio > 0 and cfg.topk > 0:
-        idx = Paged(st.idx_cache)
         for t in toks:
             b, p = t // qps, int(st.positions[t])
             nc = n_compressed(p, cfg.ratio)

@@ -212,3 +212,69 @@ def test_qnorm_invariants_and_switches():
     # neither switch: a copy, zero padded
     z = O.qnorm_rope(q, 5, table, None, 1e-6, False, False, 6)
     assert np.array_equal(z[:3], q) and np.all(z[3:] == 0.0)
+
+
+# ------------------------------------------------------------------------------------------------
+# index keys written by the compressor
+# ------------------------------------------------------------------------------------------------
+
+def scalar_index_key(latent, wk, kn_w, eps, table, pos):
+    """k = wk latent (fsum dot products), RMSNorm over its dims times kn_w, then its last 64 dims
+    turned pairwise as complex numbers by the rotary row of `pos`."""
+    d = len(wk)
+    k = [math.fsum(float(wk[o][c]) * float(latent[c]) for c in range(len(latent))) for o in range(d)]
+    inv = 1.0 / math.sqrt(math.fsum(x * x for x in k) / d + eps)
+    k = [k[o] * inv * float(kn_w[o]) for o in range(d)]
+    base = d - 64
+    for i in range(32):
+        z = complex(k[base + 2 * i], k[base + 2 * i + 1]) * complex(float(table[pos][i]), float(table[pos][32 + i]))
+        k[base + 2 * i], k[base + 2 * i + 1] = z.real, z.imag
+    return np.array(k)
+
+
+def scalar_latent(state_b, j, ratio, coff, gamma, eps):
+    """scalar_entry without its RoPE step: the fold, then RMSNorm times gamma."""
+    no_rope = np.zeros((j * ratio + 1, 64))
+    no_rope[:, :32] = 1.0                                   # cos 1, sin 0 at every position: identity
+    return scalar_entry(state_b, j, ratio, coff, gamma, eps, no_rope)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_index_key_matches_scalar_recomputation(d):
+    rng = np.random.default_rng(40 + d)
+    ratio, coff, j = 4, 2, 9
+    state_b = rng.standard_normal((coff * ratio, 2 * coff * D)).astype(np.float32)
+    gamma = (1.0 + 0.5 * rng.standard_normal(D)).astype(np.float32)
+    wk = rng.standard_normal((d, D)) * 0.05
+    kn_w = 1.0 + 0.5 * rng.standard_normal(d)
+    table = rotary_table(j * ratio + 1)
+    lat = scalar_latent(state_b, j, ratio, coff, gamma, 1e-6)
+    np.testing.assert_allclose(O.entry_latent(state_b, j, ratio, coff, gamma, 1e-6), lat, rtol=1e-12, atol=1e-12)
+    want = scalar_index_key(lat, wk, kn_w, 1e-6, table, j * ratio)
+    got = O.index_key(O.entry_latent(state_b, j, ratio, coff, gamma, 1e-6), wk, kn_w, 1e-6, table, j * ratio)
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("ctx", [300, 1024])
+def test_decode_step_scores_the_key_written_this_step(ctx):
+    """The indexer of the step sees the index key the compressor stored this step: the score of the
+    new entry j = p / 4 equals sum_h w_h ReLU(q_h . k) with k assembled by hand from the updated
+    state ring and stored as fp32 (the config's key dtype)."""
+    cfg = dataclasses.replace(I.CONFIGS["tiny_c4_f32"], name="pin_key", B=1, explicit_lens=(ctx,))
+    st = I.make_step(cfg)
+    st.cos_sin = rotary_table(ctx + 1).astype(np.float32)
+    p = ctx - 1
+    j_new = p // cfg.ratio
+    res = O.decode_step(st)
+    ring = np.array(st.state[0], np.float32, copy=True)
+    new_row = np.array(st.kv_score[0], np.float32, copy=True)
+    new_row[cfg.coff * D:] = (new_row[cfg.coff * D:] + st.ape[p % cfg.ratio]).astype(np.float32)
+    ring[p % (cfg.coff * cfg.ratio)] = new_row
+    lat = scalar_latent(ring, j_new, cfg.ratio, cfg.coff, st.norm_w, st.eps)
+    k = scalar_index_key(lat, O.bf16_decode(st.wk), st.ik_norm_w, st.eps, st.cos_sin, j_new * cfg.ratio)
+    k = k.astype(np.float32).astype(np.float64)
+    q = np.asarray(st.q_idx[0], np.float64)
+    want = math.fsum(float(st.w_idx[0][h]) * max(0.0, math.fsum(q[h] * k)) for h in range(cfg.I_h))
+    got = float(res["scores"][0][j_new])
+    assert abs(got - want) <= 1e-6 * max(1.0, abs(want))
+    assert np.array_equal(res["idx_written"][(st.idx_bt[0][j_new // 64], j_new % 64)], k.astype(np.float32))

@@ -444,15 +444,21 @@ def test_compress_update_emits_exactly_at_group_ends():
     bt = np.array([[1, 0]], np.int32)
     from dsv4_inputs import rope_table
     tab = rope_table(200)
-    emitted = []
+    emitted, keyed = [], []
+    idx = O.Paged(np.zeros((2, 64, 132), np.uint8))
+    ik = {"wk": rng.standard_normal((128, 576)) * 0.05, "kn_w": np.ones(128), "eps": 1e-6, "cache": idx,
+          "bt": np.array([[0, 1]], np.int32), "dtype": O.I8_ROWSCALE}
     for p in range(0, 23):
         ks = rng.standard_normal((1, 4 * 576)).astype(np.float32)
-        new_state, ent = O.compress_update(state, ks, np.array([p], np.int32), 1, ratio, coff, None,
-                                           np.ones(576, np.float32), 1e-6, tab, main, bt, O.F32)
+        new_state, ent, keys = O.compress_update(state, ks, np.array([p], np.int32), 1, ratio, coff, None,
+                                                 np.ones(576, np.float32), 1e-6, tab, main, bt, O.F32, ik=ik)
         state = new_state[0][None]
         emitted += list(ent.keys())
+        keyed += list(keys.keys())
     assert [j for (_, j) in emitted] == list(range(O.n_compressed(22, ratio)))
     assert set(main.written.keys()) == {(1, j) for j in range(5)}
+    assert keyed == emitted                                  # one index key per emitted entry
+    assert set(idx.written.keys()) == {(0, j) for j in range(5)}
 
 
 def test_kv_insert_slot_mapping_and_skip():
