@@ -109,6 +109,8 @@ def algorithmic_bytes(st, topk_idx=None):
         emit = [(int(p) + 1) % cfg.ratio == 0 for p in pos]
         fold_rows = cfg.ratio * coff
         b["compress"] = T * sw * 2 + sum(emit) * (fold_rows * sw // 1 + rb)
+        if cfg.topk and getattr(cfg, "ik_store", False):  # index keys: the projection once, one key row per entry
+            b["compress"] += cfg.d_I * 576 * 2 + sum(emit) * row_bytes(cfg.idx_dtype, cfg.d_I)
     if cfg.ratio and cfg.topk:
         ib = row_bytes(cfg.idx_dtype, cfg.d_I)
         nc_seq = (pos.reshape(cfg.B, qps)[:, -1] + 1) // cfg.ratio

@@ -61,8 +61,11 @@ def dsv4_padded_num_q_heads(H, cache_dtype) -> int:
 
 
 def dsv4_compress_update(kv_score, positions, q_per_seq, ratio, coff, state, ape, norm_weight, eps, cos_sin,
-                         main_cache, cache_dtype, block_table, page_size, stream=None, after_independent=False):
-    """Compressor state store + fold of the new tokens (see include/dsv4.h)."""
+                         main_cache, cache_dtype, block_table, page_size, stream=None, after_independent=False,
+                         wk=None, ik_norm_weight=None, ik_eps=1e-6, ik_cache=None, ik_dtype=BF16,
+                         ik_block_table=None):
+    """Compressor state store + fold of the new tokens, and (with wk) the index key of every new entry
+    into the indexer cache (see include/dsv4.h)."""
     T = positions.shape[0]
     p = _abi.make(_abi.CompressUpdateParams, kv_score=_ptr(kv_score), positions=_ptr(positions), T=T,
                   B=T // q_per_seq, q_per_seq=q_per_seq, ratio=ratio, coff=coff, state=_ptr(state), ape=_ptr(ape),
@@ -70,6 +73,10 @@ def dsv4_compress_update(kv_score, positions, q_per_seq, ratio, coff, state, ape
                   main_cache=_ptr(main_cache), cache_dtype=cache_dtype, page_size=page_size,
                   num_pages=main_cache.shape[0], block_table=_ptr(block_table),
                   max_pages_per_seq=block_table.shape[1], after_independent=int(after_independent))
+    if wk is not None:
+        p.wk, p.ik_norm_weight, p.ik_eps, p.ik_dim = _ptr(wk), _ptr(ik_norm_weight), ik_eps, wk.shape[0]
+        p.ik_cache, p.ik_dtype, p.ik_num_pages = _ptr(ik_cache), ik_dtype, ik_cache.shape[0]
+        p.ik_block_table, p.ik_max_pages = _ptr(ik_block_table), ik_block_table.shape[1]
     _abi.check("dsv4_compress_update", _lib.dsv4_compress_update(p, _stream(stream)))
 
 

@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libdsv4.so")
 F32, BF16, FP8_DS_MLA, I8_ROWSCALE = 0, 1, 2, 3
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_BOUNDS, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 LATENT_DIM, VALUE_DIM, ROPE_DIM, FP8_DS_MLA_BYTES = 576, 512, 64, 656
+ABI_VERSION = 2
 
 vp, i32, i64, u32, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint32, C.c_float
 
@@ -37,7 +38,9 @@ class CompressUpdateParams(C.Structure):
                 ("q_per_seq", i32), ("ratio", i32), ("coff", i32), ("state", vp), ("ape", vp),
                 ("norm_weight", vp), ("eps", f32), ("cos_sin", vp), ("max_pos", i32), ("main_cache", vp),
                 ("cache_dtype", i32), ("page_size", i32), ("num_pages", i64), ("block_table", vp),
-                ("max_pages_per_seq", i32), ("after_independent", i32)]
+                ("max_pages_per_seq", i32), ("after_independent", i32), ("wk", vp), ("ik_norm_weight", vp),
+                ("ik_eps", f32), ("ik_dim", i32), ("ik_cache", vp), ("ik_dtype", i32), ("ik_num_pages", i64),
+                ("ik_block_table", vp), ("ik_max_pages", i32)]
 
 
 class IndexerTopkParams(C.Structure):
@@ -98,7 +101,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.dsv4_last_cuda_error.restype = C.c_int
     lib.dsv4_read_device_flags.argtypes = [C.POINTER(u32)]
     lib.dsv4_read_device_flags.restype = C.c_int
-    if lib.dsv4_abi_version() != 1:
+    if lib.dsv4_abi_version() != ABI_VERSION:
         raise RuntimeError("libdsv4.so ABI version mismatch")
     _lib = lib
     return lib

@@ -119,6 +119,15 @@ int dsv4_compress_update(const dsv4_compress_update_params* p, dsv4_stream_t str
   CHECK(aligned(p->kv_score, 8) && aligned(p->state, 8) && aligned(p->norm_weight, 8) &&
             aligned(p->main_cache, 16) && (p->ape == nullptr || aligned(p->ape, 8)),
         DSV4_ERR_INVALID);
+  if (p->wk != nullptr) {
+    CHECK(p->ik_dim == 64 || p->ik_dim == 128, DSV4_ERR_UNSUPPORTED);
+    CHECK(p->ik_dtype == DSV4_F32 || p->ik_dtype == DSV4_BF16 || p->ik_dtype == DSV4_I8_ROWSCALE,
+          DSV4_ERR_UNSUPPORTED);
+    CHECK(p->ik_norm_weight && p->ik_cache && p->ik_block_table && p->ik_max_pages > 0 && p->ik_num_pages >= 0 &&
+              p->ik_eps >= 0.f,
+          DSV4_ERR_INVALID);
+    CHECK(aligned(p->wk, 4) && aligned(p->ik_norm_weight, 4) && aligned(p->ik_cache, 16), DSV4_ERR_INVALID);
+  }
   return cuda_status(launch_compress_update(*p, (cudaStream_t)stream));
 }
 

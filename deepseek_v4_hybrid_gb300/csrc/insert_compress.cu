@@ -239,10 +239,105 @@ __device__ __forceinline__ EntryCtx entry_prefetch(const dsv4_compress_update_pa
   return e;
 }
 
+// Index key of entry j (b, j) from its latent in shared memory (lat[576], the entry after its
+// RMSNorm and before its RoPE): k = wk lat, RMSNorm over ik_dim dims times ik_norm_weight, GPT-J
+// RoPE of the last 64 dims at position j * ratio, encoded into row j of the indexer cache.  All 288
+// threads: warp w computes outputs w, w + 9, ... (one 1152-byte wk row a time, read as bf16 pairs);
+// then thread i < ik_dim / 2 holds the pair (2i, 2i + 1).
+__device__ void index_key_store(const dsv4_compress_update_params& p, int b, int j, const float* lat, float* kk,
+                                float* red, int i) {
+  const int warp = i >> 5, lane = i & 31, d = p.ik_dim;
+  const uint32_t* wk = reinterpret_cast<const uint32_t*>(p.wk);
+  const float2* lat2 = reinterpret_cast<const float2*>(lat);
+  constexpr int U = D / 2 / 32;  // bf16 pairs of a wk row per lane (9)
+  constexpr int RPW = 8;         // wk rows a warp has in flight at once
+  float2 x[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) x[u] = lat2[lane + 32 * u];
+  for (int o0 = warp * RPW; o0 < d; o0 += (ROW_THREADS / 32) * RPW) {
+    uint32_t w[RPW][U];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        w[r][u] = o0 + r < d ? __ldg(wk + (int64_t)(o0 + r) * (D / 2) + lane + 32 * u) : 0u;
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+      float acc = 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        acc = fmaf(__uint_as_float(w[r][u] << 16), x[u].x, acc);
+        acc = fmaf(__uint_as_float(w[r][u] & 0xFFFF0000u), x[u].y, acc);
+      }
+      acc = warp_sum(acc);
+      if (lane == 0 && o0 + r < d) kk[o0 + r] = acc;
+    }
+  }
+  __syncthreads();
+  const bool own = i < d / 2;
+  float k0 = own ? kk[2 * i] : 0.f, k1 = own ? kk[2 * i + 1] : 0.f;
+  const float ss = warp_sum(k0 * k0 + k1 * k1);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < ROW_THREADS / 32; ++w) tot += red[w];
+  const float inv = 1.0f / sqrtf(tot / (float)d + p.ik_eps);
+  const int pr = i - (d - D_ROPE) / 2;  // rope pair of thread i (the key's last 64 dims)
+  if (own) {
+    k0 = k0 * inv * __ldg(p.ik_norm_weight + 2 * i);
+    k1 = k1 * inv * __ldg(p.ik_norm_weight + 2 * i + 1);
+    if (pr >= 0) {
+      int rp = j * p.ratio;
+      if (rp >= p.max_pos) {
+        atomicOr(&g_flags_ic, FLAG_PAGE);
+        rp = 0;
+      }
+      const float c = __ldg(p.cos_sin + (int64_t)rp * 64 + pr), s = __ldg(p.cos_sin + (int64_t)rp * 64 + 32 + pr);
+      const float y0 = k0 * c - k1 * s;
+      const float y1 = k0 * s + k1 * c;
+      k0 = y0;
+      k1 = y1;
+    }
+  }
+  float amax = 0.f;
+  if (p.ik_dtype == DSV4_I8_ROWSCALE) {  // block-uniform
+    __syncthreads();                      // red is reused
+    const float m = warp_max(own ? fmaxf(fabsf(k0), fabsf(k1)) : 0.f);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < ROW_THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
+  }
+  if (!own) return;
+  const int lp = j / p.page_size;
+  const int page = (lp < p.ik_max_pages) ? p.ik_block_table[(int64_t)b * p.ik_max_pages + lp] : -1;
+  if (page < 0 || page >= p.ik_num_pages) {
+    if (i == 0) atomicOr(&g_flags_ic, FLAG_PAGE);
+    return;
+  }
+  const int64_t slot = (int64_t)page * p.page_size + j % p.page_size;
+  uint8_t* dst = reinterpret_cast<uint8_t*>(p.ik_cache) + slot * row_bytes(p.ik_dtype, d);
+  if (p.ik_dtype == DSV4_F32) {
+    reinterpret_cast<float2*>(dst)[i] = make_float2(k0, k1);
+  } else if (p.ik_dtype == DSV4_BF16) {
+    reinterpret_cast<uint32_t*>(dst)[i] = float2_to_bf16x2_bits(k0, k1);
+  } else {
+    const float scale = amax == 0.f ? 1.f : __fdiv_rn(amax, 127.f);
+    const float c0 = fminf(fmaxf(rintf(__fdiv_rn(k0, scale)), -127.f), 127.f);
+    const float c1 = fminf(fmaxf(rintf(__fdiv_rn(k1, scale)), -127.f), 127.f);
+    reinterpret_cast<uint16_t*>(dst)[i] = (uint16_t)(((uint32_t)(int)c0 & 0xFFu) | (((uint32_t)(int)c1 & 0xFFu) << 8));
+    if (i == 0) *reinterpret_cast<float*>(dst + d) = scale;
+  }
+}
+
 // RMSNorm * weight of the folded entry (thread i holds dims 2i, 2i+1), GPT-J RoPE of the rope pairs
-// and the encoded store into the main-cache row.  All 288 threads (one block reduction).
+// and the encoded store into the main-cache row; with an index-key projection, also the entry's index
+// key (index_key_store, from the latent before the RoPE).  All 288 threads (block reductions).
 __device__ void entry_finish(const dsv4_compress_update_params& p, const EntryCtx& e, int i, float x0, float x1,
-                             float* red) {
+                             float* red, int b, int j) {
+  __shared__ __align__(16) float lat[D];
+  __shared__ float kk[128];
   float ss = warp_sum(x0 * x0 + x1 * x1);
   if ((i & 31) == 0) red[i >> 5] = ss;
   __syncthreads();
@@ -252,6 +347,7 @@ __device__ void entry_finish(const dsv4_compress_update_params& p, const EntryCt
   const float inv = 1.0f / sqrtf(tot / (float)D + p.eps);
   x0 = x0 * inv * e.g.x;
   x1 = x1 * inv * e.g.y;
+  if (p.wk != nullptr) reinterpret_cast<float2*>(lat)[i] = make_float2(x0, x1);
   if (i >= 256) {
     const float y0 = x0 * e.c - x1 * e.s;
     const float y1 = x0 * e.s + x1 * e.c;
@@ -262,6 +358,10 @@ __device__ void entry_finish(const dsv4_compress_update_params& p, const EntryCt
     if (i == 0) atomicOr(&g_flags_ic, FLAG_PAGE);
   } else {
     encode_pair_store(p.cache_dtype, e.row, i, x0, x1);
+  }
+  if (p.wk != nullptr) {  // block-uniform
+    __syncthreads();      // lat is complete; red is free again
+    index_key_store(p, b, j, lat, kk, red, i);
   }
 }
 
@@ -367,7 +467,7 @@ __device__ __forceinline__ void compress_update_body(const dsv4_compress_update_
           }
         }
       }
-      entry_finish(p, ec, i, f.a0 / f.s0, f.a1 / f.s1, red);
+      entry_finish(p, ec, i, f.a0 / f.s0, f.a1 / f.s1, red, b, j);
     }
     __syncthreads();  // the next token's store may reuse a slot this fold read
   }
@@ -468,7 +568,7 @@ __device__ __forceinline__ void compress_fold_cluster_body(const dsv4_compress_u
         A0 += qa[c].x * w0;
         A1 += qa[c].y * w1;
       }
-      entry_finish(p, ec, i, A0 / S0, A1 / S1, red);
+      entry_finish(p, ec, i, A0 / S0, A1 / S1, red, b, j);
     }
     cluster.sync();  // the fold has read the ring, and no CTA leaves while CTA 0 reads its shared memory
   } else if (rank == 0) {

@@ -77,6 +77,10 @@ class DeviceStep:
             self.main_cache = dev(st.main_cache)
             self.main_bt = dev(st.main_bt)
         self.topk_idx = None
+        self.ik_store = self.has_indexer and bool(getattr(cfg, "ik_store", False)) and st.wk is not None
+        if self.ik_store:
+            self.wk = dev(st.wk)
+            self.ik_norm_w = dev(st.ik_norm_w)
         if self.has_indexer:
             self.idx_cache = dev(st.idx_cache)
             self.idx_bt = dev(st.idx_bt)
@@ -117,9 +121,13 @@ class DeviceStep:
     def compress(self, stream=None, after_independent=False):
         if self.has_compress:
             cfg = self.cfg
+            ik = {}
+            if self.ik_store:
+                ik = dict(wk=self.wk, ik_norm_weight=self.ik_norm_w, ik_eps=self.eps, ik_cache=self.idx_cache,
+                          ik_dtype=cfg.idx_dtype, ik_block_table=self.idx_bt)
             dsv4_compress_update(self.kv_score, self.positions, cfg.q_per_seq, cfg.ratio, cfg.coff, self.state,
                                  self.ape, self.norm_w, self.eps, self.cos_sin, self.main_cache, cfg.cache_dtype,
-                                 self.main_bt, PAGE, stream=stream, after_independent=after_independent)
+                                 self.main_bt, PAGE, stream=stream, after_independent=after_independent, **ik)
 
     def indexer(self, stream=None):
         if self.has_indexer:
@@ -129,13 +137,20 @@ class DeviceStep:
         dsv4_sparse_mla_decode(self.at_params, stream=stream)
 
     def run(self, stream=None):
-        """One decode step.  With an indexer: indexer + top-k -> insert -> compress -> attention.  The
-        indexer reads none of what insert and compress write and they read none of its outputs, so
-        those two start at once (they wait for the kernel before them only before exiting) and run
-        on the SMs the indexer's CTAs leave during its top-k; attention, which needs all three,
-        waits for compress, whose completion implies the others'.  Without an indexer: insert ->
-        compress -> attention, each waiting for the one before."""
-        if self.has_indexer:
+        """One decode step.
+        With an indexer whose keys the compressor writes: compress (fold + index keys) -> indexer +
+        top-k (scores the keys written just before) -> insert -> attention.  The indexer reads none of
+        what insert writes and insert reads none of its outputs, so insert starts at once beside the
+        indexer and waits for it only before exiting; attention waits for insert, whose completion
+        implies the others'.
+        With an indexer over given keys: indexer -> insert -> compress -> attention, insert and
+        compress both starting at once beside the indexer.
+        Without an indexer: insert -> compress -> attention, each waiting for the one before."""
+        if self.ik_store:
+            self.compress(stream)
+            self.indexer(stream)
+            self.insert(stream, after_independent=True)
+        elif self.has_indexer:
             self.indexer(stream)
             self.insert(stream, after_independent=True)
             self.compress(stream, after_independent=True)

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define DSV4_ABI_VERSION 1
+#define DSV4_ABI_VERSION 2
 #define DSV4_LATENT_DIM 576
 #define DSV4_VALUE_DIM 512
 #define DSV4_ROPE_DIM 64
@@ -186,6 +186,23 @@ typedef struct dsv4_compress_update_params {
   const int32_t* block_table;  /* [B, max_pages_per_seq] main-cache pages of each sequence */
   int32_t max_pages_per_seq;
   int32_t after_independent;   /* as in dsv4_kv_insert_params */
+  /* Index-key store (optional; CSA layers whose indexer takes its keys from this compressor: API
+   * DeepseekV4Indexer, "k = k_norm(wk(latent))"; _produce_k: at group-boundary tokens, RoPE'd at
+   * the group position, quantised into the indexer K cache).  For every entry j folded by this call,
+   * with latent_j = the entry after RMSNorm * norm_weight and before its RoPE:
+   *   k = wk latent_j (fp32);  k = k / sqrt(mean(k^2) + ik_eps) * ik_norm_weight;  GPT-J RoPE of the
+   *   last 64 dims of k at position j * ratio;  stored in ik_dtype into row j of the indexer cache
+   *   (I8_ROWSCALE: scale = max|k| / 127 (1 when k = 0), code = round-half-even(k / scale) clamped
+   *   to +-127, both in fp32). */
+  const void* wk;              /* [ik_dim, 576] bf16, or NULL: no index keys */
+  const float* ik_norm_weight; /* [ik_dim] */
+  float ik_eps;
+  int32_t ik_dim;              /* 64 or 128 */
+  void* ik_cache;              /* [ik_num_pages, page_size, row] in ik_dtype (F32, BF16 or I8_ROWSCALE) */
+  int32_t ik_dtype;
+  int64_t ik_num_pages;
+  const int32_t* ik_block_table; /* [B, ik_max_pages] indexer-cache pages of each sequence */
+  int32_t ik_max_pages;
 } dsv4_compress_update_params;
 
 int dsv4_compress_update(const dsv4_compress_update_params* p, dsv4_stream_t stream);

@@ -46,9 +46,45 @@ def entry_error_ok(stored_gpu, value, dtype):
     return ok, dec
 
 
-def topk_sets_match(gpu_idx, oracle_scores, k):
-    """GPU list vs the oracle's scores: same set except near-ties at the k-th score; returns
-    (ok, exact) where exact says the two sets are identical."""
+KEY_ABS = 1e-4  # of the key row's largest element: each element is a 576-term fp32 dot product (the
+                # device sums in another order than the oracle's fp64) of RMS-normalised values
+
+
+def key_ulps(stored, dtype):
+    """Per-element bound on how far the device's encoding of a key may lie from the oracle's `stored`
+    one: one unit in the last place of the format (bf16 element, int8 code step), plus KEY_ABS of the
+    row's largest element for the fp32 arithmetic before the rounding."""
+    v = O.decode_rows(stored, dtype)
+    slack = KEY_ABS * np.max(np.abs(v))
+    if dtype == O.F32:
+        return np.zeros(v.shape) + slack
+    if dtype == O.BF16:
+        a = np.maximum(np.abs(v), 2.0 ** -126)
+        return np.exp2(np.floor(np.log2(a)) - 7) + slack
+    st = np.asarray(stored, np.uint8)
+    scale = float(np.ascontiguousarray(st[-4:]).view(np.float32)[0])
+    return np.full(v.shape, scale * 1.001) + slack
+
+
+def key_ok(stored_gpu, stored_oracle, dtype):
+    """An index key written by the device within one storage unit of the oracle's."""
+    g = O.decode_rows(stored_gpu, dtype)
+    o = O.decode_rows(stored_oracle, dtype)
+    return bool(np.all(np.abs(g - o) <= key_ulps(stored_oracle, dtype) * 1.0001))
+
+
+def new_key_score_bound(q_t, w_t, stored_key, dtype):
+    """How far the score of an entry whose key was written this step may move when the key changes by
+    at most one storage unit per element: |sum_h w_h (ReLU(q_h.k') - ReLU(q_h.k))| <= sum_h |w_h|
+    sum_d |q_hd| u_d (ReLU is 1-Lipschitz)."""
+    u = key_ulps(stored_key, dtype)
+    return float(np.sum(np.abs(np.asarray(w_t, np.float64)) * (np.abs(np.asarray(q_t, np.float64)) @ u)))
+
+
+def topk_sets_match(gpu_idx, oracle_scores, k, slack=0.0):
+    """GPU list vs the oracle's scores: same set except near-ties at the k-th score (within TIE_EPS,
+    plus `slack` when this step wrote keys the scores depend on); returns (ok, exact) where exact
+    says the two sets are identical."""
     s = np.asarray(oracle_scores, np.float32)
     n = s.shape[0]
     g = np.asarray(gpu_idx)
@@ -64,7 +100,7 @@ def topk_sets_match(gpu_idx, oracle_scores, k):
         return True, True
     kth = np.sort(s)[::-1][m - 1]
     diff = got ^ want
-    return bool(all(abs(float(s[j]) - float(kth)) <= TIE_EPS for j in diff)), False
+    return bool(all(abs(float(s[j]) - float(kth)) <= TIE_EPS + slack for j in diff)), False
 
 
 def q_out_ok(stored_gpu, stored_oracle, act_dtype):
@@ -106,19 +142,35 @@ def check_step(st, res, gpu, where=""):
             page = st.main_bt[b][j // O.PAGE]
             ok, _ = entry_error_ok(gpu["main_cache"][page, j % O.PAGE], e, cfg.cache_dtype)
             assert ok, f"{where} compressed entry {(b, j)}"
+    # index keys written by the compressor: within one storage unit of the oracle's
+    for (page, off), row in res.get("idx_written", {}).items():
+        assert key_ok(gpu["idx_cache"][page, off], row, cfg.idx_dtype), f"{where} index key row {(page, off)}"
+    new_keys = {}
+    for (b, j) in res.get("keys", {}):
+        new_keys.setdefault(b, []).append(j)
     same_sel = {}
     if cfg.ratio and cfg.topk:
         for t in res["tokens"]:
-            ok, exact = topk_sets_match(gpu["topk_idx"][t], res["scores"][t], cfg.topk)
+            b = t // cfg.q_per_seq
+            bounds = {}
+            for j in new_keys.get(b, []):
+                if j < len(res["scores"][t]):
+                    row = res["idx_written"][(int(st.idx_bt[b][j // O.PAGE]), j % O.PAGE)]
+                    bounds[j] = new_key_score_bound(O.decode_rows(st.q_idx[t], cfg.act_dtype), st.w_idx[t], row,
+                                                    cfg.idx_dtype)
+            slack = 2.0 * max(bounds.values(), default=0.0)
+            ok, exact = topk_sets_match(gpu["topk_idx"][t], res["scores"][t], cfg.topk, slack)
             assert ok, f"{where} top-k of token {t}"
             same_sel[t] = exact
             rep["tie_tokens"] += int(not exact)
             if "topk_score" in gpu and exact:
                 sel = gpu["topk_idx"][t]
+                valid = sel[sel >= 0]
                 sv = gpu["topk_score"][t][sel >= 0]
-                ref = res["scores"][t][sel[sel >= 0]]
+                ref = res["scores"][t][valid]
+                extra = np.array([bounds.get(int(j), 0.0) for j in valid])
                 scale = max(1e-30, float(np.max(np.abs(res["scores"][t]))) if len(res["scores"][t]) else 1.0)
-                assert np.all(np.abs(sv - ref) <= 1e-5 * scale + 1e-7), f"{where} top-k scores of token {t}"
+                assert np.all(np.abs(sv - ref) <= 1e-5 * scale + 1e-7 + extra), f"{where} top-k scores of token {t}"
     tol = attention_tolerance(cfg.cache_dtype)
     for t in res["tokens"]:
         if same_sel.get(t, True) is False:

@@ -91,6 +91,7 @@ def test_host_validation_rejects_bad_arguments(abi):
     assert lib.dsv4_padded_num_q_heads(64, abi.FP8_DS_MLA) == 64
     assert lib.dsv4_padded_num_q_heads(16, abi.F32) == 16
     assert lib.dsv4_padded_num_q_heads(0, abi.BF16) == -1
+    assert lib.dsv4_abi_version() == abi.ABI_VERSION == 2
 
     c = abi.make(abi.CompressUpdateParams, T=2, B=1, q_per_seq=2, ratio=8, coff=1, page_size=64,
                  max_pages_per_seq=1, max_pos=10, cache_dtype=abi.BF16)

@@ -38,6 +38,7 @@ def gpu_results(ds):
         g["state"] = to_host(ds.state)
         g["main_cache"] = to_host(ds.main_cache)
     if ds.has_indexer:
+        g["idx_cache"] = to_host(ds.idx_cache)
         g["topk_idx"] = to_host(ds.topk_idx)
         g["topk_score"] = to_host(ds.topk_score)
     return g
