@@ -85,7 +85,7 @@ def peaks():
 # ------------------------------------------------------------------------------------------------
 
 def row_bytes(dtype, width):
-    return {0: 4 * width, 1: 2 * width, 2: 656, 3: width + 4}[dtype]
+    return {0: 4 * width, 1: 2 * width, 2: 656, 3: width + 4, 4: width // 2 + width // 32}[dtype]
 
 
 def algorithmic_bytes(st, topk_idx=None):
@@ -411,7 +411,7 @@ def measure_workload(cfg, K, warmup, world, local, want_e2e):
     return res
 
 
-EXTRA_WORKLOADS = ("hca_c128_bf16", "csa_c4_fp8", "csa_c4_1m")
+EXTRA_WORKLOADS = ("hca_c128_bf16", "csa_c4_fp8", "csa_c4_1m", "csa_c4_mxfp4")
 
 
 def run_ours(args):

@@ -10,7 +10,7 @@ from __future__ import annotations
 import torch
 
 from . import _abi
-from ._abi import BF16, F32, FP8_DS_MLA, I8_ROWSCALE, Dsv4Error  # noqa: F401
+from ._abi import BF16, F32, FP8_DS_MLA, I8_ROWSCALE, MXFP4, Dsv4Error  # noqa: F401
 
 _lib = _abi.load()
 

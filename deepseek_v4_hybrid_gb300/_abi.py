@@ -11,7 +11,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libdsv4.so")
 
-F32, BF16, FP8_DS_MLA, I8_ROWSCALE = 0, 1, 2, 3
+F32, BF16, FP8_DS_MLA, I8_ROWSCALE, MXFP4 = 0, 1, 2, 3, 4
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_BOUNDS, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 LATENT_DIM, VALUE_DIM, ROPE_DIM, FP8_DS_MLA_BYTES = 576, 512, 64, 656
 ABI_VERSION = 2

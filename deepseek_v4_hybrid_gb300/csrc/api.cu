@@ -121,7 +121,8 @@ int dsv4_compress_update(const dsv4_compress_update_params* p, dsv4_stream_t str
         DSV4_ERR_INVALID);
   if (p->wk != nullptr) {
     CHECK(p->ik_dim == 64 || p->ik_dim == 128, DSV4_ERR_UNSUPPORTED);
-    CHECK(p->ik_dtype == DSV4_F32 || p->ik_dtype == DSV4_BF16 || p->ik_dtype == DSV4_I8_ROWSCALE,
+    CHECK(p->ik_dtype == DSV4_F32 || p->ik_dtype == DSV4_BF16 || p->ik_dtype == DSV4_I8_ROWSCALE ||
+              p->ik_dtype == DSV4_MXFP4,
           DSV4_ERR_UNSUPPORTED);
     CHECK(p->ik_norm_weight && p->ik_cache && p->ik_block_table && p->ik_max_pages > 0 && p->ik_num_pages >= 0 &&
               p->ik_eps >= 0.f,
@@ -145,7 +146,9 @@ int dsv4_indexer_topk(const dsv4_indexer_topk_params* p, dsv4_stream_t stream) {
   CHECK(p->ratio > 0 && p->page_size > 0 && p->max_pages_per_seq > 0 && p->num_pages >= 0, DSV4_ERR_INVALID);
   CHECK(p->topk > 0 && p->topk <= 16384 && p->max_context >= 0, DSV4_ERR_INVALID);
   CHECK(act_dtype(p->q_dtype), DSV4_ERR_UNSUPPORTED);
-  CHECK(p->k_dtype == DSV4_F32 || p->k_dtype == DSV4_BF16 || p->k_dtype == DSV4_I8_ROWSCALE, DSV4_ERR_UNSUPPORTED);
+  CHECK(p->k_dtype == DSV4_F32 || p->k_dtype == DSV4_BF16 || p->k_dtype == DSV4_I8_ROWSCALE ||
+            (p->k_dtype == DSV4_MXFP4 && p->head_dim % 32 == 0),
+        DSV4_ERR_UNSUPPORTED);
   CHECK(p->n_heads >= 1 && p->n_heads <= 128 && p->head_dim >= 16 && p->head_dim <= 256 && p->head_dim % 16 == 0,
         DSV4_ERR_UNSUPPORTED);
   CHECK((int64_t)p->q_per_seq * p->n_heads <= 256, DSV4_ERR_UNSUPPORTED);

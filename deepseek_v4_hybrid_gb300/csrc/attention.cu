@@ -606,11 +606,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc::tma_prefetch_desc(&ropemain);
         tc::tma_prefetch_desc(&ropemain64);
       }
+    }
+    pdl_wait();  // the queries, the caches and the top-k list come from earlier kernels
+    if (pidx == 0 && lane == 0 && ntiles > 0) {
       tc::mbar_arrive_expect_tx(&sm->qfull, Q_BYTES);
       for (int kb = 0; kb < NKB; ++kb)
         tc::tma_load_2d(q_mem + kb * HG * 128, &qmap, kb * 64, t * p.H + hg * HG, &sm->qfull);
     }
-    pdl_wait();  // the caches and the top-k list come from earlier kernels
     int armed_tile = -1, armed_groups = 0;
     bool ok = true;
     for (int i = 0; i < ntiles && ok; ++i) {

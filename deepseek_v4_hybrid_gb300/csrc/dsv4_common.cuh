@@ -29,6 +29,7 @@ __host__ __device__ inline int64_t row_bytes(int dtype, int width) {
     case DSV4_BF16: return 2LL * width;
     case DSV4_FP8_DS_MLA: return FP8_REC;
     case DSV4_I8_ROWSCALE: return width + 4;
+    case DSV4_MXFP4: return width / 2 + width / 32;
   }
   return 0;
 }
@@ -75,6 +76,34 @@ __device__ __forceinline__ float exp2_neg_int(int e) {
 // Scale of a UE8M0 byte: 2^(byte - 127), exact.
 __device__ __forceinline__ float ue8m0_scale(uint8_t byte) {
   return byte >= 1 ? __uint_as_float((uint32_t)byte << 23) : __uint_as_float(0x00400000u);
+}
+
+// E2M1 code (low 4 bits: sign, 2 exponent bits with bias 1, 1 mantissa bit) -> float, exact.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const uint32_t ee = (c >> 1) & 3u, m = c & 1u;
+  const float mag = ee == 0u ? 0.5f * (float)m : __uint_as_float(((ee + 126u) << 23) | (m << 22));
+  return (c & 8u) ? -mag : mag;
+}
+
+// E2M1 code of x (round to nearest, ties to the even code, saturating to +-6; the sign of x, zero
+// included, kept): the magnitude code counts the grid midpoints 0.25, 0.75, ..., 5 below |x|, with a
+// tie going to the even code.
+__device__ __forceinline__ uint32_t e2m1_code(float x) {
+  const float a = fabsf(x);
+  const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) + (uint32_t)(a >= 1.75f) +
+                     (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+  return c | (signbit(x) ? 8u : 0u);
+}
+
+// MXFP4 block exponent: the smallest integer e with 6 * 2^e >= amax, from the bits of amax (with
+// amax = f * 2^E, f in [1, 2): e = E - 2 when f <= 1.5, else E - 1), clamped to [-127, 127]; 0 for 0.
+__device__ __forceinline__ int mxfp4_exponent(float amax) {
+  if (amax == 0.0f) return 0;
+  const uint32_t bits = __float_as_uint(amax);
+  const int E = (int)((bits >> 23) & 0xFF) - 127;
+  if (E == -127) return -127;
+  const int e = ((bits & 0x7FFFFFu) <= 0x400000u) ? E - 2 : E - 1;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
 __device__ __forceinline__ uint16_t float2_to_e4m3x2(float a, float b) {

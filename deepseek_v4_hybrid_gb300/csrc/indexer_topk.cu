@@ -526,6 +526,8 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
       if (row != nullptr) {
         if (p.k_dtype == DSV4_F32) v = reinterpret_cast<const float*>(row)[e];
         else if (p.k_dtype == DSV4_BF16) v = bf16_bits_to_float(reinterpret_cast<const uint16_t*>(row)[e]);
+        else if (p.k_dtype == DSV4_MXFP4)
+          v = e2m1_value((row[e >> 1] >> ((e & 1) * 4)) & 0xFu) * ue8m0_scale(row[d / 2 + e / 32]);
         else v = (float)reinterpret_cast<const int8_t*>(row)[e];
       }
       kt_s[e * ld + kk] = v;
@@ -577,11 +579,16 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
 namespace ixtc {
 constexpr int TILE = 128;
 constexpr int KB_BYTES = TILE * 128;         // one 64-dim K-block of a key tile (128 rows x 128 B)
-constexpr int THREADS = 384;  // bf16 keys launch 320 (no expanding warps)
-static_assert((THREADS - 64) / 32 >= tk::SCAN_WARPS_MIN, "the top-k scan covers a chunk with this many warps");
+constexpr int NEXP = 2;  // warps expanding raw records (int8, MXFP4 keys): 12 warps keep 168 registers a thread
+                         // (an SM sub-partition holds 3 warps of 168 registers in its 16K)
+constexpr int THREADS_BF16 = 320;              // bf16 keys: warps 0-7 epilogue, 8 loads, 9 MMA
+constexpr int THREADS = THREADS_BF16 + NEXP * 32;  // raw records: warps 10 .. 9 + NEXP expand
+static_assert(THREADS_BF16 / 32 >= tk::SCAN_WARPS_MIN, "the top-k scan covers a chunk with this many warps");
 constexpr int W_LOAD = 8, W_MMA = 9;  // warps 10-11 expand int8 keys to bf16 (int8 caches only)
 constexpr int SCALE_RING = 16;        // int8 keys: row scales of the last 16 tiles (> stages + accumulators)
 constexpr int MAX_STAGES = 8;
+constexpr int MAX_RAW = 8;            // raw record pages in flight (int8 keys 2, MXFP4 keys up to 8)
+constexpr int KF_BF16 = 0, KF_I8 = 1, KF_MX = 2;  // key formats of the tensor-core kernel
 constexpr int FIN_MAX = 64;  // sequences whose top-k one CTA may have to run
 constexpr int WSEQ = 8;      // sequences whose head weights and entry counts are loaded up front
 constexpr int PRE_MAX = 1024;  // batches up to this size split the key tiles evenly over the CTAs
@@ -596,7 +603,10 @@ struct Args {
   int64_t num_pages;
   int T, B, qps, Ih, d, ratio, max_pages, tiles_max, max_context, K;
   int fuse_topk;  // the CTA completing a sequence runs its top-k (else a separate sliced launch)
-  int i8;         // keys are int8 records (d bytes + fp32 scale): bulk-copied pages, expanded in shared memory
+  int kf;         // key format: KF_BF16 (TMA tiles), KF_I8 (d int8 + fp32 scale) or KF_MX (MXFP4 records);
+                  // int8 and MXFP4 records arrive as bulk-copied pages and are expanded in shared memory
+  int rec;        // bytes of one raw record (int8 and MXFP4 keys)
+  int nraw;       // raw pages ring depth (pairs of 64-record pages)
   int nqs;        // query slots (2, or 1 when shared memory is short)
   const uint8_t* k_raw;  // int8 key cache
   int N, kblk, stages, tmem_cols, nacc;
@@ -604,7 +614,7 @@ struct Args {
 
 struct Smem {
   uint64_t full[MAX_STAGES], empty[MAX_STAGES], dfull[4], dempty[4], qfull[2], qempty[2], done, ebar[2];
-  uint64_t raw_full[2], raw_empty[2], sready[SCALE_RING];  // int8 keys
+  uint64_t raw_full[MAX_RAW], raw_empty[MAX_RAW], sready[SCALE_RING];  // raw records; int8 row scales
   int fin[FIN_MAX];
   int nc_tab[WSEQ][DSV4_MAX_Q_PER_SEQ];
   int pre[PRE_MAX];  // exclusive prefix of the sequences' key tiles (balanced item ranges)
@@ -689,20 +699,22 @@ __device__ __forceinline__ bool finish_seq(const Args& a, Smem* sm, uint32_t* hi
 }
 
 // One instance per key format: the bf16 one has no expanding warps (320 threads) and none of the
-// int8 branches. Both keep the 384-thread register cap: three warps of a sub-partition share its
+// raw-record branches. All keep the 384-thread register cap: three warps of a sub-partition share its
 // 16K registers, so 168 a thread.
-template <bool I8>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int KF>
+__global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
     indexer_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, Args a) {
+  constexpr bool RAW = KF != KF_BF16;  // records bulk-copied as pages and expanded to bf16 by warps 10-11
+  constexpr bool I8 = KF == KF_I8;     // int8 records: row scales applied to the finished score
   extern __shared__ __align__(1024) uint8_t dsm[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   const int q_bytes = a.kblk * a.N * 128;
   const int stage_bytes = a.kblk * KB_BYTES;
   uint8_t* stage_mem = base;                                               // stages x stage_bytes
   uint8_t* q_mem = base + a.stages * stage_bytes;                          // nqs slots x q_bytes
-  const int raw_page = 64 * (a.d + 4), raw_stage = 2 * raw_page;          // int8 records: d bytes + fp32 scale
-  uint8_t* raw_mem = q_mem + a.nqs * q_bytes;                              // int8: 2 raw stages
-  float* scale_s = reinterpret_cast<float*>(raw_mem + (I8 ? 2 * raw_stage : 0));  // int8: SCALE_RING x 128
+  const int raw_page = 64 * a.rec, raw_stage = 2 * raw_page;             // raw records: 64 a page, 2 pages a tile
+  uint8_t* raw_mem = q_mem + a.nqs * q_bytes;                              // raw records: nraw stages
+  float* scale_s = reinterpret_cast<float*>(raw_mem + (RAW ? a.nraw * raw_stage : 0));  // int8: SCALE_RING x 128
   float* w_s = scale_s + (I8 ? SCALE_RING * TILE : 0);                  // 2 groups x 256 floats
   float* w_tab = w_s + 2 * 256;                                            // WSEQ x 128 floats
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(w_tab + WSEQ * 128);      // 2 groups x qps x HIST_BINS
@@ -723,14 +735,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == W_LOAD) {
     if (lane == 0) {
       for (int s = 0; s < a.stages; ++s) {
-        tc::mbar_init(&sm->full[s], I8 ? 2 : 1);  // int8: the two expanding warps; else the loader (+ bytes)
+        tc::mbar_init(&sm->full[s], RAW ? NEXP : 1);  // raw records: the expanding warps; else the loader (+ bytes)
         tc::mbar_init(&sm->empty[s], 1);
       }
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < MAX_RAW; ++i) {
         tc::mbar_init(&sm->raw_full[i], 1);
-        tc::mbar_init(&sm->raw_empty[i], 2);
+        tc::mbar_init(&sm->raw_empty[i], NEXP);
       }
-      for (int i = 0; i < SCALE_RING; ++i) tc::mbar_init(&sm->sready[i], 2);
+      for (int i = 0; i < SCALE_RING; ++i) tc::mbar_init(&sm->sready[i], NEXP);
       for (int i = 0; i < 4; ++i) {
         tc::mbar_init(&sm->dfull[i], 1);
         tc::mbar_init(&sm->dempty[i], 4);
@@ -859,10 +871,10 @@ __global__ void __launch_bounds__(THREADS, 1)
               cur_b = b;
             }
           }
-          if (ok && I8) {
-            // raw int8 pages (whole records, untiled bulk copies) into raw stage rn % 2
-            const int rs = rn & 1;
-            ok = tc::mbar_wait_bounded(&sm->raw_empty[rs], ((rn >> 1) & 1) ^ 1, abort);
+          if (ok && RAW) {
+            // raw record pages (whole records, untiled bulk copies) into raw stage rn % nraw
+            const int rs = rn % a.nraw;
+            ok = tc::mbar_wait_bounded(&sm->raw_empty[rs], ((rn / a.nraw) & 1) ^ 1, abort);
             if (ok) {
               tc::mbar_arrive_expect_tx(&sm->raw_full[rs], (uint32_t)((p0 >= 0) + (p1 >= 0)) * (uint32_t)raw_page);
               if (p0 >= 0)
@@ -873,7 +885,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               ++rn;
             }
           } else if (ok) ok = tc::mbar_wait_bounded(&sm->empty[stage], phase ^ 1, abort);
-          if (ok && !I8) {
+          if (ok && !RAW) {
             const uint32_t bytes = (uint32_t)((p0 >= 0) + (p1 >= 0)) * a.kblk * (KB_BYTES / 2);
             uint8_t* st = stage_mem + stage * stage_bytes;
             tc::mbar_arrive_expect_tx(&sm->full[stage], bytes);
@@ -898,9 +910,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (lane == 0) {
       // drain: every issued load must land before the CTA may exit (a completed phase returns at once)
-      if (I8) {
-        for (int r = (rn > 2 ? rn - 2 : 0); r < rn; ++r)
-          tc::mbar_wait_bounded(&sm->raw_full[r & 1], (r >> 1) & 1, abort, 100000000ull);
+      if (RAW) {
+        for (int r = (rn > a.nraw ? rn - a.nraw : 0); r < rn; ++r)
+          tc::mbar_wait_bounded(&sm->raw_full[r % a.nraw], (r / a.nraw) & 1, abort, 100000000ull);
       } else {
         for (int s = 0; s < a.stages; ++s) {
           const int parity = (s < stage) ? (int)phase : (int)(phase ^ 1);
@@ -957,54 +969,87 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_wait_bounded(&sm->done, 0, abort, 100000000ull);
     }
   } else if (warp > W_MMA) {
-    // ---------------- int8 keys: warps 10-11 expand each tile's raw records into the bf16 stage
-    // (K-major, 128-byte swizzle, as TMA would write it; an int8 value is exact in bf16) and keep the
-    // row scales for the epilogue (s = scale * sum_h w_h ReLU(q_h . code), since ReLU(c x) = c ReLU(x)
-    // for c > 0)
-    if (I8) {
-      const int x = threadIdx.x - (W_MMA + 1) * 32;  // 0..63: rows x and x + 64 of each tile
-      const int rec = a.d + 4;
+    // ---------------- raw records: warps 10 .. 9 + NEXP expand each tile's records into the bf16 stage
+    // (K-major, 128-byte swizzle, as TMA would write it), thread x taking rows x, x + 32 NEXP, ... of the
+    // tile.  int8 keys:
+    // a code is exact in bf16 and the row scales are kept for the epilogue (s = scale * sum_h w_h
+    // ReLU(q_h . code), since ReLU(c x) = c ReLU(x) for c > 0).  MXFP4 keys: each E2M1 code's sign, 2
+    // exponent bits and mantissa bit are placed into a bf16's sign, lowest exponent bits and top
+    // mantissa bit, which is the bf16 code x 2^-126 (exponent-0 codes land on bf16 subnormals), and two
+    // bf16x2 multiplies by powers of two, 2^min(e - 1, 127) and 2^max(e - 128, 0), give code x 2^(e - 127)
+    // exactly for block exponent bytes e up to 252.
+    if (RAW) {
+      const int x = threadIdx.x - (W_MMA + 1) * 32;  // 0 .. 32 NEXP - 1
+      const int rec = a.rec;
       ItemIter cur;
       cur.init(a, lo, hi);
       for (int k = 0; cur.valid(); cur.next(a), ++k) {
-        const int rs = k & 1, st = k % a.stages;
-        if (!tc::mbar_wait_bounded(&sm->raw_full[rs], (k >> 1) & 1, abort) ||
+        const int rs = k % a.nraw, st = k % a.stages;
+        if (!tc::mbar_wait_bounded(&sm->raw_full[rs], (k / a.nraw) & 1, abort) ||
             !tc::mbar_wait_bounded(&sm->empty[st], ((k / a.stages) & 1) ^ 1, abort))
           break;
         const int j0 = cur.tile * TILE;
         uint8_t* stg = stage_mem + st * stage_bytes;
         float* sc = scale_s + (k % SCALE_RING) * TILE;
+        for (int r = x; r < TILE; r += NEXP * 32) {
+          if (j0 + r >= cur.nc) break;  // no key from here on: those D rows are never used
+          const uint8_t* src = raw_mem + rs * raw_stage + (r >> 6) * raw_page + (r & 63) * rec;
+          uint8_t* dstrow = stg + (r >> 3) * 1024 + (r & 7) * 128;
+          if (I8) {
+            for (int g8 = 0; g8 < a.d / 8; ++g8) {  // 8 codes -> one 16-byte chunk of 8 bf16
+              uint32_t o[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = x + 64 * h;
-          if (j0 + r >= cur.nc) continue;  // no key: its D row is never used
-          const uint8_t* src = raw_mem + rs * raw_stage + h * raw_page + (r & 63) * rec;
-          for (int g8 = 0; g8 < a.d / 8; ++g8) {  // 8 codes -> one 16-byte chunk of 8 bf16
-            uint32_t o[4];
+              for (int h4 = 0; h4 < 2; ++h4) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(src + 8 * g8 + 4 * h4) ^ 0x80808080u;
+                // code c as the float 2^23 + (c + 128), minus 2^23 + 128: exact; a small integer's bf16
+                // bits are the top half of its fp32 bits
+                float f[4];
 #pragma unroll
-            for (int h4 = 0; h4 < 2; ++h4) {
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(src + 8 * g8 + 4 * h4) ^ 0x80808080u;
-              // code c as the float 2^23 + (c + 128), minus 2^23 + 128: exact; a small integer's bf16
-              // bits are the top half of its fp32 bits
-              float f[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                f[k] = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)k)) - 8388736.0f;
-              o[2 * h4] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
-              o[2 * h4 + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
+                for (int q = 0; q < 4; ++q)
+                  f[q] = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)q)) - 8388736.0f;
+                o[2 * h4] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
+                o[2 * h4 + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
+              }
+              const int kb = g8 >> 3, ch = g8 & 7;
+              *reinterpret_cast<uint4*>(dstrow + kb * KB_BYTES + ((ch ^ (r & 7)) << 4)) =
+                  make_uint4(o[0], o[1], o[2], o[3]);
             }
-            const uint4 outv = make_uint4(o[0], o[1], o[2], o[3]);
-            const int kb = g8 >> 3, ch = g8 & 7;
-            *reinterpret_cast<uint4*>(stg + kb * KB_BYTES + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4)) = outv;
+            sc[r] = *reinterpret_cast<const float*>(src + a.d);
+          } else {
+            const uint32_t* code_w = reinterpret_cast<const uint32_t*>(src);  // d / 8 words of 8 codes
+            for (int blk = 0; blk < a.d / 32; ++blk) {
+              const uint32_t e = src[a.d / 2 + blk];
+              const uint32_t e1 = e <= 128u ? e - 1u : 127u, e2 = e <= 128u ? 0u : e - 128u;
+              const uint32_t s1b = ((e1 + 127u) << 7) * 0x00010001u, s2b = ((e2 + 127u) << 7) * 0x00010001u;
+              const __nv_bfloat162 s1 = *reinterpret_cast<const __nv_bfloat162*>(&s1b);
+              const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2b);
+              uint32_t wv[4];
+#pragma unroll
+              for (int w4 = 0; w4 < 4; ++w4) wv[w4] = code_w[blk * 4 + w4];
+#pragma unroll
+              for (int w4 = 0; w4 < 4; ++w4) {  // 8 codes -> one 16-byte chunk of 8 bf16
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const uint32_t b = (wv[w4] >> (8 * q)) & 0xFFu;
+                  uint32_t v = ((b & 0x07u) << 6) | ((b & 0x08u) << 12) | ((b & 0x70u) << 18) | ((b & 0x80u) << 24);
+                  __nv_bfloat162 bv = *reinterpret_cast<__nv_bfloat162*>(&v);
+                  bv = __hmul2(__hmul2(bv, s1), s2);
+                  o[q] = *reinterpret_cast<uint32_t*>(&bv);
+                }
+                const int g8 = blk * 4 + w4, kb = g8 >> 3, ch = g8 & 7;
+                *reinterpret_cast<uint4*>(dstrow + kb * KB_BYTES + ((ch ^ (r & 7)) << 4)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+              }
+            }
           }
-          sc[r] = *reinterpret_cast<const float*>(src + a.d);
         }
         tc::fence_proxy_async_smem();  // the expanded tile is read by the tensor cores
         __syncwarp();
         if (lane == 0) {
           tc::mbar_arrive(&sm->raw_empty[rs]);
           tc::mbar_arrive(&sm->full[st]);
-          tc::mbar_arrive(&sm->sready[k % SCALE_RING]);
+          if (I8) tc::mbar_arrive(&sm->sready[k % SCALE_RING]);
         }
       }
     }
@@ -1158,7 +1203,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 static bool use_tc_indexer(const dsv4_indexer_topk_params& p) {
   const int N = p.q_per_seq * p.n_heads;
-  return (p.k_dtype == DSV4_BF16 || p.k_dtype == DSV4_I8_ROWSCALE) && p.q_dtype == DSV4_BF16 &&
+  return (p.k_dtype == DSV4_BF16 || p.k_dtype == DSV4_I8_ROWSCALE || p.k_dtype == DSV4_MXFP4) &&
+         p.q_dtype == DSV4_BF16 &&
          (p.head_dim == 64 || p.head_dim == 128) && p.n_heads % 32 == 0 && N >= 64 && N <= 128 && N % 64 == 0 &&
          p.page_size == 64;
 }
@@ -1189,43 +1235,61 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   a.N = p.q_per_seq * p.n_heads;
   a.kblk = p.head_dim / 64;
   a.nacc = 4 * a.N <= 512 ? 4 : 2;  // TMEM accumulators (512 columns available)
-  a.i8 = p.k_dtype == DSV4_I8_ROWSCALE;
+  a.kf = p.k_dtype == DSV4_I8_ROWSCALE ? KF_I8 : (p.k_dtype == DSV4_MXFP4 ? KF_MX : KF_BF16);
+  a.rec = (int)row_bytes(p.k_dtype, p.head_dim);
+  a.nraw = 0;
   a.k_raw = reinterpret_cast<const uint8_t*>(p.k_cache);
   a.tmem_cols = a.nacc * a.N <= 64 ? 64 : (a.nacc * a.N <= 128 ? 128 : (a.nacc * a.N <= 256 ? 256 : 512));
   const size_t budget = 227 * 1024;
-  auto fixed_for = [&](int nqs) {
-    return 1024 + (size_t)nqs * a.kblk * a.N * 128 +
-           (a.i8 ? 2 * 2 * 64 * (size_t)(a.d + 4) + (size_t)SCALE_RING * TILE * 4 : 0) +
+  auto fixed_for = [&](int nqs, int nraw) {
+    return 1024 + (size_t)nqs * a.kblk * a.N * 128 + (size_t)nraw * 2 * 64 * (size_t)a.rec +
+           (a.kf == KF_I8 ? (size_t)SCALE_RING * TILE * 4 : 0) +
            (2 * 256 + WSEQ * 128) * 4 + 2 * (size_t)a.qps * HIST_BINS * 4 + sizeof(Smem);
   };
-  a.nqs = 2;  // a second query slot lets the next sequence's queries load early, if there is room
-  if ((budget - fixed_for(2)) / ((size_t)a.kblk * KB_BYTES) < 2) a.nqs = 1;
-  const size_t fixed = fixed_for(a.nqs);
-  const int stages = (int)((budget - fixed) / ((size_t)a.kblk * KB_BYTES));
+  // the first (query slots, raw pages in flight) that leaves at least two bf16 stages: a second query
+  // slot lets the next sequence's queries load early; MXFP4 records (a quarter of a bf16 tile) need a
+  // deep raw ring to keep enough bytes in flight
+  static const int kOrder[3][7][2] = {{{2, 0}, {1, 0}},
+                                      {{2, 2}, {1, 2}},
+                                      {{2, 8}, {2, 6}, {1, 8}, {1, 6}, {2, 4}, {1, 4}, {1, 2}}};
+  const int nopt = a.kf == KF_MX ? 7 : 2;
+  size_t fixed = 0;
+  int stages = 0;
+  for (int o = 0; o < nopt; ++o) {
+    a.nqs = kOrder[a.kf][o][0];
+    a.nraw = kOrder[a.kf][o][1];
+    fixed = fixed_for(a.nqs, a.nraw);
+    stages = fixed < budget ? (int)((budget - fixed) / ((size_t)a.kblk * KB_BYTES)) : 0;
+    if (stages >= 2) break;
+  }
   a.stages = stages > MAX_STAGES ? MAX_STAGES : stages;
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + (size_t)a.stages * a.kblk * KB_BYTES;
   CUtensorMap kmap, qmap;
   cudaError_t e = make_tmap_2d_bf16(&qmap, p.q, (uint64_t)p.head_dim, (uint64_t)p.T * p.n_heads, 64, (uint32_t)a.N);
   if (e != cudaSuccess) return e;
-  if (a.i8) {
-    kmap = qmap;  // int8 records are bulk-copied: the key map is not used
+  if (a.kf != KF_BF16) {
+    kmap = qmap;  // raw records are bulk-copied: the key map is not used
   } else {
     e = make_tmap_2d_bf16(&kmap, p.k_cache, (uint64_t)p.head_dim, (uint64_t)p.num_pages * 64, 64, 64);
     if (e != cudaSuccess) return e;
   }
-  e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(indexer_score_tc<false>), (int)budget);
-  if (e == cudaSuccess) e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(indexer_score_tc<true>), (int)budget);
+  e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(indexer_score_tc<KF_BF16>), (int)budget);
+  if (e == cudaSuccess) e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(indexer_score_tc<KF_I8>), (int)budget);
+  if (e == cudaSuccess) e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(indexer_score_tc<KF_MX>), (int)budget);
   if (e != cudaSuccess) return e;
   const int total = a.B * a.tiles_max;
   int grid = num_sms();
   if (grid > total) grid = total;
   if (grid < (total + FIN_MAX - 1) / FIN_MAX) grid = (total + FIN_MAX - 1) / FIN_MAX;  // <= FIN_MAX items per CTA
   if (grid <= 0) return cudaSuccess;
-  // the two expanding warps exist only for int8 keys
-  if (a.i8)
-    return launch_pdl(indexer_score_tc<true>, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/false, kmap, qmap, a);
-  return launch_pdl(indexer_score_tc<false>, dim3(grid), dim3(THREADS - 64), smem, st, /*pdl=*/false, kmap, qmap, a);
+  // the expanding warps exist only for raw records
+  if (a.kf == KF_I8)
+    return launch_pdl(indexer_score_tc<KF_I8>, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/false, kmap, qmap, a);
+  if (a.kf == KF_MX)
+    return launch_pdl(indexer_score_tc<KF_MX>, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/false, kmap, qmap, a);
+  return launch_pdl(indexer_score_tc<KF_BF16>, dim3(grid), dim3(THREADS_BF16), smem, st, /*pdl=*/false, kmap, qmap,
+                    a);
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -322,6 +322,15 @@ __device__ void index_key_store(const dsv4_compress_update_params& p, int b, int
     reinterpret_cast<float2*>(dst)[i] = make_float2(k0, k1);
   } else if (p.ik_dtype == DSV4_BF16) {
     reinterpret_cast<uint32_t*>(dst)[i] = float2_to_bf16x2_bits(k0, k1);
+  } else if (p.ik_dtype == DSV4_MXFP4) {
+    // a 32-element block is one half warp (thread i holds elements 2i, 2i + 1)
+    float m = fmaxf(fabsf(k0), fabsf(k1));
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int e = mxfp4_exponent(m);
+    const float sc = exp2_neg_int(e);
+    dst[i] = (uint8_t)(e2m1_code(k0 * sc) | (e2m1_code(k1 * sc) << 4));
+    if ((i & 15) == 0) dst[d / 2 + (i >> 4)] = (uint8_t)(e + 127);
   } else {
     const float scale = amax == 0.f ? 1.f : __fdiv_rn(amax, 127.f);
     const float c0 = fminf(fmaxf(rintf(__fdiv_rn(k0, scale)), -127.f), 127.f);

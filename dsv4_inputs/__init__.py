@@ -13,6 +13,7 @@ Workload shapes follow the five decode configurations of the hot path:
   csa_c4_fp8     128 seqs, context U[8192, 32768], 2 query tokens per seq,
                  fp8_ds_mla caches, int8 + fp32-scale indexer keys, top-k 512
   csa_c4_1m      4 seqs, context 1048576, 128 heads, top-k 2048
+  csa_c4_mxfp4   csa_c4_bf16 with its indexer keys as 68-byte MXFP4 records
 
 plus small variants (``small_*``) of the same dtypes and head counts that the
 oracle finishes in seconds while still spanning several tiles and ragged tails.
@@ -43,8 +44,8 @@ FP8_SCALE_OFF = 640
 FP8_ROPE_OFF = 512
 
 # dtype tags, equal in value to the C enum dsv4_dtype
-F32, BF16, FP8_DS_MLA, I8_ROWSCALE = 0, 1, 2, 3
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_DS_MLA: "fp8_ds_mla", I8_ROWSCALE: "i8_rowscale"}
+F32, BF16, FP8_DS_MLA, I8_ROWSCALE, MXFP4 = 0, 1, 2, 3, 4
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_DS_MLA: "fp8_ds_mla", I8_ROWSCALE: "i8_rowscale", MXFP4: "mxfp4"}
 
 
 @dataclass(frozen=True)
@@ -94,6 +95,10 @@ CONFIGS = {
                          seed=0xD5E4 + 3),
     "csa_c4_1m": Config("csa_c4_1m", B=4, q_per_seq=1, ctx=(1048576, 1048576), H=128, ratio=4, I_h=64, d_I=128,
                         topk=2048, act_dtype=BF16, cache_dtype=BF16, idx_dtype=BF16, out_dtype=BF16, seed=0xD5E4 + 4),
+    # the CSA c4 bf16 layer with its indexer keys in the 68-byte MXFP4 record
+    "csa_c4_mxfp4": Config("csa_c4_mxfp4", B=32, q_per_seq=1, ctx=(65536, 65536), H=64, ratio=4, I_h=64, d_I=128,
+                           topk=512, act_dtype=BF16, cache_dtype=BF16, idx_dtype=MXFP4, out_dtype=BF16,
+                           seed=0xD5E4 + 5),
 }
 
 # Small variants: same dtypes and head counts, ragged lengths spanning several key tiles,
@@ -113,6 +118,8 @@ SMALL_CONFIGS = {
                                           d_I=0, topk=0, explicit_lens=(300, 7)),
     "edge_first_token": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="edge_first_token", B=2,
                                             explicit_lens=(1, 4)),
+    "small_c4_mxfp4": dataclasses.replace(CONFIGS["csa_c4_mxfp4"], name="small_c4_mxfp4", B=3, q_per_seq=2,
+                                          explicit_lens=(9001, 2050, 700)),
     # 32 query heads padded to 64 by the fused query preparation
     "small_c4_h32pad": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_c4_h32pad", B=3, H=32,
                                            explicit_lens=(3000, 700, 129)),
@@ -136,6 +143,8 @@ def row_elems(dtype: int, width: int) -> tuple:
         return np.uint8, (FP8_DS_MLA_BYTES,)
     if dtype == I8_ROWSCALE:
         return np.uint8, (width + 4,)
+    if dtype == MXFP4:
+        return np.uint8, (width // 2 + width // 32,)
     raise ValueError(dtype)
 
 
@@ -211,6 +220,16 @@ class _Draw:
             rec[:, FP8_ROPE_OFF:FP8_ROPE_OFF + 128] = rope.view(np.uint8).reshape(n_rows, 128)
             # scale bytes around 2^-7 so decoded values are ~N(0,1)*0.1
             rec[:, FP8_SCALE_OFF:FP8_SCALE_OFF + 8] = rng.integers(119, 122, size=(n_rows, 8), dtype=np.uint8)
+            return rec
+        if dtype == MXFP4:
+            # E2M1 codes (magnitude codes 0..7 drawn with weights favouring small values, random sign)
+            # and block exponent bytes 122..124
+            w = np.array([4, 6, 6, 5, 4, 3, 2, 1], np.float64)
+            mag = rng.choice(8, size=(n_rows, width), p=w / w.sum()).astype(np.uint8)
+            codes = mag | (rng.integers(0, 2, size=(n_rows, width), dtype=np.uint8) << 3)
+            rec = np.zeros((n_rows, width // 2 + width // 32), np.uint8)
+            rec[:, :width // 2] = codes[:, 0::2] | (codes[:, 1::2] << 4)
+            rec[:, width // 2:] = rng.integers(122, 125, size=(n_rows, width // 32), dtype=np.uint8)
             return rec
         if dtype == I8_ROWSCALE:
             rec = np.zeros((n_rows, width + 4), np.uint8)

@@ -78,7 +78,12 @@ typedef enum dsv4_dtype {
   DSV4_FP8_DS_MLA = 2,
   /* indexer key record of head_dim + 4 bytes: head_dim int8 codes then the little-endian fp32
    * scale of the row; key = code * scale (API, _indexer_k_cache_head_dim: 128 + 4 = 132 B). */
-  DSV4_I8_ROWSCALE = 3
+  DSV4_I8_ROWSCALE = 3,
+  /* MXFP4 indexer key record of head_dim / 2 + head_dim / 32 bytes (68 B for 128 dims; API,
+   * _indexer_k_cache_head_dim): E2M1 codes, element 2i in the low nibble of byte i, then one UE8M0
+   * byte per 32 elements; key = code * 2^(byte - 127).  The encoders here take the smallest block
+   * exponent e with 6 * 2^e >= the block's max |x| and round to nearest even. */
+  DSV4_MXFP4 = 4
 } dsv4_dtype;
 
 typedef void* dsv4_stream_t; /* cudaStream_t */

@@ -62,6 +62,14 @@ def key_ulps(stored, dtype):
         a = np.maximum(np.abs(v), 2.0 ** -126)
         return np.exp2(np.floor(np.log2(a)) - 7) + slack
     st = np.asarray(stored, np.uint8)
+    if dtype == O.MXFP4:
+        # two E2M1 steps (0.5 below 2, 1 in [2, 4), 2 above) at the block's scale: a neighbouring code, or
+        # the next block exponent when the block's max sits at the exponent's boundary
+        d = v.shape[-1]
+        scale = np.repeat(np.exp2(st[d // 2:].astype(np.float64) - 127.0), O.MXFP4_BLOCK)
+        a = np.abs(v) / scale
+        step = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+        return 2.0 * step * scale + slack
     scale = float(np.ascontiguousarray(st[-4:]).view(np.float32)[0])
     return np.full(v.shape, scale * 1.001) + slack
 

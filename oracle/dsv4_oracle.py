@@ -32,6 +32,9 @@ Readings taken where the pages leave a step open (each also listed in the design
   * fp8_ds_mla record at 576 dims = 656 bytes: 512 e4m3fn | 64 bf16 rope | 8 UE8M0 bytes | 8 zero.
   * the UE8M0 exponent of a 64-dim block is the smallest e with 448 * 2^e >= amax (0 when amax = 0).
   * int8 indexer key record = 128 int8 + little-endian fp32 scale (132 bytes); k = q8 * scale.
+  * MXFP4 indexer key record = d/2 bytes of E2M1 pairs (element 2i in the low nibble) + one UE8M0
+    byte per 32 elements (68 bytes for d = 128); the block exponent is the smallest e with
+    6 * 2^e >= the block's max |x| (never saturates); queries stay bf16.
 
 Parity unpinned (model-fidelity readings the pages do not fix, so nothing outside the
 oracle can confirm them): the APE target, the RoPE position of compressed entries, the c4
@@ -51,7 +54,9 @@ FP8_BLOCK = 64
 FP8_DS_MLA_BYTES = 656
 E4M3_MAX = 448.0
 
-F32, BF16, FP8_DS_MLA, I8_ROWSCALE = 0, 1, 2, 3
+F32, BF16, FP8_DS_MLA, I8_ROWSCALE, MXFP4 = 0, 1, 2, 3, 4
+E2M1_MAX = 6.0
+MXFP4_BLOCK = 32
 
 
 # ----------------------------------------------------------------------------------------------
@@ -175,6 +180,76 @@ def i8_rowscale_decode(rec) -> np.ndarray:
     return q * s
 
 
+def e2m1_decode(code) -> np.ndarray:
+    """FP4 E2M1 code (low 4 bits) -> float64: 1 sign, 2 exponent (bias 1), 1 mantissa bit; exponent
+    0 is subnormal (m * 0.5): magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6."""
+    c = np.asarray(code, np.int64) & 0xF
+    e, m = (c >> 1) & 3, c & 1
+    mag = np.where(e == 0, 0.5 * m, (1.0 + 0.5 * m) * np.exp2(e - 1.0))
+    return np.where(c >> 3, -mag, mag)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Value -> E2M1 code, round to nearest even on the E2M1 grid, saturating to +-6."""
+    x = np.asarray(x, np.float64)
+    v = np.clip(_round_to_grid(x, 1, 0), -E2M1_MAX, E2M1_MAX)
+    a = np.abs(v)
+    code = np.zeros(a.shape, np.int64)
+    sub = a < 1.0
+    code[sub] = np.rint(a[sub] / 0.5).astype(np.int64)            # exponent field 0
+    nrm = ~sub
+    _, ex = np.frexp(a[nrm])
+    e = ex - 1
+    code[nrm] = ((e + 1) << 1) | np.rint((a[nrm] / np.exp2(e) - 1.0) * 2.0).astype(np.int64)
+    sign = (v < 0) | ((v == 0) & np.signbit(x))
+    return (code | (sign.astype(np.int64) << 3)).astype(np.uint8)
+
+
+def mxfp4_exponent(amax: float) -> int:
+    """Block exponent of an MXFP4 block: the smallest integer e with 6 * 2^e >= amax (the block's
+    largest element never saturates), clamped to the UE8M0 byte's range; 0 for an all-zero block."""
+    amax = float(amax)
+    if amax == 0.0:
+        return 0
+    e = int(np.ceil(np.log2(amax / E2M1_MAX)))
+    while E2M1_MAX * 2.0 ** (e - 1) >= amax:
+        e -= 1
+    while E2M1_MAX * 2.0 ** e < amax:
+        e += 1
+    return max(-127, min(127, e))
+
+
+def mxfp4_encode(row) -> np.ndarray:
+    """d-dim key -> MXFP4 record of d/2 + d/32 bytes ([API] _indexer_k_cache_head_dim: "MXFP4 stores
+    two values per byte plus one UE8M0 byte per 32 values", 68 B for d = 128; [MAP] "What This Repo
+    Is For": MXFP4 for indexer keys): E2M1 codes of x / 2^e (element 2i in the low nibble of byte i),
+    then one byte e + 127 per 32-element block."""
+    x = np.asarray(row, np.float64)
+    d = x.shape[0]
+    codes = np.zeros(d, np.uint8)
+    scales = np.zeros(d // MXFP4_BLOCK, np.uint8)
+    for blk in range(d // MXFP4_BLOCK):
+        seg = slice(blk * MXFP4_BLOCK, (blk + 1) * MXFP4_BLOCK)
+        e = mxfp4_exponent(np.max(np.abs(x[seg])))
+        codes[seg] = e2m1_encode(x[seg] / 2.0 ** e)
+        scales[blk] = e + 127
+    packed = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+    return np.concatenate([packed, scales])
+
+
+def mxfp4_decode(rec) -> np.ndarray:
+    """MXFP4 records [..., d/2 + d/32] -> float64 [..., d]."""
+    rec = np.asarray(rec, np.uint8)
+    nb = rec.shape[-1]
+    d = nb * 32 // 17                                              # d/2 + d/32 = 17 d / 32
+    packed = rec[..., :d // 2].astype(np.int64)
+    codes = np.stack([packed & 0xF, packed >> 4], axis=-1).reshape(rec.shape[:-1] + (d,))
+    vals = e2m1_decode(codes)
+    scale = np.exp2(rec[..., d // 2:].astype(np.float64) - 127.0)
+    return (vals.reshape(rec.shape[:-1] + (d // MXFP4_BLOCK, MXFP4_BLOCK)) * scale[..., None]).reshape(
+        rec.shape[:-1] + (d,))
+
+
 def decode_rows(stored, dtype: int) -> np.ndarray:
     """Stored rows in cache format `dtype` -> float64 values."""
     if dtype == F32:
@@ -185,6 +260,8 @@ def decode_rows(stored, dtype: int) -> np.ndarray:
         return fp8_ds_mla_decode(stored)
     if dtype == I8_ROWSCALE:
         return i8_rowscale_decode(stored)
+    if dtype == MXFP4:
+        return mxfp4_decode(stored)
     raise ValueError(dtype)
 
 
@@ -391,6 +468,8 @@ def encode_key(k, dtype: int) -> np.ndarray:
         return bf16_encode(k)
     if dtype == I8_ROWSCALE:
         return i8_rowscale_encode(np.asarray(k, np.float64).astype(np.float32))
+    if dtype == MXFP4:
+        return mxfp4_encode(k)
     raise ValueError(dtype)
 
 

@@ -74,7 +74,8 @@ def test_tiny_config_full_parity(lib, name):
 
 
 @pytest.mark.parametrize("name,seqs", [("csa_c4_bf16", [0, 17, 31]), ("hca_c128_bf16", [0, 21, 63]),
-                                       ("csa_c4_fp8", [0, 77, 127]), ("csa_c4_1m", [0, 3])])
+                                       ("csa_c4_fp8", [0, 77, 127]), ("csa_c4_1m", [0, 3]),
+                                       ("csa_c4_mxfp4", [0, 13, 31])])
 def test_full_size_sampled_parity(lib, name, seqs):
     rep, st, ds = run_and_compare(name, seqs=seqs)
     assert rep["tokens"] == len(seqs) * st.cfg.q_per_seq
