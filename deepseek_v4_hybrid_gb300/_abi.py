@@ -48,7 +48,8 @@ class IndexerTopkParams(C.Structure):
                 ("k_dtype", i32), ("num_pages", i64), ("block_table", vp), ("max_pages_per_seq", i32),
                 ("positions", vp), ("T", i32), ("B", i32), ("q_per_seq", i32), ("ratio", i32),
                 ("n_heads", i32), ("head_dim", i32), ("topk", i32), ("page_size", i32), ("max_context", i32),
-                ("topk_idx", vp), ("topk_score", vp), ("workspace", vp), ("workspace_bytes", C.c_size_t)]
+                ("topk_idx", vp), ("topk_score", vp), ("workspace", vp), ("workspace_bytes", C.c_size_t),
+                ("workspace_zeroed", i32)]
 
 
 class SparseMlaDecodeParams(C.Structure):

@@ -369,14 +369,15 @@ __device__ void write_selection(const uint32_t* bits, bool bits_global, int word
 // round_up(n, 128) entries; the histogram hist_g of their order keys is complete) into out[0, K) in
 // increasing j (out_s: their scores, may be null); gcand (n entries) holds candidates that do not fit
 // in `buf` (buf_bytes of 128-byte aligned shared memory).  Returns false if a copy timed out.
-__device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int K, int32_t* out, float* out_s,
+__device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int32_t* out, float* out_s,
                            uint64_t* gcand, uint8_t* buf, size_t buf_bytes, volatile int* abort) {
   const int tid = threadIdx.x, NT = blockDim.x;
-  if (n <= K) {  // short context: every entry, in order
+  if (n <= K) {  // short context: every entry, in order (the histogram is cleared for the next call)
     for (int x = tid; x < K; x += NT) {
       out[x] = x < n ? x : -1;
       if (out_s) out_s[x] = x < n ? __ldcg(s_g + x) : -INFINITY;
     }
+    for (int x = tid; x < HIST_BINS; x += NT) hist_g[x] = 0u;
     return true;
   }
   const size_t fixed = fixed_bytes(n);
@@ -436,6 +437,9 @@ __device__ bool topk_token(const float* s_g, const uint32_t* hist_g, int n, int 
     __syncthreads();
     return false;
   }
+  // the copy has landed: the token's global histogram is cleared for the next call (this CTA is its last
+  // reader)
+  for (int x = tid; x < HIST_BINS; x += NT) hist_g[x] = 0u;
   block_find_bin<HIST_BINS / FIND_THREADS>(hist_s, (uint32_t)K, c);
   const uint32_t bstar = c->bin;
   const int R = K - (int)c->above;  // still to choose among the candidates
@@ -690,6 +694,7 @@ __device__ __forceinline__ bool finish_seq(const Args& a, Smem* sm, uint32_t* hi
     const uint32_t tiles = (uint32_t)((seq_entries(a, b) + TILE - 1) / TILE);
     const uint32_t prev = atomicAdd(&a.bufs.seq_done[b], (uint32_t)ntile);
     if (prev + (uint32_t)ntile == tiles) {
+      a.bufs.seq_done[b] = 0u;  // complete: no CTA adds to it again in this call; cleared for the next
       const uint32_t i = atomicAdd(&sm->nfin, 1u);
       if (i < FIN_MAX) sm->fin[i] = b;
       else atomicOr(&g_flags_ix, FLAG_TOPK);
@@ -1335,12 +1340,14 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
   const float* s_g = bufs.scores + (int64_t)t * bufs.nc_stride;
   int32_t* out = p.topk_idx + (int64_t)t * K;
   float* out_s = p.topk_score ? p.topk_score + (int64_t)t * K : nullptr;
-  if (n <= K) {  // short context: slice 0 writes every entry, in order
-    if (sl == 0)
+  if (n <= K) {  // short context: slice 0 writes every entry, in order, and clears the histogram
+    if (sl == 0) {
       for (int x = tid; x < K; x += TK_THREADS) {
         out[x] = x < n ? x : -1;
         if (out_s) out_s[x] = x < n ? __ldcg(s_g + x) : -INFINITY;
       }
+      for (int x = tid; x < HIST_BINS; x += TK_THREADS) bufs.hist[(int64_t)t * HIST_BINS + x] = 0u;
+    }
     return;
   }
   const int nsl = (n + SLICE - 1) / SLICE;
@@ -1404,6 +1411,13 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
   __threadfence();
   const int R = K - (int)c->above;
   const uint32_t m = min(__ldcg(&bufs.tcnt[2 * t]), (uint32_t)n);
+  // every other slice of the token is done with its histogram and counters: cleared for the next call
+  for (int x = tid; x < HIST_BINS; x += TK_THREADS) bufs.hist[(int64_t)t * HIST_BINS + x] = 0u;
+  __syncthreads();  // m is read by every thread before the counters are cleared
+  if (tid == 0) {
+    bufs.tcnt[2 * t] = 0u;
+    bufs.tcnt[2 * t + 1] = 0u;
+  }
   const uint64_t* cand = cand_g;
   if (m <= cap) {
     for (uint32_t i = tid; i < m; i += TK_THREADS) cand_s[i] = __ldcg(cand_g + i);
@@ -1420,7 +1434,7 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
   if (p.T == 0) return cudaSuccess;
   IxLayout L = ix_layout(p);
   char* ws = reinterpret_cast<char*>(p.workspace);
-  TopkBufs bufs;
+  TopkBufs bufs;  // every call clears the histograms and counters it used before it completes
   bufs.scores = reinterpret_cast<float*>(ws + L.scores_off);
   bufs.hist = reinterpret_cast<uint32_t*>(ws + L.hist_off);
   bufs.seq_done = reinterpret_cast<uint32_t*>(ws + L.done_off);
@@ -1428,8 +1442,11 @@ cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t 
   bufs.cand = reinterpret_cast<uint64_t*>(ws + L.cand_off);
   bufs.bits = reinterpret_cast<uint32_t*>(ws + L.bits_off);
   bufs.nc_stride = (int)L.nc_stride;
-  cudaError_t e = cudaMemsetAsync(ws + L.hist_off, 0, L.tcnt_off + (size_t)p.T * 2 * sizeof(uint32_t) - L.hist_off, st);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!p.workspace_zeroed) {  // histograms and counters start at zero (every completed call leaves them so)
+    e = cudaMemsetAsync(ws + L.hist_off, 0, L.tcnt_off + (size_t)p.T * 2 * sizeof(uint32_t) - L.hist_off, st);
+    if (e != cudaSuccess) return e;
+  }
   const int max_nc = p.max_context / p.ratio;
   const bool fused = max_nc <= TOPK_FUSED_MAX;
   if (max_nc > 0 && use_tc_indexer(p)) {

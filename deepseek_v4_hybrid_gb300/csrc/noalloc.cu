@@ -54,5 +54,6 @@ extern "C" int dsv4_indexer_topk_noalloc(const dsv4_indexer_topk_params* p, dsv4
   dsv4_indexer_topk_params q = *p;
   q.workspace = scratch;
   q.workspace_bytes = DSV4_NOALLOC_SCRATCH_BYTES;
+  q.workspace_zeroed = 0;  // the array is shared by every call: always cleared first
   return dsv4_indexer_topk(&q, stream);
 }

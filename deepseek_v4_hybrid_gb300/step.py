@@ -92,9 +92,12 @@ class DeviceStep:
                                                  cfg.idx_dtype, self.idx_bt, self.positions, cfg.q_per_seq,
                                                  cfg.ratio, cfg.topk, PAGE, self.max_context, self.topk_idx,
                                                  self.topk_score)
-            self.ix_ws = _ws(dsv4_indexer_topk_workspace_bytes(self.ix_params), device)
+            # zero-filled once: every call leaves its histograms and counters cleared, so no call needs a memset
+            self.ix_ws = torch.zeros(max(int(dsv4_indexer_topk_workspace_bytes(self.ix_params)), 256),
+                                     dtype=torch.uint8, device=device)
             self.ix_params.workspace = self.ix_ws.data_ptr()
             self.ix_params.workspace_bytes = self.ix_ws.numel()
+            self.ix_params.workspace_zeroed = 1
         attn_topk = self.topk_idx
         if topk_override is not None:
             self.given_topk = dev(topk_override.astype(np.int32))

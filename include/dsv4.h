@@ -238,6 +238,11 @@ typedef struct dsv4_indexer_topk_params {
   float* topk_score;           /* [T, topk] output scores of topk_idx (-inf on padding) or NULL */
   void* workspace;             /* dsv4_indexer_topk_workspace_bytes() bytes, 256-byte aligned */
   size_t workspace_bytes;
+  int32_t workspace_zeroed;    /* 0: the call first clears the histograms and counters it keeps in the
+                                  workspace (one memset on `stream`).  1: the caller guarantees they are
+                                  zero: the workspace was zero-filled once when allocated, and every
+                                  call that completed without raising a flag left it so (each call
+                                  clears what it used before it completes) */
 } dsv4_indexer_topk_params;
 
 size_t dsv4_indexer_topk_workspace_bytes(const dsv4_indexer_topk_params* p);

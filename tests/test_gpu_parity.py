@@ -234,3 +234,25 @@ def test_qprep_in_place_and_without_switches(lib):
     assert M.dsv4_read_device_flags() == 0
     assert torch.equal(padded[:, :cfg.H].view(torch.int16), q0.view(torch.int16))
     assert torch.count_nonzero(padded[:, cfg.H:].float()) == 0
+
+
+@pytest.mark.parametrize("name", ["small_c4_bf16", "small_c4_h128", "small_c4_fp8"])
+def test_indexer_workspace_left_clean(lib, name):
+    """Calls with workspace_zeroed = 1 (no memset) rely on every completed call clearing the histograms
+    and counters it used: three calls in a row on one zero-filled workspace give the oracle's top-k
+    sets each time as a call that clears the workspace first (whose parity the step tests check)."""
+    import deepseek_v4_hybrid_gb300 as M
+    from deepseek_v4_hybrid_gb300.step import DeviceStep
+    st = I.make_step(I.SMALL_CONFIGS[name])
+    ds = DeviceStep(st)
+    assert ds.ix_params.workspace_zeroed == 1
+    ds.compress()  # the keys this step's indexer reads
+    outs = []
+    for zeroed in (1, 1, 1, 0):
+        ds.ix_params.workspace_zeroed = zeroed
+        ds.indexer()
+        torch.cuda.synchronize()
+        assert M.dsv4_read_device_flags() == 0
+        outs.append(to_host(ds.topk_idx).copy())
+    for got in outs:
+        assert np.array_equal(got, outs[-1])
