@@ -67,6 +67,9 @@ class Config:
     explicit_lens: tuple = ()
     q_prep: bool = True   # queries arrive un-normed and un-rotated: the fused insert norms, rotates and pads them
     ik_store: bool = True  # the compressor also writes each new entry's index key (CSA layers with an indexer)
+    cand_block: int = 0    # two-level candidate filtering: entries per candidate block (0 = off)
+    cand_topk: int = 0     # candidate blocks per token
+    cand_write: bool = False  # this layer's indexer publishes its best blocks (else it consumes given ones)
 
     @property
     def T(self) -> int:
@@ -95,6 +98,10 @@ CONFIGS = {
                          seed=0xD5E4 + 3),
     "csa_c4_1m": Config("csa_c4_1m", B=4, q_per_seq=1, ctx=(1048576, 1048576), H=128, ratio=4, I_h=64, d_I=128,
                         topk=2048, act_dtype=BF16, cache_dtype=BF16, idx_dtype=BF16, out_dtype=BF16, seed=0xD5E4 + 4),
+    # the CSA c4 bf16 layer as a consumer of an earlier layer's candidate blocks (8 of 16 blocks of 1024)
+    "csa_c4_cand": Config("csa_c4_cand", B=32, q_per_seq=1, ctx=(65536, 65536), H=64, ratio=4, I_h=64, d_I=128,
+                          topk=512, act_dtype=BF16, cache_dtype=BF16, idx_dtype=BF16, out_dtype=BF16,
+                          seed=0xD5E4 + 6, cand_block=1024, cand_topk=8),
     # the CSA c4 bf16 layer with its indexer keys in the 68-byte MXFP4 record
     "csa_c4_mxfp4": Config("csa_c4_mxfp4", B=32, q_per_seq=1, ctx=(65536, 65536), H=64, ratio=4, I_h=64, d_I=128,
                            topk=512, act_dtype=BF16, cache_dtype=BF16, idx_dtype=MXFP4, out_dtype=BF16,
@@ -118,6 +125,12 @@ SMALL_CONFIGS = {
                                           d_I=0, topk=0, explicit_lens=(300, 7)),
     "edge_first_token": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="edge_first_token", B=2,
                                             explicit_lens=(1, 4)),
+    # two-level candidate filtering: a consumer of given candidate blocks and a source that publishes them
+    "small_c4_cand": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_c4_cand", B=4,
+                                         explicit_lens=(20000, 9000, 2300, 700), cand_block=1024, cand_topk=3),
+    "small_c4_cand_src": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_c4_cand_src", B=3,
+                                             explicit_lens=(20000, 6000, 900), cand_block=512, cand_topk=4,
+                                             cand_write=True),
     "small_c4_mxfp4": dataclasses.replace(CONFIGS["csa_c4_mxfp4"], name="small_c4_mxfp4", B=3, q_per_seq=2,
                                           explicit_lens=(9001, 2050, 700)),
     # 32 query heads padded to 64 by the fused query preparation
@@ -270,6 +283,7 @@ class StepInputs:
     q_idx: np.ndarray = None     # [T, I_h, d_I]
     w_idx: np.ndarray = None     # [T, I_h] f32
     given_topk: np.ndarray = None  # [T, topk] int32: a fixed valid selection for standalone attention cases
+    cand_in: np.ndarray = None   # [T, cand_topk] int32: candidate blocks published by an earlier layer (consumer)
     extra: dict = field(default_factory=dict)
 
 
@@ -362,6 +376,17 @@ def make_step(cfg: Config, with_given_topk: bool = True) -> StepInputs:
         if cfg.ik_store:
             st.wk = draw.bf16("wk", (cfg.d_I, D))
             st.ik_norm_w = draw.normal_f32("ik_norm_w", (cfg.d_I,), 0.1, 1.0)
+
+    if cfg.cand_block and not cfg.cand_write:
+        # another layer's published candidates: distinct visible blocks of each token, increasing, -1 padded
+        c = np.full((T, cfg.cand_topk), -1, np.int32)
+        rng = draw.rng("cand_in")
+        for t in range(T):
+            nblk = ((int(positions[t]) + 1) // r + cfg.cand_block - 1) // cfg.cand_block
+            m = min(nblk, cfg.cand_topk)
+            if m:
+                c[t, :m] = np.sort(rng.choice(nblk, size=m, replace=False)) if nblk > m else np.arange(nblk)
+        st.cand_in = c
 
     if cfg.topk > 0 and with_given_topk:
         # an arbitrary valid selection (distinct visible indices, ascending, -1 padded) for attention-only cases

@@ -529,6 +529,41 @@ def topk_select(scores, k: int) -> np.ndarray:
     return out
 
 
+def candidate_blocks(scores, block: int, m: int) -> np.ndarray:
+    """Two-level candidate filtering, source side ([API] DeepseekV4Indexer: the indexer at
+    candidate_source_layer_id additionally publishes the top candidate_topk_blocks blocks of
+    candidate_block_size compressed positions).  Reading: a block's score is the largest score of
+    its visible entries; the m best blocks by (score desc, block index asc), listed in increasing
+    block index, -1 padded to m."""
+    s = np.asarray(scores, np.float32)
+    n = s.shape[0]
+    nblk = (n + block - 1) // block
+    keys = np.array([np.max(s[b * block:(b + 1) * block]) for b in range(nblk)], np.float64)
+    order = np.lexsort((np.arange(nblk), -keys))
+    out = np.full(m, -1, np.int32)
+    sel = np.sort(order[:min(m, nblk)])
+    out[:len(sel)] = sel
+    return out
+
+
+def masked_topk(scores, k: int, cand, block: int) -> np.ndarray:
+    """Two-level candidate filtering, consumer side ([API] DeepseekV4Indexer: later indexers mask
+    their scores to the candidate blocks before their own top-k): only entries whose block
+    (j // block) is listed in `cand` (-1 entries ignored) take part; the k best of them by (score
+    desc, j asc), or all of them when there are at most k; -1 pads to k."""
+    s = np.asarray(scores, np.float32)
+    n = s.shape[0]
+    blocks = set(int(c) for c in np.asarray(cand) if c >= 0)
+    inc = np.array([j for j in range(n) if j // block in blocks], np.int64)
+    out = np.full(k, -1, np.int32)
+    if inc.size == 0:
+        return out
+    order = inc[np.lexsort((inc, -s[inc].astype(np.float64)))]
+    m = min(k, inc.size)
+    out[:m] = order[:m]
+    return out
+
+
 # ----------------------------------------------------------------------------------------------
 # Steps a5-a6: shared-KV sparse MLA attention and split merge
 # ----------------------------------------------------------------------------------------------
@@ -636,7 +671,7 @@ def decode_step(st, seqs=None, topk_override=None):
         res["keys"] = keys
         res["idx_written"] = dict(idx.written) if idx is not None else {}
 
-    topk, scores = {}, {}
+    topk, scores, cand_out = {}, {}, {}
     if cfg.ratio > 0 and cfg.topk > 0:
         for t in toks:
             b, p = t // qps, int(st.positions[t])
@@ -645,8 +680,14 @@ def decode_step(st, seqs=None, topk_override=None):
             q_t = decode_rows(st.q_idx[t], cfg.act_dtype)
             s = indexer_scores(q_t, st.w_idx[t], keys) if nc else np.zeros(0, np.float32)
             scores[t] = s
-            topk[t] = topk_select(s, cfg.topk)
-    res["scores"], res["topk"] = scores, topk
+            cb = getattr(cfg, "cand_block", 0)
+            if cb and st.cand_in is not None:          # a consumer of another layer's candidate blocks
+                topk[t] = masked_topk(s, cfg.topk, st.cand_in[t], cb)
+            else:
+                topk[t] = topk_select(s, cfg.topk)
+            if cb and getattr(cfg, "cand_write", False):  # the candidate source publishes its best blocks
+                cand_out[t] = candidate_blocks(s, cb, cfg.cand_topk)
+    res["scores"], res["topk"], res["cand_out"] = scores, topk, cand_out
 
     out, lse = {}, {}
     for t in toks:

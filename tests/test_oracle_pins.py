@@ -542,3 +542,34 @@ def test_mxfp4_index_key_recall_against_fp32_keys():
     got = set(O.topk_select(O.indexer_scores(q, w, quant), k).tolist())
     recall = len(ref & got) / k
     assert recall >= 0.85, recall
+
+
+# ------------------------------------------------------------------------------------------------
+# two-level candidate filtering
+# ------------------------------------------------------------------------------------------------
+
+def test_candidate_blocks_brute_force():
+    rng = np.random.default_rng(41)
+    for n, block, m in [(1000, 64, 5), (4096, 512, 3), (300, 128, 8), (130, 128, 1)]:
+        s = rng.integers(-5, 6, n).astype(np.float32)           # many ties between block maxima
+        got = O.candidate_blocks(s, block, m)
+        nblk = -(-n // block)
+        best = [max(s[b * block:(b + 1) * block]) for b in range(nblk)]
+        rank = sorted(range(nblk), key=lambda b: (-best[b], b))
+        want = sorted(rank[:min(m, nblk)])
+        assert got[:len(want)].tolist() == want and np.all(got[len(want):] == -1)
+
+
+def test_masked_topk_brute_force_and_reductions():
+    rng = np.random.default_rng(42)
+    s = rng.standard_normal(5000).astype(np.float32)
+    cand = np.array([1, 4, 7, -1], np.int32)
+    got = O.masked_topk(s, 100, cand, 512)
+    inc = [j for j in range(5000) if j // 512 in (1, 4, 7)]
+    want = sorted(inc, key=lambda j: (-float(s[j]), j))[:100]
+    assert set(got.tolist()) == set(want)
+    # every block listed: plain top-k; fewer included entries than k: all of them
+    assert set(O.masked_topk(s, 100, np.arange(10), 512).tolist()) == set(O.topk_select(s, 100).tolist())
+    few = O.masked_topk(s[:700], 600, np.array([1], np.int32), 512)
+    assert sorted(few[:188].tolist()) == list(range(512, 700)) and np.all(few[188:] == -1)
+    assert np.all(O.masked_topk(s, 10, np.array([-1, -1]), 512) == -1)
