@@ -131,6 +131,20 @@ SMALL_CONFIGS = {
     "small_c4_cand_src": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_c4_cand_src", B=3,
                                              explicit_lens=(20000, 6000, 900), cand_block=512, cand_topk=4,
                                              cand_write=True),
+    # candidates with two query tokens a sequence (scored densely, masked per token), on CUDA-core fp32
+    # keys, and on rows long enough for the sliced top-k (n_c > 32768)
+    "small_c4_cand_mtp": dataclasses.replace(CONFIGS["csa_c4_fp8"], name="small_c4_cand_mtp", B=5,
+                                             explicit_lens=(9000, 4100, 2050, 3000, 7000), cand_block=256,
+                                             cand_topk=5),
+    "small_c4_cand_f32": dataclasses.replace(CONFIGS["tiny_c4_f32"], name="small_c4_cand_f32", B=5,
+                                             explicit_lens=(2400, 1300, 1029, 2000, 3333), cand_block=128,
+                                             cand_topk=3),
+    "small_c4_cand_long": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_c4_cand_long", B=5,
+                                              explicit_lens=(140000, 8000, 4000, 3000, 139001), cand_block=2048,
+                                              cand_topk=6),
+    "small_c4_cand_src_long": dataclasses.replace(CONFIGS["csa_c4_mxfp4"], name="small_c4_cand_src_long", B=2,
+                                                  q_per_seq=2, explicit_lens=(140000, 5000), cand_block=128,
+                                                  cand_topk=16, cand_write=True),
     "small_c4_mxfp4": dataclasses.replace(CONFIGS["csa_c4_mxfp4"], name="small_c4_mxfp4", B=3, q_per_seq=2,
                                           explicit_lens=(9001, 2050, 700)),
     # 32 query heads padded to 64 by the fused query preparation
@@ -378,14 +392,27 @@ def make_step(cfg: Config, with_given_topk: bool = True) -> StepInputs:
             st.ik_norm_w = draw.normal_f32("ik_norm_w", (cfg.d_I,), 0.1, 1.0)
 
     if cfg.cand_block and not cfg.cand_write:
-        # another layer's published candidates: distinct visible blocks of each token, increasing, -1 padded
-        c = np.full((T, cfg.cand_topk), -1, np.int32)
+        # another layer's published candidates: distinct visible blocks of each token, increasing, -1
+        # padded; by token: full lists, lists holding the partial last block, half-full lists, an empty
+        # list, and lists whose increasing run ends early (a smaller or equal entry, then more blocks)
+        M = cfg.cand_topk
+        c = np.full((T, M), -1, np.int32)
         rng = draw.rng("cand_in")
         for t in range(T):
             nblk = ((int(positions[t]) + 1) // r + cfg.cand_block - 1) // cfg.cand_block
-            m = min(nblk, cfg.cand_topk)
-            if m:
-                c[t, :m] = np.sort(rng.choice(nblk, size=m, replace=False)) if nblk > m else np.arange(nblk)
+            kind = t % 5
+            m = min(nblk, M) if kind != 2 else min(nblk, M) // 2
+            if t % 7 == 5:
+                m = 0
+            if m == 0:
+                continue
+            sel = rng.choice(nblk, size=m, replace=False) if nblk > m else np.arange(nblk)
+            if kind == 1 and nblk - 1 not in sel:
+                sel[0] = nblk - 1
+            sel = np.sort(sel)
+            if kind == 4 and m >= 3:
+                sel[m // 2] = sel[m // 2 - 1]  # the run ends here; the entries after it are not listed
+            c[t, :m] = sel
         st.cand_in = c
 
     if cfg.topk > 0 and with_given_topk:

@@ -546,14 +546,26 @@ def candidate_blocks(scores, block: int, m: int) -> np.ndarray:
     return out
 
 
+def listed_blocks(cand) -> list:
+    """The blocks a candidate list names: its entries up to the first one that is negative or not
+    larger than the entry before it (a source writes its blocks in increasing order, then -1; the
+    pages fix no order, this is the reading taken so that a list is one increasing run)."""
+    out = []
+    for c in np.asarray(cand).tolist():
+        if c < 0 or (out and c <= out[-1]):
+            break
+        out.append(int(c))
+    return out
+
+
 def masked_topk(scores, k: int, cand, block: int) -> np.ndarray:
     """Two-level candidate filtering, consumer side ([API] DeepseekV4Indexer: later indexers mask
     their scores to the candidate blocks before their own top-k): only entries whose block
-    (j // block) is listed in `cand` (-1 entries ignored) take part; the k best of them by (score
-    desc, j asc), or all of them when there are at most k; -1 pads to k."""
+    (j // block) is named by `cand` (listed_blocks) take part; the k best of them by (score desc,
+    j asc), or all of them when there are at most k; -1 pads to k."""
     s = np.asarray(scores, np.float32)
     n = s.shape[0]
-    blocks = set(int(c) for c in np.asarray(cand) if c >= 0)
+    blocks = set(listed_blocks(cand))
     inc = np.array([j for j in range(n) if j // block in blocks], np.int64)
     out = np.full(k, -1, np.int32)
     if inc.size == 0:
@@ -681,7 +693,9 @@ def decode_step(st, seqs=None, topk_override=None):
             s = indexer_scores(q_t, st.w_idx[t], keys) if nc else np.zeros(0, np.float32)
             scores[t] = s
             cb = getattr(cfg, "cand_block", 0)
-            if cb and st.cand_in is not None:          # a consumer of another layer's candidate blocks
+            # a consumer of another layer's candidate blocks; a token whose entries all fit in the top-k
+            # takes every entry, as without candidates ([API] DeepseekV4Indexer.forward short-context fill)
+            if cb and st.cand_in is not None and nc > cfg.topk:
                 topk[t] = masked_topk(s, cfg.topk, st.cand_in[t], cb)
             else:
                 topk[t] = topk_select(s, cfg.topk)

@@ -13,6 +13,7 @@ import pytest
 import torch
 from scipy.special import logsumexp, softmax
 
+import dsv4_inputs as I
 from oracle import dsv4_oracle as O
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_numbers.json")
@@ -573,3 +574,32 @@ def test_masked_topk_brute_force_and_reductions():
     few = O.masked_topk(s[:700], 600, np.array([1], np.int32), 512)
     assert sorted(few[:188].tolist()) == list(range(512, 700)) and np.all(few[188:] == -1)
     assert np.all(O.masked_topk(s, 10, np.array([-1, -1]), 512) == -1)
+
+
+def test_listed_blocks_is_the_increasing_run():
+    assert O.listed_blocks([2, 5, 9, -1]) == [2, 5, 9]
+    assert O.listed_blocks([2, 5, 5, 9]) == [2, 5]        # an equal entry ends the run
+    assert O.listed_blocks([4, 1, 7]) == [4]              # so does a smaller one
+    assert O.listed_blocks([-1, 3]) == [] and O.listed_blocks([]) == []
+    s = np.arange(1000, dtype=np.float32)
+    got = O.masked_topk(s, 10, np.array([1, 0, 2]), 128)   # only block 1 is listed
+    assert sorted(got.tolist()) == list(range(246, 256))
+
+
+def test_consumer_token_within_topk_takes_every_entry():
+    # a consumer token whose entries all fit in the top-k selects all of them whatever its list says;
+    # one with more entries keeps only its listed blocks
+    import dataclasses
+    cfg = dataclasses.replace(I.SMALL_CONFIGS["small_c4_cand"], B=2, explicit_lens=(400, 2200))
+    st = I.make_step(cfg)
+    st.cand_in[:] = -1
+    st.cand_in[:, 0] = 0
+    res = O.decode_step(st)
+    n0 = 400 // 4
+    assert sorted(res["topk"][0][:n0].tolist()) == list(range(n0)) and np.all(res["topk"][0][n0:] == -1)
+    n1 = 2200 // 4                                   # 550 > 512: block 0 (entries 0..549 with 1024-entry blocks)
+    assert sorted(res["topk"][1][res["topk"][1] >= 0].tolist()) == sorted(
+        O.topk_select(res["scores"][1], cfg.topk)[:512].tolist())
+    st.cand_in[1, 0] = 1                              # a block past the token's entries: nothing is listed
+    res = O.decode_step(st)
+    assert np.all(res["topk"][1] == -1) and n1 > cfg.topk

@@ -18,8 +18,18 @@ def test_oracle_step_runs_and_is_consistent(name):
             p = int(st.positions[t])
             nc = O.n_compressed(p, cfg.ratio)
             sel = res["topk"][t]
-            assert np.sum(sel >= 0) == min(nc, cfg.topk)
+            avail = nc
+            if cfg.cand_block and not cfg.cand_write and nc > cfg.topk:
+                # a candidate consumer: only entries of its listed blocks
+                listed = set(O.listed_blocks(st.cand_in[t]))
+                avail = sum(1 for j in range(nc) if j // cfg.cand_block in listed)
+                assert all(j // cfg.cand_block in listed for j in sel[sel >= 0])
+            assert np.sum(sel >= 0) == min(avail, cfg.topk)
             assert np.all(sel[sel >= 0] < nc)
+            if cfg.cand_block and cfg.cand_write:
+                cb = res["cand_out"][t]
+                nblk = -(-nc // cfg.cand_block)
+                assert np.sum(cb >= 0) == min(nblk, cfg.cand_topk) and np.all(np.diff(cb[cb >= 0]) > 0)
     # every emitting token wrote exactly one main-cache row at j = p // ratio
     if cfg.ratio:
         emit = [(t // cfg.q_per_seq, int(st.positions[t]) // cfg.ratio) for t in range(cfg.T)
