@@ -114,8 +114,29 @@ def algorithmic_bytes(st, topk_idx=None):
     if cfg.ratio and cfg.topk:
         ib = row_bytes(cfg.idx_dtype, cfg.d_I)
         nc_seq = (pos.reshape(cfg.B, qps)[:, -1] + 1) // cfg.ratio
-        keys = int(nc_seq.sum()) * ib
-        b["indexer"] = keys + T * cfg.I_h * cfg.d_I * act + T * cfg.I_h * 4 + T * cfg.topk * 8
+        n_keys = int(nc_seq.sum())
+        cb = getattr(cfg, "cand_block", 0)
+        if cb and not cfg.cand_write:
+            # a candidate consumer needs the keys of the blocks its tokens name (the increasing run of
+            # each list), or every key of a token whose entries fit in the top-k
+            n_keys = 0
+            for s_ in range(cfg.B):
+                need = set()
+                for t in range(s_ * qps, s_ * qps + qps):
+                    nc_t = (int(pos[t]) + 1) // cfg.ratio
+                    if nc_t <= cfg.topk:
+                        need |= set(range(nc_t))
+                        continue
+                    prev = -1
+                    for blk in st.cand_in[t].tolist():
+                        if blk <= prev:
+                            break
+                        need |= set(range(blk * cb, min((blk + 1) * cb, nc_t)))
+                        prev = blk
+                n_keys += len(need)
+        b["indexer"] = n_keys * ib + T * cfg.I_h * cfg.d_I * act + T * cfg.I_h * 4 + T * cfg.topk * 8
+        if cb:
+            b["indexer"] += T * cfg.cand_topk * 4  # the candidate lists read or written
     # attention: q + out + SWA rows + compressed rows (union of the sequence's selections)
     rows = 0
     for s in range(cfg.B):
@@ -411,7 +432,7 @@ def measure_workload(cfg, K, warmup, world, local, want_e2e):
     return res
 
 
-EXTRA_WORKLOADS = ("hca_c128_bf16", "csa_c4_fp8", "csa_c4_1m", "csa_c4_mxfp4")
+EXTRA_WORKLOADS = ("hca_c128_bf16", "csa_c4_fp8", "csa_c4_1m", "csa_c4_mxfp4", "csa_c4_cand", "csa_c4_src")
 
 
 def run_ours(args):

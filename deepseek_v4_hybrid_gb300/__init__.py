@@ -81,7 +81,10 @@ def dsv4_compress_update(kv_score, positions, q_per_seq, ratio, coff, state, ape
 
 
 def indexer_topk_params(q, q_dtype, weights, k_cache, k_dtype, block_table, positions, q_per_seq, ratio, topk,
-                        page_size, max_context, topk_idx=None, topk_score=None, workspace=None):
+                        page_size, max_context, topk_idx=None, topk_score=None, workspace=None, cand_blocks=None,
+                        cand_block_size=0, cand_write=False):
+    """Parameter struct of dsv4_indexer_topk.  cand_blocks ([T, cand_topk] int32) with cand_block_size > 0
+    turns on two-level candidate filtering: read by a consumer, written by the source (cand_write)."""
     T, n_heads, head_dim = q.shape
     return _abi.make(_abi.IndexerTopkParams, q=_ptr(q), q_dtype=q_dtype, weights=_ptr(weights),
                      k_cache=_ptr(k_cache), k_dtype=k_dtype, num_pages=k_cache.shape[0],
@@ -89,7 +92,9 @@ def indexer_topk_params(q, q_dtype, weights, k_cache, k_dtype, block_table, posi
                      positions=_ptr(positions), T=T, B=T // q_per_seq, q_per_seq=q_per_seq, ratio=ratio,
                      n_heads=n_heads, head_dim=head_dim, topk=topk, page_size=page_size, max_context=max_context,
                      topk_idx=_ptr(topk_idx), topk_score=_ptr(topk_score), workspace=_ptr(workspace),
-                     workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+                     workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+                     cand_blocks=_ptr(cand_blocks), cand_block_size=cand_block_size if cand_blocks is not None else 0,
+                     cand_topk=0 if cand_blocks is None else cand_blocks.shape[1], cand_write=int(cand_write))
 
 
 def dsv4_indexer_topk_workspace_bytes(params) -> int:

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libdsv4.so")
 F32, BF16, FP8_DS_MLA, I8_ROWSCALE, MXFP4 = 0, 1, 2, 3, 4
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_BOUNDS, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 LATENT_DIM, VALUE_DIM, ROPE_DIM, FP8_DS_MLA_BYTES = 576, 512, 64, 656
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 vp, i32, i64, u32, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint32, C.c_float
 
@@ -49,7 +49,8 @@ class IndexerTopkParams(C.Structure):
                 ("positions", vp), ("T", i32), ("B", i32), ("q_per_seq", i32), ("ratio", i32),
                 ("n_heads", i32), ("head_dim", i32), ("topk", i32), ("page_size", i32), ("max_context", i32),
                 ("topk_idx", vp), ("topk_score", vp), ("workspace", vp), ("workspace_bytes", C.c_size_t),
-                ("workspace_zeroed", i32)]
+                ("workspace_zeroed", i32), ("cand_blocks", vp), ("cand_block_size", i32), ("cand_topk", i32),
+                ("cand_write", i32)]
 
 
 class SparseMlaDecodeParams(C.Structure):

@@ -153,6 +153,12 @@ int dsv4_indexer_topk(const dsv4_indexer_topk_params* p, dsv4_stream_t stream) {
         DSV4_ERR_UNSUPPORTED);
   CHECK((int64_t)p->q_per_seq * p->n_heads <= 256, DSV4_ERR_UNSUPPORTED);
   CHECK(p->max_context / p->ratio <= (1 << 20), DSV4_ERR_UNSUPPORTED);
+  if (p->cand_block_size != 0) {
+    const int cb = p->cand_block_size;
+    CHECK(cb >= 128 && cb <= 65536 && (cb & (cb - 1)) == 0, DSV4_ERR_INVALID);
+    CHECK(p->cand_topk >= 1 && p->cand_topk <= 64 && (p->cand_write == 0 || p->cand_write == 1), DSV4_ERR_INVALID);
+    CHECK(p->T == 0 || (p->cand_blocks != nullptr && aligned(p->cand_blocks, 4)), DSV4_ERR_INVALID);
+  }
   if (p->T == 0) return DSV4_OK;
   CHECK(p->q && p->weights && p->k_cache && p->block_table && p->positions && p->topk_idx, DSV4_ERR_INVALID);
   CHECK(aligned(p->q, 16) && aligned(p->k_cache, 16) && aligned(p->weights, 4), DSV4_ERR_INVALID);

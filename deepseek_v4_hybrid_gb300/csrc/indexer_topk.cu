@@ -96,6 +96,42 @@ __device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool
 }
 
 // ------------------------------------------------------------------------------------------------
+// Two-level candidate filtering ("vllm.models.deepseek_v41.attention", DeepseekV4Indexer: the source
+// indexer publishes each token's best blocks of candidate_block_size entries, later indexers keep to
+// them).  A token's list names the blocks of its increasing run: its entries up to the first one that
+// is negative or not larger than the entry before it.
+// ------------------------------------------------------------------------------------------------
+struct CandArgs {
+  int32_t* blocks;  // [T][M]; null: no candidate filtering
+  int M;            // entries a token
+  int lg;           // log2 of the entries of a block (7 .. 16)
+  int write;        // 1: the source (publishes), 0: a consumer (reads)
+};
+
+__host__ inline CandArgs cand_args(const dsv4_indexer_topk_params& p) {
+  CandArgs c{nullptr, 0, 0, 0};
+  if (p.cand_block_size > 0) {
+    c.blocks = p.cand_blocks;
+    c.M = p.cand_topk;
+    while ((1 << c.lg) < p.cand_block_size) ++c.lg;
+    c.write = p.cand_write;
+  }
+  return c;
+}
+
+// Whether list row[0, M) names block blk.
+__device__ __forceinline__ bool cand_names(const int32_t* row, int M, int blk) {
+  int prev = -1;
+  for (int i = 0; i < M; ++i) {
+    const int c = __ldg(row + i);
+    if (c <= prev) return false;
+    if (c >= blk) return c == blk;
+    prev = c;
+  }
+  return false;
+}
+
+// ------------------------------------------------------------------------------------------------
 // Top-k of one token, run by one whole CTA once the token's scores and histogram are complete.
 // The histogram and the score row reach shared memory by bulk (TMA) copies, the row in 16 KB chunks
 // with up to four in flight (plain loads would go through an L1 that the kernels' large shared
@@ -123,7 +159,9 @@ constexpr int SCAN_WARPS_MIN = 8;  // the kernels run top-k with at least 8 warp
 struct Ctl {
   uint64_t bar[NBUF + 1];  // chunk buffers, histogram
   uint32_t bin, above, cnt, ncand;
-  int wt[40];  // block scan scratch
+  uint32_t total;  // block_find_bin: the sum of the histogram
+  int run;         // candidate filtering: entries of the token's list that name blocks
+  int wt[40];      // block scan scratch
 };
 static_assert(sizeof(Ctl) <= CTL_BYTES, "top-k control block");
 
@@ -142,9 +180,12 @@ __device__ __forceinline__ int cand_j(uint64_t v) {
 __host__ __device__ inline int bitmap_words(int n) { return (n + 127) / 128 * 4; }
 __device__ __forceinline__ int bit_word(int j) { return ((j >> 7) << 2) | (j & 3); }
 __device__ __forceinline__ uint32_t bit_mask(int j) { return 1u << ((j >> 2) & 31); }
+// Candidate filtering: one bit per 128-entry block of the row, set when the block lies in a block the
+// token's list names.
+__host__ __device__ inline int incl_words(int n) { return ((n + 127) / 128 + 31) / 32; }
 
 __host__ __device__ inline size_t hist_offset(int n) {
-  return (CTL_BYTES + RBINS * 4 + (size_t)bitmap_words(n) * 4 + 127) / 128 * 128;
+  return (CTL_BYTES + RBINS * 4 + (size_t)bitmap_words(n) * 4 + (size_t)incl_words(n) * 4 + 127) / 128 * 128;
 }
 __host__ __device__ inline size_t fixed_bytes(int n) {
   return hist_offset(n) + (size_t)HIST_BINS * 4 + (size_t)NBUF * CHUNK * 4;
@@ -202,6 +243,7 @@ __device__ __forceinline__ void block_find_bin(const uint32_t* h, uint32_t rem, 
   }
   int total;
   const uint32_t excl = (uint32_t)block_excl_scan((int)sum, c->wt, &total);
+  if (tid == 0) c->total = (uint32_t)total;
   if (tid < FIND_THREADS && excl < rem && excl + sum >= rem) {
     uint32_t cum = excl;
 #pragma unroll
@@ -221,15 +263,17 @@ __device__ __forceinline__ void block_find_bin(const uint32_t* h, uint32_t rem, 
 // j_base + 128 nblocks - 1 (j_base a multiple of 128, nblocks <= CHUNK / 128; entries >= n are
 // ignored).  Entries with bin > bstar set their bit in `bits` (every word of the chunk's blocks
 // below `words` is written, 16 bytes at a time), entries in bstar are appended to `cand` (capacity
-// ccap) through the counter *ncand.  bits (16-byte aligned), cand and ncand may be in shared or
-// global memory.  Warp w owns the consecutive blocks w P .. w P + P - 1 (P <= SCAN_B); lane l reads
-// entries 4 l .. 4 l + 3 of a block as one float4, and the four ballots of "bin > bstar" are the
-// block's four bitmap words.  Candidates are rare: each lane counts its own, the warp takes its slots
-// with one atomic, and each lane writes its candidates to consecutive slots.
+// ccap) through the counter *ncand.  With an inclusion bitmap `incl` (candidate filtering), entries of
+// 128-entry blocks whose bit is clear take no part, and all_in selects every other entry (no
+// candidates).  bits (16-byte aligned), cand and ncand may be in shared or global memory.  Warp w
+// owns the consecutive blocks w P .. w P + P - 1 (P <= SCAN_B); lane l reads entries 4 l .. 4 l + 3
+// of a block as one float4, and the four ballots of "bin > bstar" are the block's four bitmap words.
+// Candidates are rare: each lane counts its own, the warp takes its slots with one atomic, and each
+// lane writes its candidates to consecutive slots.
 constexpr int SCAN_B = CHUNK / 128 / SCAN_WARPS_MIN;  // 128-entry blocks of a chunk per warp (4)
 __device__ __forceinline__ void scan_chunk(const float* sb, int nblocks, int j_base, int n, uint32_t bstar,
                                            uint32_t* bits, int words, uint64_t* cand, uint32_t ccap,
-                                           uint32_t* ncand) {
+                                           uint32_t* ncand, const uint32_t* incl = nullptr, bool all_in = false) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
   const float4* sb4 = reinterpret_cast<const float4*>(sb);
   const int per = (nblocks + NW - 1) / NW;  // <= SCAN_B since NW >= SCAN_WARPS_MIN
@@ -241,39 +285,45 @@ __device__ __forceinline__ void scan_chunk(const float* sb, int nblocks, int j_b
     v[i] = (i < per && blk < nblocks) ? sb4[blk * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   int lc = 0;  // this lane's candidates
+  const bool want_cand = !all_in;
 #pragma unroll
   for (int i = 0; i < SCAN_B; ++i) {
     const int blk = b0 + i;
     const bool live = i < per && blk < nblocks;  // warp-uniform
-    const int nv = live ? n - (j_base + blk * 128 + 4 * lane) : 0;  // entries c < nv of the lane are valid
+    const int gb = (j_base >> 7) + blk;
+    const bool inb = incl == nullptr || (live && ((incl[gb >> 5] >> (gb & 31)) & 1u));  // warp-uniform
+    const int nv = live && inb ? n - (j_base + blk * 128 + 4 * lane) : 0;  // entries c < nv of the lane count
     const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint32_t sw[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint32_t bin = order_key(e[c]) >> HIST_SHIFT;
-      sw[c] = __ballot_sync(0xffffffffu, c < nv && bin > bstar);
-      lc += (c < nv && bin == bstar) ? 1 : 0;
+      sw[c] = __ballot_sync(0xffffffffu, c < nv && (all_in || bin > bstar));
+      lc += (want_cand && c < nv && bin == bstar) ? 1 : 0;
     }
     const int wg = ((j_base >> 7) + blk) * 4;
     if (lane == 0 && live && wg < words) *reinterpret_cast<uint4*>(bits + wg) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
   }
   const int wtot = __reduce_add_sync(0xffffffffu, lc);
   if (wtot == 0) return;  // warp-uniform
-  int incl = lc;
+  int scan = lc;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
+    const int u = __shfl_up_sync(0xffffffffu, scan, o);
+    if (lane >= o) scan += u;
   }
   uint32_t base = 0;
   if (lane == 0) base = atomicAdd(ncand, (uint32_t)wtot);
-  uint32_t idx = __shfl_sync(0xffffffffu, base, 0) + (uint32_t)(incl - lc);
+  uint32_t idx = __shfl_sync(0xffffffffu, base, 0) + (uint32_t)(scan - lc);
   if (lc == 0) return;
 #pragma unroll
   for (int i = 0; i < SCAN_B; ++i) {
     const int blk = b0 + i;
     const int j0 = j_base + blk * 128 + 4 * lane;
-    const int nv = (i < per && blk < nblocks) ? n - j0 : 0;
+    const int gb = (j_base >> 7) + blk;
+    const bool live = i < per && blk < nblocks;
+    const bool inb = incl == nullptr || (live && ((incl[gb >> 5] >> (gb & 31)) & 1u));
+    const int nv = live && inb ? n - j0 : 0;
     const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -286,32 +336,38 @@ __device__ __forceinline__ void scan_chunk(const float* sb, int nblocks, int j_b
   }
 }
 
-// Exact choice of the R largest of m candidate values (unique), OR-ed into the bitmap: a radix
-// select of 10-bit digits that stops at the first digit whose bin holds exactly the entries still
-// needed.  rb: RBINS shared bins.  Whole CTA.
+// Threshold of the R largest (0 < R < m) of m unique values get(i) < 2^(TOP + 10): a radix select of
+// 10-bit digits from bit TOP down that stops at the first digit whose bin holds exactly the values
+// still needed; the R largest are the values >= the result.  rb: RBINS shared bins.  Whole CTA.
+template <int TOP, typename Get>
+__device__ uint64_t radix_threshold(uint32_t m, int R, uint32_t* rb, Ctl* c, Get get) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  uint64_t prefix = 0, thr = 0;
+  uint32_t rem = (uint32_t)R;
+  for (int shift = TOP; shift >= 0; shift -= 10) {
+    for (int x = tid; x < RBINS; x += NT) rb[x] = 0u;
+    __syncthreads();
+    const uint64_t hmask = shift == TOP ? 0ull : (~0ull << (shift + 10)) & ((1ull << (TOP + 10)) - 1ull);
+    for (uint32_t i = tid; i < m; i += NT) {
+      const uint64_t v = get(i);
+      if ((v & hmask) == prefix) atomicAdd(&rb[(v >> shift) & (RBINS - 1)], 1u);
+    }
+    __syncthreads();
+    block_find_bin<RBINS / FIND_THREADS>(rb, rem, c);
+    prefix |= (uint64_t)c->bin << shift;
+    rem -= c->above;
+    thr = prefix;
+    if (c->cnt == rem) break;  // every value of this digit is needed: v >= prefix selects them
+  }
+  return thr;
+}
+
+// Exact choice of the R largest of m candidate values (unique), OR-ed into the bitmap.  Whole CTA.
 __device__ void select_candidates(const uint64_t* cand, uint32_t m, int R, uint32_t* rb, Ctl* c, uint32_t* bits) {
   const int tid = threadIdx.x, NT = blockDim.x;
   if (R <= 0) return;
-  uint64_t thr = 0;
-  if ((uint32_t)R < m) {
-    uint64_t prefix = 0;
-    uint32_t rem = (uint32_t)R;
-    for (int shift = 30; shift >= 0; shift -= 10) {
-      for (int x = tid; x < RBINS; x += NT) rb[x] = 0u;
-      __syncthreads();
-      const uint64_t hmask = shift == 30 ? 0ull : ((1ull << 40) - 1ull) & ~((1ull << (shift + 10)) - 1ull);
-      for (uint32_t i = tid; i < m; i += NT) {
-        const uint64_t v = cand[i];
-        if ((v & hmask) == prefix) atomicAdd(&rb[(v >> shift) & (RBINS - 1)], 1u);
-      }
-      __syncthreads();
-      block_find_bin<RBINS / FIND_THREADS>(rb, rem, c);
-      prefix |= (uint64_t)c->bin << shift;
-      rem -= c->above;
-      thr = prefix;
-      if (c->cnt == rem) break;  // every candidate of this digit is needed: v >= prefix selects them
-    }
-  }
+  const uint64_t thr =
+      (uint32_t)R < m ? radix_threshold<30>(m, R, rb, c, [&](uint32_t i) { return cand[i]; }) : 0ull;
   for (uint32_t i = tid; i < m; i += NT) {
     const uint64_t v = cand[i];
     if (v >= thr) {
@@ -365,12 +421,94 @@ __device__ void write_selection(const uint32_t* bits, bool bits_global, int word
   }
 }
 
+// Inclusion bitmap (incl_words(n) words of shared memory) of a consumer token with list row[0, M) and
+// blocks of 2^lg entries: bit g set when 128-entry block g of the row lies in a named block.  Whole CTA.
+__device__ void build_incl(const int32_t* row, int M, int lg, int n, uint32_t* incl, Ctl* c) {
+  const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31;
+  const int nb = (n + 127) >> 7, iw = incl_words(n);
+  for (int x = tid; x < iw; x += NT) incl[x] = 0u;
+  if (tid < 32) {  // the run: the first entry that is negative or not above the one before ends it
+    int run = M;
+    for (int base = 0; base < M; base += 32) {
+      const int i = base + lane;
+      const int ci = i < M ? __ldg(row + i) : 0;
+      const int cp = i == 0 ? -1 : (i < M ? __ldg(row + i - 1) : 0);
+      const unsigned bad = __ballot_sync(0xffffffffu, i < M && ci <= cp);
+      if (bad) {
+        run = base + __ffs(bad) - 1;
+        break;
+      }
+    }
+    if (lane == 0) c->run = run;
+  }
+  __syncthreads();
+  const int sh = lg - 7, per = 1 << sh;  // 128-entry blocks of a candidate block
+  const int run = c->run;
+  for (int x = tid; x < run * per; x += NT) {
+    const int blk = __ldg(row + (x >> sh));
+    if (blk > ((nb - 1) >> sh)) continue;  // past the row
+    const int g = (blk << sh) + (x & (per - 1));
+    if (g < nb) atomicOr(&incl[g >> 5], 1u << (g & 31));
+  }
+  __syncthreads();
+}
+
+// The source's publication for one token: out[0, M) = the M blocks of 2^lg entries with the largest
+// block score (the largest score of the block's entries j < n; ties: lower block first) in increasing
+// order, or every block then -1 when there are at most M.  The row s_g is read from global memory
+// (16-byte aligned, room for round_up(n, 128) entries); buf: shared memory of at least
+// CTL_BYTES + 4 RBINS + 4 ceil(n / 2^lg) bytes.  Whole CTA.
+__device__ void publish_blocks(const float* s_g, int n, int lg, int M, int32_t* out, uint8_t* buf) {
+  const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31, warp = tid >> 5, NW = NT >> 5;
+  const int nblk = n > 0 ? ((n - 1) >> lg) + 1 : 0;
+  if (nblk <= M) {
+    for (int x = tid; x < M; x += NT) out[x] = x < nblk ? x : -1;
+    return;
+  }
+  Ctl* c = reinterpret_cast<Ctl*>(buf);
+  uint32_t* rb = reinterpret_cast<uint32_t*>(buf + CTL_BYTES);
+  uint32_t* bkey = rb + RBINS;  // order key of each block's largest score
+  for (int x = tid; x < nblk; x += NT) bkey[x] = 0u;
+  __syncthreads();
+  const int n128 = (n + 127) >> 7;
+  for (int g = warp; g < n128; g += NW) {
+    const int j0 = (g << 7) + 4 * lane;
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(s_g + j0));
+    uint32_t k = 0u;  // below every score's order key
+    if (j0 < n) k = order_key(v.x);
+    if (j0 + 1 < n) k = max(k, order_key(v.y));
+    if (j0 + 2 < n) k = max(k, order_key(v.z));
+    if (j0 + 3 < n) k = max(k, order_key(v.w));
+    k = __reduce_max_sync(0xffffffffu, k);
+    if (lane == 0) atomicMax(&bkey[(g << 7) >> lg], k);
+  }
+  __syncthreads();
+  // value of block i: its key, then the lower block first (blocks < 2^20)
+  auto val = [&](uint32_t i) { return ((uint64_t)bkey[i] << J_BITS) | (uint64_t)((1u << J_BITS) - 1u - i); };
+  const uint64_t thr = radix_threshold<50>((uint32_t)nblk, M, rb, c, val);
+  // the M selected blocks in increasing order: thread i takes a run of blocks
+  const int per = (nblk + NT - 1) / NT;
+  const int k0 = min(nblk, tid * per), k1 = min(nblk, k0 + per);
+  int cnt = 0;
+  for (int i = k0; i < k1; ++i) cnt += val((uint32_t)i) >= thr ? 1 : 0;
+  int total;
+  int pos = block_excl_scan(cnt, c->wt, &total);
+  for (int i = k0; i < k1; ++i)
+    if (val((uint32_t)i) >= thr && pos < M) out[pos++] = i;
+  for (int x = total + tid; x < M; x += NT) out[x] = -1;  // never: exactly M values are >= thr
+  __syncthreads();
+}
+
 // The whole CTA selects the top K of token scores s_g[0, n) (row 16-byte aligned with room for
 // round_up(n, 128) entries; the histogram hist_g of their order keys is complete) into out[0, K) in
 // increasing j (out_s: their scores, may be null); gcand (n entries) holds candidates that do not fit
-// in `buf` (buf_bytes of 128-byte aligned shared memory).  Returns false if a copy timed out.
+// in `buf` (buf_bytes of 128-byte aligned shared memory).  A consumer of candidate blocks passes its
+// list crow[0, cM) (blocks of 2^clg entries): when n > K only entries of named blocks take part (the
+// histogram counts only those), and when they are at most K all of them are selected.  Returns false
+// if a copy timed out.
 __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int32_t* out, float* out_s,
-                           uint64_t* gcand, uint8_t* buf, size_t buf_bytes, volatile int* abort) {
+                           uint64_t* gcand, uint8_t* buf, size_t buf_bytes, volatile int* abort,
+                           const int32_t* crow = nullptr, int cM = 0, int clg = 0) {
   const int tid = threadIdx.x, NT = blockDim.x;
   if (n <= K) {  // short context: every entry, in order (the histogram is cleared for the next call)
     for (int x = tid; x < K; x += NT) {
@@ -390,6 +528,7 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
   uint32_t* rb = reinterpret_cast<uint32_t*>(buf + CTL_BYTES);
   const int words = bitmap_words(n);
   uint32_t* bits = rb + RBINS;
+  uint32_t* incl = crow ? bits + words : nullptr;  // consumer: named 128-entry blocks
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(buf + hist_offset(n));
   uint8_t* chunks = reinterpret_cast<uint8_t*>(hist_s + HIST_BINS);
   uint64_t* cand_s = reinterpret_cast<uint64_t*>(buf + fixed);
@@ -428,6 +567,7 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
     tc::bulk_load(hist_s, hist_g, HIST_BINS * 4, &c->bar[NBUF]);
     for (int cc = 0; cc < min(NBUF, nchunks); ++cc) issue(cc);
   }
+  if (incl) build_incl(crow, cM, clg, n, incl, c);  // while the copies are in flight
 
   // 1. threshold bin
   if (!__syncthreads_and(tc::mbar_wait_bounded(&c->bar[NBUF], 0, abort))) {
@@ -441,9 +581,11 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
   // reader)
   for (int x = tid; x < HIST_BINS; x += NT) hist_g[x] = 0u;
   block_find_bin<HIST_BINS / FIND_THREADS>(hist_s, (uint32_t)K, c);
+  // a consumer whose named blocks hold at most K entries (the histogram counts them) takes all of them
+  const bool all_in = incl != nullptr && c->total <= (uint32_t)K;
   const uint32_t bstar = c->bin;
-  const int R = K - (int)c->above;  // still to choose among the candidates
-  const uint32_t C = c->cnt;        // scores in the threshold bin
+  const int R = all_in ? 0 : K - (int)c->above;  // still to choose among the candidates
+  const uint32_t C = all_in ? 0u : c->cnt;       // scores in the threshold bin
   uint64_t* cand = C <= cap ? cand_s : gcand;
   const uint32_t ccap = C <= cap ? cap : (uint32_t)n;
 
@@ -455,7 +597,8 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
       break;
     }
     const float* sb = reinterpret_cast<const float*>(chunks + (size_t)(cc % NBUF) * CHUNK * 4);
-    scan_chunk(sb, min(CHUNK, n128 - cc * CHUNK) >> 7, cc * CHUNK, n, bstar, bits, words, cand, ccap, &c->ncand);
+    scan_chunk(sb, min(CHUNK, n128 - cc * CHUNK) >> 7, cc * CHUNK, n, bstar, bits, words, cand, ccap, &c->ncand,
+               incl, all_in);
     if (cc + NBUF < nchunks) {
       tc::fence_proxy_async_smem();  // reads of this buffer come before the next copy into it
       __syncthreads();
@@ -496,6 +639,20 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
   const int nc_last = visible_entries(p, t0 + qps - 1);  // largest n_c among the seq's tokens
   const int j0 = tile * IX_TILE;
   if (j0 >= nc_last) return;
+  // candidate consumer: the tokens whose list names this tile's block (or whose entries all fit in the
+  // top-k); a tile no token counts is not scored
+  uint32_t incm = 0xFu;
+  if (p.cand_block_size > 0 && !p.cand_write) {
+    const int lg = __ffs(p.cand_block_size) - 1;
+    incm = 0u;
+    for (int k = 0; k < qps; ++k) {
+      const int nk = visible_entries(p, t0 + k);
+      if (j0 < nk && (nk <= p.topk || cand_names(p.cand_blocks + (int64_t)(t0 + k) * p.cand_topk, p.cand_topk,
+                                                   j0 >> lg)))
+        incm |= 1u << k;
+    }
+    if (incm == 0u) return;  // block-uniform
+  }
 
   float* q_s = smem;                         // [qps][Ih][d]
   float* w_s = q_s + qps * Ih * d;           // [qps][Ih]
@@ -554,7 +711,7 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
       acc *= kscale;  // int8 keys: code . q, then the row scale
       s = fmaf(w_s[k * Ih + h], fmaxf(acc, 0.f), s);
     }
-    const bool on = j < nc;
+    const bool on = j < nc && ((incm >> k) & 1u);
     if (on) bufs.scores[(int64_t)t * bufs.nc_stride + j] = s;
     hist_add_warp(bufs.hist + (int64_t)t * HIST_BINS, order_key(s) >> HIST_SHIFT, on);
   }
@@ -614,6 +771,12 @@ struct Args {
   int nqs;        // query slots (2, or 1 when shared memory is short)
   const uint8_t* k_raw;  // int8 key cache
   int N, kblk, stages, tmem_cols, nacc;
+  // candidate filtering: lists [T][cM] of blocks of 2^clg entries (2^csh tiles)
+  int32_t* cand;
+  int cM, clg, csh;
+  int cskip;   // consumer with one token a sequence: only the tiles of named blocks are scored
+  int cmask;   // consumer with more tokens a sequence: every tile scored, each token's named blocks counted
+  int cwrite;  // the source: publishes each token's best blocks after its top-k
 };
 
 struct Smem {
@@ -642,33 +805,67 @@ __device__ __forceinline__ int page_of(const Args& a, int b, int lp) {
   return pg;
 }
 
-// Walks the valid (sequence, tile) items of the flat range [lo, hi) in order without divisions.
+// Key tiles of sequence b (nc entries) that the kernel scores: every tile, or for a candidate consumer
+// with one token a sequence and nc > K, the tiles of the named blocks that hold entries (the named
+// blocks increase, so only the last of them can be partial).
+__device__ int live_tiles(const Args& a, int b, int nc) {
+  const int nt = (nc + TILE - 1) / TILE;
+  if (!a.cskip || nc <= a.K) return nt;
+  const int32_t* row = a.cand + (int64_t)b * a.cM;
+  const int last = (nt - 1) >> a.csh;  // the block holding the last entry
+  int prev = -1, tiles = 0;
+  for (int i0 = 0; i0 < a.cM; i0 += 8) {
+    int blk[8];  // eight list entries loaded together
+#pragma unroll
+    for (int u = 0; u < 8; ++u) blk[u] = i0 + u < a.cM ? __ldg(row + i0 + u) : -1;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (blk[u] <= prev || blk[u] > last) return tiles;  // the run ends, or the block lies past the entries
+      tiles += min(1 << a.csh, nt - (blk[u] << a.csh));
+      prev = blk[u];
+    }
+  }
+  return tiles;
+}
+
+// Tile of slot v of sequence b: the slot itself, or slot v of the concatenated named blocks.
+__device__ __forceinline__ int slot_tile(const Args& a, const int32_t* row, int v) {
+  return row ? (__ldg(row + (v >> a.csh)) << a.csh) | (v & ((1 << a.csh) - 1)) : v;
+}
+__device__ __forceinline__ const int32_t* slot_row(const Args& a, int b, int nc) {
+  return (a.cskip && nc > a.K) ? a.cand + (int64_t)b * a.cM : nullptr;
+}
+
+// Walks the items of the flat range [lo, hi) of the (sequence, slot) grid in order without divisions;
+// slot v < live_tiles of sequence b is its v-th scored tile.
 struct ItemIter {
-  int it, hi, b, tile, nc;
+  int it, hi, b, v, nt, nc, tile;
+  __device__ __forceinline__ void enter(const Args& a) {
+    nc = seq_entries(a, b);
+    nt = live_tiles(a, b, nc);
+  }
   __device__ __forceinline__ void init(const Args& a, int lo, int hi_) {
     it = lo;
     hi = hi_;
     b = lo / a.tiles_max;
-    tile = lo % a.tiles_max;
-    nc = it < hi ? seq_entries(a, b) : 0;
+    v = lo % a.tiles_max;
+    nt = 0;
+    if (it < hi) enter(a);
     skip(a);
   }
-  // moves past tiles beyond the end of the current sequence
+  // moves past slots beyond the end of the current sequence (nt <= tiles_max)
   __device__ __forceinline__ void skip(const Args& a) {
-    while (it < hi && tile * TILE >= nc) {
-      it += a.tiles_max - tile;
+    while (it < hi && v >= nt) {
+      it += a.tiles_max - v;
       ++b;
-      tile = 0;
-      if (it < hi) nc = seq_entries(a, b);
+      v = 0;
+      if (it < hi) enter(a);
     }
+    if (it < hi) tile = slot_tile(a, slot_row(a, b, nc), v);
   }
   __device__ __forceinline__ void next(const Args& a) {
     ++it;
-    if (++tile == a.tiles_max) {
-      ++b;
-      tile = 0;
-      if (it < hi) nc = seq_entries(a, b);
-    }
+    ++v;
     skip(a);
   }
   __device__ __forceinline__ bool valid() const { return it < hi; }
@@ -691,7 +888,7 @@ __device__ __forceinline__ bool finish_seq(const Args& a, Smem* sm, uint32_t* hi
   __threadfence();  // this thread's scores and histogram counts before the counter below
   if (!tc::group_sync(&sm->ebar[g], ephase, abort)) return false;
   if (row == 0) {
-    const uint32_t tiles = (uint32_t)((seq_entries(a, b) + TILE - 1) / TILE);
+    const uint32_t tiles = (uint32_t)live_tiles(a, b, seq_entries(a, b));
     const uint32_t prev = atomicAdd(&a.bufs.seq_done[b], (uint32_t)ntile);
     if (prev + (uint32_t)ntile == tiles) {
       a.bufs.seq_done[b] = 0u;  // complete: no CTA adds to it again in this call; cleared for the next
@@ -767,7 +964,7 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
     if (a.B <= PRE_MAX) {
       // the tile counts first (independent loads, all in flight together), then the scan
 #pragma unroll 4
-      for (int b = lane; b < a.B; b += 32) sm->pre[b] = (seq_entries(a, b) + TILE - 1) / TILE;
+      for (int b = lane; b < a.B; b += 32) sm->pre[b] = live_tiles(a, b, seq_entries(a, b));
       __syncwarp();
       int running = 0;
       for (int b0 = 0; b0 < a.B; b0 += 32) {
@@ -844,18 +1041,21 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
     uint32_t phase = 0;
     bool stop = false;
     const uint64_t pol = tc::l2_policy_evict_first();
-    for (int base_it = lo; base_it < hi && !stop; base_it += 32) {
-      const int it = base_it + lane;
-      int vb = -1, pg0 = -1, pg1 = -1;
-      if (it < hi) {
-        const int b = it / a.tiles_max, tile = it % a.tiles_max;
-        const int nc = seq_entries(a, b);
-        const int j0 = tile * TILE;
-        if (j0 < nc) {
-          vb = b;
-          pg0 = page_of(a, b, j0 / 64);
-          pg1 = (j0 + 64 < nc) ? page_of(a, b, j0 / 64 + 1) : -1;
+    ItemIter cur;  // every lane walks the same items; lane i keeps the i-th of each group of 32
+    cur.init(a, lo, hi);
+    while (cur.valid() && !stop) {
+      int vb = -1, pg0 = -1, pg1 = -1, j0 = 0, nc = 0;
+      for (int i = 0; i < 32 && cur.valid(); ++i) {
+        if (lane == i) {
+          vb = cur.b;
+          j0 = cur.tile * TILE;
+          nc = cur.nc;
         }
+        cur.next(a);
+      }
+      if (vb >= 0) {  // the block-table pages of the 32 items, looked up together
+        pg0 = page_of(a, vb, j0 / 64);
+        pg1 = (j0 + 64 < nc) ? page_of(a, vb, j0 / 64 + 1) : -1;
       }
       for (int i = 0; i < 32; ++i) {
         const int b = __shfl_sync(0xffffffffu, vb, i);
@@ -1152,12 +1352,21 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->dempty[acc]);
       const int j = cur.tile * TILE + row;
+      uint32_t incm = 0xFu;  // tokens that count this tile (a consumer: those whose list names its block)
+      if (a.cmask) {
+        incm = 0u;
+#pragma unroll
+        for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q)
+          if (q < a.qps && (nc_tok[q] <= a.K ||
+                            cand_names(a.cand + (int64_t)(b * a.qps + q) * a.cM, a.cM, cur.tile >> a.csh)))
+            incm |= 1u << q;
+      }
 #pragma unroll
       for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q) {
         if (q < a.qps) {
           sk[q] *= kscale;  // 1 for bf16 keys
           const int t = b * a.qps + q;
-          const bool on = j < nc_tok[q];
+          const bool on = j < nc_tok[q] && ((incm >> q) & 1u);
           if (on) a.bufs.scores[(int64_t)t * a.bufs.nc_stride + j] = sk[q];
           hist_add_warp(hist_g + q * HIST_BINS, order_key(sk[q]) >> HIST_SHIFT, on);
         }
@@ -1183,23 +1392,29 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
     for (int q = 0; q < a.qps; ++q) {
       const int t = b * a.qps + q;
       const int n = visible_entries(a.positions, t, a.max_context, a.ratio);
-      if (!tk::topk_token(a.bufs.scores + (int64_t)t * a.bufs.nc_stride, a.bufs.hist + (int64_t)t * HIST_BINS, n, a.K,
-                          a.topk_idx + (int64_t)t * a.K, a.topk_score ? a.topk_score + (int64_t)t * a.K : nullptr,
-                          a.bufs.cand + (int64_t)t * a.bufs.nc_stride, tbuf, tbytes, abort)) {
+      const float* srow = a.bufs.scores + (int64_t)t * a.bufs.nc_stride;
+      if (!tk::topk_token(srow, a.bufs.hist + (int64_t)t * HIST_BINS, n, a.K, a.topk_idx + (int64_t)t * a.K,
+                          a.topk_score ? a.topk_score + (int64_t)t * a.K : nullptr,
+                          a.bufs.cand + (int64_t)t * a.bufs.nc_stride, tbuf, tbytes, abort,
+                          (a.cskip || a.cmask) ? a.cand + (int64_t)t * a.cM : nullptr, a.cM, a.clg)) {
         if (threadIdx.x == 0) atomicOr(&g_flags_ix, FLAG_TIMEOUT);
         return;
       }
+      if (a.cwrite) tk::publish_blocks(srow, n, a.clg, a.cM, a.cand + (int64_t)t * a.cM, tbuf);
     }
   }
-  // sequences without a visible entry have no tile (nobody completes them): all -1
+  // sequences without a scored tile (no visible entry, or a consumer's list naming none) are completed
+  // by nobody: all -1 (the source publishes no block)
   for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-    if (seq_entries(a, b) != 0) continue;
+    if (live_tiles(a, b, seq_entries(a, b)) != 0) continue;
     for (int q = 0; q < a.qps; ++q) {
       const int t = b * a.qps + q;
       for (int x = threadIdx.x; x < a.K; x += blockDim.x) {
         a.topk_idx[(int64_t)t * a.K + x] = -1;
         if (a.topk_score) a.topk_score[(int64_t)t * a.K + x] = -INFINITY;
       }
+      if (a.cwrite)
+        for (int x = threadIdx.x; x < a.cM; x += blockDim.x) a.cand[(int64_t)t * a.cM + x] = -1;
     }
   }
 }
@@ -1245,6 +1460,14 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   a.nraw = 0;
   a.k_raw = reinterpret_cast<const uint8_t*>(p.k_cache);
   a.tmem_cols = a.nacc * a.N <= 64 ? 64 : (a.nacc * a.N <= 128 ? 128 : (a.nacc * a.N <= 256 ? 256 : 512));
+  const CandArgs ca = cand_args(p);
+  a.cand = ca.blocks;
+  a.cM = ca.M;
+  a.clg = ca.lg;
+  a.csh = ca.blocks ? ca.lg - 7 : 0;
+  a.cskip = ca.blocks && !ca.write && p.q_per_seq == 1;
+  a.cmask = ca.blocks && !ca.write && p.q_per_seq > 1;
+  a.cwrite = ca.blocks && ca.write;
   const size_t budget = 227 * 1024;
   auto fixed_for = [&](int nqs, int nraw) {
     return 1024 + (size_t)nqs * a.kblk * a.N * 128 + (size_t)nraw * 2 * 64 * (size_t)a.rec +
@@ -1313,11 +1536,21 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(dsv4_indexer_topk_para
   __syncthreads();
   const int t = blockIdx.x;
   const int n = visible_entries(p, t);
-  if (!tk::topk_token(bufs.scores + (int64_t)t * bufs.nc_stride, bufs.hist + (int64_t)t * HIST_BINS, n, p.topk,
-                      p.topk_idx + (int64_t)t * p.topk, p.topk_score ? p.topk_score + (int64_t)t * p.topk : nullptr,
-                      bufs.cand + (int64_t)t * bufs.nc_stride, tsm, TK_SMEM, &abort_s) &&
-      threadIdx.x == 0)
-    atomicOr(&g_flags_ix, FLAG_TIMEOUT);
+  const bool has_cand = p.cand_block_size > 0;
+  const int lg = has_cand ? __ffs(p.cand_block_size) - 1 : 0;
+  int32_t* crow = has_cand ? p.cand_blocks + (int64_t)t * p.cand_topk : nullptr;
+  const float* srow = bufs.scores + (int64_t)t * bufs.nc_stride;
+  if (!tk::topk_token(srow, bufs.hist + (int64_t)t * HIST_BINS, n, p.topk, p.topk_idx + (int64_t)t * p.topk,
+                      p.topk_score ? p.topk_score + (int64_t)t * p.topk : nullptr,
+                      bufs.cand + (int64_t)t * bufs.nc_stride, tsm, TK_SMEM, &abort_s,
+                      has_cand && !p.cand_write ? crow : nullptr, p.cand_topk, lg)) {
+    if (threadIdx.x == 0) atomicOr(&g_flags_ix, FLAG_TIMEOUT);
+    return;
+  }
+  if (has_cand && p.cand_write) {
+    __syncthreads();
+    tk::publish_blocks(srow, n, lg, p.cand_topk, crow, tsm);
+  }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1326,6 +1559,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(dsv4_indexer_topk_para
 // bitmap and appends its candidates to the token's list; the CTA that finishes the token's last
 // slice chooses among the candidates and writes the selection (no CTA waits for another).
 // ------------------------------------------------------------------------------------------------
+constexpr int INCL_MAX_WORDS = (1 << 20) / 128 / 32;  // inclusion bitmap of the longest row
 constexpr int SLICE_CHUNKS = 2;  // 8192-score slices: more CTAs per long row (measured faster than 16384)
 constexpr int SLICE = SLICE_CHUNKS * tk::CHUNK;  // 8192 scores
 
@@ -1340,6 +1574,9 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
   const float* s_g = bufs.scores + (int64_t)t * bufs.nc_stride;
   int32_t* out = p.topk_idx + (int64_t)t * K;
   float* out_s = p.topk_score ? p.topk_score + (int64_t)t * K : nullptr;
+  const bool has_cand = p.cand_block_size > 0;
+  const int lg = has_cand ? __ffs(p.cand_block_size) - 1 : 0;
+  int32_t* crow = has_cand ? p.cand_blocks + (int64_t)t * p.cand_topk : nullptr;
   if (n <= K) {  // short context: slice 0 writes every entry, in order, and clears the histogram
     if (sl == 0) {
       for (int x = tid; x < K; x += TK_THREADS) {
@@ -1347,6 +1584,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
         if (out_s) out_s[x] = x < n ? __ldcg(s_g + x) : -INFINITY;
       }
       for (int x = tid; x < HIST_BINS; x += TK_THREADS) bufs.hist[(int64_t)t * HIST_BINS + x] = 0u;
+      if (has_cand && p.cand_write) tk::publish_blocks(s_g, n, lg, p.cand_topk, crow, tsm);
     }
     return;
   }
@@ -1356,8 +1594,9 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
   uint32_t* rb = reinterpret_cast<uint32_t*>(tsm + CTL_BYTES);
   uint32_t* hist_s = rb + RBINS;
   uint8_t* chunks = reinterpret_cast<uint8_t*>(hist_s + HIST_BINS);
-  uint64_t* cand_s = reinterpret_cast<uint64_t*>(chunks + (size_t)SLICE * 4);
-  const size_t fixed = CTL_BYTES + RBINS * 4 + HIST_BINS * 4 + (size_t)SLICE * 4;
+  uint32_t* incl = reinterpret_cast<uint32_t*>(chunks + (size_t)SLICE * 4);  // consumer: named 128-entry blocks
+  uint64_t* cand_s = reinterpret_cast<uint64_t*>(incl + INCL_MAX_WORDS);
+  const size_t fixed = CTL_BYTES + RBINS * 4 + HIST_BINS * 4 + (size_t)SLICE * 4 + INCL_MAX_WORDS * 4;
   const uint32_t cap = (uint32_t)((TK_SMEM - fixed) / 8);
   const int words = bitmap_words(n);
   uint32_t* bits_g = bufs.bits + (int64_t)t * (bufs.nc_stride / 32);  // nc_stride / 32 >= bitmap_words(n)
@@ -1382,16 +1621,20 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
     }
   }
   __syncthreads();
+  const bool consume = has_cand && !p.cand_write;
+  if (consume) build_incl(crow, p.cand_topk, lg, n, incl, c);  // while the copies are in flight
   bool ok = __syncthreads_and(tc::mbar_wait_bounded(&c->bar[NBUF], 0, &abort_s));
+  bool all_in = false;  // a consumer whose named blocks hold at most K entries takes all of them
   if (ok) {
     block_find_bin<HIST_BINS / FIND_THREADS>(hist_s, (uint32_t)K, c);
+    all_in = consume && c->total <= (uint32_t)K;
     const uint32_t bstar = c->bin;
     for (int cc = 0; cc < nch && ok; ++cc) {
       ok = __syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc], 0, &abort_s));
       if (ok)
         scan_chunk(reinterpret_cast<const float*>(chunks + (size_t)cc * CHUNK * 4),
                    min(CHUNK, n128 - j_lo - cc * CHUNK) >> 7, j_lo + cc * CHUNK, n, bstar, bits_g, words, cand_g,
-                   (uint32_t)n, &bufs.tcnt[2 * t]);
+                   (uint32_t)n, &bufs.tcnt[2 * t], consume ? incl : nullptr, all_in);
     }
   }
   if (!ok) {
@@ -1409,7 +1652,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
   __syncthreads();
   if (!last_s) return;
   __threadfence();
-  const int R = K - (int)c->above;
+  const int R = all_in ? 0 : K - (int)c->above;
   const uint32_t m = min(__ldcg(&bufs.tcnt[2 * t]), (uint32_t)n);
   // every other slice of the token is done with its histogram and counters: cleared for the next call
   for (int x = tid; x < HIST_BINS; x += TK_THREADS) bufs.hist[(int64_t)t * HIST_BINS + x] = 0u;
@@ -1428,6 +1671,10 @@ __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_top
   __threadfence();
   __syncthreads();
   write_selection(bits_g, true, words, K, out, out_s, nullptr, s_g, c, reinterpret_cast<int*>(cand_s));
+  if (has_cand && p.cand_write) {
+    __syncthreads();
+    tk::publish_blocks(s_g, n, lg, p.cand_topk, crow, tsm);
+  }
 }
 
 cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t st) {

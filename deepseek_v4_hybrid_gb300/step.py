@@ -88,10 +88,20 @@ class DeviceStep:
             self.w_idx = dev(st.w_idx)
             self.topk_idx = torch.empty((T, cfg.topk), dtype=torch.int32, device=device)
             self.topk_score = torch.empty((T, cfg.topk), dtype=torch.float32, device=device)
+            # two-level candidate filtering: a consumer reads another layer's blocks, the source writes its own
+            self.cand_blocks = None
+            self.cand_write = bool(getattr(cfg, "cand_write", False))
+            if getattr(cfg, "cand_block", 0):
+                if self.cand_write:
+                    self.cand_blocks = torch.full((T, cfg.cand_topk), -7, dtype=torch.int32, device=device)
+                else:
+                    self.cand_blocks = dev(st.cand_in.astype(np.int32))
             self.ix_params = indexer_topk_params(self.q_idx, cfg.act_dtype, self.w_idx, self.idx_cache,
                                                  cfg.idx_dtype, self.idx_bt, self.positions, cfg.q_per_seq,
                                                  cfg.ratio, cfg.topk, PAGE, self.max_context, self.topk_idx,
-                                                 self.topk_score)
+                                                 self.topk_score, cand_blocks=self.cand_blocks,
+                                                 cand_block_size=getattr(cfg, "cand_block", 0),
+                                                 cand_write=self.cand_write)
             # zero-filled once: every call leaves its histograms and counters cleared, so no call needs a memset
             self.ix_ws = torch.zeros(max(int(dsv4_indexer_topk_workspace_bytes(self.ix_params)), 256),
                                      dtype=torch.uint8, device=device)
@@ -167,4 +177,6 @@ class DeviceStep:
         d = {k: getattr(self, k) for k in self.STEP_INPUTS if getattr(self, k, None) is not None}
         if self.q_prep:
             d["q"] = self.q_in
+        if getattr(self, "cand_blocks", None) is not None and not self.cand_write:
+            d["cand_blocks"] = self.cand_blocks  # the blocks an earlier layer published this step
         return d

@@ -102,6 +102,10 @@ CONFIGS = {
     "csa_c4_cand": Config("csa_c4_cand", B=32, q_per_seq=1, ctx=(65536, 65536), H=64, ratio=4, I_h=64, d_I=128,
                           topk=512, act_dtype=BF16, cache_dtype=BF16, idx_dtype=BF16, out_dtype=BF16,
                           seed=0xD5E4 + 6, cand_block=1024, cand_topk=8),
+    # the CSA c4 bf16 layer as the candidate source (publishes 8 blocks of 1024 per token)
+    "csa_c4_src": Config("csa_c4_src", B=32, q_per_seq=1, ctx=(65536, 65536), H=64, ratio=4, I_h=64, d_I=128,
+                         topk=512, act_dtype=BF16, cache_dtype=BF16, idx_dtype=BF16, out_dtype=BF16,
+                         seed=0xD5E4 + 7, cand_block=1024, cand_topk=8, cand_write=True),
     # the CSA c4 bf16 layer with its indexer keys in the 68-byte MXFP4 record
     "csa_c4_mxfp4": Config("csa_c4_mxfp4", B=32, q_per_seq=1, ctx=(65536, 65536), H=64, ratio=4, I_h=64, d_I=128,
                            topk=512, act_dtype=BF16, cache_dtype=BF16, idx_dtype=MXFP4, out_dtype=BF16,

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define DSV4_ABI_VERSION 2
+#define DSV4_ABI_VERSION 3
 #define DSV4_LATENT_DIM 576
 #define DSV4_VALUE_DIM 512
 #define DSV4_ROPE_DIM 64
@@ -243,6 +243,23 @@ typedef struct dsv4_indexer_topk_params {
                                   zero: the workspace was zero-filled once when allocated, and every
                                   call that completed without raising a flag left it so (each call
                                   clears what it used before it completes) */
+  /* Two-level candidate filtering (API DeepseekV4Indexer: candidate_block_size,
+     candidate_topk_blocks, candidate_write).  Off when cand_block_size is 0 (cand_blocks unused).
+     Compressed entry j lies in candidate block j / cand_block_size.
+     cand_write = 1 (the candidate source): scoring and top-k as above, and cand_blocks[t] receives
+       the cand_topk blocks with the largest block score (the largest s[t][j] of the block's entries
+       j < n_c; ties: lower block first), listed in increasing order, then -1 padding; every block
+       when there are at most cand_topk.
+     cand_write = 0 (a consumer): cand_blocks[t] names token t's blocks: its entries up to the first
+       one that is negative or not larger than the entry before it.  When n_c > topk, only entries of
+       named blocks take part: topk_idx[t] = the min(topk, their count) best of them (same order and
+       padding as above); when n_c <= topk every entry is selected as without candidates.  With one
+       query token a sequence (q_per_seq = 1) the blocks that are not named are never read or scored
+       on the tensor-core path. */
+  int32_t* cand_blocks;        /* [T, cand_topk] int32: read (consumer) or written (source) */
+  int32_t cand_block_size;     /* 0 (off) or a power of two, 128 .. 65536 */
+  int32_t cand_topk;           /* 1 .. 64 blocks per token */
+  int32_t cand_write;          /* 0: consumer, 1: source */
 } dsv4_indexer_topk_params;
 
 size_t dsv4_indexer_topk_workspace_bytes(const dsv4_indexer_topk_params* p);

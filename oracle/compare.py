@@ -111,6 +111,44 @@ def topk_sets_match(gpu_idx, oracle_scores, k, slack=0.0):
     return bool(all(abs(float(s[j]) - float(kth)) <= TIE_EPS + slack for j in diff)), False
 
 
+def included_entries(cand_row, nc, block):
+    """Entries j < nc of the blocks a consumer's list names, increasing."""
+    listed = O.listed_blocks(cand_row)
+    return np.array([j for b in listed for j in range(b * block, min((b + 1) * block, nc))], np.int64)
+
+
+def masked_topk_match(gpu_idx, oracle_scores, k, inc, slack=0.0):
+    """topk_sets_match for a candidate consumer: every selected entry lies in `inc` (the included
+    entries, increasing), and the selection matches the oracle's top-k among them."""
+    g = np.asarray(gpu_idx)
+    valid = g[g >= 0]
+    if not np.all(np.isin(valid, inc)):
+        return False, False
+    sub = np.where(g >= 0, np.searchsorted(inc, np.maximum(g, 0)), -1)  # positions within inc
+    return topk_sets_match(sub, np.asarray(oracle_scores, np.float32)[inc], k, slack)
+
+
+def cand_blocks_match(gpu_row, oracle_scores, block, m, slack=0.0):
+    """The source's published blocks vs the oracle's scores: every block when there are at most m;
+    else m distinct increasing blocks whose set differs from the oracle's only in blocks whose block
+    score lies within TIE_EPS (+ slack) of the oracle's m-th best block score."""
+    s = np.asarray(oracle_scores, np.float32)
+    n = s.shape[0]
+    nblk = -(-n // block)
+    g = np.asarray(gpu_row)
+    if nblk <= m:
+        return bool(np.array_equal(g, np.concatenate([np.arange(nblk), np.full(m - nblk, -1)])))
+    if np.any(g < 0) or np.any(g >= nblk) or np.any(np.diff(g) <= 0):
+        return False
+    want = O.candidate_blocks(s, block, m)
+    diff = set(g.tolist()) ^ set(want.tolist())
+    if not diff:
+        return True
+    bmax = np.array([np.max(s[b * block:(b + 1) * block]) for b in range(nblk)], np.float64)
+    mth = np.sort(bmax)[::-1][m - 1]
+    return bool(all(abs(bmax[b] - mth) <= TIE_EPS + slack for b in diff))
+
+
 def q_out_ok(stored_gpu, stored_oracle, act_dtype):
     """Prepared query heads: padding heads exactly zero; the others within one unit in the last place
     of the activation format (the device normalises in fp32, the oracle in fp64) plus 1e-6 of the
@@ -167,8 +205,17 @@ def check_step(st, res, gpu, where=""):
                     bounds[j] = new_key_score_bound(O.decode_rows(st.q_idx[t], cfg.act_dtype), st.w_idx[t], row,
                                                     cfg.idx_dtype)
             slack = 2.0 * max(bounds.values(), default=0.0)
-            ok, exact = topk_sets_match(gpu["topk_idx"][t], res["scores"][t], cfg.topk, slack)
+            nc = len(res["scores"][t])
+            cb = getattr(cfg, "cand_block", 0)
+            if cb and not getattr(cfg, "cand_write", False) and nc > cfg.topk:
+                inc = included_entries(st.cand_in[t], nc, cb)
+                ok, exact = masked_topk_match(gpu["topk_idx"][t], res["scores"][t], cfg.topk, inc, slack)
+            else:
+                ok, exact = topk_sets_match(gpu["topk_idx"][t], res["scores"][t], cfg.topk, slack)
             assert ok, f"{where} top-k of token {t}"
+            if cb and getattr(cfg, "cand_write", False) and "cand_out" in gpu:
+                assert cand_blocks_match(gpu["cand_out"][t], res["scores"][t], cb, cfg.cand_topk, slack), \
+                    f"{where} published candidate blocks of token {t}"
             same_sel[t] = exact
             rep["tie_tokens"] += int(not exact)
             if "topk_score" in gpu and exact:

@@ -91,7 +91,7 @@ def test_host_validation_rejects_bad_arguments(abi):
     assert lib.dsv4_padded_num_q_heads(64, abi.FP8_DS_MLA) == 64
     assert lib.dsv4_padded_num_q_heads(16, abi.F32) == 16
     assert lib.dsv4_padded_num_q_heads(0, abi.BF16) == -1
-    assert lib.dsv4_abi_version() == abi.ABI_VERSION == 2
+    assert lib.dsv4_abi_version() == abi.ABI_VERSION == 3
 
     c = abi.make(abi.CompressUpdateParams, T=2, B=1, q_per_seq=2, ratio=8, coff=1, page_size=64,
                  max_pages_per_seq=1, max_pos=10, cache_dtype=abi.BF16)
@@ -111,6 +111,16 @@ def test_host_validation_rejects_bad_arguments(abi):
     assert lib.dsv4_indexer_topk(ix, None) == abi.ERR_UNSUPPORTED     # fp8 record is not an indexer key dtype
     ix.k_dtype, ix.head_dim = abi.BF16, 100
     assert lib.dsv4_indexer_topk(ix, None) == abi.ERR_UNSUPPORTED
+    ix.head_dim, ix.cand_block_size, ix.cand_topk = 128, 1000, 8
+    assert lib.dsv4_indexer_topk(ix, None) == abi.ERR_INVALID         # candidate block not a power of two
+    ix.cand_block_size = 64
+    assert lib.dsv4_indexer_topk(ix, None) == abi.ERR_INVALID         # below one 128-entry tile
+    ix.cand_block_size, ix.cand_topk = 1024, 65
+    assert lib.dsv4_indexer_topk(ix, None) == abi.ERR_INVALID         # more than 64 blocks a token
+    ix.cand_topk = 8
+    assert lib.dsv4_indexer_topk(ix, None) == abi.ERR_INVALID         # no candidate list
+    ix.cand_blocks, ix.cand_write = 0x10002, 0
+    assert lib.dsv4_indexer_topk(ix, None) == abi.ERR_INVALID         # misaligned list
 
     at = abi.make(abi.SparseMlaDecodeParams, T=1, B=1, q_per_seq=1, H=256, page_size=64, window=128, ratio=4,
                   swa_max_pages=1, max_context=100, q_dtype=abi.BF16, out_dtype=abi.BF16, cache_dtype=abi.BF16)

@@ -41,6 +41,8 @@ def gpu_results(ds):
         g["idx_cache"] = to_host(ds.idx_cache)
         g["topk_idx"] = to_host(ds.topk_idx)
         g["topk_score"] = to_host(ds.topk_score)
+        if ds.cand_blocks is not None and ds.cand_write:
+            g["cand_out"] = to_host(ds.cand_blocks)
     return g
 
 
@@ -75,7 +77,8 @@ def test_tiny_config_full_parity(lib, name):
 
 @pytest.mark.parametrize("name,seqs", [("csa_c4_bf16", [0, 17, 31]), ("hca_c128_bf16", [0, 21, 63]),
                                        ("csa_c4_fp8", [0, 77, 127]), ("csa_c4_1m", [0, 3]),
-                                       ("csa_c4_mxfp4", [0, 13, 31])])
+                                       ("csa_c4_mxfp4", [0, 13, 31]), ("csa_c4_cand", [0, 4, 5, 31]),
+                                       ("csa_c4_src", [0, 9, 31])])
 def test_full_size_sampled_parity(lib, name, seqs):
     rep, st, ds = run_and_compare(name, seqs=seqs)
     assert rep["tokens"] == len(seqs) * st.cfg.q_per_seq
