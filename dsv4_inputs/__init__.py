@@ -433,6 +433,56 @@ def make_step(cfg: Config, with_given_topk: bool = True) -> StepInputs:
     return st
 
 
+# ------------------------------------------------------------------------------------------------
+# Prefill: P tokens of every sequence from position 0, on caches that hold nothing yet
+# ------------------------------------------------------------------------------------------------
+
+@dataclass
+class PrefillInputs:
+    """A prefill of positions 0 .. P-1 of each of B sequences.  `base` holds every token (token (b, p)
+    at row b * P + p of its per-token arrays) and the caches, whose rows hold seeded garbage until
+    the prefill writes them; chunk() cuts the decode step of some consecutive positions of every
+    sequence out of it, sharing those caches (what one chunk writes, the next reads)."""
+    cfg: Config
+    P: int
+    base: StepInputs
+
+    def chunk(self, p0: int, n: int) -> StepInputs:
+        """The step of positions p0 .. p0 + n - 1 of every sequence (T = B * n, sequence-major)."""
+        cfg, P, st = self.cfg, self.P, self.base
+        rows = (np.arange(cfg.B)[:, None] * P + p0 + np.arange(n)[None, :]).reshape(-1)
+        ccfg = dataclasses.replace(cfg, q_per_seq=n, explicit_lens=tuple([p0 + n] * cfg.B))
+        tok = lambda a: None if a is None else a[rows]  # noqa: E731
+        return dataclasses.replace(st, cfg=ccfg, ctx_len=np.full(cfg.B, p0 + n, np.int64), positions=st.positions[rows],
+                                   kv_new=st.kv_new[rows], slot_mapping=st.slot_mapping[rows], q=st.q[rows],
+                                   kv_score=tok(st.kv_score), q_idx=tok(st.q_idx), w_idx=tok(st.w_idx),
+                                   given_topk=None, cand_in=None, extra={})
+
+    def spans(self, chunk: int):
+        """(p0, n) of the chunks of `chunk` positions (the last one ragged)."""
+        return [(p0, min(chunk, self.P - p0)) for p0 in range(0, self.P, chunk)]
+
+
+def make_prefill(cfg: Config, P: int) -> PrefillInputs:
+    """Inputs of a P-token prefill of B sequences: the decode-step generator with every position a
+    new token (pages for all P positions; caches, state ring and indexer keys seeded garbage)."""
+    assert P >= 1
+    full = dataclasses.replace(cfg, q_per_seq=P, explicit_lens=tuple([P] * cfg.B), cand_block=0)
+    return PrefillInputs(cfg=dataclasses.replace(cfg, explicit_lens=tuple([P] * cfg.B)), P=P,
+                         base=make_step(full, with_given_topk=False))
+
+
+PREFILL_CONFIGS = {
+    # (layer configuration, prompt length): c4 with the indexer (top-k below n_c late in the prompt,
+    # ragged last chunk), fp32 keys on the CUDA-core indexer, c128 without an indexer, and the
+    # full-size c4 bf16 prefill the benchmark times
+    "prefill_c4_small": (dataclasses.replace(CONFIGS["csa_c4_bf16"], name="prefill_c4_small", B=3, topk=32), 301),
+    "prefill_c4_f32": (dataclasses.replace(CONFIGS["tiny_c4_f32"], name="prefill_c4_f32", B=2, topk=16), 150),
+    "prefill_c128_small": (dataclasses.replace(CONFIGS["hca_c128_bf16"], name="prefill_c128_small", B=2), 300),
+    "prefill_c4_bf16": (dataclasses.replace(CONFIGS["csa_c4_bf16"], name="prefill_c4_bf16", B=16), 512),
+}
+
+
 def max_compressed(cfg: Config) -> int:
     L = context_lengths(cfg)
     return int(L.max() // cfg.ratio) if cfg.ratio else 0

@@ -713,3 +713,39 @@ def decode_step(st, seqs=None, topk_override=None):
         out[t], lse[t] = mqa_decode(q_att[t], rows, st.sink, st.softmax_scale)
     res["out"], res["lse"] = out, lse
     return res
+
+
+# ----------------------------------------------------------------------------------------------
+# Chunked prefill
+# ----------------------------------------------------------------------------------------------
+
+def apply_step(st, res) -> None:
+    """Commits one step's writes to the caches of `st` in place: its SWA rows, the compressor state of
+    the sequences it ran, its compressed entries and index keys."""
+    for (pg, off), row in res["swa_written"].items():
+        st.swa_cache[pg, off] = row
+    for b, ring in res.get("state", {}).items():
+        st.state[b] = ring
+    for (pg, off), row in res.get("main_written", {}).items():
+        st.main_cache[pg, off] = row
+    for (pg, off), row in res.get("idx_written", {}).items():
+        st.idx_cache[pg, off] = row
+
+
+def prefill(chunks) -> dict:
+    """Chunked prefill ([ASCEND] §8 "The prefill path": the same chain -- query/KV prologue, SWA
+    insert, compressor, indexer, sparse attention -- for every prompt token; [API]
+    DeepseekV4Attention.PREFILL_CHUNK_SIZE: in fixed-size chunks).  `chunks` gives the steps of
+    consecutive positions of every sequence from position 0, sharing one set of caches; each runs
+    decode_step and its writes are committed before the next.  Returns {(b, p): {"out", "lse",
+    "topk", "q_out"}} for every token."""
+    out = {}
+    for st in chunks:
+        res = decode_step(st)
+        qps = st.cfg.q_per_seq
+        for t in res["tokens"]:
+            b, p = t // qps, int(st.positions[t])
+            out[(b, p)] = {"out": res["out"][t], "lse": res["lse"][t], "topk": res["topk"].get(t),
+                           "q_out": res["q_out"].get(t)}
+        apply_step(st, res)
+    return out

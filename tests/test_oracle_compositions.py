@@ -278,3 +278,79 @@ def test_decode_step_scores_the_key_written_this_step(ctx):
     got = float(res["scores"][0][j_new])
     assert abs(got - want) <= 1e-6 * max(1.0, abs(want))
     assert np.array_equal(res["idx_written"][(st.idx_bt[0][j_new // 64], j_new % 64)], k.astype(np.float32))
+
+
+# ------------------------------------------------------------------------------------------------
+# chunked prefill: the chain over consecutive chunks from position 0
+# ------------------------------------------------------------------------------------------------
+
+def _prefill(name, P, chunk, **kw):
+    cfg, _ = I.PREFILL_CONFIGS[name]
+    pf = I.make_prefill(dataclasses.replace(cfg, **kw), P)
+    toks = O.prefill(pf.chunk(p0, n) for p0, n in pf.spans(chunk))
+    return pf, toks
+
+
+@pytest.mark.parametrize("name,P", [("prefill_c4_f32", 70), ("prefill_c128_small", 260)])
+def test_prefill_does_not_depend_on_the_chunk_size(name, P):
+    """Each token reads only rows written at its own or earlier positions, so chunks of 4, 1 and 3
+    positions give the same results and the same caches, bit for bit."""
+    kw = {"B": 1, "H": 8} if name == "prefill_c128_small" else {}
+    ref_pf, ref = _prefill(name, P, 4, **kw)
+    for c in (1, 3):
+        pf, got = _prefill(name, P, c, **kw)
+        assert got.keys() == ref.keys()
+        for k, v in ref.items():
+            assert np.array_equal(got[k]["out"], v["out"]) and np.array_equal(got[k]["lse"], v["lse"]), (c, k)
+            assert (v["topk"] is None) == (got[k]["topk"] is None)
+            if v["topk"] is not None:
+                assert np.array_equal(got[k]["topk"], v["topk"]), (c, k)
+        for f in ("swa_cache", "state", "main_cache", "idx_cache"):
+            a, b = getattr(ref_pf.base, f), getattr(pf.base, f)
+            assert (a is None) == (b is None) and (a is None or np.array_equal(a, b)), (c, f)
+
+
+def test_prefill_of_100_tokens_gives_25_entries_and_attends_them_all():
+    """"DeepSeek-V4 Inference on Ascend", §8 "The prefill path": a 100-token prefill through a c4 layer
+    leaves 25 compressed entries, the indexer's top-k of those 25 is all of them, and the attention of
+    the last token scores the window plus the chosen entries.  Rebuilt here from the inputs alone: the
+    window rows are the tokens' kv rotated at their positions, entry j is the scalar fold of the state
+    rows of positions 4j - 4 .. 4j + 3."""
+    cfg, _ = I.PREFILL_CONFIGS["prefill_c4_f32"]
+    cfg = dataclasses.replace(cfg, B=1, H=4, topk=64)
+    pf = I.make_prefill(cfg, 100)
+    st = pf.base
+    st.cos_sin = rotary_table(101).astype(np.float32)
+    main_before = st.main_cache.copy()
+    toks = O.prefill(pf.chunk(p0, n) for p0, n in pf.spans(4))
+    ratio, coff = cfg.ratio, cfg.coff
+    # the 25 entries, and nothing past them
+    ents = []
+    for j in range(25):
+        ring = np.zeros((coff * ratio, 2 * coff * D), np.float32)
+        for pos in range(max(0, 4 * j - 4), 4 * j + 4):
+            r = np.array(st.kv_score[pos], np.float32, copy=True)
+            r[coff * D:] = (r[coff * D:] + st.ape[pos % ratio]).astype(np.float32)
+            ring[pos % (coff * ratio)] = r
+        e = scalar_entry(ring, j, ratio, coff, st.norm_w, st.eps, st.cos_sin).astype(np.float32)
+        got = st.main_cache[st.main_bt[0][j // 64], j % 64]
+        np.testing.assert_allclose(got.astype(np.float64), e.astype(np.float64), rtol=1e-6, atol=1e-7)
+        ents.append(got.astype(np.float64))
+    for j in range(25, st.main_cache.shape[0] * 64):
+        pg = st.main_bt[0][j // 64] if j // 64 < st.main_bt.shape[1] else -1
+        if pg >= 0:
+            assert np.array_equal(st.main_cache[pg, j % 64], main_before[pg, j % 64])
+    last = toks[(0, 99)]
+    assert sorted(last["topk"][:25].tolist()) == list(range(25)) and np.all(last["topk"][25:] == -1)
+    rows = [np.asarray(scalar_rotate([float(x) for x in st.kv_new[pos]], pos, st.cos_sin), np.float32)
+            .astype(np.float64) for pos in range(100)]
+    R = np.stack(rows + ents)
+    assert R.shape[0] == 100 + 25
+    q = np.asarray(st.q[99], np.float64)
+    for h in range(cfg.H):
+        inv = 1.0 / math.sqrt(math.fsum(x * x for x in q[h]) / D + st.eps)
+        qh = np.asarray(scalar_rotate([q[h][c] * inv * float(st.q_norm_w[c]) for c in range(D)], 99, st.cos_sin),
+                        np.float32).astype(np.float64)
+        logits = np.concatenate([st.softmax_scale * (R @ qh), [float(st.sink[h])]])
+        want = (softmax(logits)[:-1, None] * R[:, :DV]).sum(axis=0)
+        np.testing.assert_allclose(last["out"][h], want, rtol=1e-6, atol=1e-9)
