@@ -334,12 +334,16 @@ def measure_workload(cfg, K, warmup, world, local, want_e2e):
     # each replica's step (and each call alone) captured once as a CUDA graph: the library never
     # synchronises, so the calls replay with no host launch gaps
     graph_step, graph_call = [], {c: [] for c in calls}
+    launches_step = None  # the library's kernels in one step: its launch counter across one capture
     for ds in reps_ds:
         for _ in range(max(warmup, 3)):
             ds.run()
         g = torch.cuda.CUDAGraph()
+        n0 = M.dsv4_kernel_launches()
         with torch.cuda.graph(g):
             ds.run()
+        if launches_step is None:
+            launches_step = M.dsv4_kernel_launches() - n0
         graph_step.append(g)
         for c in calls:
             gc = torch.cuda.CUDAGraph()
@@ -375,7 +379,7 @@ def measure_workload(cfg, K, warmup, world, local, want_e2e):
     per_call_us = {c: rotating_call_us(torch, [g.replay for g in graph_call[c]], rounds) for c in calls}
 
     res = {"ms_per_step": ms_per_step, "value": job_tokens_per_s(cfg.T, world, ms_per_step), "calls_us": per_call_us,
-           "clocks": clocks, "wall_s_timed": wall, "gpu_launches": int(K * launches_per_step(ds0)),
+           "clocks": clocks, "wall_s_timed": wall, "gpu_launches": int(K * launches_step),
            "step_algorithmic_gbs": sum(alg.values()) / (ms_per_step * 1e-3) / 1e9,
            "config": {"workload": cfg.name, "batch_per_gpu": cfg.B, "q_per_seq": cfg.q_per_seq,
                       "context": ctx_range,
@@ -432,6 +436,64 @@ def measure_workload(cfg, K, warmup, world, local, want_e2e):
     return res
 
 
+def measure_prefill(name, K, warmup, local):
+    """Times a chunked prefill (every position of every sequence from 0, four positions of each
+    sequence a chunk, the chain's calls for each chunk) captured as one CUDA graph: CUDA events around
+    each replay, an L2-sized buffer written before each (the prefill's caches fit in L2).  Value:
+    prompt tokens per second."""
+    import torch
+    import dsv4_inputs as I
+    import deepseek_v4_hybrid_gb300 as M
+    from deepseek_v4_hybrid_gb300.step import PrefillRunner
+    cfg, P = I.PREFILL_CONFIGS[name]
+    pf = I.make_prefill(cfg, P)
+    runner = PrefillRunner(pf, chunk=4)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(warmup, 3)):
+        runner.run()
+    torch.cuda.synchronize()
+    flags = M.dsv4_read_device_flags()
+    if flags:
+        raise SystemExit(f"kernels raised range/timeout flags {flags:#x} during warm-up of {name}; not timing")
+    alg = 0
+    for (p0, n), ds in zip(runner.spans, runner.steps):
+        topk = ds.topk_idx.cpu().numpy() if ds.has_indexer else None
+        alg += sum(algorithmic_bytes(pf.chunk(p0, n), topk).values())
+    g = torch.cuda.CUDAGraph()
+    n0 = M.dsv4_kernel_launches()
+    with torch.cuda.graph(g):
+        runner.run()
+    launches = M.dsv4_kernel_launches() - n0
+    l2 = int(torch.cuda.get_device_properties(local).L2_cache_size)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    for k in range(K):
+        flush.fill_(float(k))
+        ev[k][0].record(stream)
+        g.replay()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    peak, peak_kind = peaks()
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"metric": "prefill tokens/s per GB300", "value": cfg.B * P / (ms * 1e-3), "unit": "tokens/s",
+            "ms_per_prefill": ms, "steps": K, "gpu_launches": int(K * launches), "clocks": clocks,
+            "dtype": {0: "f32", 1: "bf16"}[cfg.act_dtype] + "/" + I.DTYPE_NAMES[cfg.cache_dtype],
+            "algorithmic_gbs": gbs, "frac_of_hbm": gbs / peak, "peak_kind": peak_kind,
+            "config": {"workload": name, "batch_per_gpu": cfg.B, "prompt": P, "chunk": 4, "chunks": len(runner.spans),
+                       "heads": cfg.H, "ratio": cfg.ratio, "indexer": [cfg.I_h, cfg.d_I], "topk": cfg.topk,
+                       "l2": f"a {2 * l2 // 2**20} MiB buffer written before each timed prefill"}}
+
+
+PREFILL_WORKLOADS = ("prefill_c4_bf16",)
+
 EXTRA_WORKLOADS = ("hca_c128_bf16", "csa_c4_fp8", "csa_c4_1m", "csa_c4_mxfp4", "csa_c4_cand", "csa_c4_src")
 
 
@@ -468,6 +530,8 @@ def run_ours(args):
                                              "calls_roofline", "step_algorithmic_gbs", "clocks", "gpu_launches")}
             extra[name]["unit"] = "tokens/s"
             extra[name]["steps"] = min(K, 500)
+        for name in PREFILL_WORKLOADS:
+            extra[name] = measure_prefill(name, max(3, min(K, 20)), args.warmup, local)
         line["extra_workloads"] = extra
     if rank == 0 and not args.no_cpu_baseline:
         st = I.make_step(cfg)
@@ -497,15 +561,6 @@ def oracle_single_core(config, seconds):
         return {"value": d["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": d["sample"]}
     except Exception:
         return None
-
-
-def launches_per_step(ds):
-    n = 1 + 2  # insert, attention partial + merge
-    if ds.has_compress:
-        n += 1
-    if ds.has_indexer:
-        n += 2
-    return n
 
 
 def run_reference(args):

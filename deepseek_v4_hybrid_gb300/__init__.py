@@ -133,6 +133,11 @@ def dsv4_sparse_mla_decode(params, stream=None):
     _abi.check("dsv4_sparse_mla_decode", _lib.dsv4_sparse_mla_decode(params, _stream(stream)))
 
 
+def dsv4_kernel_launches() -> int:
+    """Kernels the library has enqueued (or recorded into a graph) since it was loaded."""
+    return int(_lib.dsv4_kernel_launches())
+
+
 def dsv4_read_device_flags() -> int:
     """Synchronises and returns (and clears) the kernels' range-check flags."""
     f = _abi.u32(0)

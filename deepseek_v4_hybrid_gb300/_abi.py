@@ -66,7 +66,7 @@ class SparseMlaDecodeParams(C.Structure):
 EXPORTS = ["dsv4_kv_insert", "dsv4_compress_update", "dsv4_indexer_topk_workspace_bytes", "dsv4_indexer_topk",
            "dsv4_sparse_mla_decode_workspace_bytes", "dsv4_sparse_mla_decode", "dsv4_abi_version",
            "dsv4_status_string", "dsv4_last_cuda_error", "dsv4_read_device_flags", "dsv4_indexer_topk_noalloc",
-           "dsv4_qnorm_rope_kv_insert", "dsv4_padded_num_q_heads"]
+           "dsv4_qnorm_rope_kv_insert", "dsv4_padded_num_q_heads", "dsv4_kernel_launches"]
 
 # bytes of the scratch array built into the library for dsv4_indexer_topk_noalloc
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -101,6 +101,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.dsv4_status_string.argtypes = [C.c_int]
     lib.dsv4_status_string.restype = C.c_char_p
     lib.dsv4_last_cuda_error.restype = C.c_int
+    lib.dsv4_kernel_launches.argtypes = []
+    lib.dsv4_kernel_launches.restype = C.c_uint64
     lib.dsv4_read_device_flags.argtypes = [C.POINTER(u32)]
     lib.dsv4_read_device_flags.restype = C.c_int
     if lib.dsv4_abi_version() != ABI_VERSION:

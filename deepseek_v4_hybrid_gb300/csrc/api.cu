@@ -1,5 +1,6 @@
 // C ABI entry points: host-side argument validation, then the kernel launches.
 // The declarations, argument meanings and error behaviour are documented in include/dsv4.h.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -11,6 +12,7 @@ using namespace dsv4;
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+std::atomic<unsigned long long> g_kernel_launches{0};
 
 int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return DSV4_OK;
@@ -32,9 +34,16 @@ bool act_dtype(int d) { return d == DSV4_F32 || d == DSV4_BF16; }
 
 void dsv4::record_cuda_error(int e) { g_last_cuda_error = e; }
 
+cudaError_t dsv4::count_launch(cudaError_t e) {
+  if (e == cudaSuccess) g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
 extern "C" {
 
 int dsv4_abi_version(void) { return DSV4_ABI_VERSION; }
+
+uint64_t dsv4_kernel_launches(void) { return g_kernel_launches.load(std::memory_order_relaxed); }
 
 const char* dsv4_status_string(int s) {
   switch (s) {

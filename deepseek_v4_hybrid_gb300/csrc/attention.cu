@@ -1090,10 +1090,10 @@ static cudaError_t launch_mla_partial_tc(const dsv4_sparse_mla_decode_params& p,
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   if (fp8)
-    return cudaLaunchKernelEx(&cfg, mla_partial_tc<true>, qmap, swamap64, mainmap, mainmap64, ropeswa64, ropemain,
-                              ropemain64, a);
-  return cudaLaunchKernelEx(&cfg, mla_partial_tc<false>, qmap, swamap64, mainmap, mainmap64, ropeswa64, ropemain,
-                            ropemain64, a);
+    return count_launch(cudaLaunchKernelEx(&cfg, mla_partial_tc<true>, qmap, swamap64, mainmap, mainmap64, ropeswa64,
+                                           ropemain, ropemain64, a));
+  return count_launch(cudaLaunchKernelEx(&cfg, mla_partial_tc<false>, qmap, swamap64, mainmap, mainmap64, ropeswa64,
+                                         ropemain, ropemain64, a));
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -28,6 +28,9 @@ cudaError_t read_flags_attention(uint32_t* f);
 // Makes `e` the value dsv4_last_cuda_error() reports on this thread.
 void record_cuda_error(int e);
 
+// Counts one kernel enqueued by the library (dsv4_kernel_launches()); `e` is the launch's status.
+cudaError_t count_launch(cudaError_t e);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace dsv4
@@ -55,7 +58,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return count_launch(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
 }
 
 }  // namespace dsv4

@@ -67,7 +67,9 @@ static IxLayout ix_layout(const dsv4_indexer_topk_params& p) {
   L.scores_off = 0;
   L.hist_off = align_up(L.scores_off + (size_t)p.T * L.nc_stride * sizeof(float), 256);
   L.done_off = L.hist_off + (size_t)p.T * HIST_BINS * sizeof(uint32_t);  // zeroed together with hist
-  L.tcnt_off = L.done_off + (size_t)p.B * sizeof(uint32_t);                // zeroed together with hist
+  // completion counters: one a sequence, or one a token when the tensor-core kernel takes each query
+  // token as its own sequence (T >= B)
+  L.tcnt_off = L.done_off + (size_t)p.T * sizeof(uint32_t);                // zeroed together with hist
   L.cand_off = align_up(L.tcnt_off + (size_t)p.T * 2 * sizeof(uint32_t), 256);
   L.bits_off = align_up(L.cand_off + (size_t)p.T * L.nc_stride * sizeof(uint64_t), 256);
   L.total = align_up(L.bits_off + (size_t)p.T * (L.nc_stride / 32) * sizeof(uint32_t), 256);
@@ -79,7 +81,7 @@ size_t indexer_topk_workspace(const dsv4_indexer_topk_params& p) { return ix_lay
 struct TopkBufs {
   float* scores;       // [T][nc_stride]
   uint32_t* hist;      // [T][HIST_BINS] counts of the scores' top 12 order-key bits
-  uint32_t* seq_done;  // [B] key tiles of the sequence scored so far (tensor-core path)
+  uint32_t* seq_done;  // [T] key tiles of the sequence (or token) scored so far (tensor-core path)
   uint64_t* cand;      // [T][nc_stride] top-k candidates that do not fit in shared memory
   uint32_t* tcnt;      // [T][2] sliced top-k: candidates appended, slices finished
   uint32_t* bits;      // [T][nc_stride / 32] sliced top-k: selection bitmap (layout of bitmap_words)
@@ -764,6 +766,8 @@ struct Args {
   int64_t num_pages;
   int T, B, qps, Ih, d, ratio, max_pages, tiles_max, max_context, K;
   int fuse_topk;  // the CTA completing a sequence runs its top-k (else a separate sliced launch)
+  int bt_div;     // block-table row of item sequence b: b / bt_div (q_per_seq when each query token is
+                  // taken as its own sequence, else 1)
   int kf;         // key format: KF_BF16 (TMA tiles), KF_I8 (d int8 + fp32 scale) or KF_MX (MXFP4 records);
                   // int8 and MXFP4 records arrive as bulk-copied pages and are expanded in shared memory
   int rec;        // bytes of one raw record (int8 and MXFP4 keys)
@@ -797,7 +801,7 @@ __device__ __forceinline__ int seq_entries(const Args& a, int b) {
 
 __device__ __forceinline__ int page_of(const Args& a, int b, int lp) {
   if (lp >= a.max_pages) return -1;
-  const int pg = a.block_table[(int64_t)b * a.max_pages + lp];
+  const int pg = a.block_table[(int64_t)(b / a.bt_div) * a.max_pages + lp];
   if (pg < 0 || pg >= a.num_pages) {
     atomicOr(&g_flags_ix, FLAG_PAGE);
     return -1;
@@ -1421,8 +1425,15 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
 
 }  // namespace ixtc
 
+// The tensor-core kernel multiplies each key tile by the queries of all of a sequence's tokens (N =
+// q_per_seq x n_heads columns, 64 or 128).  With more columns it takes every query token as its own
+// sequence (N = n_heads; the tokens of a sequence then read its keys once each).
+static bool tc_per_token(const dsv4_indexer_topk_params& p) {
+  return p.q_per_seq * p.n_heads > 128 && (p.n_heads == 64 || p.n_heads == 128);
+}
+
 static bool use_tc_indexer(const dsv4_indexer_topk_params& p) {
-  const int N = p.q_per_seq * p.n_heads;
+  const int N = tc_per_token(p) ? p.n_heads : p.q_per_seq * p.n_heads;
   return (p.k_dtype == DSV4_BF16 || p.k_dtype == DSV4_I8_ROWSCALE || p.k_dtype == DSV4_MXFP4) &&
          p.q_dtype == DSV4_BF16 &&
          (p.head_dim == 64 || p.head_dim == 128) && p.n_heads % 32 == 0 && N >= 64 && N <= 128 && N % 64 == 0 &&
@@ -1439,9 +1450,11 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   a.weights = p.weights;
   a.bufs = bufs;
   a.num_pages = p.num_pages;
+  const bool per_token = tc_per_token(p);
   a.T = p.T;
-  a.B = p.B;
-  a.qps = p.q_per_seq;
+  a.B = per_token ? p.T : p.B;
+  a.qps = per_token ? 1 : p.q_per_seq;
+  a.bt_div = per_token ? p.q_per_seq : 1;
   a.Ih = p.n_heads;
   a.d = p.head_dim;
   a.ratio = p.ratio;
@@ -1452,7 +1465,7 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   a.fuse_topk = max_nc <= TOPK_FUSED_MAX;
   a.topk_idx = p.topk_idx;
   a.topk_score = p.topk_score;
-  a.N = p.q_per_seq * p.n_heads;
+  a.N = a.qps * p.n_heads;
   a.kblk = p.head_dim / 64;
   a.nacc = 4 * a.N <= 512 ? 4 : 2;  // TMEM accumulators (512 columns available)
   a.kf = p.k_dtype == DSV4_I8_ROWSCALE ? KF_I8 : (p.k_dtype == DSV4_MXFP4 ? KF_MX : KF_BF16);
@@ -1465,8 +1478,8 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   a.cM = ca.M;
   a.clg = ca.lg;
   a.csh = ca.blocks ? ca.lg - 7 : 0;
-  a.cskip = ca.blocks && !ca.write && p.q_per_seq == 1;
-  a.cmask = ca.blocks && !ca.write && p.q_per_seq > 1;
+  a.cskip = ca.blocks && !ca.write && a.qps == 1;
+  a.cmask = ca.blocks && !ca.write && a.qps > 1;
   a.cwrite = ca.blocks && ca.write;
   const size_t budget = 227 * 1024;
   auto fixed_for = [&](int nqs, int nraw) {

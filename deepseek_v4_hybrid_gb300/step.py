@@ -35,26 +35,33 @@ class DeviceStep:
     # per-step inputs (copied host -> device every step in the end-to-end measurement)
     STEP_INPUTS = ("q", "kv_new", "slot_mapping", "positions", "kv_score", "q_idx", "w_idx")
 
-    def __init__(self, st, device="cuda", topk_override=None):
+    # caches, block tables and weights: what the steps of one prefill share (see PrefillRunner)
+    SHARED = ("swa_cache", "swa_bt", "cos_sin", "q_norm_w", "state", "ape", "norm_w", "main_cache", "main_bt",
+              "wk", "ik_norm_w", "idx_cache", "idx_bt")
+
+    def __init__(self, st, device="cuda", topk_override=None, shared=None):
+        """shared: device tensors (by the names in SHARED) to use instead of uploading st's."""
         cfg = st.cfg
         self.cfg, self.device = cfg, device
         dev = lambda a: to_device(a, device)  # noqa: E731
+        shared = shared or {}
+        keep = lambda name, a: shared[name] if name in shared else dev(a)  # noqa: E731
         self.positions = dev(st.positions.astype(np.int32))
         self.kv_new = dev(st.kv_new)
         self.slot_mapping = dev(st.slot_mapping.astype(np.int64))
-        self.swa_cache = dev(st.swa_cache)
-        self.swa_bt = dev(st.swa_bt)
+        self.swa_cache = keep("swa_cache", st.swa_cache)
+        self.swa_bt = keep("swa_bt", st.swa_bt)
         self.max_context = int(st.ctx_len.max())
         T, H = cfg.T, cfg.H
         # with query preparation, the fused insert turns the raw queries q_in [T, H, 576] into the
         # attention's q [T, H_pad, 576]; the sink of the padding heads is -inf
         self.q_prep = bool(getattr(cfg, "q_prep", False))
         self.H_pad = dsv4_padded_num_q_heads(H, cfg.cache_dtype) if self.q_prep else H
-        self.cos_sin = dev(st.cos_sin)
+        self.cos_sin = keep("cos_sin", st.cos_sin)
         if self.q_prep:
             self.q_in = dev(st.q)
             self.q = torch.empty((T, self.H_pad, 576), dtype=self.q_in.dtype, device=device)
-            self.q_norm_w = dev(st.q_norm_w)
+            self.q_norm_w = keep("q_norm_w", st.q_norm_w)
             sink = np.full(self.H_pad, -np.inf, np.float32)
             sink[:H] = st.sink
             self.sink = dev(sink)
@@ -71,19 +78,19 @@ class DeviceStep:
         self.q_idx = self.w_idx = None
         if self.has_compress:
             self.kv_score = dev(st.kv_score)
-            self.state = dev(st.state)
-            self.ape = dev(st.ape)
-            self.norm_w = dev(st.norm_w)
-            self.main_cache = dev(st.main_cache)
-            self.main_bt = dev(st.main_bt)
+            self.state = keep("state", st.state)
+            self.ape = keep("ape", st.ape)
+            self.norm_w = keep("norm_w", st.norm_w)
+            self.main_cache = keep("main_cache", st.main_cache)
+            self.main_bt = keep("main_bt", st.main_bt)
         self.topk_idx = None
         self.ik_store = self.has_indexer and bool(getattr(cfg, "ik_store", False)) and st.wk is not None
         if self.ik_store:
-            self.wk = dev(st.wk)
-            self.ik_norm_w = dev(st.ik_norm_w)
+            self.wk = keep("wk", st.wk)
+            self.ik_norm_w = keep("ik_norm_w", st.ik_norm_w)
         if self.has_indexer:
-            self.idx_cache = dev(st.idx_cache)
-            self.idx_bt = dev(st.idx_bt)
+            self.idx_cache = keep("idx_cache", st.idx_cache)
+            self.idx_bt = keep("idx_bt", st.idx_bt)
             self.q_idx = dev(st.q_idx)
             self.w_idx = dev(st.w_idx)
             self.topk_idx = torch.empty((T, cfg.topk), dtype=torch.int32, device=device)
@@ -180,3 +187,22 @@ class DeviceStep:
         if getattr(self, "cand_blocks", None) is not None and not self.cand_write:
             d["cand_blocks"] = self.cand_blocks  # the blocks an earlier layer published this step
         return d
+
+
+class PrefillRunner:
+    """Chunked prefill on the device: the decode chain over consecutive chunks of `chunk` positions of
+    every sequence, from position 0 ("DeepSeek-V4 Inference on Ascend", §8 "The prefill path";
+    "vllm.models.deepseek_v41.attention", DeepseekV4Attention.PREFILL_CHUNK_SIZE = 4).  One DeviceStep
+    a chunk, all over one set of device caches, state ring and weights: what a chunk writes, the next
+    one reads.  run() issues the chunks in order on one stream (graph-capturable)."""
+
+    def __init__(self, pf, chunk=4, device="cuda"):
+        self.spans = pf.spans(chunk)
+        first = DeviceStep(pf.chunk(*self.spans[0]), device)
+        shared = {k: getattr(first, k) for k in DeviceStep.SHARED if getattr(first, k, None) is not None}
+        self.steps = [first] + [DeviceStep(pf.chunk(p0, n), device, shared=shared) for p0, n in self.spans[1:]]
+        self.shared = shared
+
+    def run(self, stream=None):
+        for s in self.steps:
+            s.run(stream)

@@ -140,6 +140,12 @@ SMALL_CONFIGS = {
     "small_c4_cand_mtp": dataclasses.replace(CONFIGS["csa_c4_fp8"], name="small_c4_cand_mtp", B=5,
                                              explicit_lens=(9000, 4100, 2050, 3000, 7000), cand_block=256,
                                              cand_topk=5),
+    # three query tokens a sequence: more query columns than one tensor-core tile takes, so the
+    # indexer takes each token as its own sequence (plain, and as a candidate consumer)
+    "small_c4_q3": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_c4_q3", B=4, q_per_seq=3,
+                                       explicit_lens=(9000, 3001, 700, 2050)),
+    "small_c4_cand_q3": dataclasses.replace(CONFIGS["csa_c4_bf16"], name="small_c4_cand_q3", B=3, q_per_seq=3,
+                                            explicit_lens=(12000, 5003, 2400), cand_block=512, cand_topk=4),
     "small_c4_cand_f32": dataclasses.replace(CONFIGS["tiny_c4_f32"], name="small_c4_cand_f32", B=5,
                                              explicit_lens=(2400, 1300, 1029, 2000, 3333), cand_block=128,
                                              cand_topk=3),

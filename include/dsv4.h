@@ -334,6 +334,11 @@ int dsv4_abi_version(void);
 const char* dsv4_status_string(int status);
 /* The cudaError_t of the last failed CUDA call made by this thread inside the library. */
 int dsv4_last_cuda_error(void);
+/* Kernels the library has enqueued since it was loaded, over all threads and devices.  A launch made
+ * while the stream is being captured counts once, when it is recorded into the graph; replays of
+ * that graph are not counted, so (count after - count before) around one capture is the kernels one
+ * replay runs.  cudaMemsetAsync calls are not kernels of the library and are not counted. */
+uint64_t dsv4_kernel_launches(void);
 /* Synchronises the current device, returns the OR of the flags the kernels raised since the
  * previous call in *flags and clears them:
  *   bit 0 (1): a block-table page, slot or position out of range (the access was skipped),

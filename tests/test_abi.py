@@ -24,12 +24,12 @@ def abi():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(dsv4_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|uint64_t|const char\*)\s+(dsv4_\w+)\s*\(", text, re.M)))
 
 
 def test_exports_every_declared_symbol(abi):
     names = declared_functions()
-    assert len(names) == 13
+    assert len(names) == 14
     out = subprocess.run(["nm", "-D", "--defined-only", abi.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (dsv4_\w+)", out))
     assert set(names) <= exported, set(names) - exported
@@ -129,3 +129,5 @@ def test_host_validation_rejects_bad_arguments(abi):
     assert lib.dsv4_sparse_mla_decode(at, None) == abi.ERR_INVALID      # null pointers
     assert lib.dsv4_sparse_mla_decode_workspace_bytes(at) > 0
     assert lib.dsv4_status_string(abi.ERR_BOUNDS).decode().startswith("a kernel skipped")
+    n0 = lib.dsv4_kernel_launches()
+    assert lib.dsv4_indexer_topk(ix, None) != abi.OK and lib.dsv4_kernel_launches() == n0  # refused: nothing launched
