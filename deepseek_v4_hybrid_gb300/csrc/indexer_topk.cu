@@ -261,78 +261,73 @@ __device__ __forceinline__ void block_find_bin(const uint32_t* h, uint32_t rem, 
   __syncthreads();
 }
 
-// Bitmap words and candidates of one chunk of scores in shared memory: sb holds entries j_base ..
-// j_base + 128 nblocks - 1 (j_base a multiple of 128, nblocks <= CHUNK / 128; entries >= n are
-// ignored).  Entries with bin > bstar set their bit in `bits` (every word of the chunk's blocks
-// below `words` is written, 16 bytes at a time), entries in bstar are appended to `cand` (capacity
-// ccap) through the counter *ncand.  With an inclusion bitmap `incl` (candidate filtering), entries of
-// 128-entry blocks whose bit is clear take no part, and all_in selects every other entry (no
-// candidates).  bits (16-byte aligned), cand and ncand may be in shared or global memory.  Warp w
-// owns the consecutive blocks w P .. w P + P - 1 (P <= SCAN_B); lane l reads entries 4 l .. 4 l + 3
-// of a block as one float4, and the four ballots of "bin > bstar" are the block's four bitmap words.
-// Candidates are rare: each lane counts its own, the warp takes its slots with one atomic, and each
-// lane writes its candidates to consecutive slots.
-constexpr int SCAN_B = CHUNK / 128 / SCAN_WARPS_MIN;  // 128-entry blocks of a chunk per warp (4)
+// Bitmap words and candidates of scores in shared memory: sb holds entries j_base .. j_base + 128
+// nblocks - 1 (j_base a multiple of 128; entries >= n are ignored).  Entries with bin > bstar set
+// their bit in `bits` (every word of the scanned blocks below `words` is written, 16 bytes at a
+// time), entries in bstar are appended to `cand` (capacity ccap) through the counter *ncand.  With an
+// inclusion bitmap `incl` (candidate filtering), entries of 128-entry blocks whose bit is clear take
+// no part, and all_in selects every other entry (no candidates).  bits (16-byte aligned), cand and
+// ncand may be in shared or global memory.  Warp w owns the consecutive blocks w P .. w P + P - 1 (P =
+// ceil(nblocks / warps)), taken SCAN_B at a time: lane l reads entries 4 l .. 4 l + 3 of a block as
+// one float4, and the four ballots of "bin > bstar" are the block's four bitmap words.  Candidates
+// are rare: per group of SCAN_B blocks each lane counts its own, the warp takes their slots with one
+// atomic, and each lane writes its candidates to consecutive slots from the scores in its registers.
+constexpr int SCAN_B = CHUNK / 128 / SCAN_WARPS_MIN;  // 128-entry blocks a warp reads at once (4)
 __device__ __forceinline__ void scan_chunk(const float* sb, int nblocks, int j_base, int n, uint32_t bstar,
                                            uint32_t* bits, int words, uint64_t* cand, uint32_t ccap,
                                            uint32_t* ncand, const uint32_t* incl = nullptr, bool all_in = false) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
   const float4* sb4 = reinterpret_cast<const float4*>(sb);
-  const int per = (nblocks + NW - 1) / NW;  // <= SCAN_B since NW >= SCAN_WARPS_MIN
-  const int b0 = warp * per;
-  float4 v[SCAN_B];
+  const int per = (nblocks + NW - 1) / NW;
+  const int b0 = min(nblocks, warp * per), b1 = min(nblocks, b0 + per);
+  for (int g = b0; g < b1; g += SCAN_B) {
+    float4 v[SCAN_B];
 #pragma unroll
-  for (int i = 0; i < SCAN_B; ++i) {
-    const int blk = b0 + i;
-    v[i] = (i < per && blk < nblocks) ? sb4[blk * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  int lc = 0;  // this lane's candidates
-  const bool want_cand = !all_in;
+    for (int i = 0; i < SCAN_B; ++i) v[i] = g + i < b1 ? sb4[(g + i) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    int nvs[SCAN_B];
+    int lc = 0;  // this lane's candidates in the group
 #pragma unroll
-  for (int i = 0; i < SCAN_B; ++i) {
-    const int blk = b0 + i;
-    const bool live = i < per && blk < nblocks;  // warp-uniform
-    const int gb = (j_base >> 7) + blk;
-    const bool inb = incl == nullptr || (live && ((incl[gb >> 5] >> (gb & 31)) & 1u));  // warp-uniform
-    const int nv = live && inb ? n - (j_base + blk * 128 + 4 * lane) : 0;  // entries c < nv of the lane count
-    const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-    uint32_t sw[4];
+    for (int i = 0; i < SCAN_B; ++i) {
+      const int blk = g + i;
+      const int gb = (j_base >> 7) + blk;
+      const bool live = blk < b1 && (incl == nullptr || ((incl[gb >> 5] >> (gb & 31)) & 1u));  // warp-uniform
+      nvs[i] = live ? n - (j_base + blk * 128 + 4 * lane) : 0;  // entries c < nvs[i] of the lane count
+      const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint32_t sw[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t bin = order_key(e[c]) >> HIST_SHIFT;
-      sw[c] = __ballot_sync(0xffffffffu, c < nv && (all_in || bin > bstar));
-      lc += (want_cand && c < nv && bin == bstar) ? 1 : 0;
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t bin = order_key(e[c]) >> HIST_SHIFT;
+        sw[c] = __ballot_sync(0xffffffffu, c < nvs[i] && (all_in || bin > bstar));
+        lc += (!all_in && c < nvs[i] && bin == bstar) ? 1 : 0;
+      }
+      const int wg = gb * 4;
+      if (lane == 0 && blk < b1 && wg < words)
+        *reinterpret_cast<uint4*>(bits + wg) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
     }
-    const int wg = ((j_base >> 7) + blk) * 4;
-    if (lane == 0 && live && wg < words) *reinterpret_cast<uint4*>(bits + wg) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
-  }
-  const int wtot = __reduce_add_sync(0xffffffffu, lc);
-  if (wtot == 0) return;  // warp-uniform
-  int scan = lc;
+    // the group's candidates, written while its scores are in registers: one atomic for the warp
+    const int wtot = __reduce_add_sync(0xffffffffu, lc);
+    if (wtot == 0) continue;  // warp-uniform
+    int scan = lc;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, scan, o);
-    if (lane >= o) scan += u;
-  }
-  uint32_t base = 0;
-  if (lane == 0) base = atomicAdd(ncand, (uint32_t)wtot);
-  uint32_t idx = __shfl_sync(0xffffffffu, base, 0) + (uint32_t)(scan - lc);
-  if (lc == 0) return;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, scan, o);
+      if (lane >= o) scan += u;
+    }
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(ncand, (uint32_t)wtot);
+    uint32_t idx = __shfl_sync(0xffffffffu, base, 0) + (uint32_t)(scan - lc);
+    if (lc == 0) continue;
 #pragma unroll
-  for (int i = 0; i < SCAN_B; ++i) {
-    const int blk = b0 + i;
-    const int j0 = j_base + blk * 128 + 4 * lane;
-    const int gb = (j_base >> 7) + blk;
-    const bool live = i < per && blk < nblocks;
-    const bool inb = incl == nullptr || (live && ((incl[gb >> 5] >> (gb & 31)) & 1u));
-    const int nv = live && inb ? n - j0 : 0;
-    const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    for (int i = 0; i < SCAN_B; ++i) {
+      const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      const int j0 = j_base + (g + i) * 128 + 4 * lane;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t key = order_key(e[c]);
-      if (c < nv && (key >> HIST_SHIFT) == bstar) {
-        if (idx < ccap) cand[idx] = cand_value(key, j0 + c);
-        ++idx;
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t key = order_key(e[c]);
+        if (c < nvs[i] && (key >> HIST_SHIFT) == bstar) {
+          if (idx < ccap) cand[idx] = cand_value(key, j0 + c);
+          ++idx;
+        }
       }
     }
   }
@@ -591,9 +586,19 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
   uint64_t* cand = C <= cap ? cand_s : gcand;
   const uint32_t ccap = C <= cap ? cap : (uint32_t)n;
 
-  // 2. selection bitmap and candidates, chunk by chunk
+  // 2. selection bitmap and candidates: a resident row in one pass once all of it has landed, a
+  // longer one chunk by chunk
   int stop = nchunks;  // first chunk not consumed
-  for (int cc = 0; cc < nchunks; ++cc) {
+  if (resident) {
+    bool ok = true;
+    for (int cc = 0; cc < nchunks && ok; ++cc) ok = tc::mbar_wait_bounded(&c->bar[cc], 0, abort);
+    if (__syncthreads_and(ok))
+      scan_chunk(reinterpret_cast<const float*>(chunks), n128 >> 7, 0, n, bstar, bits, words, cand, ccap, &c->ncand,
+                 incl, all_in);
+    else
+      stop = 0;
+  }
+  for (int cc = 0; cc < nchunks && !resident; ++cc) {
     if (!__syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc % NBUF], (cc / NBUF) & 1, abort))) {
       stop = cc;
       break;
