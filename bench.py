@@ -283,9 +283,8 @@ def replica_count(step_bytes, l2_bytes):
 
 
 def rotating_call_us(torch, replays, reps):
-    """GPU time of one call: the replicas' graphs of that call replayed back to back in rotation,
-    `reps` rounds, between two CUDA events on the launching stream, divided by the calls made (the
-    host stays ahead of the GPU, so no host launch gap enters)."""
+    """GPU time of one replay: the given graphs replayed back to back in rotation, `reps` rounds,
+    between two CUDA events on the launching stream, divided by the replays made."""
     stream = torch.cuda.current_stream()
     for f in replays:
         f()
@@ -331,30 +330,44 @@ def measure_workload(cfg, K, warmup, world, local, want_e2e):
     del st
 
     calls = ["insert", "compress", "indexer", "attention"]
-    # each replica's step (and each call alone) captured once as a CUDA graph: the library never
-    # synchronises, so the calls replay with no host launch gaps
-    graph_step, graph_call = [], {c: [] for c in calls}
-    launches_step = None  # the library's kernels in one step: its launch counter across one capture
+    # CUDA graphs: each replica's step alone, and the R replicas' steps back to back in one graph (the
+    # replicas in rotation, as R layers of one model graph would run), so that consecutive steps are
+    # not separated by host graph launches; each call likewise, CALL_ROUNDS rounds of the R replicas'
+    # calls in one graph.  The library never synchronises, so nothing inside a graph waits on the host.
+    CALL_ROUNDS = 4
     for ds in reps_ds:
         for _ in range(max(warmup, 3)):
             ds.run()
+    torch.cuda.synchronize()
+    graph_single = []
+    launches_step = None  # the library's kernels in one step: its launch counter across one capture
+    for ds in reps_ds:
         g = torch.cuda.CUDAGraph()
         n0 = M.dsv4_kernel_launches()
         with torch.cuda.graph(g):
             ds.run()
         if launches_step is None:
             launches_step = M.dsv4_kernel_launches() - n0
-        graph_step.append(g)
-        for c in calls:
-            gc = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gc):
-                getattr(ds, c)()
-            graph_call[c].append(gc)
+        graph_single.append(g)
+    graph_multi = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_multi):
+        for ds in reps_ds:
+            ds.run()
+    graph_call = {}
+    for c in calls:
+        gc = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gc):
+            for _ in range(CALL_ROUNDS):
+                for ds in reps_ds:
+                    getattr(ds, c)()
+        graph_call[c] = gc
     for _ in range(3):
-        for g in graph_step:
-            g.replay()
+        graph_multi.replay()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    # exactly K steps: K // R replays of the R-step graph, then K % R single steps
+    plan = [graph_multi] * (K // R) + [graph_single[k] for k in range(K % R)]
+    steps_of = [R] * (K // R) + [1] * (K % R)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(len(plan))]
     sampler = ClockSampler(local)
     if world > 1:
         import torch.distributed as dist
@@ -363,23 +376,26 @@ def measure_workload(cfg, K, warmup, world, local, want_e2e):
     sampler.start()
     time.sleep(0.2)
     wall0 = time.perf_counter()
-    for k in range(K):
+    for k, g in enumerate(plan):
         ev[k][0].record(stream)
-        graph_step[k % R].replay()
+        g.replay()
         ev[k][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms_per_step = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    ms_per_step = sum(e[0].elapsed_time(e[1]) for e in ev) / sum(steps_of)
     ms_per_step = max_over_ranks(ms_per_step, world, "cuda")
-    # per-call breakdown: each call's graphs, replicas in rotation
-    rounds = max(1, min(K, 400) // R)
-    per_call_us = {c: rotating_call_us(torch, [g.replay for g in graph_call[c]], rounds) for c in calls}
+    # per-call breakdown: each call's graph (CALL_ROUNDS x R calls, replicas in rotation), CUDA events
+    # around a few replays, divided by the calls made
+    reps = max(1, min(K, 400) // (R * CALL_ROUNDS))
+    per_call_us = {c: rotating_call_us(torch, [graph_call[c].replay], reps) / (R * CALL_ROUNDS) for c in calls}
 
     res = {"ms_per_step": ms_per_step, "value": job_tokens_per_s(cfg.T, world, ms_per_step), "calls_us": per_call_us,
            "clocks": clocks, "wall_s_timed": wall, "gpu_launches": int(K * launches_step),
+           "timing": (f"steps: CUDA graphs of the {R} replicas' steps back to back ({K // R} replays) + {K % R} "
+                      f"single-step graphs; calls: graphs of {CALL_ROUNDS} x {R} calls"),
            "step_algorithmic_gbs": sum(alg.values()) / (ms_per_step * 1e-3) / 1e9,
            "config": {"workload": cfg.name, "batch_per_gpu": cfg.B, "q_per_seq": cfg.q_per_seq,
                       "context": ctx_range,
@@ -431,7 +447,7 @@ def measure_workload(cfg, K, warmup, world, local, want_e2e):
     res["calls_roofline"] = {c: {"algorithmic_bytes": int(alg[c]), "us": per_call_us[c],
                                  "frac": alg[c] / (per_call_us[c] * 1e-6) / 1e9 / peak if per_call_us[c] > 0 else None}
                              for c in calls if c in alg}
-    del reps_ds, ds0, graph_step, graph_call
+    del reps_ds, ds0, graph_single, graph_multi, graph_call
     torch.cuda.empty_cache()
     return res
 
@@ -516,7 +532,7 @@ def run_ours(args):
         "config": dict(head["config"], parallelism=f"replicas x{world} (per-sequence)"),
         "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "roofline": head["roofline"],
         "calls_us": head["calls_us"], "calls_roofline": head["calls_roofline"],
-        "step_algorithmic_gbs": head["step_algorithmic_gbs"], "clocks": head["clocks"],
+        "step_algorithmic_gbs": head["step_algorithmic_gbs"], "clocks": head["clocks"], "timing": head["timing"],
         "wall_s_timed": head["wall_s_timed"],
     }
     if world == 1 and not args.no_extra:
@@ -527,7 +543,8 @@ def run_ours(args):
                 continue
             r = measure_workload(I.ALL_CONFIGS[name], min(K, 500), args.warmup, 1, local, want_e2e=False)
             extra[name] = {k: r[k] for k in ("value", "ms_per_step", "dtype", "config", "roofline", "calls_us",
-                                             "calls_roofline", "step_algorithmic_gbs", "clocks", "gpu_launches")}
+                                             "calls_roofline", "step_algorithmic_gbs", "clocks", "gpu_launches",
+                                             "timing")}
             extra[name]["unit"] = "tokens/s"
             extra[name]["steps"] = min(K, 500)
         for name in PREFILL_WORKLOADS:
