@@ -163,6 +163,7 @@ struct Ctl {
   uint32_t bin, above, cnt, ncand;
   uint32_t total;  // block_find_bin: the sum of the histogram
   int run;         // candidate filtering: entries of the token's list that name blocks
+  int last;        // topk_part: this CTA completed the token's count
   int wt[40];      // block scan scratch
 };
 static_assert(sizeof(Ctl) <= CTL_BYTES, "top-k control block");
@@ -630,6 +631,141 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
                   s_g, c, reinterpret_cast<int*>(cand_s));
   __syncthreads();  // the buffer may be reused right away
   return true;
+}
+constexpr int INCL_MAX_WORDS = (1 << 20) / 128 / 32;  // inclusion bitmap of the longest row
+
+// One CTA's part of a token's top-k that several CTAs share, a slice of the row each: the scores
+// s_g[j_lo, j_hi) (j_lo a multiple of 128; entries >= n ignored) are scanned against the threshold
+// bin of the token's complete histogram into the token's selection bitmap bits_g and candidate list
+// cand_g (counter tcnt[0]).  `mine` of the token's `total` units are this CTA's (counter tcnt[1]); the
+// CTA that adds the last of them chooses among the candidates, writes the selection (out, out_s),
+// clears the histogram and both counters and, for a candidate source (pub_row), publishes the
+// token's best blocks.  A consumer passes its list (crow, cM, clg): only its named blocks take part.
+// When n <= K the last CTA writes every entry.  Returns 1 if this CTA was the last, 0 if not, -1 if a
+// copy timed out (the token's output is then left as it was; the caller raises the flag).  Whole
+// CTA; buf: buf_bytes of 128-byte aligned shared memory.
+__device__ __noinline__ int topk_part(const float* s_g, uint32_t* hist_g, int n, int K, int j_lo, int j_hi, uint32_t mine,
+                         uint32_t total, uint32_t* bits_g, uint64_t* cand_g, uint32_t* tcnt, int32_t* out,
+                         float* out_s, uint8_t* buf, size_t buf_bytes, volatile int* abort, const int32_t* crow,
+                         int cM, int clg, int32_t* pub_row, int pub_M) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  Ctl* c = reinterpret_cast<Ctl*>(buf);
+  uint32_t* rb = reinterpret_cast<uint32_t*>(buf + CTL_BYTES);
+  uint32_t* hist_s = rb + RBINS;
+  uint8_t* chunks = reinterpret_cast<uint8_t*>(hist_s + HIST_BINS);
+  uint32_t* incl = reinterpret_cast<uint32_t*>(chunks + (size_t)NBUF * CHUNK * 4);
+  uint64_t* cand_s = reinterpret_cast<uint64_t*>(incl + INCL_MAX_WORDS);
+  const size_t fixed = CTL_BYTES + RBINS * 4 + HIST_BINS * 4 + (size_t)NBUF * CHUNK * 4 + INCL_MAX_WORDS * 4;
+  const uint32_t cap = buf_bytes > fixed ? (uint32_t)((buf_bytes - fixed) / 8) : 0u;
+  auto count_done = [&]() {  // this CTA's units, after all its writes; true for the CTA that completes the count
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) c->last = atomicAdd(&tcnt[1], mine) + mine == total;
+    __syncthreads();
+    return c->last != 0;
+  };
+  if (n <= K) {  // short context: the last CTA writes every entry, in order
+    if (!count_done()) return 0;
+    for (int x = tid; x < K; x += NT) {
+      out[x] = x < n ? x : -1;
+      if (out_s) out_s[x] = x < n ? __ldcg(s_g + x) : -INFINITY;
+    }
+    for (int x = tid; x < HIST_BINS; x += NT) hist_g[x] = 0u;
+    if (tid == 0) tcnt[1] = 0u;
+    if (pub_row) {
+      __syncthreads();
+      publish_blocks(s_g, n, clg, pub_M, pub_row, buf);
+    }
+    __syncthreads();
+    return 1;
+  }
+  if ((size_t)K > 2 * (size_t)cap) {  // the selection is listed over the candidate area (never short here)
+    if (tid == 0) atomicOr(&g_flags_ix, FLAG_TOPK);
+    return -1;
+  }
+  const int n128 = (n + 127) & ~127;
+  const int hi = min(j_hi, n128);
+  const int nchunks = hi > j_lo ? (hi - j_lo + CHUNK - 1) / CHUNK : 0;
+  const int words = bitmap_words(n);
+  if (tid == 0) {
+    c->bin = 0;
+    c->above = 0;
+    c->cnt = 0;
+    for (int i = 0; i <= NBUF; ++i) tc::mbar_init(&c->bar[i], 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int cc) {
+    const uint32_t bytes = (uint32_t)min(CHUNK, hi - j_lo - cc * CHUNK) * 4u;
+    uint64_t* bar = &c->bar[cc % NBUF];
+    tc::mbar_arrive_expect_tx(bar, bytes);
+    tc::bulk_load(chunks + (size_t)(cc % NBUF) * CHUNK * 4, s_g + j_lo + (size_t)cc * CHUNK, bytes, bar);
+  };
+  if (tid == 0) {
+    asm volatile("fence.proxy.async;" ::: "memory");  // scores and counts came through the generic proxy
+    tc::mbar_arrive_expect_tx(&c->bar[NBUF], HIST_BINS * 4);
+    tc::bulk_load(hist_s, hist_g, HIST_BINS * 4, &c->bar[NBUF]);
+    for (int cc = 0; cc < min(NBUF, nchunks); ++cc) issue(cc);
+  }
+  if (crow) build_incl(crow, cM, clg, n, incl, c);  // while the copies are in flight
+  const bool ok = __syncthreads_and(tc::mbar_wait_bounded(&c->bar[NBUF], 0, abort));
+  bool all_in = false;  // a consumer whose named blocks hold at most K entries takes all of them
+  int stop = ok ? nchunks : 0;
+  if (ok) {
+    block_find_bin<HIST_BINS / FIND_THREADS>(hist_s, (uint32_t)K, c);
+    all_in = crow != nullptr && c->total <= (uint32_t)K;
+    const uint32_t bstar = c->bin;
+    for (int cc = 0; cc < nchunks; ++cc) {
+      if (!__syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc % NBUF], (cc / NBUF) & 1, abort))) {
+        stop = cc;
+        break;
+      }
+      scan_chunk(reinterpret_cast<const float*>(chunks + (size_t)(cc % NBUF) * CHUNK * 4),
+                 min(CHUNK, hi - j_lo - cc * CHUNK) >> 7, j_lo + cc * CHUNK, n, bstar, bits_g, words, cand_g,
+                 (uint32_t)n, &tcnt[0], crow ? incl : nullptr, all_in);
+      if (cc + NBUF < nchunks) {
+        tc::fence_proxy_async_smem();  // reads of this buffer come before the next copy into it
+        __syncthreads();
+        if (tid == 0) issue(cc + NBUF);
+      }
+    }
+  }
+  if (stop < nchunks || !ok) {
+    if (tid == 0) {  // copies in flight land before the buffer is given back
+      if (!ok) tc::mbar_wait_bounded(&c->bar[NBUF], 0, abort, 100000000ull);
+      for (int cc = stop; cc < min(nchunks, stop + NBUF); ++cc)
+        tc::mbar_wait_bounded(&c->bar[cc % NBUF], (cc / NBUF) & 1, abort, 100000000ull);
+    }
+    __syncthreads();
+    return -1;  // the token's count never completes: its output stays as it was (flagged)
+  }
+  if (!count_done()) return 0;
+  // the last CTA: every other part of the token is done with the histogram and the counters
+  __threadfence();
+  const int R = all_in ? 0 : K - (int)c->above;
+  const uint32_t m = min(__ldcg(&tcnt[0]), (uint32_t)n);
+  for (int x = tid; x < HIST_BINS; x += NT) hist_g[x] = 0u;
+  __syncthreads();  // m is read by every thread before the counters are cleared
+  if (tid == 0) {
+    tcnt[0] = 0u;
+    tcnt[1] = 0u;
+  }
+  const uint64_t* cand = cand_g;
+  if (m <= cap) {
+    for (uint32_t i = tid; i < m; i += NT) cand_s[i] = __ldcg(cand_g + i);
+    __syncthreads();
+    cand = cand_s;
+  }
+  select_candidates(cand, m, R, rb, c, bits_g);
+  __threadfence();
+  __syncthreads();
+  write_selection(bits_g, true, words, K, out, out_s, nullptr, s_g, c, reinterpret_cast<int*>(cand_s));
+  if (pub_row) {
+    __syncthreads();
+    publish_blocks(s_g, n, clg, pub_M, pub_row, buf);
+  }
+  __syncthreads();
+  return 1;
 }
 }  // namespace tk
 
@@ -1577,122 +1713,30 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(dsv4_indexer_topk_para
 // bitmap and appends its candidates to the token's list; the CTA that finishes the token's last
 // slice chooses among the candidates and writes the selection (no CTA waits for another).
 // ------------------------------------------------------------------------------------------------
-constexpr int INCL_MAX_WORDS = (1 << 20) / 128 / 32;  // inclusion bitmap of the longest row
 constexpr int SLICE_CHUNKS = 2;  // 8192-score slices: more CTAs per long row (measured faster than 16384)
 constexpr int SLICE = SLICE_CHUNKS * tk::CHUNK;  // 8192 scores
 
 __global__ void __launch_bounds__(TK_THREADS) topk_slice_kernel(dsv4_indexer_topk_params p, TopkBufs bufs) {
-  using namespace tk;
   extern __shared__ __align__(128) uint8_t tsm[];
-  __shared__ int abort_s, last_s;
+  __shared__ int abort_s;
   pdl_launch_dependents();
   pdl_wait();
-  const int t = blockIdx.y, sl = blockIdx.x, tid = threadIdx.x;
+  const int t = blockIdx.y, sl = blockIdx.x;
   const int n = visible_entries(p, t), K = p.topk;
-  const float* s_g = bufs.scores + (int64_t)t * bufs.nc_stride;
-  int32_t* out = p.topk_idx + (int64_t)t * K;
-  float* out_s = p.topk_score ? p.topk_score + (int64_t)t * K : nullptr;
+  const int nsl = n <= K ? 1 : (n + SLICE - 1) / SLICE;  // a short row: slice 0 writes every entry
+  if (sl >= nsl) return;  // block-uniform
+  if (threadIdx.x == 0) abort_s = 0;
+  __syncthreads();
   const bool has_cand = p.cand_block_size > 0;
   const int lg = has_cand ? __ffs(p.cand_block_size) - 1 : 0;
   int32_t* crow = has_cand ? p.cand_blocks + (int64_t)t * p.cand_topk : nullptr;
-  if (n <= K) {  // short context: slice 0 writes every entry, in order, and clears the histogram
-    if (sl == 0) {
-      for (int x = tid; x < K; x += TK_THREADS) {
-        out[x] = x < n ? x : -1;
-        if (out_s) out_s[x] = x < n ? __ldcg(s_g + x) : -INFINITY;
-      }
-      for (int x = tid; x < HIST_BINS; x += TK_THREADS) bufs.hist[(int64_t)t * HIST_BINS + x] = 0u;
-      if (has_cand && p.cand_write) tk::publish_blocks(s_g, n, lg, p.cand_topk, crow, tsm);
-    }
-    return;
-  }
-  const int nsl = (n + SLICE - 1) / SLICE;
-  if (sl >= nsl) return;  // block-uniform
-  Ctl* c = reinterpret_cast<Ctl*>(tsm);
-  uint32_t* rb = reinterpret_cast<uint32_t*>(tsm + CTL_BYTES);
-  uint32_t* hist_s = rb + RBINS;
-  uint8_t* chunks = reinterpret_cast<uint8_t*>(hist_s + HIST_BINS);
-  uint32_t* incl = reinterpret_cast<uint32_t*>(chunks + (size_t)SLICE * 4);  // consumer: named 128-entry blocks
-  uint64_t* cand_s = reinterpret_cast<uint64_t*>(incl + INCL_MAX_WORDS);
-  const size_t fixed = CTL_BYTES + RBINS * 4 + HIST_BINS * 4 + (size_t)SLICE * 4 + INCL_MAX_WORDS * 4;
-  const uint32_t cap = (uint32_t)((TK_SMEM - fixed) / 8);
-  const int words = bitmap_words(n);
-  uint32_t* bits_g = bufs.bits + (int64_t)t * (bufs.nc_stride / 32);  // nc_stride / 32 >= bitmap_words(n)
-  uint64_t* cand_g = bufs.cand + (int64_t)t * bufs.nc_stride;
-  const int j_lo = sl * SLICE;
-  const int n128 = (n + 127) & ~127;
-  const int nch = min(SLICE_CHUNKS, (n128 - j_lo + CHUNK - 1) / CHUNK);
-  if (tid == 0) {
-    abort_s = 0;
-    c->bin = 0;
-    c->above = 0;
-    c->cnt = 0;
-    for (int i = 0; i <= NBUF; ++i) tc::mbar_init(&c->bar[i], 1);
-    tc::fence_barrier_init();
-    asm volatile("fence.proxy.async;" ::: "memory");  // scores and counts came through the generic proxy
-    tc::mbar_arrive_expect_tx(&c->bar[NBUF], HIST_BINS * 4);
-    tc::bulk_load(hist_s, bufs.hist + (int64_t)t * HIST_BINS, HIST_BINS * 4, &c->bar[NBUF]);
-    for (int cc = 0; cc < nch; ++cc) {
-      const uint32_t bytes = (uint32_t)min(CHUNK, n128 - j_lo - cc * CHUNK) * 4u;
-      tc::mbar_arrive_expect_tx(&c->bar[cc], bytes);
-      tc::bulk_load(chunks + (size_t)cc * CHUNK * 4, s_g + j_lo + (size_t)cc * CHUNK, bytes, &c->bar[cc]);
-    }
-  }
-  __syncthreads();
-  const bool consume = has_cand && !p.cand_write;
-  if (consume) build_incl(crow, p.cand_topk, lg, n, incl, c);  // while the copies are in flight
-  bool ok = __syncthreads_and(tc::mbar_wait_bounded(&c->bar[NBUF], 0, &abort_s));
-  bool all_in = false;  // a consumer whose named blocks hold at most K entries takes all of them
-  if (ok) {
-    block_find_bin<HIST_BINS / FIND_THREADS>(hist_s, (uint32_t)K, c);
-    all_in = consume && c->total <= (uint32_t)K;
-    const uint32_t bstar = c->bin;
-    for (int cc = 0; cc < nch && ok; ++cc) {
-      ok = __syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc], 0, &abort_s));
-      if (ok)
-        scan_chunk(reinterpret_cast<const float*>(chunks + (size_t)cc * CHUNK * 4),
-                   min(CHUNK, n128 - j_lo - cc * CHUNK) >> 7, j_lo + cc * CHUNK, n, bstar, bits_g, words, cand_g,
-                   (uint32_t)n, &bufs.tcnt[2 * t], consume ? incl : nullptr, all_in);
-    }
-  }
-  if (!ok) {
-    if (tid == 0) {  // copies in flight land before the CTA leaves
-      tc::mbar_wait_bounded(&c->bar[NBUF], 0, &abort_s, 100000000ull);
-      for (int cc = 0; cc < nch; ++cc) tc::mbar_wait_bounded(&c->bar[cc], 0, &abort_s, 100000000ull);
-      atomicOr(&g_flags_ix, FLAG_TIMEOUT);
-    }
-    return;  // the token's count never completes: its output stays as it was (flagged)
-  }
-  // the CTA that finishes the token's last slice makes the final choice
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) last_s = atomicAdd(&bufs.tcnt[2 * t + 1], 1u) == (uint32_t)(nsl - 1);
-  __syncthreads();
-  if (!last_s) return;
-  __threadfence();
-  const int R = all_in ? 0 : K - (int)c->above;
-  const uint32_t m = min(__ldcg(&bufs.tcnt[2 * t]), (uint32_t)n);
-  // every other slice of the token is done with its histogram and counters: cleared for the next call
-  for (int x = tid; x < HIST_BINS; x += TK_THREADS) bufs.hist[(int64_t)t * HIST_BINS + x] = 0u;
-  __syncthreads();  // m is read by every thread before the counters are cleared
-  if (tid == 0) {
-    bufs.tcnt[2 * t] = 0u;
-    bufs.tcnt[2 * t + 1] = 0u;
-  }
-  const uint64_t* cand = cand_g;
-  if (m <= cap) {
-    for (uint32_t i = tid; i < m; i += TK_THREADS) cand_s[i] = __ldcg(cand_g + i);
-    __syncthreads();
-    cand = cand_s;
-  }
-  select_candidates(cand, m, R, rb, c, bits_g);
-  __threadfence();
-  __syncthreads();
-  write_selection(bits_g, true, words, K, out, out_s, nullptr, s_g, c, reinterpret_cast<int*>(cand_s));
-  if (has_cand && p.cand_write) {
-    __syncthreads();
-    tk::publish_blocks(s_g, n, lg, p.cand_topk, crow, tsm);
-  }
+  const int r = tk::topk_part(bufs.scores + (int64_t)t * bufs.nc_stride, bufs.hist + (int64_t)t * HIST_BINS, n, K,
+                              sl * SLICE, (sl + 1) * SLICE, 1u, (uint32_t)nsl, bufs.bits + (int64_t)t * (bufs.nc_stride / 32),
+                              bufs.cand + (int64_t)t * bufs.nc_stride, &bufs.tcnt[2 * t], p.topk_idx + (int64_t)t * K,
+                              p.topk_score ? p.topk_score + (int64_t)t * K : nullptr, tsm, TK_SMEM, &abort_s,
+                              has_cand && !p.cand_write ? crow : nullptr, p.cand_topk, lg,
+                              has_cand && p.cand_write ? crow : nullptr, p.cand_topk);
+  if (r < 0 && threadIdx.x == 0) atomicOr(&g_flags_ix, FLAG_TIMEOUT);
 }
 
 cudaError_t launch_indexer_topk(const dsv4_indexer_topk_params& p, cudaStream_t st) {
