@@ -165,7 +165,8 @@ class DeviceStep:
         implies the others'.
         With an indexer over given keys: indexer -> insert -> compress -> attention, insert and
         compress both starting at once beside the indexer.
-        Without an indexer: insert -> compress -> attention, each waiting for the one before."""
+        Without an indexer: compress -> insert -> attention, the insert (which touches nothing the
+        compressor reads or writes) starting at once beside the compressor."""
         if self.ik_store:
             self.compress(stream)
             self.indexer(stream)
@@ -174,9 +175,11 @@ class DeviceStep:
             self.indexer(stream)
             self.insert(stream, after_independent=True)
             self.compress(stream, after_independent=True)
+        elif self.has_compress:
+            self.compress(stream)
+            self.insert(stream, after_independent=True)
         else:
             self.insert(stream)
-            self.compress(stream)
         self.attention(stream)
 
     def step_input_tensors(self):
