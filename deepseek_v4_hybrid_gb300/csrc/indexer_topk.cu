@@ -867,7 +867,8 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
 // (times the key's row scale for int8 keys).
 //
 // Persistent CTAs (one per SM), each owning a contiguous range of (sequence, 128-key tile) items: an
-// even share of the valid tiles.  Warp 8 streams key tiles with TMA (two 64-row pages x d/64
+// even share of the work, counted as the valid tiles plus a few tiles' worth for every sequence a CTA
+// starts on.  Warp 8 streams key tiles with TMA (two 64-row pages x d/64
 // K-blocks of 128 B, 128-byte swizzle) into a ring of stages (int8 keys: the two record pages by
 // bulk copy into a ring of two raw stages, which warps 10-11 expand into the stages), and each
 // sequence's Q block into one of two Q slots (one when shared memory is short); its 32 lanes look
@@ -896,6 +897,8 @@ constexpr int KF_BF16 = 0, KF_I8 = 1, KF_MX = 2;  // key formats of the tensor-c
 constexpr int FIN_MAX = 64;  // sequences whose top-k one CTA may have to run
 constexpr int WSEQ = 8;      // sequences whose head weights and entry counts are loaded up front
 constexpr int PRE_MAX = 1024;  // batches up to this size split the key tiles evenly over the CTAs
+constexpr int SEQ_START_UNITS = 5;  // tiles' worth of time a CTA spends moving on to another sequence
+                                    // (traced: CTAs that do end about 4.5 us, 5 tiles, later)
 
 struct Args {
   const int32_t* positions;
@@ -1074,7 +1077,7 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
   pdl_wait();  // nothing below runs before the kernels ahead of this one have finished
   // Set-up, arranged so that the loading warp issues its first copies as early as possible: it
   // initialises the mbarriers and works out the CTA's range [lo, hi) of the (sequence, tile) grid (an
-  // even share of the sequences' valid tiles, from a prefix over their tile counts), announces both on
+  // even share of the work, from a prefix over the sequences' tile counts), announces both on
   // named barrier BAR_SETUP and goes straight on to loading.  The MMA warp allocates TMEM and announces
   // it on BAR_TMEM to the epilogue warps, which meanwhile clear their histograms and load the head
   // weights and entry counts of the CTA's sequences.
@@ -1107,9 +1110,14 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
     }
     int r0 = (int)((int64_t)blockIdx.x * total / gridDim.x), r1 = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
     if (a.B <= PRE_MAX) {
-      // the tile counts first (independent loads, all in flight together), then the scan
+      // the work of each sequence in tile units (its tiles, plus SEQ_START_UNITS for starting on it:
+      // the histogram flush and counter update of the sequence left and the next queries), all loaded
+      // first (independent loads, all in flight together), then the scan
 #pragma unroll 4
-      for (int b = lane; b < a.B; b += 32) sm->pre[b] = live_tiles(a, b, seq_entries(a, b));
+      for (int b = lane; b < a.B; b += 32) {
+        const int nt = live_tiles(a, b, seq_entries(a, b));
+        sm->pre[b] = nt > 0 ? nt + SEQ_START_UNITS : 0;
+      }
       __syncwarp();
       int running = 0;
       for (int b0 = 0; b0 < a.B; b0 += 32) {
@@ -1125,7 +1133,7 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
         running += __shfl_sync(0xffffffffu, incl, 31);
       }
       __syncwarp();
-      auto dense = [&](int x) {  // grid position of valid tile number x
+      auto dense = [&](int x) {  // grid position of work unit x (a sequence's start units: its first tile)
         if (x >= running) return total;
         int l = 0, r = a.B - 1;  // last b with pre[b] <= x (it has a tile, since x < pre[b + 1])
         while (l < r) {
@@ -1133,7 +1141,7 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
           if (sm->pre[m] <= x) l = m;
           else r = m - 1;
         }
-        return l * a.tiles_max + (x - sm->pre[l]);
+        return l * a.tiles_max + max(0, x - sm->pre[l] - SEQ_START_UNITS);
       };
       r0 = dense((int)((int64_t)blockIdx.x * running / gridDim.x));
       r1 = dense((int)((int64_t)(blockIdx.x + 1) * running / gridDim.x));
