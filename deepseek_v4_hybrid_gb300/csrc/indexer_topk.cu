@@ -334,6 +334,66 @@ __device__ __forceinline__ void scan_chunk(const float* sb, int nblocks, int j_b
   }
 }
 
+// The bitmap words and candidates of a whole resident row in one pass, as scan_chunk, but without
+// atomics: each warp appends its candidates (found by ballots, in lane order within each column of a
+// block) to its own region regs + warp * C, where C is the threshold bin's count (the histogram counts
+// the same scores, so a region never overflows; writes beyond it are dropped), then the regions are
+// packed in warp order into cand[0, m) and c->ncand = m.  Whole CTA; regs and cand in shared memory.
+__device__ void scan_resident(const float* sb, int nblocks, int n, uint32_t bstar, uint32_t* bits, int words,
+                              uint64_t* regs, uint32_t C, uint64_t* cand, Ctl* c, const uint32_t* incl,
+                              bool all_in) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
+  const float4* sb4 = reinterpret_cast<const float4*>(sb);
+  const int per = (nblocks + NW - 1) / NW;
+  const int b0 = min(nblocks, warp * per), b1 = min(nblocks, b0 + per);
+  uint64_t* my = regs + (size_t)warp * C;
+  uint32_t cnt = 0;  // warp-uniform
+  const unsigned below = (1u << lane) - 1u;
+  for (int g = b0; g < b1; g += SCAN_B) {
+    float4 v[SCAN_B];
+#pragma unroll
+    for (int i = 0; i < SCAN_B; ++i) v[i] = g + i < b1 ? sb4[(g + i) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < SCAN_B; ++i) {
+      const int blk = g + i;
+      const bool live = blk < b1 && (incl == nullptr || ((incl[blk >> 5] >> (blk & 31)) & 1u));  // warp-uniform
+      const int j0 = blk * 128 + 4 * lane;
+      const int nv = live ? n - j0 : 0;
+      const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint32_t sw[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t key = order_key(e[q]);
+        const uint32_t bin = key >> HIST_SHIFT;
+        sw[q] = __ballot_sync(0xffffffffu, q < nv && (all_in || bin > bstar));
+        if (!all_in) {
+          const unsigned cm = __ballot_sync(0xffffffffu, q < nv && bin == bstar);
+          if (cm) {  // warp-uniform
+            const uint32_t at = cnt + (uint32_t)__popc(cm & below);
+            if (((cm >> lane) & 1u) && at < C) my[at] = cand_value(key, j0 + q);
+            cnt += (uint32_t)__popc(cm);
+          }
+        }
+      }
+      if (lane == 0 && blk < b1 && 4 * blk < words)
+        *reinterpret_cast<uint4*>(bits + 4 * blk) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+    }
+  }
+  if (lane == 0) c->wt[warp] = (int)min(cnt, C);
+  __syncthreads();
+  uint32_t base = 0, total = 0;
+  for (int w = 0; w < NW; ++w) {
+    const uint32_t k = (uint32_t)c->wt[w];
+    base += w < warp ? k : 0u;
+    total += k;
+  }
+  const uint32_t mine = min(cnt, C);
+  for (uint32_t i = lane; i < mine; i += 32) cand[base + i] = my[i];
+  __syncthreads();
+  if (threadIdx.x == 0) c->ncand = total;
+  __syncthreads();
+}
+
 // Threshold of the R largest (0 < R < m) of m unique values get(i) < 2^(TOP + 10): a radix select of
 // 10-bit digits from bit TOP down that stops at the first digit whose bin holds exactly the values
 // still needed; the R largest are the values >= the result.  rb: RBINS shared bins.  Whole CTA.
@@ -593,11 +653,14 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
   if (resident) {
     bool ok = true;
     for (int cc = 0; cc < nchunks && ok; ++cc) ok = tc::mbar_wait_bounded(&c->bar[cc], 0, abort);
-    if (__syncthreads_and(ok))
+    if (!__syncthreads_and(ok))
+      stop = 0;
+    else if ((size_t)C * ((blockDim.x >> 5) + 1) <= cap)  // per-warp regions above the packed list
+      scan_resident(reinterpret_cast<const float*>(chunks), n128 >> 7, n, bstar, bits, words, cand_s + C, C, cand_s,
+                    c, incl, all_in);
+    else
       scan_chunk(reinterpret_cast<const float*>(chunks), n128 >> 7, 0, n, bstar, bits, words, cand, ccap, &c->ncand,
                  incl, all_in);
-    else
-      stop = 0;
   }
   for (int cc = 0; cc < nchunks && !resident; ++cc) {
     if (!__syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc % NBUF], (cc / NBUF) & 1, abort))) {
