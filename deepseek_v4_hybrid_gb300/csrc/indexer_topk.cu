@@ -135,11 +135,11 @@ __device__ __forceinline__ bool cand_names(const int32_t* row, int M, int blk) {
 
 // ------------------------------------------------------------------------------------------------
 // Top-k of one token, run by one whole CTA once the token's scores and histogram are complete.
-// The histogram and the score row reach shared memory by bulk (TMA) copies, the row in 16 KB chunks
-// with up to four in flight (plain loads would go through an L1 that the kernels' large shared
-// memory leaves almost no room).
+// The score row reaches shared memory by bulk (TMA) copies in 16 KB chunks with up to four in flight
+// (plain loads would go through an L1 that the kernels' large shared memory leaves almost no room).
 //  1. From the histogram, the bin B* holding the k-th best score and the count A of scores above it
-//     (256 threads own 16 bins each, a block scan from the top finds the crossing thread).
+//     (256 threads own 16 bins each, read straight from L2; a block scan from the top finds the
+//     crossing thread).
 //  2. One pass over the scores: lane l of a warp takes entries 4l .. 4l + 3 of a 128-entry block;
 //     the four ballots of "bin > B*" are the block's four words of the selection bitmap (bit l of
 //     word c = entry 4l + c), and entries in B* are appended to a candidate list as (low 20 key
@@ -223,10 +223,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wt, int* total) {
   return r;
 }
 
-// The bin of shared histogram h (256 * PER bins) where the count from the top first reaches rem:
-// c->bin, the count in the bins above it: c->above, its own count: c->cnt.  Thread i < 256 owns
-// bins [256 PER - PER (i + 1), 256 PER - PER i) (the top bins first).  Called by the whole CTA.
-template <int PER>
+// The bin of histogram h (256 * PER bins; in shared memory, or with GLOBAL in global memory, read
+// through L2) where the count from the top first reaches rem: c->bin, the count in the bins above
+// it: c->above, its own count: c->cnt.  Thread i < 256 owns bins [256 PER - PER (i + 1), 256 PER -
+// PER i) (the top bins first).  Called by the whole CTA.
+template <int PER, bool GLOBAL = false>
 __device__ __forceinline__ void block_find_bin(const uint32_t* h, uint32_t rem, Ctl* c) {
   const int tid = threadIdx.x;
   uint32_t v[PER];
@@ -235,7 +236,7 @@ __device__ __forceinline__ void block_find_bin(const uint32_t* h, uint32_t rem, 
     const uint4* src = reinterpret_cast<const uint4*>(h + FIND_THREADS * PER - PER * (tid + 1));
 #pragma unroll
     for (int q = 0; q < PER / 4; ++q) {
-      const uint4 u = src[q];
+      const uint4 u = GLOBAL ? __ldcg(src + q) : src[q];
       v[4 * q] = u.x;
       v[4 * q + 1] = u.y;
       v[4 * q + 2] = u.z;
@@ -618,27 +619,17 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
     tc::bulk_load(chunks + (size_t)(cc % NBUF) * CHUNK * 4, s_g + (size_t)cc * CHUNK, bytes, bar);
   };
   if (tid == 0) {
-    // the scores and counts were written through the generic proxy (possibly by other CTAs): order
-    // them before the bulk copies read them
+    // the scores were written through the generic proxy (possibly by other CTAs): order them before
+    // the bulk copies read them
     asm volatile("fence.proxy.async;" ::: "memory");
-    tc::mbar_arrive_expect_tx(&c->bar[NBUF], HIST_BINS * 4);
-    tc::bulk_load(hist_s, hist_g, HIST_BINS * 4, &c->bar[NBUF]);
     for (int cc = 0; cc < min(NBUF, nchunks); ++cc) issue(cc);
   }
   if (incl) build_incl(crow, cM, clg, n, incl, c);  // while the copies are in flight
 
-  // 1. threshold bin
-  if (!__syncthreads_and(tc::mbar_wait_bounded(&c->bar[NBUF], 0, abort))) {
-    if (tid == 0)  // copies in flight land before the buffer is given back
-      for (int cc = 0; cc < min(NBUF, nchunks); ++cc) tc::mbar_wait_bounded(&c->bar[cc], 0, abort, 100000000ull);
-    for (int x = tid; x < K; x += NT) out[x] = -1;
-    __syncthreads();
-    return false;
-  }
-  // the copy has landed: the token's global histogram is cleared for the next call (this CTA is its last
-  // reader)
+  // 1. threshold bin, from the global histogram read through L2 (each counting thread loads its own
+  // 16 bins), which is then cleared for the next call (this CTA is its last reader)
+  block_find_bin<HIST_BINS / FIND_THREADS, true>(hist_g, (uint32_t)K, c);
   for (int x = tid; x < HIST_BINS; x += NT) hist_g[x] = 0u;
-  block_find_bin<HIST_BINS / FIND_THREADS>(hist_s, (uint32_t)K, c);
   // a consumer whose named blocks hold at most K entries (the histogram counts them) takes all of them
   const bool all_in = incl != nullptr && c->total <= (uint32_t)K;
   const uint32_t bstar = c->bin;
