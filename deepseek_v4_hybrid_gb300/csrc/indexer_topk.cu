@@ -924,7 +924,7 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
 // even share of the work, counted as the valid tiles plus a few tiles' worth for every sequence a CTA
 // starts on.  Warp 8 streams key tiles with TMA (two 64-row pages x d/64
 // K-blocks of 128 B, 128-byte swizzle) into a ring of stages (int8 keys: the two record pages by
-// bulk copy into a ring of two raw stages, which warps 10-11 expand into the stages), and each
+// bulk copy into a ring of raw stages, which warps 10-13 expand into the stages), and each
 // sequence's Q block into one of two Q slots (one when shared memory is short); its 32 lanes look
 // up the block-table pages of 32 items at a time.  One thread of warp 9 issues the tcgen05 MMAs
 // (M = 128, K = 16 steps) into a ring of TMEM accumulators.  Warps 0-7 are two epilogue groups of
@@ -938,12 +938,13 @@ __global__ void __launch_bounds__(IX_TILE) indexer_score_simt(dsv4_indexer_topk_
 namespace ixtc {
 constexpr int TILE = 128;
 constexpr int KB_BYTES = TILE * 128;         // one 64-dim K-block of a key tile (128 rows x 128 B)
-constexpr int NEXP = 2;  // warps expanding raw records (int8, MXFP4 keys): 12 warps keep 168 registers a thread
-                         // (an SM sub-partition holds 3 warps of 168 registers in its 16K)
+constexpr int NEXP = 4;  // warps expanding raw records (int8, MXFP4 keys), one record row a thread: with 14
+                         // warps two SM sub-partitions hold 4 of them, so these instances keep to 128
+                         // registers a thread (4 x 32 x 128 = the 16K of a sub-partition)
 constexpr int THREADS_BF16 = 320;              // bf16 keys: warps 0-7 epilogue, 8 loads, 9 MMA
 constexpr int THREADS = THREADS_BF16 + NEXP * 32;  // raw records: warps 10 .. 9 + NEXP expand
 static_assert(THREADS_BF16 / 32 >= tk::SCAN_WARPS_MIN, "the top-k scan covers a chunk with this many warps");
-constexpr int W_LOAD = 8, W_MMA = 9;  // warps 10-11 expand int8 keys to bf16 (int8 caches only)
+constexpr int W_LOAD = 8, W_MMA = 9;  // warps 10 .. 9 + NEXP expand raw records (int8, MXFP4 caches)
 constexpr int SCALE_RING = 16;        // int8 keys: row scales of the last 16 tiles (> stages + accumulators)
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_RAW = 8;            // raw record pages in flight (int8 keys 2, MXFP4 keys up to 8)
@@ -1102,13 +1103,13 @@ __device__ __forceinline__ bool finish_seq(const Args& a, Smem* sm, uint32_t* hi
   return true;
 }
 
-// One instance per key format: the bf16 one has no expanding warps (320 threads) and none of the
-// raw-record branches. All keep the 384-thread register cap: three warps of a sub-partition share its
-// 16K registers, so 168 a thread.
+// One instance per key format: the bf16 one has no expanding warps (320 threads, at most three warps
+// on a sub-partition: 168 registers a thread) and none of the raw-record branches; the raw-record
+// ones run 14 warps at 128 registers a thread (the 512-thread bound sets that cap).
 template <int KF>
-__global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
+__global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
     indexer_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, Args a) {
-  constexpr bool RAW = KF != KF_BF16;  // records bulk-copied as pages and expanded to bf16 by warps 10-11
+  constexpr bool RAW = KF != KF_BF16;  // records bulk-copied as pages and expanded to bf16 by warps 10-13
   constexpr bool I8 = KF == KF_I8;     // int8 records: row scales applied to the finished score
   extern __shared__ __align__(1024) uint8_t dsm[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
@@ -1520,7 +1521,28 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : THREADS, 1)
       }
       float sk[DSV4_MAX_Q_PER_SEQ] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(acc * a.N);
-      for (int c0 = 0; c0 < a.N; c0 += 64) {
+      // raw-record instances read 32 columns at a time (one token's heads: n_heads is a multiple of
+      // 32) to keep to their 128 registers
+      for (int c0 = 0; c0 < a.N && RAW; c0 += 32) {
+        uint32_t r[32];
+        tc::tmem_ld32_nowait(lane_addr + c0, r);
+        tc::tmem_wait_ld_regs<32>(r);
+        const float4* w4 = reinterpret_cast<const float4*>(w_g + c0);
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 w = w4[i];
+          p[0] = fmaf(w.x, fmaxf(__uint_as_float(r[4 * i + 0]), 0.f), p[0]);
+          p[1] = fmaf(w.y, fmaxf(__uint_as_float(r[4 * i + 1]), 0.f), p[1]);
+          p[2] = fmaf(w.z, fmaxf(__uint_as_float(r[4 * i + 2]), 0.f), p[2]);
+          p[3] = fmaf(w.w, fmaxf(__uint_as_float(r[4 * i + 3]), 0.f), p[3]);
+        }
+        const int k0 = c0 / a.Ih;
+#pragma unroll
+        for (int q = 0; q < DSV4_MAX_Q_PER_SEQ; ++q)
+          if (q == k0) sk[q] += (p[0] + p[1]) + (p[2] + p[3]);
+      }
+      for (int c0 = 0; c0 < a.N && !RAW; c0 += 64) {
         uint32_t r[64];
         tc::tmem_ld32_nowait(lane_addr + c0, r);
         tc::tmem_ld32_nowait(lane_addr + c0 + 32, r + 32);
