@@ -259,3 +259,36 @@ def test_indexer_workspace_left_clean(lib, name):
         outs.append(to_host(ds.topk_idx).copy())
     for got in outs:
         assert np.array_equal(got, outs[-1])
+
+
+def test_two_level_chain_source_feeds_consumer(lib):
+    """The candidate source publishes its tokens' best blocks on the device; a later layer (its own keys
+    and queries, the same positions) consumes exactly those lists: the consumer's selection matches the
+    oracle given the same lists, and every selected entry lies in a published block."""
+    import dataclasses
+    from deepseek_v4_hybrid_gb300.step import DeviceStep
+    src_cfg = I.SMALL_CONFIGS["small_c4_cand_src"]
+    st_a = I.make_step(src_cfg)
+    ds_a = DeviceStep(st_a)
+    ds_a.run()
+    torch.cuda.synchronize()
+    assert lib.dsv4_read_device_flags() == 0
+    published = to_host(ds_a.cand_blocks).copy()
+    res_a = O.decode_step(st_a)
+    for t in res_a["tokens"]:
+        assert CMP.cand_blocks_match(published[t], res_a["scores"][t], src_cfg.cand_block, src_cfg.cand_topk)
+    cons_cfg = dataclasses.replace(src_cfg, name="chain_consumer", cand_write=False, seed=src_cfg.seed + 99)
+    st_b = I.make_step(cons_cfg)
+    st_b.cand_in = published
+    ds_b = DeviceStep(st_b)
+    ds_b.run()
+    torch.cuda.synchronize()
+    assert lib.dsv4_read_device_flags() == 0
+    res_b = O.decode_step(st_b)
+    CMP.check_step(st_b, res_b, gpu_results(ds_b), where="chain consumer")
+    sel = to_host(ds_b.topk_idx)
+    for t in res_b["tokens"]:
+        nc = len(res_b["scores"][t])
+        if nc > cons_cfg.topk:
+            blocks = set(published[t][published[t] >= 0].tolist())
+            assert all(j // cons_cfg.cand_block in blocks for j in sel[t][sel[t] >= 0])
