@@ -1128,17 +1128,19 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = a.B * a.tiles_max;
-  pdl_launch_dependents();
-  pdl_wait();  // nothing below runs before the kernels ahead of this one have finished
-  // Set-up, arranged so that the loading warp issues its first copies as early as possible: it
-  // initialises the mbarriers and works out the CTA's range [lo, hi) of the (sequence, tile) grid (an
-  // even share of the work, from a prefix over the sequences' tile counts), announces both on
-  // named barrier BAR_SETUP and goes straight on to loading.  The MMA warp allocates TMEM and announces
-  // it on BAR_TMEM to the epilogue warps, which meanwhile clear their histograms and load the head
-  // weights and entry counts of the CTA's sequences.
+  // Set-up that reads nothing in global memory runs before the dependency wait, while the kernel
+  // ahead finishes (the launch lets this grid start early): the loading warp initialises the
+  // mbarriers and prefetches the tensor maps, the MMA warp allocates TMEM, the epilogue warps clear
+  // their histograms.  After the wait the loading warp works out the CTA's range [lo, hi) of the
+  // (sequence, tile) grid (an even share of the work, from a prefix over the sequences' tile counts),
+  // announces it on named barrier BAR_SETUP and goes straight on to loading; the MMA warp announces
+  // TMEM on BAR_TMEM to the epilogue warps, which meanwhile load the head weights and entry counts of
+  // the CTA's sequences.
   constexpr uint32_t BAR_SETUP = 1, BAR_TMEM = 2, BAR_EPI = 3;
   if (warp == W_LOAD) {
     if (lane == 0) {
+      tc::tma_prefetch_desc(&kmap);
+      tc::tma_prefetch_desc(&qmap);
       for (int s = 0; s < a.stages; ++s) {
         tc::mbar_init(&sm->full[s], RAW ? NEXP : 1);  // raw records: the expanding warps; else the loader (+ bytes)
         tc::mbar_init(&sm->empty[s], 1);
@@ -1163,6 +1165,7 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
       sm->abort = 0;
       tc::fence_barrier_init();
     }
+    pdl_wait();  // nothing below runs before the kernels ahead of this one have finished
     int r0 = (int)((int64_t)blockIdx.x * total / gridDim.x), r1 = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
     if (a.B <= PRE_MAX) {
       // the work of each sequence in tile units (its tiles, plus SEQ_START_UNITS for starting on it:
@@ -1211,16 +1214,22 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
     tc::tmem_alloc(&sm->tmem_base, a.tmem_cols);
     tc::tmem_relinquish();
     tc::tc_fence_before();
+    pdl_wait();
     tc::named_bar_arrive(BAR_TMEM, 32 + 256);
     tc::named_bar_sync(BAR_SETUP, blockDim.x);
   } else if (warp < W_LOAD) {
     const int g = warp >> 2;
     for (int x = threadIdx.x & 127; x < a.qps * HIST_BINS; x += 128) hist_s[g * a.qps * HIST_BINS + x] = 0;
+    pdl_wait();
     tc::named_bar_sync(BAR_SETUP, blockDim.x);
   } else {
+    pdl_wait();
     tc::named_bar_sync(BAR_SETUP, blockDim.x);
   }
   const int lo = sm->range[0], hi = sm->range[1];
+  // every thread is past its dependency wait: the kernels after this one may start from here on (so
+  // when one of them starts, everything before this kernel has finished)
+  pdl_launch_dependents();
   // head weights and per-token entry counts of the CTA's sequences, when there are few of them
   // (epilogue warps only)
   const int b_first = lo / a.tiles_max;
@@ -1241,19 +1250,18 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
 
   if (warp == W_LOAD) {
     // ---------------- TMA producer (lane 0 issues; all lanes look up pages 32 items at a time)
-    if (lane == 0) {
-      tc::tma_prefetch_desc(&kmap);
-      tc::tma_prefetch_desc(&qmap);
-    }
     int stage = 0, cur_b = -1, qn = 0, rn = 0;
     uint32_t phase = 0;
     bool stop = false;
     const uint64_t pol = tc::l2_policy_evict_first();
     ItemIter cur;  // every lane walks the same items; lane i keeps the i-th of each group of 32
     cur.init(a, lo, hi);
+    // the first group is only as large as the stages, so that the first copies go out after a few steps
+    // of the walk (each step is a short dependent chain; a whole group of 32 took about 3 us)
+    int group = a.stages;
     while (cur.valid() && !stop) {
       int vb = -1, pg0 = -1, pg1 = -1, j0 = 0, nc = 0;
-      for (int i = 0; i < 32 && cur.valid(); ++i) {
+      for (int i = 0; i < group && cur.valid(); ++i) {
         if (lane == i) {
           vb = cur.b;
           j0 = cur.tile * TILE;
@@ -1265,7 +1273,7 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
         pg0 = page_of(a, vb, j0 / 64);
         pg1 = (j0 + 64 < nc) ? page_of(a, vb, j0 / 64 + 1) : -1;
       }
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < group; ++i) {
         const int b = __shfl_sync(0xffffffffu, vb, i);
         const int p0 = __shfl_sync(0xffffffffu, pg0, i);
         const int p1 = __shfl_sync(0xffffffffu, pg1, i);
@@ -1320,6 +1328,7 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
           break;
         }
       }
+      group = 32;
     }
     if (lane == 0) {
       // drain: every issued load must land before the CTA may exit (a completed phase returns at once)
@@ -1751,10 +1760,10 @@ static cudaError_t launch_indexer_score_tc(const dsv4_indexer_topk_params& p, co
   if (grid <= 0) return cudaSuccess;
   // the expanding warps exist only for raw records
   if (a.kf == KF_I8)
-    return launch_pdl(indexer_score_tc<KF_I8>, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/false, kmap, qmap, a);
+    return launch_pdl(indexer_score_tc<KF_I8>, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/true, kmap, qmap, a);
   if (a.kf == KF_MX)
-    return launch_pdl(indexer_score_tc<KF_MX>, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/false, kmap, qmap, a);
-  return launch_pdl(indexer_score_tc<KF_BF16>, dim3(grid), dim3(THREADS_BF16), smem, st, /*pdl=*/false, kmap, qmap,
+    return launch_pdl(indexer_score_tc<KF_MX>, dim3(grid), dim3(THREADS), smem, st, /*pdl=*/true, kmap, qmap, a);
+  return launch_pdl(indexer_score_tc<KF_BF16>, dim3(grid), dim3(THREADS_BF16), smem, st, /*pdl=*/true, kmap, qmap,
                     a);
 }
 
