@@ -194,7 +194,8 @@ __host__ __device__ inline size_t fixed_bytes(int n) {
   return hist_offset(n) + (size_t)HIST_BINS * 4 + (size_t)NBUF * CHUNK * 4;
 }
 
-// Exclusive prefix sum of one value per thread over the CTA; *total gets the sum.
+// Exclusive prefix sum of one value per thread over the CTA; *total gets the sum.  Warp scans by
+// shuffles, then every thread adds up the totals of the warps before its own (wt: 32 ints).
 __device__ __forceinline__ int block_excl_scan(int v, int* wt, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int incl = v;
@@ -205,22 +206,15 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wt, int* total) {
   }
   if (lane == 31) wt[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const int w = lane < nw ? wt[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += u;
-    }
-    if (lane < nw) wt[lane] = wi - w;
-    if (lane == 31) wt[32] = wi;
+  int before = 0, all = 0;
+  for (int w = 0; w < nw; ++w) {
+    const int t = wt[w];
+    before += w < warp ? t : 0;
+    all += t;
   }
-  __syncthreads();
-  const int r = wt[warp] + incl - v;
-  *total = wt[32];
-  __syncthreads();
-  return r;
+  *total = all;
+  __syncthreads();  // wt is free again for the next call
+  return before + incl - v;
 }
 
 // The bin of histogram h (256 * PER bins; in shared memory, or with GLOBAL in global memory, read
@@ -335,64 +329,96 @@ __device__ __forceinline__ void scan_chunk(const float* sb, int nblocks, int j_b
   }
 }
 
-// The bitmap words and candidates of a whole resident row in one pass, as scan_chunk, but without
-// atomics: each warp appends its candidates (found by ballots, in lane order within each column of a
-// block) to its own region regs + warp * C, where C is the threshold bin's count (the histogram counts
-// the same scores, so a region never overflows; writes beyond it are dropped), then the regions are
-// packed in warp order into cand[0, m) and c->ncand = m.  Whole CTA; regs and cand in shared memory.
-__device__ void scan_resident(const float* sb, int nblocks, int n, uint32_t bstar, uint32_t* bits, int words,
-                              uint64_t* regs, uint32_t C, uint64_t* cand, Ctl* c, const uint32_t* incl,
-                              bool all_in) {
+// The bitmap words of a whole resident row in one pass (sb: the row from entry 0; nblk 128-entry
+// blocks): entries above the threshold bin in `bits`, entries in it in `cbits` (same layout), entries j
+// >= n and, with `incl`, blocks not named in neither (all_in: every other entry in bits).  Warp w takes
+// blocks w, w + NW, ..., GB at a time with all of a group's scores loaded first; per column two
+// ballots and no branch.  With both bin edges among the non-negative scores (FAST) the float bits are
+// compared as signed integers, which orders them as the order keys do.
+template <bool FAST>
+__device__ __forceinline__ void scan_bits_t(const float4* sb4, int nblk, int n, uint32_t lo, uint32_t hi,
+                                            bool none_above, uint32_t* bits, uint32_t* cbits, const uint32_t* incl,
+                                            bool all_in) {
+  constexpr int GB = 7;  // blocks a warp loads at once (28 registers)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
-  const float4* sb4 = reinterpret_cast<const float4*>(sb);
-  const int per = (nblocks + NW - 1) / NW;
-  const int b0 = min(nblocks, warp * per), b1 = min(nblocks, b0 + per);
-  uint64_t* my = regs + (size_t)warp * C;
-  uint32_t cnt = 0;  // warp-uniform
-  const unsigned below = (1u << lane) - 1u;
-  for (int g = b0; g < b1; g += SCAN_B) {
-    float4 v[SCAN_B];
+  for (int g0 = warp; g0 < nblk; g0 += GB * NW) {
+    float4 v[GB];
 #pragma unroll
-    for (int i = 0; i < SCAN_B; ++i) v[i] = g + i < b1 ? sb4[(g + i) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < GB; ++k) {
+      const int blk = g0 + k * NW;
+      v[k] = blk < nblk ? sb4[blk * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
-    for (int i = 0; i < SCAN_B; ++i) {
-      const int blk = g + i;
-      const bool live = blk < b1 && (incl == nullptr || ((incl[blk >> 5] >> (blk & 31)) & 1u));  // warp-uniform
-      const int j0 = blk * 128 + 4 * lane;
-      const int nv = live ? n - j0 : 0;
-      const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-      uint32_t sw[4];
+    for (int k = 0; k < GB; ++k) {
+      const int blk = g0 + k * NW;
+      if (blk >= nblk) break;  // warp-uniform
+      const float e[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      uint32_t sw[4], cw[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t key = order_key(e[q]);
-        const uint32_t bin = key >> HIST_SHIFT;
-        sw[q] = __ballot_sync(0xffffffffu, q < nv && (all_in || bin > bstar));
-        if (!all_in) {
-          const unsigned cm = __ballot_sync(0xffffffffu, q < nv && bin == bstar);
-          if (cm) {  // warp-uniform
-            const uint32_t at = cnt + (uint32_t)__popc(cm & below);
-            if (((cm >> lane) & 1u) && at < C) my[at] = cand_value(key, j0 + q);
-            cnt += (uint32_t)__popc(cm);
-          }
+      for (int c = 0; c < 4; ++c) {
+        bool ge, gt;
+        if (FAST) {
+          const int xb = __float_as_int(e[c]);
+          ge = xb >= (int)lo;
+          gt = !none_above && xb >= (int)hi;
+        } else {
+          const uint32_t key = order_key(e[c]);
+          ge = key >= lo;
+          gt = !none_above && key >= hi;
+        }
+        sw[c] = __ballot_sync(0xffffffffu, gt);
+        cw[c] = __ballot_sync(0xffffffffu, ge);
+      }
+      const int rem = n - blk * 128;  // >= 1
+      const bool live = incl == nullptr || ((incl[blk >> 5] >> (blk & 31)) & 1u);
+      if (rem < 128 || !live || all_in) {  // warp-uniform: the row's last block, or candidate filtering
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int kk = rem >= 128 ? 32 : (rem - c + 3) >> 2;  // lanes holding an entry j < n in column c
+          const uint32_t vm = live ? (kk >= 32 ? ~0u : (1u << kk) - 1u) : 0u;
+          sw[c] = all_in ? vm : sw[c] & vm;
+          cw[c] = all_in ? 0u : cw[c] & vm;
         }
       }
-      if (lane == 0 && blk < b1 && 4 * blk < words)
+      if (lane == 0) {
         *reinterpret_cast<uint4*>(bits + 4 * blk) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+        *reinterpret_cast<uint4*>(cbits + 4 * blk) =
+            make_uint4(cw[0] & ~sw[0], cw[1] & ~sw[1], cw[2] & ~sw[2], cw[3] & ~sw[3]);
+      }
     }
   }
-  if (lane == 0) c->wt[warp] = (int)min(cnt, C);
-  __syncthreads();
-  uint32_t base = 0, total = 0;
-  for (int w = 0; w < NW; ++w) {
-    const uint32_t k = (uint32_t)c->wt[w];
-    base += w < warp ? k : 0u;
-    total += k;
+}
+__device__ __forceinline__ void scan_bits(const float* sb, int nblk, int n, uint32_t bstar, uint32_t* bits,
+                                          uint32_t* cbits, const uint32_t* incl, bool all_in) {
+  const uint32_t lo = bstar << HIST_SHIFT, hi = (bstar + 1u) << HIST_SHIFT;
+  const bool none_above = bstar == (uint32_t)(HIST_BINS - 1);
+  const float4* sb4 = reinterpret_cast<const float4*>(sb);
+  if (lo >= 0x80000000u)
+    scan_bits_t<true>(sb4, nblk, n, lo - 0x80000000u, none_above ? 0u : hi - 0x80000000u, none_above, bits, cbits,
+                      incl, all_in);
+  else
+    scan_bits_t<false>(sb4, nblk, n, lo, hi, none_above, bits, cbits, incl, all_in);
+}
+
+// The entries marked in cbits (words words; row sb in shared memory) listed as candidate values into
+// cand[0, min(m, cap)); c->ncand = m.  Thread i takes words i, i + NT, ...  Whole CTA.
+__device__ void list_cands(const float* sb, const uint32_t* cbits, int words, uint64_t* cand, uint32_t cap, Ctl* c) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  int cnt = 0;
+  for (int w = tid; w < words; w += NT) cnt += __popc(cbits[w]);
+  int total;
+  uint32_t pos = (uint32_t)block_excl_scan(cnt, c->wt, &total);
+  for (int w = tid; w < words; w += NT) {
+    uint32_t m = cbits[w];
+    while (m) {
+      const int l = __ffs(m) - 1;
+      m &= m - 1;
+      const int j = ((w >> 2) << 7) | (l << 2) | (w & 3);
+      if (pos < cap) cand[pos] = cand_value(order_key(sb[j]), j);
+      ++pos;
+    }
   }
-  const uint32_t mine = min(cnt, C);
-  for (uint32_t i = lane; i < mine; i += 32) cand[base + i] = my[i];
-  __syncthreads();
-  if (threadIdx.x == 0) c->ncand = total;
-  __syncthreads();
+  if (tid == 0) c->ncand = (uint32_t)total;
 }
 
 // Threshold of the R largest (0 < R < m) of m unique values get(i) < 2^(TOP + 10): a radix select of
@@ -611,7 +637,8 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
     for (int i = 0; i <= NBUF; ++i) tc::mbar_init(&c->bar[i], 1);
     tc::fence_barrier_init();
   }
-  __syncthreads();
+  // (no barrier here: the other threads touch the control block and the mbarriers only after the
+  // barriers inside the threshold search below)
   auto issue = [&](int cc) {
     const uint32_t bytes = (uint32_t)min(CHUNK, n128 - cc * CHUNK) * 4u;
     uint64_t* bar = &c->bar[cc % NBUF];
@@ -644,14 +671,14 @@ __device__ bool topk_token(const float* s_g, uint32_t* hist_g, int n, int K, int
   if (resident) {
     bool ok = true;
     for (int cc = 0; cc < nchunks && ok; ++cc) ok = tc::mbar_wait_bounded(&c->bar[cc], 0, abort);
-    if (!__syncthreads_and(ok))
+    if (!__syncthreads_and(ok)) {
       stop = 0;
-    else if ((size_t)C * ((blockDim.x >> 5) + 1) <= cap)  // per-warp regions above the packed list
-      scan_resident(reinterpret_cast<const float*>(chunks), n128 >> 7, n, bstar, bits, words, cand_s + C, C, cand_s,
-                    c, incl, all_in);
-    else
-      scan_chunk(reinterpret_cast<const float*>(chunks), n128 >> 7, 0, n, bstar, bits, words, cand, ccap, &c->ncand,
-                 incl, all_in);
+    } else {  // the threshold bin's entries marked in a second bitmap (over the unused histogram area)
+      uint32_t* cbits = hist_s;
+      scan_bits(reinterpret_cast<const float*>(chunks), n128 >> 7, n, bstar, bits, cbits, incl, all_in);
+      __syncthreads();
+      list_cands(reinterpret_cast<const float*>(chunks), cbits, words, cand, ccap, c);
+    }
   }
   for (int cc = 0; cc < nchunks && !resident; ++cc) {
     if (!__syncthreads_and(tc::mbar_wait_bounded(&c->bar[cc % NBUF], (cc / NBUF) & 1, abort))) {
@@ -1080,21 +1107,33 @@ struct ItemIter {
 // Called by the group's four warps, with bounded group barriers.
 __device__ __forceinline__ bool finish_seq(const Args& a, Smem* sm, uint32_t* hist_g, int b, int ntile, int g, int row,
                                            uint32_t* ephase, volatile int* abort) {
+  uint32_t tiles = 0;
+  if (row == 0) tiles = (uint32_t)live_tiles(a, b, seq_entries(a, b));  // its load overlaps the flush
   if (!tc::group_sync(&sm->ebar[g], ephase, abort)) return false;
-  for (int x = row; x < a.qps * HIST_BINS; x += 128) {
-    const uint32_t v = hist_g[x];
-    if (v) {
-      atomicAdd(&a.bufs.hist[(int64_t)(b * a.qps + x / HIST_BINS) * HIST_BINS + (x % HIST_BINS)], v);
-      hist_g[x] = 0;
+  // 4 bins at a time (the histograms are 16-byte aligned, qps x HIST_BINS a multiple of 512)
+  uint4* h4 = reinterpret_cast<uint4*>(hist_g);
+#pragma unroll 4
+  for (int x4 = row; x4 < a.qps * (HIST_BINS / 4); x4 += 128) {
+    const uint4 v = h4[x4];
+    if (v.x | v.y | v.z | v.w) {
+      const int x = 4 * x4;
+      uint32_t* dst = a.bufs.hist + (int64_t)(b * a.qps + x / HIST_BINS) * HIST_BINS + (x % HIST_BINS);
+      if (v.x) atomicAdd(dst, v.x);
+      if (v.y) atomicAdd(dst + 1, v.y);
+      if (v.z) atomicAdd(dst + 2, v.z);
+      if (v.w) atomicAdd(dst + 3, v.w);
+      h4[x4] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   __threadfence();  // this thread's scores and histogram counts before the counter below
   if (!tc::group_sync(&sm->ebar[g], ephase, abort)) return false;
   if (row == 0) {
-    const uint32_t tiles = (uint32_t)live_tiles(a, b, seq_entries(a, b));
     const uint32_t prev = atomicAdd(&a.bufs.seq_done[b], (uint32_t)ntile);
     if (prev + (uint32_t)ntile == tiles) {
       a.bufs.seq_done[b] = 0u;  // complete: no CTA adds to it again in this call; cleared for the next
+      // the other CTAs' scores and counts (each fenced before its own counter update) are visible to
+      // this CTA's top-k, which reads them after a CTA barrier
+      __threadfence();
       const uint32_t i = atomicAdd(&sm->nfin, 1u);
       if (i < FIN_MAX) sm->fin[i] = b;
       else atomicOr(&g_flags_ix, FLAG_TOPK);
@@ -1620,8 +1659,9 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
     tc::tmem_dealloc(tmem, a.tmem_cols);
   }
   if (sm->abort || !a.fuse_topk) return;  // block-uniform
-  // ---------------- top-k of the sequences this CTA completed, in the now idle shared memory
-  __threadfence();
+  // ---------------- top-k of the sequences this CTA completed, in the now idle shared memory (the
+  // thread that completed a sequence fenced after seeing its count; the barrier above orders the
+  // other threads after it)
   uint8_t* tbuf = base;
   const size_t tbytes = (size_t)(reinterpret_cast<uint8_t*>(sm) - base);
   const int nfin = min((int)sm->nfin, FIN_MAX);
@@ -1629,7 +1669,8 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
     const int b = sm->fin[f];
     for (int q = 0; q < a.qps; ++q) {
       const int t = b * a.qps + q;
-      const int n = visible_entries(a.positions, t, a.max_context, a.ratio);
+      const int n = (pre && b - b_first < WSEQ) ? sm->nc_tab[b - b_first][q]
+                                                 : visible_entries(a.positions, t, a.max_context, a.ratio);
       const float* srow = a.bufs.scores + (int64_t)t * a.bufs.nc_stride;
       if (!tk::topk_token(srow, a.bufs.hist + (int64_t)t * HIST_BINS, n, a.K, a.topk_idx + (int64_t)t * a.K,
                           a.topk_score ? a.topk_score + (int64_t)t * a.K : nullptr,
