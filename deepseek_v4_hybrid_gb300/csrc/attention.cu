@@ -922,23 +922,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0 && sm->abort) atomicOr(&g_flags_at, FLAG_TIMEOUT);
   if (a.cluster_merge) {
     // ---------------- merge of the chunks inside the cluster (every thread of every CTA reaches the
-    // three cluster barriers, whatever happened before: nothing here waits on a flag)
+    // two cluster barriers, whatever happened before: nothing here waits on a flag).  CTA c owns value
+    // dims [c WS, (c + 1) WS) of the 64 x 512 output block; every CTA pushes its scaled partial of each
+    // owner's dims into that owner's shared memory (a slot per sender over its idle Q and tile
+    // buffers), and each owner sums its slots locally.
     cg::cluster_group cl = cg::this_cluster();
     const int nc = a.n_chunks, crank = (int)cl.block_rank();
     const bool smx = warp < 8;
+    const int h = 32 * hf + lane;
+    const float sink_l2 = (smx && p.sink) ? p.sink[hg * HG + h] * 1.4426950408889634f : -INFINITY;
     if (smx) sm->lred[hf][qd][lane] = lsum;
     __syncthreads();
     if (smx && qd == 0) {
       float l = 0.f;
 #pragma unroll
       for (int w = 0; w < 4; ++w) l += sm->lred[hf][w][lane];
-      sm->cml[32 * hf + lane] = make_float2(have_o ? mref : -INFINITY, l);
+      sm->cml[h] = make_float2(have_o ? mref : -INFINITY, l);
     }
-    cl.sync();  // every chunk's (max, sum) per head is in its shared memory
-    float* ot = reinterpret_cast<float*>(kv_mem);  // [64 heads][512 values] fp32 = 128 KB
+    const int WS = ((DV + nc - 1) / nc + 3) & ~3;  // value dims an owner sums (a multiple of 4)
+    float* recv = reinterpret_cast<float*>(q_mem);  // [sender][head][WS] fp32, <= 136 KB of the 216 KB
+    cl.sync();  // every chunk's (max, sum) per head is in its shared memory and its buffers are idle
     if (smx) {
-      const int h = 32 * hf + lane;
-      const float sink_l2 = p.sink ? p.sink[hg * HG + h] * 1.4426950408889634f : -INFINITY;
       // every chunk's (max, sum) of head h read at once: a remote read's latency is paid once, not nc times
       float2 ml[MAX_MERGE_CLUSTER];
 #pragma unroll
@@ -956,63 +960,60 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (crank == 0 && qd == 0 && p.lse)
         p.lse[(int64_t)t * p.H + hg * HG + h] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
       __syncwarp();
-      // this chunk's O^T scaled by its weight, as [head][value] rows in the idle tile buffer
-      for (int m = 0; m < 4; ++m) {
-        uint32_t o[32];
+      // the weights of the warp's 32 heads (0 for a chunk without output)
+      float wgt[32];
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 f4 = *reinterpret_cast<const float4*>(&sm->mrow[warp][k]);
+        wgt[k] = have_o ? f4.x : 0.f;
+        wgt[k + 1] = have_o ? f4.y : 0.f;
+        wgt[k + 2] = have_o ? f4.z : 0.f;
+        wgt[k + 3] = have_o ? f4.w : 0.f;
+      }
+      // this chunk's O^T scaled by the weights, value dim d = 128 m + R of heads 32 hf .. + 31, pushed
+      // to the owner of d; two TMEM loads in flight at a time
+      for (int m = 0; m < 4; m += 2) {
+        uint32_t o[64];
         if (have_o) {
           tc::tmem_ld32_nowait(lane_base + COL_O + 64 * m + 32 * hf, o);
-          tc::tmem_wait_ld_regs<32>(o);
+          tc::tmem_ld32_nowait(lane_base + COL_O + 64 * (m + 1) + 32 * hf, o + 32);
+          tc::tmem_wait_ld_regs<64>(o);
         }
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float f = sm->mrow[warp][k];
-          ot[(32 * hf + k) * DV + 128 * m + R] = (f == 0.f || !have_o) ? 0.f : __uint_as_float(o[k]) * f;
+        for (int u = 0; u < 2; ++u) {
+          const int d = 128 * (m + u) + R, own = d / WS;
+          float* dst = cl.map_shared_rank(recv, own) + ((size_t)crank * HG + 32 * hf) * WS + (d - own * WS);
+#pragma unroll
+          for (int k = 0; k < 32; ++k)  // (a zero weight gives 0 whatever O^T holds, NaN included)
+            dst[k * WS] = wgt[k] == 0.f ? 0.f : __uint_as_float(o[32 * u + k]) * wgt[k];
         }
       }
     }
-    cl.sync();  // every chunk's scaled partial is staged
+    cl.sync();  // every chunk's partials are in their owners' shared memory (no remote access after this)
     {
-      // this CTA sums its share of the 64 x 512 block over the cluster and writes the output
-      constexpr int TOTAL4 = HG * DV / 4;
-      const int per = (TOTAL4 + nc - 1) / nc;
-      const int x0 = crank * per, x1 = min(TOTAL4, x0 + per);
+      // this CTA sums its dims [d0, d0 + 4 w4) over the senders' slots and writes the output
+      const int d0 = min(DV, crank * WS), w4 = (min(DV, d0 + WS) - d0) / 4;
       const int64_t obase = ((int64_t)t * p.H + hg * HG) * DV;
-      // XB outputs a thread at a time: all their remote reads (from every CTA of the cluster) are
-      // issued before any is summed or stored, so their latencies overlap
-      constexpr int XB = 3;
-      for (int xb = x0 + (int)threadIdx.x; xb < x1; xb += XB * THREADS) {
-        float4 v[XB][MAX_MERGE_CLUSTER];
-#pragma unroll
-        for (int c = 0; c < MAX_MERGE_CLUSTER; ++c) {
-          const float4* src = reinterpret_cast<const float4*>(cl.map_shared_rank(ot, c < nc ? c : 0));
-#pragma unroll
-          for (int j = 0; j < XB; ++j) {
-            const int x = xb + j * THREADS;
-            v[j][c] = (c < nc && x < x1) ? src[x] : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
+      for (int x = threadIdx.x; x < HG * w4; x += THREADS) {
+        const int hh = x / w4, q = x - hh * w4;
+        const float4* src = reinterpret_cast<const float4*>(recv + (size_t)hh * WS) + q;
+        float4 acc = src[0];
+        for (int c = 1; c < nc; ++c) {
+          const float4 v = src[(size_t)c * HG * WS / 4];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
         }
-#pragma unroll
-        for (int j = 0; j < XB; ++j) {
-          const int x = xb + j * THREADS;
-          if (x >= x1) break;
-          float4 acc = v[j][0];
-#pragma unroll
-          for (int c = 1; c < MAX_MERGE_CLUSTER; ++c) {
-            acc.x += v[j][c].x;
-            acc.y += v[j][c].y;
-            acc.z += v[j][c].z;
-            acc.w += v[j][c].w;
-          }
-          if (p.out_dtype == DSV4_F32) {
-            reinterpret_cast<float4*>(p.out)[obase / 4 + x] = acc;
-          } else {
-            reinterpret_cast<uint2*>(p.out)[obase / 4 + x] =
-                make_uint2(float2_to_bf16x2_bits(acc.x, acc.y), float2_to_bf16x2_bits(acc.z, acc.w));
-          }
+        const int64_t o = obase + (int64_t)hh * DV + d0 + 4 * q;
+        if (p.out_dtype == DSV4_F32) {
+          reinterpret_cast<float4*>(p.out)[o / 4] = acc;
+        } else {
+          reinterpret_cast<uint2*>(p.out)[o / 4] =
+              make_uint2(float2_to_bf16x2_bits(acc.x, acc.y), float2_to_bf16x2_bits(acc.z, acc.w));
         }
       }
     }
-    cl.sync();  // no CTA leaves while another still reads its shared memory
   }
   if (warp == W_MMA) {
     // no MMA may still write TMEM when it is released (already true unless the CTA aborted)
