@@ -1180,6 +1180,16 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
     if (lane == 0) {
       tc::tma_prefetch_desc(&kmap);
       tc::tma_prefetch_desc(&qmap);
+      // L2 hints while the kernel ahead finishes (they hand no value over): the positions, and for the
+      // first two sequences of the CTA's share of an even split (its range proper needs the positions)
+      // their block-table rows, queries and head weights
+      tc::prefetch_l2(a.positions, (size_t)a.T * 4);
+      const int g0 = (int)((int64_t)blockIdx.x * total / gridDim.x);
+      for (int b = g0 / a.tiles_max; b < min(a.B, g0 / a.tiles_max + 2); ++b) {
+        tc::prefetch_l2(a.block_table + (int64_t)(b / a.bt_div) * a.max_pages, (size_t)a.max_pages * 4);
+        tc::prefetch_l2(a.weights + (int64_t)b * a.qps * a.Ih, (size_t)a.N * 4);
+        for (int kb = 0; kb < a.kblk; ++kb) tc::tma_prefetch_2d(&qmap, kb * 64, b * a.qps * a.Ih);
+      }
       for (int s = 0; s < a.stages; ++s) {
         tc::mbar_init(&sm->full[s], RAW ? NEXP : 1);  // raw records: the expanding warps; else the loader (+ bytes)
         tc::mbar_init(&sm->empty[s], 1);

@@ -12,6 +12,7 @@
 
 #include "dsv4_common.cuh"
 #include "dsv4_launch.h"
+#include "tc_ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -484,7 +485,21 @@ __device__ __forceinline__ void compress_update_body(const dsv4_compress_update_
 
 __global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compress_update_params p) {
   pdl_launch_dependents();
-  if (!p.after_independent) pdl_wait();
+  if (!p.after_independent) {
+    // while the kernel ahead finishes: the sequence's new rows and state ring, and a slice of wk
+    // (every sequence's index key reads all of it), into L2
+    if (threadIdx.x == 0) {
+      const int b = blockIdx.x, half = p.coff * D, nslots = p.coff * p.ratio;
+      tc::prefetch_l2(p.kv_score + (int64_t)b * p.q_per_seq * 2 * half, (size_t)p.q_per_seq * 2 * half * 4);
+      tc::prefetch_l2(p.state + (int64_t)b * nslots * 2 * half, (size_t)nslots * 2 * half * 4);
+      if (p.wk != nullptr) {
+        const size_t wb = (size_t)p.ik_dim * D * 2, slice = (wb / gridDim.x + 127) / 128 * 128;
+        if ((size_t)b * slice < wb)
+          tc::prefetch_l2(reinterpret_cast<const uint8_t*>(p.wk) + (size_t)b * slice, min(slice, wb - (size_t)b * slice));
+      }
+    }
+    pdl_wait();
+  }
   compress_update_body(p);
   if (p.after_independent) pdl_wait();  // completes only after the kernel before it
 }
@@ -607,7 +622,17 @@ __device__ __forceinline__ void compress_fold_cluster_body(const dsv4_compress_u
 __global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
     compress_fold_cluster_kernel(dsv4_compress_update_params p) {
   pdl_launch_dependents();
-  if (!p.after_independent) pdl_wait();
+  if (!p.after_independent) {
+    // while the kernel ahead finishes: this CTA's 16 ring rows of the sequence (slots 16 rank .. + 15,
+    // whatever the position) and its new rows, into L2
+    if (threadIdx.x == 0) {
+      const int b = blockIdx.y, rank = (int)cg::this_cluster().block_rank();
+      tc::prefetch_l2(p.state + ((int64_t)b * p.ratio + rank * (p.ratio / FOLD_CTAS)) * 2 * D,
+                      (size_t)(p.ratio / FOLD_CTAS) * 2 * D * 4);
+      if (rank == 0) tc::prefetch_l2(p.kv_score + (int64_t)b * p.q_per_seq * 2 * D, (size_t)p.q_per_seq * 2 * D * 4);
+    }
+    pdl_wait();
+  }
   compress_fold_cluster_body(p);
   if (p.after_independent) pdl_wait();  // completes only after the kernel before it
 }

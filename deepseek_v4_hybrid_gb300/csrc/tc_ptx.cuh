@@ -305,6 +305,28 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_amn_bmn(int M, int N) {
 }
 
 
+// A hint that brings the 16-byte aligned part of [ptr, ptr + bytes) of global memory into L2, in 64 KB
+// pieces.  It hands no value to the thread, so it may be issued before a dependency wait on memory
+// that an earlier kernel may still be writing (L2 is where the writes land; the loads that read the
+// values still come after the wait).
+__device__ __forceinline__ void prefetch_l2(const void* ptr, size_t bytes) {
+  uint64_t a = (reinterpret_cast<uint64_t>(ptr) + 15) & ~uint64_t(15);
+  const uint64_t e = (reinterpret_cast<uint64_t>(ptr) + bytes) & ~uint64_t(15);
+  while (a < e) {
+    const uint32_t n = (uint32_t)((e - a) < 65536u ? (e - a) : 65536u);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(n) : "memory");
+    a += n;
+  }
+}
+
+// The same hint for the box of a 2D tensor map at coordinates (x, y).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Plain (untiled) bulk copy of `bytes` from global to shared memory, completing on `bar`; both
 // addresses 16-byte aligned and `bytes` a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
