@@ -44,6 +44,19 @@ namespace dsv4 {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
+// Start of a kernel that is either after_independent (its work needs nothing from the kernels ahead:
+// their dependents may start at once, and it waits for them only before exiting) or not (it waits
+// first and lets its own dependents start only then, so that when a kernel after it starts, every
+// kernel before this one has finished).
+__device__ __forceinline__ void pdl_start(bool after_independent) {
+  if (after_independent) {
+    pdl_launch_dependents();
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
+}
+
 // `pdl` false launches plainly (the kernel's pdl_wait() then returns at once).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,

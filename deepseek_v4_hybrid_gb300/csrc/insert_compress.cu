@@ -57,8 +57,7 @@ __device__ __forceinline__ void kv_insert_body(const dsv4_kv_insert_params& p) {
 }
 
 __global__ void __launch_bounds__(ROW_THREADS) kv_insert_kernel(dsv4_kv_insert_params p) {
-  pdl_launch_dependents();
-  if (!p.after_independent) pdl_wait();
+  pdl_start(p.after_independent != 0);
   kv_insert_body(p);
   if (p.after_independent) pdl_wait();  // completes only after the kernel before it
 }
@@ -154,8 +153,7 @@ __device__ __forceinline__ void qprep_head(const uint8_t* src, uint8_t* dst, boo
 }
 
 __global__ void __launch_bounds__(ROW_THREADS) qnorm_rope_kv_insert_kernel(dsv4_qnorm_rope_kv_insert_params p) {
-  pdl_launch_dependents();
-  if (!p.after_independent) pdl_wait();
+  pdl_start(p.after_independent != 0);
   const int t = blockIdx.x, y = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = (p.H_pad + QP_HEADS - 1) / QP_HEADS;
   if (y < ngroups) {
@@ -484,8 +482,9 @@ __device__ __forceinline__ void compress_update_body(const dsv4_compress_update_
 }
 
 __global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compress_update_params p) {
-  pdl_launch_dependents();
-  if (!p.after_independent) {
+  if (p.after_independent) {
+    pdl_launch_dependents();
+  } else {
     // while the kernel ahead finishes: the sequence's new rows and state ring, and a slice of wk
     // (every sequence's index key reads all of it), into L2
     if (threadIdx.x == 0) {
@@ -499,6 +498,7 @@ __global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compr
       }
     }
     pdl_wait();
+    pdl_launch_dependents();
   }
   compress_update_body(p);
   if (p.after_independent) pdl_wait();  // completes only after the kernel before it
@@ -621,8 +621,9 @@ __device__ __forceinline__ void compress_fold_cluster_body(const dsv4_compress_u
 
 __global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
     compress_fold_cluster_kernel(dsv4_compress_update_params p) {
-  pdl_launch_dependents();
-  if (!p.after_independent) {
+  if (p.after_independent) {
+    pdl_launch_dependents();
+  } else {
     // while the kernel ahead finishes: this CTA's 16 ring rows of the sequence (slots 16 rank .. + 15,
     // whatever the position) and its new rows, into L2
     if (threadIdx.x == 0) {
@@ -632,6 +633,7 @@ __global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
       if (rank == 0) tc::prefetch_l2(p.kv_score + (int64_t)b * p.q_per_seq * 2 * D, (size_t)p.q_per_seq * 2 * D * 4);
     }
     pdl_wait();
+    pdl_launch_dependents();
   }
   compress_fold_cluster_body(p);
   if (p.after_independent) pdl_wait();  // completes only after the kernel before it

@@ -107,11 +107,14 @@ typedef struct dsv4_kv_insert_params {
   const float* cos_sin;        /* [max_pos, 64] (32 cos | 32 sin) or NULL = rows already rotated */
   int32_t max_pos;
   int32_t after_independent;   /* 0: the kernel waits for the kernel before it on `stream` before it
-                                  starts its work (always safe).  1: the caller guarantees that the
-                                  kernel before it on `stream` neither reads nor writes anything this
-                                  call reads or writes (as the indexer call of the same step); the
-                                  kernel then does its work at once and waits for that kernel only
-                                  before it exits, so its completion still implies the earlier one's */
+                                  starts its work (always safe), and lets the kernels after it start
+                                  only once that wait is over.  1: the caller guarantees that the
+                                  kernels before it on `stream`, back to and including the last one
+                                  launched with 0 (or any other kernel), neither read nor write
+                                  anything this call reads or writes (as the insert and the
+                                  compressor of one step); the kernel then does its work at once
+                                  and waits for the kernel before it only before it exits, so its
+                                  completion still implies the earlier ones' */
 } dsv4_kv_insert_params;
 
 int dsv4_kv_insert(const dsv4_kv_insert_params* p, dsv4_stream_t stream);

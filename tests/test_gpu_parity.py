@@ -140,23 +140,31 @@ def test_topk_ties_and_negative_scores(lib, mode):
 
 
 @pytest.mark.parametrize("name", ["small_c4_bf16", "small_c128_bf16", "small_c4_fp8"])
-def test_after_independent_gives_the_same_caches(lib, name):
+@pytest.mark.parametrize("order", ["indexer_first", "compress_first"])
+def test_after_independent_gives_the_same_caches(lib, name, order):
     """insert and compress with after_independent (start at once, wait for the kernel before them only
-    before exiting) write exactly what they write when they wait first, also when each runs right
-    after the indexer call, as in the decode step."""
+    before exiting) write exactly what they write when they wait first: right after the indexer call
+    (indexer -> insert -> compress), and the insert right after the compressor (compress -> insert ->
+    indexer, the order of the decode step when the compressor writes the index keys)."""
     from deepseek_v4_hybrid_gb300.step import DeviceStep
     import deepseek_v4_hybrid_gb300 as M
     st = I.make_step(I.SMALL_CONFIGS[name])
     out = {}
     for late in (False, True):
         ds = DeviceStep(st)
-        ds.indexer()
-        ds.insert(after_independent=late)
-        ds.compress(after_independent=late)
+        if order == "indexer_first":
+            ds.indexer()
+            ds.insert(after_independent=late)
+            ds.compress(after_independent=late)
+        else:
+            ds.compress()
+            ds.insert(after_independent=late)
+            ds.indexer()
         ds.attention()
         torch.cuda.synchronize()
         assert M.dsv4_read_device_flags() == 0
-        out[late] = {k: to_host(getattr(ds, k)) for k in ("swa_cache", "main_cache", "state", "out")
+        out[late] = {k: to_host(getattr(ds, k)) for k in ("swa_cache", "main_cache", "state", "idx_cache",
+                                                          "topk_idx", "out")
                      if getattr(ds, k, None) is not None}
     for k, v in out[False].items():
         assert np.array_equal(v, out[True][k]), k
