@@ -1216,7 +1216,27 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
     }
     pdl_wait();  // nothing below runs before the kernels ahead of this one have finished
     int r0 = (int)((int64_t)blockIdx.x * total / gridDim.x), r1 = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
-    if (a.B <= PRE_MAX) {
+    if (a.B <= 32) {
+      // the same as below with one sequence a lane, in registers: the prefix by shuffles, and the
+      // sequence a work unit falls in by one ballot (the last lane whose prefix is not above it)
+      const int nt = lane < a.B ? live_tiles(a, lane, seq_entries(a, lane)) : 0;
+      const int v = nt > 0 ? nt + SEQ_START_UNITS : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      const int running = __shfl_sync(0xffffffffu, incl, 31), pre_b = incl - v;
+      auto dense = [&](int x) {
+        const unsigned m = __ballot_sync(0xffffffffu, lane < a.B && pre_b <= x);  // bit 0 always set
+        const int l = 31 - __clz(m);
+        const int pl = __shfl_sync(0xffffffffu, pre_b, l);
+        return x >= running ? total : l * a.tiles_max + max(0, x - pl - SEQ_START_UNITS);
+      };
+      r0 = dense((int)((int64_t)blockIdx.x * running / gridDim.x));
+      r1 = dense((int)((int64_t)(blockIdx.x + 1) * running / gridDim.x));
+    } else if (a.B <= PRE_MAX) {
       // the work of each sequence in tile units (its tiles, plus SEQ_START_UNITS for starting on it:
       // the histogram flush and counter update of the sequence left and the next queries), all loaded
       // first (independent loads, all in flight together), then the scan
