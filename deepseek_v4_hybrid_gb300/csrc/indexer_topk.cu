@@ -1142,6 +1142,18 @@ __device__ __forceinline__ bool finish_seq(const Args& a, Smem* sm, uint32_t* hi
   return true;
 }
 
+// The MMAs of one key tile: K-block kb, 16-dim step s of the keys (A: 128 rows of 128 B a K-block)
+// against the queries (B: N rows of 128 B a K-block), accumulating from the second on.
+template <int KBLK>
+__device__ __forceinline__ void issue_tile(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t idesc, int N) {
+#pragma unroll
+  for (int kb = 0; kb < KBLK; ++kb)
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      tc::mma_bf16(d_tmem, ad + (uint64_t)((kb * KB_BYTES + s * 32) >> 4), bd + (uint64_t)((kb * N * 128 + s * 32) >> 4),
+                   idesc, (kb | s) != 0);
+}
+
 // One instance per key format: the bf16 one has no expanding warps (320 threads, at most three warps
 // on a sub-partition: 168 registers a thread) and none of the raw-record branches; the raw-record
 // ones run 14 warps at 128 registers a thread (the 512-thread bound sets that cap).
@@ -1415,8 +1427,13 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
     }
   } else if (warp == W_MMA) {
     if (lane == 0) {
-      // ---------------- MMA issuer
+      // ---------------- MMA issuer (one thread; its instruction issue sets the pace of the key
+      // stream, so the descriptors are built once and advanced by constant offsets: a descriptor's
+      // start address is its low 14 bits in 16-byte units, and every shared address here is below
+      // 256 KB)
       const uint32_t idesc = tc::idesc_bf16_f32(TILE, a.N);
+      const uint64_t adesc0 = tc::sdesc_k_sw128(tc::smem_addr(stage_mem));
+      const uint64_t qdesc0 = tc::sdesc_k_sw128(tc::smem_addr(q_mem));
       int stage = 0, acc = 0, cur_b = -1, qn = 0, slot = 0;
       uint32_t phase = 0, aphase = 0;
       ItemIter cur;
@@ -1431,17 +1448,13 @@ __global__ void __launch_bounds__(KF == 0 ? THREADS_BF16 : 512, 1)
         if (!tc::mbar_wait_bounded(&sm->full[stage], phase, abort)) break;
         if (!tc::mbar_wait_bounded(&sm->dempty[acc], aphase ^ 1, abort)) break;
         tc::tc_fence_after();
-        const uint32_t a_addr = tc::smem_addr(stage_mem + stage * stage_bytes);
-        const uint32_t q_addr = tc::smem_addr(q_mem + slot * q_bytes);
+        const uint64_t ad = adesc0 + (uint64_t)((stage * stage_bytes) >> 4);
+        const uint64_t bd = qdesc0 + (uint64_t)((slot * q_bytes) >> 4);
         const uint32_t d_tmem = tmem + (uint32_t)(acc * a.N);
-        for (int kb = 0; kb < a.kblk; ++kb) {
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint64_t ad = tc::sdesc_k_sw128(a_addr + kb * KB_BYTES + s * 32);
-            const uint64_t bd = tc::sdesc_k_sw128(q_addr + kb * a.N * 128 + s * 32);
-            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0);
-          }
-        }
+        if (a.kblk == 2)
+          issue_tile<2>(d_tmem, ad, bd, idesc, a.N);
+        else
+          issue_tile<1>(d_tmem, ad, bd, idesc, a.N);
         tc::mma_commit(&sm->empty[stage]);
         tc::mma_commit(&sm->dfull[acc]);
         const int b_now = cur.b;
