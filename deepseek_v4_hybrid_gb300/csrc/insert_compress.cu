@@ -485,12 +485,18 @@ __global__ void __launch_bounds__(ROW_THREADS) compress_update_kernel(dsv4_compr
   if (p.after_independent) {
     pdl_launch_dependents();
   } else {
-    // while the kernel ahead finishes: the sequence's new rows and state ring, and a slice of wk
-    // (every sequence's index key reads all of it), into L2
+    // while the kernel ahead finishes: the sequence's new rows, its state ring when it folds this step,
+    // and a slice of wk (every sequence's index key reads all of it), into L2
     if (threadIdx.x == 0) {
       const int b = blockIdx.x, half = p.coff * D, nslots = p.coff * p.ratio;
       tc::prefetch_l2(p.kv_score + (int64_t)b * p.q_per_seq * 2 * half, (size_t)p.q_per_seq * 2 * half * 4);
-      tc::prefetch_l2(p.state + (int64_t)b * nslots * 2 * half, (size_t)nslots * 2 * half * 4);
+      // the ring only when a token of the sequence folds an entry this step (positions read relaxed)
+      bool emits = false;
+      for (int k = 0; k < p.q_per_seq; ++k) {
+        const int pos = tc::ld_relaxed_s32(p.positions + b * p.q_per_seq + k);
+        emits |= pos >= 0 && (pos + 1) % p.ratio == 0;
+      }
+      if (emits) tc::prefetch_l2(p.state + (int64_t)b * nslots * 2 * half, (size_t)nslots * 2 * half * 4);
       if (p.wk != nullptr) {
         const size_t wb = (size_t)p.ik_dim * D * 2, slice = (wb / gridDim.x + 127) / 128 * 128;
         if ((size_t)b * slice < wb)
@@ -625,11 +631,17 @@ __global__ void __cluster_dims__(FOLD_CTAS, 1, 1) __launch_bounds__(ROW_THREADS)
     pdl_launch_dependents();
   } else {
     // while the kernel ahead finishes: this CTA's 16 ring rows of the sequence (slots 16 rank .. + 15,
-    // whatever the position) and its new rows, into L2
+    // whatever the position) when the sequence folds this step, and its new rows, into L2
     if (threadIdx.x == 0) {
       const int b = blockIdx.y, rank = (int)cg::this_cluster().block_rank();
-      tc::prefetch_l2(p.state + ((int64_t)b * p.ratio + rank * (p.ratio / FOLD_CTAS)) * 2 * D,
-                      (size_t)(p.ratio / FOLD_CTAS) * 2 * D * 4);
+      bool emits = false;  // (positions read relaxed: the ring rows are read only by a fold)
+      for (int k = 0; k < p.q_per_seq; ++k) {
+        const int pos = tc::ld_relaxed_s32(p.positions + b * p.q_per_seq + k);
+        emits |= pos >= 0 && (pos + 1) % p.ratio == 0;
+      }
+      if (emits)
+        tc::prefetch_l2(p.state + ((int64_t)b * p.ratio + rank * (p.ratio / FOLD_CTAS)) * 2 * D,
+                        (size_t)(p.ratio / FOLD_CTAS) * 2 * D * 4);
       if (rank == 0) tc::prefetch_l2(p.kv_score + (int64_t)b * p.q_per_seq * 2 * D, (size_t)p.q_per_seq * 2 * D * 4);
     }
     pdl_wait();

@@ -319,6 +319,14 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr, size_t bytes) {
   }
 }
 
+// A relaxed (atomic, unordered) load of a value that an earlier kernel may still be writing: for
+// choosing what to prefetch before a dependency wait (a stale value only makes a hint useless).
+__device__ __forceinline__ int ld_relaxed_s32(const int32_t* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // The same hint for the box of a 2D tensor map at coordinates (x, y).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
