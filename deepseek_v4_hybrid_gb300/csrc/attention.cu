@@ -260,8 +260,11 @@ __global__ void __launch_bounds__(AT_THREADS) mla_partial_simt(dsv4_sparse_mla_d
 // quarter) and heads 32 (w >> 2) .. + 31; a tile's per-head maxima are reduced across lanes by a
 // shuffle transpose-reduce and across the four row quarters in shared memory.  A masked row of a
 // loaded half gets zero V (it may hold anything, and 0 x NaN would poison O); PV skips halves that
-// were not loaded.  At the end the same warps turn O^T into [head][value] rows in the idle tile
-// buffer and store the unnormalised O and the chunk's (max, sum) per head.
+// were not loaded.  At the end, when a token's chunks form a cluster (up to 8), the same warps push
+// their O^T scaled by the chunk's log-sum-exp weight into the shared memory of the CTA that owns
+// each value-dim slice, and every owner sums its slots and writes its slice of the output; with more
+// chunks they turn O^T into [head][value] rows in the idle tile buffer and store the unnormalised O
+// and the chunk's (max, sum) per head for mla_merge.
 //
 // fp8_ds_mla caches (656-byte records: 512 e4m3 codes, 64 bf16 rope dims, 8 UE8M0 block exponents)
 // run the same kernel with the tile converted in shared memory: the codes of K-block kb < 8 (64 B

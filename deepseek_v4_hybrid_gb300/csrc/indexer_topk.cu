@@ -142,8 +142,9 @@ __device__ __forceinline__ bool cand_names(const int32_t* row, int M, int blk) {
 //     crossing thread).
 //  2. One pass over the scores: lane l of a warp takes entries 4l .. 4l + 3 of a 128-entry block;
 //     the four ballots of "bin > B*" are the block's four words of the selection bitmap (bit l of
-//     word c = entry 4l + c), and entries in B* are appended to a candidate list as (low 20 key
-//     bits, j) values.
+//     word c = entry 4l + c), and entries in B* go to a list of candidate values (low 20 key bits,
+//     j): a resident row through a second bitmap (four more ballots, no branch) listed afterwards,
+//     a longer row chunk by chunk through per-warp slots.
 //  3. The k - A largest candidates (larger score first, then smaller j: the values are unique) by a
 //     radix select of 10-bit digits over the 40-bit values, stopping at the first digit whose bin
 //     holds exactly the entries still needed; they are added to the bitmap.
